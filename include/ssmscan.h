@@ -1,0 +1,140 @@
+/*
+ * ssmscan.h -- C ABI of libssmscan, the Mamba2 selective-state scan on sm_103a.
+ *
+ * The operation (for every sequence i, head h, head-dim row p and token t of
+ * the sequence, in token order; g(h) = h / (n_heads / n_groups)):
+ *
+ *     dA          = exp(dt[t,h] * A[h])
+ *     S[h,p,:]    = dA * S[h,p,:] + dt[t,h] * x[t,h,p] * B[t,g(h),:]
+ *     y[t,h,p]    = S[h,p,:] . C[t,g(h),:] + D[h] * x[t,h,p]
+ *
+ * S is the fp32 recurrent state of sequence i.  It lives in slot i of
+ * state_slots and persists between calls.  Defined by:
+ *   - "The llama journey", Day 14: the ssm_scan_f32_group kernel body (decay
+ *     exp(dt*A) with a scalar A per head, input term B*x*dt, y = state . C
+ *     from the state that already includes token t, one B/C per group of
+ *     contiguous heads);
+ *   - "The llama journey", Day 12: the SSM_SCAN tensor table (state
+ *     [seq][head][dim][d_state]; x [token][head][dim]; dt [token][head];
+ *     B, C [token][group][d_state]);
+ *   - "keep the Mamba2 scan state in registers, stage tokens by chunk"
+ *     (gllm PR 90), "What changes" and "Testing": batches mix fresh and
+ *     resuming sequences; state is fp32 and moves between slot and registers.
+ * The skip term D[h] * x[t,h,p] is part of the operation.  dt is used as given
+ * (no softplus or bias is applied here).
+ *
+ * Memory and ownership (all calls):
+ *   - Every pointer is CUDA device memory owned by the caller.  The library
+ *     allocates nothing and never synchronises the stream; work is enqueued on
+ *     `stream` (a cudaStream_t passed as void*; NULL = the legacy default
+ *     stream) and its execution errors surface at the caller's next sync.
+ *   - Tokens of all sequences are packed: sequence i owns tokens
+ *     [seq_starts[i], seq_starts[i] + seq_lens[i]) of the n_tokens rows of
+ *     x, dt, B, C and y.  Tokens owned by no sequence are neither read nor
+ *     written.
+ *   - resume_flags[i] != 0: start from slot i.  == 0: start from zero; the
+ *     slot's old contents are never read (they may be NaN).  After the call
+ *     slot i holds the state after the sequence's last token.  A zero-length
+ *     sequence writes no y; a fresh one still leaves a zero slot.
+ *   - Layouts (row-major, contiguous, fp32 unless stated):
+ *       state_slots [n_seqs][n_heads][head_dim][d_state]   in/out
+ *       x           [n_tokens][n_heads][head_dim]
+ *       dt          [n_tokens][n_heads]
+ *       A, D        [n_heads]
+ *       B, C        [n_tokens][n_groups][d_state]
+ *       y           [n_tokens][n_heads][head_dim]               out
+ *       seq_starts, seq_lens, resume_flags   int32 [n_seqs], device memory
+ *   - y must not overlap any input; inputs are read only.
+ *   - Alignment: state_slots, B and C 16-byte aligned (the state moves as
+ *     128-bit vectors); the others 4-byte aligned.
+ *
+ * Preconditions checked only on the device metadata's request: sequence
+ * ranges must lie in [0, n_tokens) and not overlap.  With the environment
+ * variable SSM_SCAN_CHECK=1 the library copies the metadata to the host,
+ * synchronises and rejects bad ranges with SSM_ERR_INVALID_ARG (debug only).
+ *
+ * Errors: host-checkable faults return before any launch:
+ *   SSM_ERR_INVALID_ARG  null pointer, negative size, n_heads % n_groups != 0,
+ *                        misaligned pointer, bad tuning value;
+ *   SSM_ERR_UNSUPPORTED  d_state not a multiple of 4, d_state > 1024;
+ *   SSM_ERR_CUDA         a CUDA call or launch failed (cudaGetLastError);
+ *   SSM_ERR_TIMEOUT      reserved for bounded device waits.
+ * n_seqs == 0 is a successful no-op.
+ */
+#ifndef SSMSCAN_H
+#define SSMSCAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SSM_OK = 0,
+    SSM_ERR_INVALID_ARG = -1,
+    SSM_ERR_UNSUPPORTED = -2,
+    SSM_ERR_CUDA = -3,
+    SSM_ERR_TIMEOUT = -4
+} ssm_status;
+
+/* Kernel path selection for ssm_scan_tuned. */
+enum {
+    SSM_PATH_AUTO = 0,     /* decode when n_tokens == n_seqs, else prefill */
+    SSM_PATH_DECODE = 1,   /* warp-per-row kernel; correct for any lengths */
+    SSM_PATH_PREFILL = 2   /* chunk-staged kernel; correct for any lengths */
+};
+
+/*
+ * Launch-shape overrides for ssm_scan_tuned.  Zero in any field means "pick
+ * automatically".  Every combination that is accepted computes the same
+ * result (up to float association); unsupported values give
+ * SSM_ERR_INVALID_ARG.
+ *   path             SSM_PATH_*
+ *   lanes_per_row    lanes of a warp that share one state row: 1,2,4,8,16,32
+ *   rows_per_thread  state rows each lane holds (1, 2 or 4; <= lanes_per_row)
+ *   rows_per_cta     prefill: state rows per thread block (a multiple of the
+ *                    rows one warp holds, at most 256 threads); decode: ignored
+ *   chunk_tokens     prefill: tokens staged in shared memory per chunk (1..256)
+ *   ctas_per_sm      decode: if > 0, the grid is capped at this many blocks
+ *                    per SM and warps loop over the remaining rows
+ */
+typedef struct {
+    int path;
+    int lanes_per_row;
+    int rows_per_thread;
+    int rows_per_cta;
+    int chunk_tokens;
+    int ctas_per_sm;
+} ssm_scan_tuning;
+
+/*
+ * The scan.  Advances every sequence of the batch through its tokens, writes
+ * y for each of them and leaves each sequence's final state in its slot.
+ * n_tokens is the number of packed token rows of x, dt, B, C and y.
+ */
+int ssm_scan(float *state_slots, const float *x, const float *dt,
+             const float *A, const float *B, const float *C, const float *D,
+             float *y, const int32_t *seq_starts, const int32_t *seq_lens,
+             const int32_t *resume_flags, int n_seqs, int n_tokens,
+             int n_heads, int head_dim, int d_state, int n_groups,
+             void *stream);
+
+/* The same operation with explicit launch-shape choices (tests, tuning). */
+int ssm_scan_tuned(float *state_slots, const float *x, const float *dt,
+                   const float *A, const float *B, const float *C,
+                   const float *D, float *y, const int32_t *seq_starts,
+                   const int32_t *seq_lens, const int32_t *resume_flags,
+                   int n_seqs, int n_tokens, int n_heads, int head_dim,
+                   int d_state, int n_groups, const ssm_scan_tuning *tuning,
+                   void *stream);
+
+/* Text for a status code (static storage; never NULL). */
+const char *ssm_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSMSCAN_H */

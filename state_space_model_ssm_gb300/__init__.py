@@ -1,0 +1,13 @@
+"""libssmscan: the Mamba2 selective-state scan as sm_103a CUDA kernels.
+
+    from state_space_model_ssm_gb300 import ssm_scan
+    y = ssm_scan(state_slots, x, dt, A, B, C, D, seq_starts, seq_lens, resume_flags)
+
+The C ABI is declared in ``include/ssmscan.h``; ``binding`` wraps it with
+ctypes.  ``workloads`` draws the seeded synthetic inputs.
+"""
+from .binding import (PATH_AUTO, PATH_DECODE, PATH_PREFILL, SsmScanError, Tuning,  # noqa: F401
+                      load, ssm_scan, status_string)
+
+__all__ = ["ssm_scan", "Tuning", "SsmScanError", "PATH_AUTO", "PATH_DECODE",
+           "PATH_PREFILL", "load", "status_string"]

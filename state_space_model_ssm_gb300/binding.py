@@ -1,0 +1,149 @@
+"""ctypes binding of libssmscan (argument marshalling only).
+
+Every step of the scan runs in the CUDA kernels of ``libssmscan.so``; this
+module checks tensor dtypes, devices and shapes, passes raw device pointers and
+the current CUDA stream, and turns a nonzero status into an exception.  If the
+library has not been built it raises: there is no other implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libssmscan.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "ssmscan.h")
+
+SSM_OK = 0
+SSM_ERR_INVALID_ARG = -1
+SSM_ERR_UNSUPPORTED = -2
+SSM_ERR_CUDA = -3
+SSM_ERR_TIMEOUT = -4
+
+PATH_AUTO, PATH_DECODE, PATH_PREFILL = 0, 1, 2
+
+_lib = None
+_lock = threading.Lock()
+
+
+class SsmScanError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+class Tuning(ctypes.Structure):
+    """Launch-shape overrides (``ssm_scan_tuning``); zero fields mean automatic."""
+    _fields_ = [("path", ctypes.c_int), ("lanes_per_row", ctypes.c_int),
+                ("rows_per_thread", ctypes.c_int), ("rows_per_cta", ctypes.c_int),
+                ("chunk_tokens", ctypes.c_int), ("ctas_per_sm", ctypes.c_int)]
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SCAN_ARGS = [_P] * 11 + [_I] * 6
+
+
+def load():
+    """Open libssmscan.so (built by ``state_space_model_ssm_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"libssmscan is not built ({LIB_PATH} missing); run "
+                    "`python -m state_space_model_ssm_gb300.build`")
+            lib = ctypes.CDLL(LIB_PATH)
+            lib.ssm_scan.restype = _I
+            lib.ssm_scan.argtypes = _SCAN_ARGS + [_P]
+            lib.ssm_scan_tuned.restype = _I
+            lib.ssm_scan_tuned.argtypes = _SCAN_ARGS + [ctypes.POINTER(Tuning), _P]
+            lib.ssm_status_string.restype = ctypes.c_char_p
+            lib.ssm_status_string.argtypes = [_I]
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load().ssm_status_string(int(status)).decode()
+    except Exception:  # library missing: still give a readable message
+        return {0: "ok", -1: "invalid argument", -2: "unsupported geometry",
+                -3: "CUDA error", -4: "device wait timed out"}.get(int(status), "unknown status")
+
+
+def declared_functions(header: str = HEADER):
+    """Names of the functions declared in the public C header."""
+    text = open(header).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w[\w\s\*]*?\b(ssm_\w+)\s*\(", text, flags=re.M)))
+
+
+def scan_raw(state, x, dt, A, B, C, D, y, seq_starts, seq_lens, resume,
+             n_seqs, n_tokens, n_heads, head_dim, d_state, n_groups,
+             stream=0, tuning: Tuning | None = None) -> int:
+    """Call the C ABI with integer pointers; returns the status code."""
+    lib = load()
+    args = [_P(int(p) if p else None) for p in
+            (state, x, dt, A, B, C, D, y, seq_starts, seq_lens, resume)]
+    args += [int(n_seqs), int(n_tokens), int(n_heads), int(head_dim), int(d_state), int(n_groups)]
+    if tuning is None:
+        return lib.ssm_scan(*args, _P(int(stream) if stream else None))
+    return lib.ssm_scan_tuned(*args, ctypes.byref(tuning), _P(int(stream) if stream else None))
+
+
+def _check(t, name, dtype, device, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def ssm_scan(state_slots, x, dt, A, B, C, D, seq_starts, seq_lens, resume_flags,
+             y=None, *, tuning: Tuning | None = None, stream=None):
+    """Run the scan on the current CUDA stream (or ``stream``).
+
+    state_slots [n,H,P,N] fp32 (updated in place), x [T,H,P], dt [T,H], A [H],
+    B/C [T,G,N], D [H] fp32; seq_starts/seq_lens/resume_flags [n] int32; all on
+    one CUDA device.  Returns y [T,H,P] (allocated if not given).
+    """
+    dev = state_slots.device
+    if dev.type != "cuda":
+        raise ValueError("the scan runs on CUDA tensors only")
+    n, H, P, N = state_slots.shape
+    T = x.shape[0]
+    G = B.shape[1]
+    f32, i32 = torch.float32, torch.int32
+    _check(state_slots, "state_slots", f32, dev)
+    _check(x, "x", f32, dev, (T, H, P))
+    _check(dt, "dt", f32, dev, (T, H))
+    _check(A, "A", f32, dev, (H,))
+    _check(B, "B", f32, dev, (T, G, N))
+    _check(C, "C", f32, dev, (T, G, N))
+    _check(D, "D", f32, dev, (H,))
+    for nm, t in (("seq_starts", seq_starts), ("seq_lens", seq_lens), ("resume_flags", resume_flags)):
+        _check(t, nm, i32, dev, (n,))
+    if y is None:
+        y = torch.empty((T, H, P), dtype=f32, device=dev)
+    _check(y, "y", f32, dev, (T, H, P))
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    with torch.cuda.device(dev):
+        rc = scan_raw(state_slots.data_ptr(), x.data_ptr(), dt.data_ptr(), A.data_ptr(),
+                      B.data_ptr(), C.data_ptr(), D.data_ptr(), y.data_ptr(),
+                      seq_starts.data_ptr(), seq_lens.data_ptr(), resume_flags.data_ptr(),
+                      n, T, H, P, N, G, stream=handle, tuning=tuning)
+    if rc != SSM_OK:
+        raise SsmScanError(rc, "ssm_scan")
+    return y

@@ -1,0 +1,269 @@
+// libssmscan C ABI: argument checks, path and launch-shape choice.
+//
+// Everything here runs on the host and returns before any launch when an
+// argument is wrong.  Nothing is allocated and the stream is never
+// synchronised (except in the opt-in SSM_SCAN_CHECK=1 debug mode).
+#include <climits>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <vector>
+#include <algorithm>
+
+#include "../../include/ssmscan.h"
+#include "scan_common.cuh"
+
+namespace {
+
+constexpr int kMaxDState = 1024;
+constexpr int kMaxDevices = 64;
+
+int pow2ceil(int v)
+{
+    int p = 1;
+    while (p < v)
+        p <<= 1;
+    return p;
+}
+
+bool is_pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Smallest compiled float4-per-lane count that covers a row of N4 float4
+// chunks with `lanes` lanes, or 0 when no compiled kernel fits.
+int pick_vpl(int N4, int lanes, int rpt, bool (*supported)(int, int, int))
+{
+    const int need = (N4 + lanes - 1) / lanes;
+    for (int v = 1; v <= 8; v <<= 1)
+        if (v >= need && supported(lanes, v, rpt))
+            return v;
+    return 0;
+}
+
+struct DeviceInfo {
+    int sms = 0;
+    int smem_optin = 0;
+};
+
+int device_info(DeviceInfo *out)
+{
+    static DeviceInfo cache[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices)
+        return SSM_ERR_CUDA;
+    if (cache[dev].sms == 0) {
+        DeviceInfo d;
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return SSM_ERR_CUDA;
+        if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return SSM_ERR_CUDA;
+        cache[dev] = d;
+    }
+    *out = cache[dev];
+    return SSM_OK;
+}
+
+bool check_env()
+{
+    static int v = -1;
+    if (v < 0) {
+        const char *e = std::getenv("SSM_SCAN_CHECK");
+        v = (e && e[0] && std::strcmp(e, "0") != 0) ? 1 : 0;
+    }
+    return v == 1;
+}
+
+// Debug mode: copy the sequence table to the host and check the ranges.
+int check_metadata(const ssm::ScanArgs &a, cudaStream_t stream)
+{
+    const size_t n = (size_t)a.n_seqs;
+    std::vector<int32_t> st(n), ln(n);
+    if (cudaMemcpyAsync(st.data(), a.seq_starts, n * sizeof(int32_t), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+        cudaMemcpyAsync(ln.data(), a.seq_lens, n * sizeof(int32_t), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    std::vector<std::pair<int32_t, int32_t>> ranges;
+    for (size_t i = 0; i < n; ++i) {
+        if (st[i] < 0 || ln[i] < 0 || (long long)st[i] + ln[i] > a.n_tokens)
+            return SSM_ERR_INVALID_ARG;
+        if (ln[i] > 0)
+            ranges.emplace_back(st[i], st[i] + ln[i]);
+    }
+    std::sort(ranges.begin(), ranges.end());
+    for (size_t i = 1; i < ranges.size(); ++i)
+        if (ranges[i].first < ranges[i - 1].second)
+            return SSM_ERR_INVALID_ARG;
+    return SSM_OK;
+}
+
+int scan_impl(float *state, const float *x, const float *dt, const float *A, const float *B,
+              const float *C, const float *D, float *y, const int32_t *seq_starts,
+              const int32_t *seq_lens, const int32_t *resume, int n_seqs, int n_tokens,
+              int H, int P, int N, int G, const ssm_scan_tuning *tun, void *stream_v)
+{
+    // ---- host-checkable arguments ----
+    if (n_seqs < 0 || n_tokens < 0 || H <= 0 || P <= 0 || N <= 0 || G <= 0)
+        return SSM_ERR_INVALID_ARG;
+    if (H % G != 0)
+        return SSM_ERR_INVALID_ARG;
+    if (N % 4 != 0 || N > kMaxDState)
+        return SSM_ERR_UNSUPPORTED;
+    if ((long long)H * P > INT_MAX / 2)
+        return SSM_ERR_UNSUPPORTED;
+    if (n_seqs == 0)
+        return SSM_OK;
+    if (!state || !A || !D || !seq_starts || !seq_lens || !resume)
+        return SSM_ERR_INVALID_ARG;
+    if (n_tokens > 0 && (!x || !dt || !B || !C || !y))
+        return SSM_ERR_INVALID_ARG;
+    if (!aligned(state, 16) || !aligned(B, 16) || !aligned(C, 16))
+        return SSM_ERR_INVALID_ARG;
+    if (!aligned(x, 4) || !aligned(dt, 4) || !aligned(A, 4) || !aligned(D, 4) || !aligned(y, 4) ||
+        !aligned(seq_starts, 4) || !aligned(seq_lens, 4) || !aligned(resume, 4))
+        return SSM_ERR_INVALID_ARG;
+
+    ssm_scan_tuning t;
+    std::memset(&t, 0, sizeof t);
+    if (tun)
+        t = *tun;
+    if (t.path < SSM_PATH_AUTO || t.path > SSM_PATH_PREFILL || t.lanes_per_row < 0 ||
+        t.rows_per_thread < 0 || t.rows_per_cta < 0 || t.chunk_tokens < 0 || t.chunk_tokens > 256 ||
+        t.ctas_per_sm < 0)
+        return SSM_ERR_INVALID_ARG;
+    if (t.lanes_per_row && (!is_pow2(t.lanes_per_row) || t.lanes_per_row > 32))
+        return SSM_ERR_INVALID_ARG;
+    if (t.rows_per_thread && !is_pow2(t.rows_per_thread))
+        return SSM_ERR_INVALID_ARG;
+
+    DeviceInfo dev;
+    int rc = device_info(&dev);
+    if (rc != SSM_OK)
+        return rc;
+
+    ssm::ScanArgs a;
+    a.state = state; a.x = x; a.dt = dt; a.A = A; a.B = B; a.C = C; a.D = D; a.y = y;
+    a.seq_starts = seq_starts; a.seq_lens = seq_lens; a.resume = resume;
+    a.n_seqs = n_seqs; a.n_tokens = n_tokens; a.H = H; a.P = P; a.N = N; a.G = G;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_v);
+
+    if (check_env()) {
+        rc = check_metadata(a, stream);
+        if (rc != SSM_OK)
+            return rc;
+    }
+
+    const int N4 = N / 4;
+    int path = t.path;
+    if (path == SSM_PATH_AUTO)
+        path = (n_tokens == n_seqs) ? SSM_PATH_DECODE : SSM_PATH_PREFILL;
+
+    if (path == SSM_PATH_DECODE) {
+        const int lanes = t.lanes_per_row ? t.lanes_per_row : std::min(32, pow2ceil(N4));
+        const int rpt = t.rows_per_thread ? t.rows_per_thread
+                                          : ((lanes == 32 && N4 <= 32) ? 2 : 1);
+        const int vpl = pick_vpl(N4, lanes, rpt, ssm::decode_supported);
+        if (rpt > lanes || vpl == 0)
+            return SSM_ERR_INVALID_ARG;
+        ssm::DecodeGeom g;
+        g.rows_per_warp = (32 / lanes) * rpt;
+        g.tasks_per_seq = (H * P + g.rows_per_warp - 1) / g.rows_per_warp;
+        g.n_tasks = (long long)n_seqs * g.tasks_per_seq;
+        long long grid = (g.n_tasks + ssm::kDecodeWarps - 1) / ssm::kDecodeWarps;
+        if (t.ctas_per_sm > 0)
+            grid = std::min<long long>(grid, (long long)t.ctas_per_sm * dev.sms);
+        grid = std::min<long long>(grid, INT_MAX);
+        if (ssm::launch_decode(a, g, lanes, vpl, rpt, (int)grid, stream) != cudaSuccess)
+            return SSM_ERR_CUDA;
+        return SSM_OK;
+    }
+
+    // ---- prefill ----
+    const int lanes = t.lanes_per_row ? t.lanes_per_row : std::min(32, pow2ceil((N + 31) / 32));
+    const int rpt = t.rows_per_thread ? t.rows_per_thread : 1;
+    const int vpl = pick_vpl(N4, lanes, rpt, ssm::prefill_supported);
+    if (rpt > lanes || vpl == 0)
+        return SSM_ERR_INVALID_ARG;
+    const int rows_per_warp = (32 / lanes) * rpt;
+    ssm::PrefillGeom g;
+    g.rows_per_group = (H / G) * P;
+    if (t.rows_per_cta) {
+        if (t.rows_per_cta % rows_per_warp != 0 || (t.rows_per_cta / rpt) * lanes > 256)
+            return SSM_ERR_INVALID_ARG;
+        g.rows_per_cta = t.rows_per_cta;
+    } else {
+        // Largest block (up to 4 warps) that still gives every SM a block.
+        int warps = 4;
+        while (warps > 1) {
+            const long long runs = (g.rows_per_group + warps * rows_per_warp - 1) / (warps * rows_per_warp);
+            if ((long long)n_seqs * G * runs >= dev.sms)
+                break;
+            warps >>= 1;
+        }
+        g.rows_per_cta = warps * rows_per_warp;
+    }
+    const int threads = (g.rows_per_cta / rpt) * lanes;
+    g.runs_per_group = (g.rows_per_group + g.rows_per_cta - 1) / g.rows_per_cta;
+    g.heads_cap = (P + g.rows_per_cta - 2) / P + 1;
+    const long long n_ctas = (long long)n_seqs * G * g.runs_per_group;
+    if (n_ctas > INT_MAX)
+        return SSM_ERR_UNSUPPORTED;
+    // dt of one chunk is carried in 4 registers per thread.
+    const int dt_cap = 4 * threads;
+    if (t.chunk_tokens) {
+        g.chunk = t.chunk_tokens;
+        if (g.chunk * g.heads_cap > dt_cap ||
+            ssm::prefill_smem_bytes(g, N) > (size_t)dev.smem_optin)
+            return SSM_ERR_INVALID_ARG;
+    } else {
+        g.chunk = 32;
+        while (g.chunk > 1 && (g.chunk * g.heads_cap > dt_cap ||
+                               ssm::prefill_smem_bytes(g, N) > (size_t)std::min(dev.smem_optin, 112 * 1024)))
+            g.chunk >>= 1;
+        if (ssm::prefill_smem_bytes(g, N) > (size_t)dev.smem_optin)
+            return SSM_ERR_UNSUPPORTED;
+    }
+    const size_t smem = ssm::prefill_smem_bytes(g, N);
+    if (ssm::launch_prefill(a, g, lanes, vpl, rpt, smem, dev.sms, stream) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    return SSM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ssm_scan(float *state_slots, const float *x, const float *dt, const float *A, const float *B,
+             const float *C, const float *D, float *y, const int32_t *seq_starts,
+             const int32_t *seq_lens, const int32_t *resume_flags, int n_seqs, int n_tokens,
+             int n_heads, int head_dim, int d_state, int n_groups, void *stream)
+{
+    return scan_impl(state_slots, x, dt, A, B, C, D, y, seq_starts, seq_lens, resume_flags, n_seqs,
+                     n_tokens, n_heads, head_dim, d_state, n_groups, nullptr, stream);
+}
+
+int ssm_scan_tuned(float *state_slots, const float *x, const float *dt, const float *A,
+                   const float *B, const float *C, const float *D, float *y,
+                   const int32_t *seq_starts, const int32_t *seq_lens, const int32_t *resume_flags,
+                   int n_seqs, int n_tokens, int n_heads, int head_dim, int d_state, int n_groups,
+                   const ssm_scan_tuning *tuning, void *stream)
+{
+    return scan_impl(state_slots, x, dt, A, B, C, D, y, seq_starts, seq_lens, resume_flags, n_seqs,
+                     n_tokens, n_heads, head_dim, d_state, n_groups, tuning, stream);
+}
+
+const char *ssm_status_string(int status)
+{
+    switch (status) {
+    case SSM_OK: return "ok";
+    case SSM_ERR_INVALID_ARG: return "invalid argument";
+    case SSM_ERR_UNSUPPORTED: return "unsupported geometry";
+    case SSM_ERR_CUDA: return "CUDA error";
+    case SSM_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,142 @@
+// Shared definitions of the sm_103a scan kernels (device side and launchers).
+//
+// Operation (for sequence i, head h, head-dim row p, token t; g = h/(H/G)):
+//   dA = exp(dt[t,h]*A[h]);  S[h,p,:] = dA*S[h,p,:] + dt[t,h]*x[t,h,p]*B[t,g,:];
+//   y[t,h,p] = S[h,p,:].C[t,g,:] + D[h]*x[t,h,p]
+// ("The llama journey", Day 14 kernel body; the D skip term is part of the
+// operation here.)
+//
+// A "row" is one (head, head-dim) pair: its flattened index r = h*P + p is
+// also its offset inside a token of x/y and inside a state slot (times N).
+// Rows of one group are contiguous in that flattened order, so a run of rows
+// inside one group shares B and C.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ssm {
+
+struct ScanArgs {
+    float *state;              // [n][H][P][N]
+    const float *x;            // [T][H][P]
+    const float *dt;           // [T][H]
+    const float *A;            // [H]
+    const float *B;            // [T][G][N]
+    const float *C;            // [T][G][N]
+    const float *D;            // [H]
+    float *y;                  // [T][H][P]
+    const int32_t *seq_starts; // [n]
+    const int32_t *seq_lens;   // [n]
+    const int32_t *resume;     // [n]
+    int n_seqs, n_tokens, H, P, N, G;
+};
+
+// Launch geometry of the chunk-staged prefill kernel.
+struct PrefillGeom {
+    int rows_per_group;  // (H/G)*P
+    int runs_per_group;  // thread blocks per (sequence, group)
+    int rows_per_cta;    // state rows a block owns
+    int chunk;           // tokens staged per chunk
+    int heads_cap;       // most heads one block's rows can touch
+};
+
+// Launch geometry of the warp-per-row decode kernel.
+struct DecodeGeom {
+    int rows_per_warp;   // (32/LANES)*RPT
+    int tasks_per_seq;   // ceil(H*P / rows_per_warp)
+    long long n_tasks;   // n_seqs * tasks_per_seq
+};
+
+constexpr unsigned kFullMask = 0xffffffffu;
+
+template <int X>
+struct Log2 { static constexpr int value = 1 + Log2<X / 2>::value; };
+template <>
+struct Log2<1> { static constexpr int value = 0; };
+
+// Sum RPT per-row partial sums over the LANES lanes that share those rows.
+// The first log2(RPT) butterfly levels also transpose: at each level a lane
+// keeps half of its values and receives its partner's matching half, so the
+// shuffle count is (RPT-1) + log2(LANES/RPT) instead of RPT*log2(LANES).
+// On return every lane holds the full sum of row `reduced_row<LANES,RPT>(j)`.
+template <int LANES, int RPT>
+__device__ __forceinline__ float reduce_rows(float (&v)[RPT], int j)
+{
+    static_assert(RPT <= LANES, "more rows than lanes");
+    constexpr int LV = Log2<RPT>::value;
+#pragma unroll
+    for (int level = 0, cnt = RPT, off = LANES / 2; level < LV; ++level, cnt /= 2, off /= 2) {
+        const bool hi = (j & off) != 0;
+#pragma unroll
+        for (int m = 0; m < cnt / 2; ++m) {
+            const float send = hi ? v[2 * m] : v[2 * m + 1];
+            const float keep = hi ? v[2 * m + 1] : v[2 * m];
+            v[m] = keep + __shfl_xor_sync(kFullMask, send, off);
+        }
+    }
+    float s = v[0];
+#pragma unroll
+    for (int off = LANES / (2 * RPT); off >= 1; off /= 2)
+        s += __shfl_xor_sync(kFullMask, s, off);
+    return s;
+}
+
+// Which of the RPT rows lane j's reduced sum belongs to.
+template <int LANES, int RPT>
+__device__ __forceinline__ int reduced_row(int j)
+{
+    constexpr int LV = Log2<RPT>::value;
+    constexpr int LL = Log2<LANES>::value;
+    int r = 0;
+#pragma unroll
+    for (int k = 0; k < LV; ++k)
+        r |= ((j >> (LL - 1 - k)) & 1) << k;
+    return r;
+}
+
+// True for one lane per reduced row (the lane whose low bits are zero).
+template <int LANES, int RPT>
+__device__ __forceinline__ bool reduced_writer(int j)
+{
+    return (j & (LANES / RPT - 1)) == 0;
+}
+
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem)
+{
+    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+
+__device__ __forceinline__ void cp_async4(void *smem, const void *gmem)
+{
+    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit()
+{
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// Host-side launchers (defined in prefill.cu / decode.cu).  Return a
+// cudaError_t from the launch, or cudaErrorInvalidValue for a shape with no
+// compiled kernel.
+cudaError_t launch_prefill(const ScanArgs &a, const PrefillGeom &g, int lanes,
+                           int vpl, int rpt, size_t smem_bytes, int sms,
+                           cudaStream_t stream);
+bool prefill_supported(int lanes, int vpl, int rpt);
+size_t prefill_smem_bytes(const PrefillGeom &g, int N);
+
+cudaError_t launch_decode(const ScanArgs &a, const DecodeGeom &g, int lanes,
+                          int vpl, int rpt, int grid, cudaStream_t stream);
+bool decode_supported(int lanes, int vpl, int rpt);
+constexpr int kDecodeWarps = 8;
+
+}  // namespace ssm

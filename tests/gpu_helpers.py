@@ -1,0 +1,69 @@
+"""Helpers for the GPU parity tests: run the CUDA scan with guard bands and
+compare with the CPU oracle under the stated tolerance."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from state_space_model_ssm_gb300 import binding as bd
+
+# Sequential fp32 kernels: max |gpu - ref| <= TOL * (1 + |ref|), elementwise.
+TOL = 1e-4
+GUARD = 64   # floats of NaN canary on each side of y and of the state slots
+
+
+def _guarded(shape, fill, device):
+    numel = int(np.prod(shape)) if len(shape) else 1
+    buf = torch.full((numel + 2 * GUARD,), fill, dtype=torch.float32, device=device)
+    return buf, buf[GUARD:GUARD + numel].view(*shape)
+
+
+def run_gpu(inp, tuning=None, device="cuda", stream=None, y_fill=float("nan")):
+    """Run libssmscan on a ScanInputs bundle; returns (y, state) as float64
+    numpy arrays.  Checks that the NaN guard bands around y and the state are
+    intact afterwards."""
+    d = inp.to(device)
+    sbuf, state = _guarded(tuple(inp.state.shape), float("nan"), device)
+    state.copy_(d.state)
+    ybuf, y = _guarded(tuple(inp.x.shape), y_fill, device)
+    bd.ssm_scan(state, d.x, d.dt, d.A, d.B, d.C, d.D, d.seq_starts, d.seq_lens, d.resume,
+                y=y, tuning=tuning, stream=stream)
+    torch.cuda.synchronize()
+    for buf in (sbuf, ybuf):
+        head, tail = buf[:GUARD], buf[-GUARD:]
+        assert torch.isnan(head).all() and torch.isnan(tail).all(), "guard band overwritten"
+    return y.double().cpu().numpy(), state.double().cpu().numpy()
+
+
+def covered_tokens(inp):
+    mask = np.zeros(inp.n_tokens, dtype=bool)
+    for s, L in zip(inp.seq_starts.tolist(), inp.seq_lens.tolist()):
+        mask[s:s + L] = True
+    return mask
+
+
+def assert_parity(inp, y_gpu, s_gpu, y_ref, s_ref, heads=None, tol=TOL):
+    """y minus its exact skip term D*x, and the final state, within
+    tol * (1 + |ref|); tokens outside every sequence untouched (NaN)."""
+    H = inp.geom.n_heads
+    hsel = np.arange(H) if heads is None else np.asarray(sorted(heads))
+    mask = covered_tokens(inp)
+    x = inp.x.double().numpy()
+    D = inp.D.double().numpy()
+    dx = D[None, :, None] * x
+    yg = (y_gpu - dx)[mask][:, hsel]
+    yr = (y_ref - dx)[mask][:, hsel]
+    assert np.isfinite(yg).all(), "non-finite y from the GPU"
+    err = np.abs(yg - yr)
+    bound = tol * (1.0 + np.abs(yr))
+    worst = np.unravel_index(np.argmax(err / bound), err.shape) if err.size else None
+    assert np.all(err <= bound), (
+        f"y parity: max err {err.max():.3e}, worst at {worst}, ref {yr[worst]:.6e}, gpu {yg[worst]:.6e}")
+    if (~mask).any():
+        assert np.all(np.isnan(y_gpu[~mask])), "y written for a token owned by no sequence"
+    sg, sr = s_gpu[:, hsel], s_ref[:, hsel]
+    assert np.isfinite(sg).all(), "non-finite state from the GPU"
+    serr = np.abs(sg - sr)
+    sbound = tol * (1.0 + np.abs(sr))
+    assert np.all(serr <= sbound), f"state parity: max err {serr.max():.3e}"
+    return float(err.max() if err.size else 0.0), float(serr.max() if serr.size else 0.0)

@@ -1,0 +1,99 @@
+"""The C ABI without a GPU: the library loads, exports every function the
+public header declares, and rejects bad arguments on the host before any
+launch (these calls never reach the device, so fake but aligned pointers are
+safe: every case below fails a host check)."""
+import ctypes
+
+import pytest
+
+from state_space_model_ssm_gb300 import binding as bd
+
+GOOD = dict(n_seqs=2, n_tokens=8, n_heads=4, head_dim=16, d_state=32, n_groups=2)
+PTR = 0x10000   # 16-byte aligned, never dereferenced (each call below fails a host check)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from state_space_model_ssm_gb300 import build
+    build.build()
+    return bd.load()
+
+
+def _call(lib, tuning=None, **over):
+    ptrs = dict(state=PTR, x=PTR, dt=PTR, A=PTR, B=PTR, C=PTR, D=PTR, y=PTR,
+                seq_starts=PTR, seq_lens=PTR, resume=PTR)
+    sizes = dict(GOOD)
+    for k, v in over.items():
+        (ptrs if k in ptrs else sizes)[k] = v
+    return bd.scan_raw(**ptrs, **sizes, tuning=tuning)
+
+
+def test_header_declares_the_scan_entry_points():
+    names = bd.declared_functions()
+    assert {"ssm_scan", "ssm_scan_tuned", "ssm_status_string"} <= set(names)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in bd.declared_functions():
+        assert hasattr(lib, name), f"libssmscan does not export {name}"
+
+
+def test_status_strings(lib):
+    for code, text in [(0, "ok"), (-1, "invalid argument"), (-2, "unsupported geometry"),
+                       (-3, "CUDA error"), (-4, "device wait timed out"), (7, "unknown status")]:
+        assert bd.status_string(code) == text
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(n_seqs=-1), bd.SSM_ERR_INVALID_ARG),
+    (dict(n_tokens=-3), bd.SSM_ERR_INVALID_ARG),
+    (dict(n_heads=0), bd.SSM_ERR_INVALID_ARG),
+    (dict(head_dim=0), bd.SSM_ERR_INVALID_ARG),
+    (dict(n_groups=3), bd.SSM_ERR_INVALID_ARG),           # 4 heads % 3 groups
+    (dict(d_state=30), bd.SSM_ERR_UNSUPPORTED),           # not a multiple of 4
+    (dict(d_state=2048), bd.SSM_ERR_UNSUPPORTED),         # above the supported maximum
+    (dict(state=0), bd.SSM_ERR_INVALID_ARG),
+    (dict(x=0), bd.SSM_ERR_INVALID_ARG),
+    (dict(y=0), bd.SSM_ERR_INVALID_ARG),
+    (dict(seq_lens=0), bd.SSM_ERR_INVALID_ARG),
+    (dict(resume=0), bd.SSM_ERR_INVALID_ARG),
+    (dict(state=PTR + 4), bd.SSM_ERR_INVALID_ARG),        # state must be 16-byte aligned
+    (dict(B=PTR + 8), bd.SSM_ERR_INVALID_ARG),
+    (dict(C=PTR + 12), bd.SSM_ERR_INVALID_ARG),
+    (dict(x=PTR + 2), bd.SSM_ERR_INVALID_ARG),            # 4-byte alignment for the rest
+    (dict(seq_starts=PTR + 1), bd.SSM_ERR_INVALID_ARG),
+])
+def test_host_rejects_bad_arguments(lib, over, expect):
+    assert _call(lib, **over) == expect
+
+
+def test_empty_batch_is_a_noop(lib):
+    # n_seqs == 0 returns before touching any pointer or the device
+    assert _call(lib, n_seqs=0, state=0, x=0, y=0) == bd.SSM_OK
+
+
+@pytest.mark.parametrize("field,value", [
+    ("path", 3), ("path", -1), ("lanes_per_row", 3), ("lanes_per_row", 64),
+    ("rows_per_thread", 3), ("chunk_tokens", 257), ("chunk_tokens", -1), ("ctas_per_sm", -2),
+])
+def test_host_rejects_bad_tuning(lib, field, value):
+    t = bd.Tuning()
+    setattr(t, field, value)
+    # a misaligned-free, otherwise valid call: the tuning check alone must fail
+    assert _call(lib, tuning=t) == bd.SSM_ERR_INVALID_ARG
+
+
+def test_tuning_struct_layout_matches_header():
+    import re
+    text = open(bd.HEADER).read()
+    body = re.search(r"typedef struct \{(.*?)\} ssm_scan_tuning;", text, re.S).group(1)
+    fields = re.findall(r"int\s+(\w+);", body)
+    assert fields == [f[0] for f in bd.Tuning._fields_]
+    assert ctypes.sizeof(bd.Tuning) == 4 * len(fields)
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    z = torch.zeros(1, 1, 1, 4)
+    with pytest.raises(ValueError):
+        bd.ssm_scan(z, z, z, z, z, z, z, z, z, z)

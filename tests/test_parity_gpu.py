@@ -1,0 +1,189 @@
+"""Parity of the CUDA scan with the CPU oracle (needs a GB300).
+
+Every case draws seeded inputs, runs libssmscan through the C ABI and the
+oracle on the same inputs, and compares y (minus its exact D*x skip term) and
+the final state elementwise within 1e-4 * (1 + |ref|)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from state_space_model_ssm_gb300 import binding as bd
+from state_space_model_ssm_gb300.workloads import Geometry, make_inputs, workload
+from tests.gpu_helpers import assert_parity, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from state_space_model_ssm_gb300 import build
+    build.build()
+    bd.load()
+
+
+def _tuning(path=0, lanes=0, rpt=0, rows=0, chunk=0, ctas=0):
+    return bd.Tuning(path, lanes, rpt, rows, chunk, ctas)
+
+
+PATHS = [("auto", None), ("decode", _tuning(path=bd.PATH_DECODE)),
+         ("prefill", _tuning(path=bd.PATH_PREFILL))]
+
+
+@pytest.mark.parametrize("name", ["tiny", "edge_p96_n100"])
+@pytest.mark.parametrize("path", PATHS, ids=[p[0] for p in PATHS])
+def test_parity_small_workloads(name, path):
+    inp = workload(name)
+    y_ref, s_ref = oracle.scan_inputs(inp)
+    y, s = run_gpu(inp, tuning=path[1])
+    assert_parity(inp, y, s, y_ref, s_ref)
+
+
+def test_parity_skip_term_zero():
+    """D = 0: y is the state readout alone."""
+    inp = workload("tiny")
+    inp.D.zero_()
+    y_ref, s_ref = oracle.scan_inputs(inp)
+    y, s = run_gpu(inp)
+    assert_parity(inp, y, s, y_ref, s_ref)
+
+
+def test_parity_decode_16x1_multi_step():
+    """Three consecutive decode steps on the same 16 slots (Nemotron-H geometry)."""
+    inp = workload("decode_16x1")
+    dev = inp.to("cuda")
+    state = dev.state.clone()
+    s_ref = inp.state.double().numpy()
+    for step in range(3):
+        step_inp = workload("decode_16x1", seed=100 + step)
+        d = step_inp.to("cuda")
+        y = bd.ssm_scan(state, d.x, d.dt, d.A, d.B, d.C, d.D, d.seq_starts, d.seq_lens, d.resume)
+        y_ref, s_ref = oracle.scan(step_inp.x, step_inp.dt, step_inp.A, step_inp.B, step_inp.C,
+                                   step_inp.D, s_ref, step_inp.seq_starts, step_inp.seq_lens,
+                                   step_inp.resume)
+        torch.cuda.synchronize()
+        assert_parity(step_inp, y.double().cpu().numpy(), state.double().cpu().numpy(), y_ref, s_ref)
+
+
+def test_parity_prefill_1x4096():
+    inp = workload("prefill_1x4096")
+    y_ref, s_ref = oracle.scan_inputs(inp)
+    y, s = run_gpu(inp)
+    assert_parity(inp, y, s, y_ref, s_ref)
+
+
+def test_parity_ragged_12():
+    inp = workload("ragged_12")
+    y_ref, s_ref = oracle.scan_inputs(inp)
+    y, s = run_gpu(inp)
+    assert_parity(inp, y, s, y_ref, s_ref)
+
+
+def test_parity_edge_n1024():
+    inp = workload("edge_n1024")
+    y_ref, s_ref = oracle.scan_inputs(inp)
+    y, s = run_gpu(inp)
+    assert_parity(inp, y, s, y_ref, s_ref)
+
+
+def test_parity_long_4x16384_sampled_heads():
+    """Full size (T = 65536): the oracle computes three heads (in three groups)
+    of every sequence; those outputs are compared element by element."""
+    inp = workload("long_4x16384")
+    heads = [0, 37, 63]
+    y_ref, s_ref = oracle.scan_inputs(inp, heads=heads)
+    y, s = run_gpu(inp)
+    assert_parity(inp, y, s, y_ref, s_ref, heads=heads)
+
+
+# Launch shapes: every accepted (lanes, rows per thread, rows per block, chunk)
+# must give the same result.
+PREFILL_SHAPES = [
+    (4, 1, 8, 32), (4, 1, 32, 32), (4, 1, 64, 7), (8, 1, 32, 16), (16, 1, 16, 5),
+    (32, 1, 8, 1), (8, 2, 16, 32), (16, 4, 32, 32), (4, 2, 64, 32), (8, 2, 64, 13),
+]
+
+
+@pytest.mark.parametrize("lanes,rpt,rows,chunk", PREFILL_SHAPES)
+def test_parity_prefill_launch_shapes(lanes, rpt, rows, chunk):
+    inp = workload("tiny")
+    y_ref, s_ref = oracle.scan_inputs(inp)
+    t = _tuning(path=bd.PATH_PREFILL, lanes=lanes, rpt=rpt, rows=rows, chunk=chunk)
+    y, s = run_gpu(inp, tuning=t)
+    assert_parity(inp, y, s, y_ref, s_ref)
+
+
+DECODE_SHAPES = [(32, 1, 0), (32, 2, 0), (32, 4, 0), (16, 2, 0), (16, 1, 0), (8, 1, 0), (32, 2, 1)]
+
+
+@pytest.mark.parametrize("lanes,rpt,ctas", DECODE_SHAPES)
+def test_parity_decode_launch_shapes(lanes, rpt, ctas):
+    inp = make_inputs(Geometry(8, 24, 128, 2), [1, 3, 1, 0, 2], [1, 0, 1, 1, 0], seed=21)
+    y_ref, s_ref = oracle.scan_inputs(inp)
+    t = _tuning(path=bd.PATH_DECODE, lanes=lanes, rpt=rpt, ctas=ctas)
+    y, s = run_gpu(inp, tuning=t)
+    assert_parity(inp, y, s, y_ref, s_ref)
+
+
+@pytest.mark.parametrize("geom", [Geometry(3, 5, 4, 1), Geometry(6, 7, 12, 3), Geometry(2, 33, 36, 2),
+                                  Geometry(4, 10, 64, 4), Geometry(2, 8, 256, 1)],
+                         ids=lambda g: f"H{g.n_heads}P{g.head_dim}N{g.d_state}G{g.n_groups}")
+@pytest.mark.parametrize("path", PATHS[1:], ids=[p[0] for p in PATHS[1:]])
+def test_parity_odd_geometries(geom, path):
+    inp = make_inputs(geom, [19, 1, 0, 40], [0, 1, 1, 1], seed=8)
+    y_ref, s_ref = oracle.scan_inputs(inp)
+    y, s = run_gpu(inp, tuning=path[1])
+    assert_parity(inp, y, s, y_ref, s_ref)
+
+
+def test_zero_length_and_unowned_tokens():
+    """Zero-length sequences (fresh -> zero slot, resumed -> unchanged) and
+    token rows owned by no sequence (never written)."""
+    inp = make_inputs(Geometry(4, 16, 32, 2), [0, 0, 9, 4], [0, 1, 0, 1], seed=12,
+                      starts=[0, 0, 3, 14], n_tokens=20)
+    y_ref, s_ref = oracle.scan_inputs(inp)
+    for path in PATHS:
+        y, s = run_gpu(inp, tuning=path[1])
+        assert_parity(inp, y, s, y_ref, s_ref)
+        assert np.array_equal(s[0], np.zeros_like(s[0]))
+        assert np.array_equal(s[1], inp.state[1].double().numpy())
+
+
+def test_split_resume_equals_one_call():
+    """A sequence run as two calls (the second resuming) matches one call."""
+    geom = Geometry(8, 32, 64, 2)
+    inp = make_inputs(geom, [300], [1], seed=13)
+    y_one, s_one = run_gpu(inp)
+    k = 123
+    a = make_inputs(geom, [k], [1], seed=13)
+    a.x, a.dt, a.B, a.C = inp.x[:k], inp.dt[:k], inp.B[:k], inp.C[:k]
+    a.A, a.D, a.state = inp.A, inp.D, inp.state
+    y1, s1 = run_gpu(a)
+    b = make_inputs(geom, [300 - k], [1], seed=13)
+    b.x, b.dt, b.B, b.C = inp.x[k:], inp.dt[k:], inp.B[k:], inp.C[k:]
+    b.A, b.D = inp.A, inp.D
+    b.state = torch.from_numpy(s1).float()
+    y2, s2 = run_gpu(b)
+    y_ref, s_ref = oracle.scan_inputs(inp)
+    assert_parity(inp, np.concatenate([y1, y2]), s2, y_ref, s_ref)
+    assert_parity(inp, y_one, s_one, y_ref, s_ref)
+
+
+def test_runs_on_a_side_stream():
+    inp = workload("tiny")
+    y_ref, s_ref = oracle.scan_inputs(inp)
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        y, s = run_gpu(inp, stream=st)
+    assert_parity(inp, y, s, y_ref, s_ref)
+
+
+def test_bad_arguments_raise_before_launch():
+    inp = workload("tiny").to("cuda")
+    with pytest.raises(bd.SsmScanError) as e:
+        bd.ssm_scan(inp.state, inp.x, inp.dt, inp.A, inp.B, inp.C, inp.D, inp.seq_starts,
+                    inp.seq_lens, inp.resume, tuning=_tuning(path=bd.PATH_PREFILL, lanes=4, rows=12))
+    assert e.value.status == bd.SSM_ERR_INVALID_ARG
+    with pytest.raises(TypeError):
+        bd.ssm_scan(inp.state.double(), inp.x, inp.dt, inp.A, inp.B, inp.C, inp.D,
+                    inp.seq_starts, inp.seq_lens, inp.resume)
