@@ -1,0 +1,497 @@
+#!/usr/bin/env python3
+"""Benchmark of the Mamba2 selective-state scan on GB300 (libssmscan).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step is one scan call over the 1 x 4096-token prefill workload at
+Nemotron-H geometry (64 heads x 64 x 128 state, 8 groups, fp32): state
+load, chunk staging, discretisation, state update, y readout and state store,
+all in the prefill kernel.  The same run also times the 16 x 1 decode step
+(300 steps over rotating slot sets) and reports it under "decode".
+
+Prints one JSON line (rank 0).  Under torchrun every rank scans its own
+batch (weak scaling, no collective on the data path); the step time is the
+maximum over ranks.  `--impl reference` times the CPU oracle instead, on the
+host cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from state_space_model_ssm_gb300.workloads import WORKLOADS, workload  # noqa: E402
+
+METRIC = "scan tokens/s (1×4096 prefill), decode µs (16×1); % of HBM/FP32 roofline"
+# gllm PR 90, "Results": 1 x 4096 prefill in 3.5 ms and 16 x 1 decode in 32 us on an
+# RTX PRO 6000 (sm_120, 300 W cap); another machine's figures, quoted as context.
+PAGE_PREFILL_MS = 3.5
+PAGE_DECODE_US = 32.0
+FP32_LANES_PER_SM = 128
+L2_FLUSH_BYTES = 256 << 20
+DECODE_STEPS = 300
+DECODE_SLOT_SETS = 8          # 8 x 32 MiB of slots rotate, 2x the 129 MB L2
+KERNEL_SOURCES = {
+    "prefill_kernel": ["state_space_model_ssm_gb300/csrc/prefill.cu",
+                       "state_space_model_ssm_gb300/csrc/scan_common.cuh"],
+    "decode_kernel": ["state_space_model_ssm_gb300/csrc/decode.cu",
+                      "state_space_model_ssm_gb300/csrc/scan_common.cuh"],
+}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- helpers
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "sm_max_mhz": 2070.0}, "fallback"
+
+
+def source_hash(kernel: str) -> str:
+    h = hashlib.sha1()
+    for rel in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+def ncu_traffic(kernel: str, workload_name: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel source changed since that capture."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    want = source_hash(kernel)
+    for line in open(path):
+        f = line.split()
+        if len(f) >= 4 and f[0] == workload_name and f[1] == kernel:
+            kv = dict(x.split("=", 1) for x in f[2:] if "=" in x)
+            if kv.get("src") == want:
+                return int(kv["bytes_per_launch"])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sms, maxs, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [v.strip() for v in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sms.append(float(f[0]))
+                maxs.append(float(f[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sms:
+            return None
+        loaded = [s for s in sms if s > 0.5 * max(sms)] or sms
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(maxs),
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+def event_pair():
+    return torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_prefill(args, world, rank, dev):
+    from state_space_model_ssm_gb300 import binding as bd
+
+    inp = workload("prefill_1x4096", seed=WORKLOADS["prefill_1x4096"]["seed"] + 1000 * rank)
+    d = inp.to(dev)
+    state = d.state.clone()
+    y = torch.empty_like(d.x)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        bd.ssm_scan(state, d.x, d.dt, d.A, d.B, d.C, d.D, d.seq_starts, d.seq_lens, d.resume, y=y)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    evs = [event_pair() for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    for e0, e1 in evs:
+        flush.zero_()                 # L2 flushed between timed steps
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    times_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
+    step_ms = sum(times_ms) / len(times_ms)
+    return inp, d, step_ms, times_ms
+
+
+def run_prefill_e2e(args, dev, inp):
+    """Same metric through the public call with host buffers: every step copies
+    the inputs from pinned host memory and reads y and the state back."""
+    from state_space_model_ssm_gb300 import binding as bd
+
+    host_in = {k: v.pin_memory() for k, v in inp.tensors().items()}
+    dbuf = {k: torch.empty_like(v, device=dev) for k, v in inp.tensors().items()}
+    y = torch.empty_like(dbuf["x"])
+    y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    s_host = torch.empty(inp.state.shape, dtype=torch.float32).pin_memory()
+    in_keys = ["x", "dt", "A", "B", "C", "D", "seq_starts", "seq_lens", "resume"]
+    if int(inp.resume.sum()) > 0:
+        in_keys.append("state")
+    h2d = sum(host_in[k].numel() * host_in[k].element_size() for k in in_keys)
+    d2h = y.numel() * 4 + inp.state.numel() * 4
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        for k in in_keys:
+            dbuf[k].copy_(host_in[k], non_blocking=True)
+        bd.ssm_scan(dbuf["state"], dbuf["x"], dbuf["dt"], dbuf["A"], dbuf["B"], dbuf["C"],
+                    dbuf["D"], dbuf["seq_starts"], dbuf["seq_lens"], dbuf["resume"], y=y)
+        y_host.copy_(y, non_blocking=True)
+        s_host.copy_(dbuf["state"], non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    n = max(3, min(args.steps, 20))
+    e0, e1 = event_pair()
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / n
+    return ms, h2d, d2h
+
+
+def run_decode(dev, rank):
+    """16 x 1 decode at Nemotron-H geometry: 300 steps, each on one of 8
+    rotating 16-slot sets (cold: 256 MiB of slots, twice the L2), plus the same
+    300 steps on one slot set replayed as a CUDA graph (warm)."""
+    from state_space_model_ssm_gb300 import binding as bd
+
+    base = workload("decode_16x1", seed=WORKLOADS["decode_16x1"]["seed"] + 1000 * rank)
+    d = base.to(dev)
+    sets = [d.state.clone() for _ in range(DECODE_SLOT_SETS)]
+    y = torch.empty_like(d.x)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(state):
+        bd.ssm_scan(state, d.x, d.dt, d.A, d.B, d.C, d.D, d.seq_starts, d.seq_lens, d.resume, y=y)
+
+    for i in range(10):
+        step(sets[i % DECODE_SLOT_SETS])
+    torch.cuda.synchronize(dev)
+    evs = [event_pair() for _ in range(DECODE_STEPS)]
+    for i, (e0, e1) in enumerate(evs):
+        e0.record(stream)
+        step(sets[i % DECODE_SLOT_SETS])
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    cold = [e0.elapsed_time(e1) * 1e3 for e0, e1 in evs]
+
+    # Back-to-back stream of 300 steps over the rotating sets (launch gaps included).
+    e0, e1 = event_pair()
+    e0.record(stream)
+    for i in range(DECODE_STEPS):
+        step(sets[i % DECODE_SLOT_SETS])
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    stream_us = e0.elapsed_time(e1) * 1e3 / DECODE_STEPS
+
+    # Warm: the same slots every step, replayed from a CUDA graph.
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        step(sets[0])
+    stream.wait_stream(side)
+    torch.cuda.synchronize(dev)
+    with torch.cuda.graph(g):
+        for _ in range(DECODE_STEPS):
+            step(sets[0])
+    g.replay()
+    torch.cuda.synchronize(dev)
+    e0, e1 = event_pair()
+    e0.record(stream)
+    g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    warm_graph_us = e0.elapsed_time(e1) * 1e3 / DECODE_STEPS
+    return dict(cold_us=statistics.median(cold), cold_mean_us=sum(cold) / len(cold),
+                stream_us=stream_us, warm_graph_us=warm_graph_us)
+
+
+def prefill_algorithmic(inp):
+    T = int(inp.seq_lens.sum())
+    H, P, N, G = inp.geom.n_heads, inp.geom.head_dim, inp.geom.d_state, inp.geom.n_groups
+    updates = T * H * P * N
+    fp32_ops = 3 * updates                      # FMUL dt*x*B, FFMA decay, FFMA C-dot
+    n = inp.n_seqs
+    state_in = 4 * n * H * P * N * int(inp.resume.sum() > 0)
+    bytes_ = 4 * (2 * T * H * P + 2 * T * G * N + T * H + 2 * H) + state_in + 4 * n * H * P * N
+    return updates, fp32_ops, bytes_
+
+
+def decode_algorithmic(inp):
+    H, P, N, G = inp.geom.n_heads, inp.geom.head_dim, inp.geom.d_state, inp.geom.n_groups
+    n = inp.n_seqs
+    T = int(inp.seq_lens.sum())
+    state_bytes = 2 * 4 * n * H * P * N
+    other = 4 * (2 * T * H * P + 2 * T * G * N + T * H + 2 * H) + 3 * 4 * n
+    return state_bytes, state_bytes + other
+
+
+def cpu_baseline_prefill(inp, budget_s=20.0):
+    """The oracle, as it stands, on the host cores: the full 1 x 4096 workload
+    once with every core, then on one core for a head sample."""
+    import oracle
+    cores = os.cpu_count() or 1
+    t = time.perf_counter()
+    oracle.scan_inputs(inp, n_threads=cores)
+    wall = time.perf_counter() - t
+    T = int(inp.seq_lens.sum())
+    heads = list(range(0, inp.geom.n_heads, 8))
+    t = time.perf_counter()
+    oracle.scan_inputs(inp, n_threads=1, heads=heads)
+    wall1 = (time.perf_counter() - t) * inp.geom.n_heads / len(heads)
+    return {"value": T / wall, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"full 1x{T} prefill workload, one run on {cores} threads (fp64 C oracle)",
+            "single_core_value": T / wall1,
+            "single_core_sample": f"{len(heads)} of {inp.geom.n_heads} heads on 1 thread, scaled"}
+
+
+def ours(args):
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU for --impl ours")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    from state_space_model_ssm_gb300 import build as _build
+    if rank == 0:
+        _build.build()
+    barrier(world)
+    from state_space_model_ssm_gb300 import binding as bd
+    bd.load()
+
+    peaks, peaks_src = measured_peaks()
+    props = torch.cuda.get_device_properties(dev)
+    sms = props.multi_processor_count
+    sampler = ClockSampler(local)
+    sampler.start()
+    inp, d, step_ms, times = run_prefill(args, world, rank, dev)
+    clocks = sampler.stop()
+    step_ms_max = max_over_ranks(step_ms, world, dev)
+
+    T = int(inp.seq_lens.sum())
+    updates, fp32_ops, alg_bytes = prefill_algorithmic(inp)
+    value = world * T / (step_ms_max * 1e-3)
+    sm_max = (clocks or {}).get("sm_max_mhz") or peaks.get("sm_max_mhz", 2070.0)
+    peak_ops = sms * FP32_LANES_PER_SM * sm_max * 1e6
+    achieved = fp32_ops / (step_ms * 1e-3)
+    traffic = ncu_traffic("prefill_kernel", "prefill_1x4096")
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": step_ms_max,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": value / (world * 4096 / (PAGE_PREFILL_MS * 1e-3)),
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": "prefill_1x4096", "what": WORKLOADS["prefill_1x4096"]["what"],
+                   "n_seqs": 1, "tokens_per_rank": T, "geometry": "H=64 P=64 N=128 G=8",
+                   "l2": "flushed between timed steps (256 MiB write)",
+                   "parallelism": f"dp{world} (independent sequences per GPU)",
+                   "vs_baseline_ref": "gllm PR 90: 3.5 ms on RTX PRO 6000 (context, another machine)"},
+        "roofline": {"bound": "alu", "achieved": achieved / 1e12, "peak": peak_ops / 1e12,
+                     "unit": "T fp32-ops/s", "frac": achieved / peak_ops,
+                     "traffic": traffic,
+                     "peak_basis": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x {sm_max:.0f} MHz (max clock)",
+                     "algorithmic": f"{fp32_ops} FP32 ops per launch (3 per element-update)",
+                     "hbm_frac": (alg_bytes / (step_ms * 1e-3)) / (peaks["hbm_gbs"] * 1e9),
+                     "hbm_peak_src": peaks_src},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "step_ms_min": min(times),
+        "step_ms_median": statistics.median(times),
+    }
+    if clocks and clocks.get("sm_mhz"):
+        line["roofline"]["frac_at_sampled_clock"] = achieved / (sms * FP32_LANES_PER_SM * clocks["sm_mhz"] * 1e6)
+
+    if not args.no_e2e:
+        e2e_ms, h2d, d2h = run_prefill_e2e(args, dev, inp)
+        e2e_ms = max_over_ranks(e2e_ms, world, dev)
+        line["e2e"] = {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s",
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "ms_per_step": e2e_ms}
+    if not args.no_decode:
+        dec = run_decode(dev, rank)
+        dinp = workload("decode_16x1")
+        sbytes, dbytes = decode_algorithmic(dinp)
+        cold_s = dec["cold_us"] * 1e-6
+        line["decode"] = {
+            "us_per_step": dec["cold_us"],
+            "what": "16 resuming sequences x 1 token, 300 steps over 8 rotating slot sets (cold L2)",
+            "us_per_step_mean": dec["cold_mean_us"],
+            "us_per_step_stream": dec["stream_us"],
+            "us_per_step_warm_graph": dec["warm_graph_us"],
+            "roofline": {"bound": "hbm", "achieved": dbytes / cold_s / 1e9,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": dbytes / cold_s / 1e9 / peaks["hbm_gbs"],
+                         "state_frac": sbytes / cold_s / 1e9 / peaks["hbm_gbs"],
+                         "traffic": ncu_traffic("decode_kernel", "decode_16x1"),
+                         "peak_src": peaks_src,
+                         "algorithmic": f"{dbytes} bytes per launch ({sbytes} of state)"},
+            "vs_page": PAGE_DECODE_US / dec["cold_us"],
+        }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_prefill(inp)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+# ---------------------------------------------------------------- reference arm
+
+def reference(args):
+    """The CPU oracle as it stands, on the host cores, on a bounded sample of
+    the 1 x 4096 prefill workload: each step runs the oracle on a subset of
+    heads sized so the whole run stays within about two minutes."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    inp = workload("prefill_1x4096")
+    H = inp.geom.n_heads
+    cores = os.cpu_count() or 1
+    t = time.perf_counter()
+    oracle.scan_inputs(inp, n_threads=cores, heads=[0, 1, 2, 3])
+    per_head = (time.perf_counter() - t) / 4
+    total_steps = max(1, args.steps + args.warmup)
+    heads_per_step = int(max(1, min(H, 120.0 / total_steps / max(per_head, 1e-6))))
+    heads = list(range(heads_per_step))
+    for _ in range(args.warmup):
+        oracle.scan_inputs(inp, n_threads=cores, heads=heads)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.scan_inputs(inp, n_threads=cores, heads=heads)
+    wall = (time.perf_counter() - t) / max(1, args.steps)
+    T = int(inp.seq_lens.sum())
+    value = T * (heads_per_step / H) / wall
+    sample = (f"{heads_per_step} of {H} heads of the 1x{T} prefill per step "
+              f"(tokens/s scaled by the head fraction), fp64 C oracle")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": wall * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "prefill_1x4096", "what": WORKLOADS["prefill_1x4096"]["what"]},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        reference(args)
+    else:
+        ours(args)
+
+
+if __name__ == "__main__":
+    main()
