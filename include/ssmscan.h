@@ -81,9 +81,12 @@ typedef enum {
 
 /* Kernel path selection for ssm_scan_tuned. */
 enum {
-    SSM_PATH_AUTO = 0,     /* decode when n_tokens == n_seqs, else prefill */
-    SSM_PATH_DECODE = 1,   /* warp-per-row kernel; correct for any lengths */
-    SSM_PATH_PREFILL = 2   /* chunk-staged kernel; correct for any lengths */
+    SSM_PATH_AUTO = 0,           /* decode when n_tokens == n_seqs, else prefill */
+    SSM_PATH_DECODE = 1,         /* warp-per-row kernel; correct for any lengths */
+    SSM_PATH_PREFILL = 2,        /* chunk-staged kernel, decay-rescaled state with packed
+                                    fp32x2 FMAs; correct for any lengths */
+    SSM_PATH_PREFILL_DIRECT = 3  /* chunk-staged kernel stepping S itself (one multiply
+                                    more per state element); correct for any lengths */
 };
 
 /*
@@ -93,10 +96,12 @@ enum {
  * SSM_ERR_INVALID_ARG.
  *   path             SSM_PATH_*
  *   lanes_per_row    lanes of a warp that share one state row: 1,2,4,8,16,32
- *   rows_per_thread  state rows each lane holds (1, 2 or 4; <= lanes_per_row)
+ *   rows_per_thread  state rows each lane holds (1, 2 or 4; <= lanes_per_row;
+ *                    1 on SSM_PATH_PREFILL)
  *   rows_per_cta     prefill: state rows per thread block (a multiple of the
  *                    rows one warp holds, at most 256 threads); decode: ignored
- *   chunk_tokens     prefill: tokens staged in shared memory per chunk (1..256)
+ *   chunk_tokens     prefill: tokens staged in shared memory per chunk (1..256;
+ *                    at most 32 on SSM_PATH_PREFILL)
  *   ctas_per_sm      decode: if > 0, the grid is capped at this many blocks
  *                    per SM and warps loop over the remaining rows
  */

@@ -6,8 +6,9 @@
 The C ABI is declared in ``include/ssmscan.h``; ``binding`` wraps it with
 ctypes.  ``workloads`` draws the seeded synthetic inputs.
 """
-from .binding import (PATH_AUTO, PATH_DECODE, PATH_PREFILL, SsmScanError, Tuning,  # noqa: F401
+from .binding import (PATH_AUTO, PATH_DECODE, PATH_PREFILL, PATH_PREFILL_DIRECT,  # noqa: F401
+                      SsmScanError, Tuning,
                       load, ssm_scan, status_string)
 
 __all__ = ["ssm_scan", "Tuning", "SsmScanError", "PATH_AUTO", "PATH_DECODE",
-           "PATH_PREFILL", "load", "status_string"]
+           "PATH_PREFILL", "PATH_PREFILL_DIRECT", "load", "status_string"]

@@ -24,7 +24,7 @@ SSM_ERR_UNSUPPORTED = -2
 SSM_ERR_CUDA = -3
 SSM_ERR_TIMEOUT = -4
 
-PATH_AUTO, PATH_DECODE, PATH_PREFILL = 0, 1, 2
+PATH_AUTO, PATH_DECODE, PATH_PREFILL, PATH_PREFILL_DIRECT = 0, 1, 2, 3
 
 _lib = None
 _lock = threading.Lock()

@@ -129,7 +129,7 @@ int scan_impl(float *state, const float *x, const float *dt, const float *A, con
     std::memset(&t, 0, sizeof t);
     if (tun)
         t = *tun;
-    if (t.path < SSM_PATH_AUTO || t.path > SSM_PATH_PREFILL || t.lanes_per_row < 0 ||
+    if (t.path < SSM_PATH_AUTO || t.path > SSM_PATH_PREFILL_DIRECT || t.lanes_per_row < 0 ||
         t.rows_per_thread < 0 || t.rows_per_cta < 0 || t.chunk_tokens < 0 || t.chunk_tokens > 256 ||
         t.ctas_per_sm < 0)
         return SSM_ERR_INVALID_ARG;
@@ -181,11 +181,17 @@ int scan_impl(float *state, const float *x, const float *dt, const float *A, con
     }
 
     // ---- prefill ----
+    const bool scaled = (path == SSM_PATH_PREFILL);
     const int lanes = t.lanes_per_row ? t.lanes_per_row : std::min(32, pow2ceil((N + 31) / 32));
     const int rpt = t.rows_per_thread ? t.rows_per_thread : 1;
-    const int vpl = pick_vpl(N4, lanes, rpt, ssm::prefill_supported);
+    const int vpl = pick_vpl(N4, lanes, rpt, scaled ? ssm::prefill_scaled_supported : ssm::prefill_supported);
     if (rpt > lanes || vpl == 0)
         return SSM_ERR_INVALID_ARG;
+    if (scaled && t.chunk_tokens > ssm::kScaledMaxChunk)
+        return SSM_ERR_INVALID_ARG;
+    auto smem_of = [&](const ssm::PrefillGeom &gg) {
+        return scaled ? ssm::prefill_scaled_smem_bytes(gg, N) : ssm::prefill_smem_bytes(gg, N);
+    };
     const int rows_per_warp = (32 / lanes) * rpt;
     ssm::PrefillGeom g;
     g.rows_per_group = (H / G) * P;
@@ -210,23 +216,24 @@ int scan_impl(float *state, const float *x, const float *dt, const float *A, con
     const long long n_ctas = (long long)n_seqs * G * g.runs_per_group;
     if (n_ctas > INT_MAX)
         return SSM_ERR_UNSUPPORTED;
-    // dt of one chunk is carried in 4 registers per thread.
-    const int dt_cap = 4 * threads;
+    // The direct kernel carries one chunk's dt in 4 registers per thread.
+    const int dt_cap = scaled ? INT_MAX : 4 * threads;
+    const size_t smem_cap = (size_t)(N > 256 ? dev.smem_optin : std::min(dev.smem_optin, 112 * 1024));
     if (t.chunk_tokens) {
         g.chunk = t.chunk_tokens;
-        if (g.chunk * g.heads_cap > dt_cap ||
-            ssm::prefill_smem_bytes(g, N) > (size_t)dev.smem_optin)
+        if ((long long)g.chunk * g.heads_cap > dt_cap || smem_of(g) > (size_t)dev.smem_optin)
             return SSM_ERR_INVALID_ARG;
     } else {
         g.chunk = 32;
-        while (g.chunk > 1 && (g.chunk * g.heads_cap > dt_cap ||
-                               ssm::prefill_smem_bytes(g, N) > (size_t)std::min(dev.smem_optin, 112 * 1024)))
+        while (g.chunk > 1 && ((long long)g.chunk * g.heads_cap > dt_cap || smem_of(g) > smem_cap))
             g.chunk >>= 1;
-        if (ssm::prefill_smem_bytes(g, N) > (size_t)dev.smem_optin)
+        if (smem_of(g) > (size_t)dev.smem_optin)
             return SSM_ERR_UNSUPPORTED;
     }
-    const size_t smem = ssm::prefill_smem_bytes(g, N);
-    if (ssm::launch_prefill(a, g, lanes, vpl, rpt, smem, dev.sms, stream) != cudaSuccess)
+    const size_t smem = smem_of(g);
+    const cudaError_t e = scaled ? ssm::launch_prefill_scaled(a, g, lanes, vpl, smem, stream)
+                                 : ssm::launch_prefill(a, g, lanes, vpl, rpt, smem, dev.sms, stream);
+    if (e != cudaSuccess)
         return SSM_ERR_CUDA;
     return SSM_OK;
 }

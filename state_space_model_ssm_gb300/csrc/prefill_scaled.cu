@@ -1,0 +1,363 @@
+// Prefill kernel of the Mamba2 scan with a decay-rescaled state (sm_103a).
+//
+// Same work mapping, register layout and chunk staging as prefill.cu, but the
+// registers hold U = S / Lambda instead of S, where Lambda is the decay
+// accumulated since an anchor token.  Because Lambda_t = dA_t * Lambda_{t-1},
+//
+//     S_t = dA_t S_{t-1} + dt_t x_t B_t   <=>   U_t = U_{t-1} + (dt_t / Lambda_t) x_t B_t
+//     y_t = S_t . C_t + D x_t             =    Lambda_t (U_t . C_t) + D x_t
+//
+// so each state element costs one multiply-add for the update and one for the
+// readout (the decay multiply of the direct form disappears), and both run as
+// packed fp32x2 FMAs (two lanes of work per instruction on sm_100-class SMs).
+//
+// Lambda must stay inside the fp32 range, so the reference is re-anchored:
+// at the first token of every chunk and whenever the running log-decay
+// sum(dt*A) of the chunk crosses a multiple of kAnchorSpan, U is multiplied by
+// the decay since the previous anchor and Lambda restarts at 1.  Between
+// anchors |log Lambda| < kAnchorSpan, so 1/Lambda < e^40.  At the end of each
+// chunk U is scaled back to S, which makes every chunk's coefficients
+// independent of the previous chunk.
+//
+// Per chunk and head one warp computes, lane = token, the coefficients
+//     c_t = dt_t / Lambda_t,   Lambda_t,   r_t (anchor multiplier, 1 elsewhere)
+// with a warp prefix sum (anchor placement) and a segmented prefix product of
+// dA = exp(dt*A) (Lambda, ~1 ulp per factor; no exp of long sums).
+//
+// The rescaling is an algebraic identity of the recurrence defined by "The
+// llama journey", Day 14 (decay exp(dt*A), input dt*x*B, y from the updated
+// state); only the rounding differs from the direct form.
+#include "scan_common.cuh"
+
+namespace ssm {
+
+namespace {
+
+constexpr float kAnchorSpan = 40.f;
+constexpr int kDtPerWarp = 4;     // heads per warp whose next-chunk dt is prefetched
+
+struct ScaledSmem {
+    float *base;
+    int cb, cx, cc;     // floats per buffer: B (= C), x, coefficients (float4 per token and head)
+    __device__ __forceinline__ float *B(int b) const { return base + b * cb; }
+    __device__ __forceinline__ float *C(int b) const { return base + 2 * cb + b * cb; }
+    __device__ __forceinline__ float *X(int b) const { return base + 4 * cb + b * cx; }
+    __device__ __forceinline__ float4 *Coef(int b) const
+    {
+        return reinterpret_cast<float4 *>(base + 4 * cb + 2 * cx + b * cc);
+    }
+    __device__ __forceinline__ float *Y() const { return base + 4 * cb + 2 * cx + 2 * cc; }
+};
+
+__device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
+
+// Coefficients of one head for one chunk of n <= 32 tokens; lane = token.
+// out[t * stride] = {dt_t / Lambda_t, Lambda_t, r_t, 0}.
+__device__ __forceinline__ void chunk_coefficients(float dt, float A, int n, int lane,
+                                                   float4 *out, int stride)
+{
+    const bool live = lane < n;
+    const float a = live ? dt * A : 0.f;
+    float L = a;                                   // inclusive prefix sum of dt*A
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float v = __shfl_up_sync(kFullMask, L, off);
+        if (lane >= off)
+            L += v;
+    }
+    const float bucket = floorf(L * (1.f / kAnchorSpan));
+    const float prev_bucket = __shfl_up_sync(kFullMask, bucket, 1);
+    const bool anchor = (lane == 0) || (bucket != prev_bucket);
+    const float dA = expf(a);
+    // segmented inclusive prefix product; an anchor token starts a segment at 1
+    float lam = anchor ? 1.f : dA;
+    int seg = anchor ? 1 : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float lo = __shfl_up_sync(kFullMask, lam, off);
+        const int so = __shfl_up_sync(kFullMask, seg, off);
+        if (lane >= off && !seg) {
+            lam *= lo;
+            seg = so;
+        }
+    }
+    const float lam_prev = __shfl_up_sync(kFullMask, lam, 1);
+    const float r = anchor ? (lane == 0 ? dA : lam_prev * dA) : 1.f;
+    if (live)
+        out[lane * stride] = make_float4(dt / lam, lam, r, 0.f);
+}
+
+}  // namespace
+
+size_t prefill_scaled_smem_bytes(const PrefillGeom &g, int N)
+{
+    const size_t cx = ((size_t)g.chunk * g.rows_per_cta + 3) & ~(size_t)3;
+    const size_t per_buf = (size_t)g.chunk * (2 * (size_t)N + 4 * (size_t)g.heads_cap) + cx;
+    return (2 * per_buf + (size_t)g.chunk * g.rows_per_cta) * sizeof(float);
+}
+
+template <int LANES, int VPL, bool EXACT>
+__global__ void __launch_bounds__(256, 1)
+prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
+{
+    extern __shared__ __align__(16) float smem[];
+    const int N = a.N, N4 = a.N >> 2, P = a.P, H = a.H;
+    const long long HP = (long long)H * P;
+    ScaledSmem sm;
+    sm.base = smem;
+    sm.cb = geo.chunk * N;
+    sm.cx = (geo.chunk * geo.rows_per_cta + 3) & ~3;     // keeps the float4 coefficients 16-byte aligned
+    sm.cc = geo.chunk * geo.heads_cap * 4;
+
+    // ---- A1 work mapping: (sequence, group, run of rows) ----
+    const int ctas_per_seq = a.G * geo.runs_per_group;
+    const int seq = blockIdx.x / ctas_per_seq;
+    const int rem = blockIdx.x - seq * ctas_per_seq;
+    const int grp = rem / geo.runs_per_group;
+    const int run = rem - grp * geo.runs_per_group;
+    const int r0 = grp * geo.rows_per_group + run * geo.rows_per_cta;
+    const int nrows = min(geo.rows_per_cta, geo.rows_per_group - run * geo.rows_per_cta);
+    const int h0 = r0 / P;
+    const int nheads = (r0 + nrows - 1) / P - h0 + 1;
+
+    const int tok_start = a.seq_starts[seq];
+    const int len = a.seq_lens[seq];
+    const bool resume = a.resume[seq] != 0;
+
+    const int tid = threadIdx.x, nthr = blockDim.x;
+    const int lane = tid & 31, warp = tid >> 5, nwarps = nthr >> 5;
+    const int j = lane % LANES;
+    const int row_raw = warp * (32 / LANES) + lane / LANES;
+    const bool rvalid = row_raw < nrows;
+    const int rl = rvalid ? row_raw : nrows - 1;
+    const int hl = (r0 + rl) / P - h0;
+    const float Dv = a.D[h0 + hl];
+    const bool ywriter = (j == 0) && rvalid;
+
+    // ---- A2 state load: U = S at the start ----
+    float2 u[VPL][2];
+    {
+        const float *slot = a.state + ((long long)seq * HP + r0 + rl) * N;
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) {
+            const int c = k * LANES + j;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (resume && rvalid && (EXACT || c < N4))
+                v = *reinterpret_cast<const float4 *>(slot + 4 * c);
+            u[k][0] = f2(v.x, v.y);
+            u[k][1] = f2(v.z, v.w);
+        }
+    }
+
+    const float *Bg = a.B + (long long)grp * N;
+    const float *Cg = a.C + (long long)grp * N;
+    const long long tokN = (long long)a.G * N;
+
+    // ---- A3 staging of B, C and x for chunk c0 into buffer buf ----
+    auto stage = [&](int c0, int buf) {
+        const int t0 = c0 * geo.chunk;
+        const int cnt = min(geo.chunk, len - t0);
+        const long long tok0 = (long long)tok_start + t0;
+        {
+            int t = tid / N4, v = tid - (tid / N4) * N4;
+            const int dt_ = nthr / N4, dv = nthr - dt_ * N4;
+            for (; t < cnt;) {
+                const long long goff = (tok0 + t) * tokN + 4 * v;
+                cp_async16(sm.B(buf) + t * N + 4 * v, Bg + goff);
+                cp_async16(sm.C(buf) + t * N + 4 * v, Cg + goff);
+                t += dt_;
+                v += dv;
+                if (v >= N4) { v -= N4; ++t; }
+            }
+        }
+        {
+            int t = tid / nrows, r = tid - (tid / nrows) * nrows;
+            const int dt_ = nthr / nrows, dr = nthr - dt_ * nrows;
+            for (; t < cnt;) {
+                cp_async4(sm.X(buf) + t * geo.rows_per_cta + r, a.x + (tok0 + t) * HP + r0 + r);
+                t += dt_;
+                r += dr;
+                if (r >= nrows) { r -= nrows; ++t; }
+            }
+        }
+        cp_async_commit();
+    };
+
+    // ---- A4: dt of chunk c0 for this warp's heads (head hh goes to warp (hh + c0) % nwarps) ----
+    float dtp[kDtPerWarp];
+    auto load_dt = [&](int c0) {
+        const int t0 = c0 * geo.chunk;
+        const int cnt = min(geo.chunk, len - t0);
+        const int first = ((warp - c0) % nwarps + nwarps) % nwarps;
+#pragma unroll
+        for (int q = 0; q < kDtPerWarp; ++q) {
+            const int hh = first + q * nwarps;
+            dtp[q] = 0.f;
+            if (hh < nheads && lane < cnt)
+                dtp[q] = a.dt[((long long)tok_start + t0 + lane) * H + h0 + hh];
+        }
+    };
+    auto coefficients = [&](int c0, int buf) {
+        const int t0 = c0 * geo.chunk;
+        const int cnt = min(geo.chunk, len - t0);
+        const int first = ((warp - c0) % nwarps + nwarps) % nwarps;
+        int q = 0;
+        for (int hh = first; hh < nheads; hh += nwarps, ++q) {
+            float dtv;
+            if (q < kDtPerWarp) {
+                dtv = dtp[0];
+#pragma unroll
+                for (int qq = 1; qq < kDtPerWarp; ++qq)
+                    if (qq == q) dtv = dtp[qq];
+            } else {
+                dtv = lane < cnt ? a.dt[((long long)tok_start + t0 + lane) * H + h0 + hh] : 0.f;
+            }
+            chunk_coefficients(dtv, a.A[h0 + hh], cnt, lane, sm.Coef(buf) + hh, geo.heads_cap);
+        }
+    };
+
+    const int n_chunks = (len + geo.chunk - 1) / geo.chunk;
+    if (n_chunks > 0) {
+        stage(0, 0);
+        load_dt(0);
+        coefficients(0, 0);
+    }
+
+    for (int c = 0; c < n_chunks; ++c) {
+        const int buf = c & 1;
+        const bool more = (c + 1) < n_chunks;
+        if (more) {
+            stage(c + 1, buf ^ 1);
+            load_dt(c + 1);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();
+
+        const int cnt = min(geo.chunk, len - c * geo.chunk);
+        const float *sB = sm.B(buf), *sC = sm.C(buf), *sX = sm.X(buf);
+        const float4 *sCf = sm.Coef(buf) + hl;
+        float *sY = sm.Y();
+        for (int tt = 0; tt < cnt; ++tt) {
+            const float4 cf = sCf[tt * geo.heads_cap];      // {dt/Lambda, Lambda, r, -}
+            if (cf.z != 1.f) {                              // re-anchor: U <- r U
+                const float2 r2 = f2(cf.z, cf.z);
+#pragma unroll
+                for (int k = 0; k < VPL; ++k) {
+                    u[k][0] = __fmul2_rn(u[k][0], r2);
+                    u[k][1] = __fmul2_rn(u[k][1], r2);
+                }
+            }
+            const float xv = sX[tt * geo.rows_per_cta + rl];
+            const float alpha = xv * cf.x;
+            const float2 a2 = f2(alpha, alpha);
+            float2 acc0 = f2(0.f, 0.f), acc1 = acc0, acc2 = acc0, acc3 = acc0;
+            const float *bt = sB + tt * N;
+            const float *ct = sC + tt * N;
+#pragma unroll
+            for (int k = 0; k < VPL; ++k) {
+                const int cidx = k * LANES + j;
+                if (EXACT || cidx < N4) {
+                    const float4 b = *reinterpret_cast<const float4 *>(bt + 4 * cidx);
+                    const float4 cc = *reinterpret_cast<const float4 *>(ct + 4 * cidx);
+                    u[k][0] = __ffma2_rn(a2, f2(b.x, b.y), u[k][0]);        // A5
+                    u[k][1] = __ffma2_rn(a2, f2(b.z, b.w), u[k][1]);
+                    if (k & 1) {                                             // A6
+                        acc2 = __ffma2_rn(u[k][0], f2(cc.x, cc.y), acc2);
+                        acc3 = __ffma2_rn(u[k][1], f2(cc.z, cc.w), acc3);
+                    } else {
+                        acc0 = __ffma2_rn(u[k][0], f2(cc.x, cc.y), acc0);
+                        acc1 = __ffma2_rn(u[k][1], f2(cc.z, cc.w), acc1);
+                    }
+                }
+            }
+            const float2 s2 = __fadd2_rn(__fadd2_rn(acc0, acc2), __fadd2_rn(acc1, acc3));
+            float part[1] = {s2.x + s2.y};
+            const float ysum = reduce_rows<LANES, 1>(part, j);
+            if (ywriter)
+                sY[tt * geo.rows_per_cta + rl] = fmaf(cf.y, ysum, Dv * xv);
+        }
+        {   // back to S at the chunk end: U <- Lambda_last U
+            const float lam = sCf[(cnt - 1) * geo.heads_cap].y;
+            const float2 l2 = f2(lam, lam);
+#pragma unroll
+            for (int k = 0; k < VPL; ++k) {
+                u[k][0] = __fmul2_rn(u[k][0], l2);
+                u[k][1] = __fmul2_rn(u[k][1], l2);
+            }
+        }
+        if (more)
+            coefficients(c + 1, buf ^ 1);
+        __syncthreads();
+
+        const long long tok0 = (long long)tok_start + c * geo.chunk;
+        {
+            int t = tid / nrows, r = tid - (tid / nrows) * nrows;
+            const int dt_ = nthr / nrows, dr = nthr - dt_ * nrows;
+            for (; t < cnt;) {
+                a.y[(tok0 + t) * HP + r0 + r] = sY[t * geo.rows_per_cta + r];
+                t += dt_;
+                r += dr;
+                if (r >= nrows) { r -= nrows; ++t; }
+            }
+        }
+    }
+
+    // ---- A7 state store ----
+    if (rvalid) {
+        float *slot = a.state + ((long long)seq * HP + r0 + rl) * N;
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) {
+            const int c = k * LANES + j;
+            if (EXACT || c < N4)
+                *reinterpret_cast<float4 *>(slot + 4 * c) =
+                    make_float4(u[k][0].x, u[k][0].y, u[k][1].x, u[k][1].y);
+        }
+    }
+}
+
+namespace {
+
+template <int LANES, int VPL>
+cudaError_t launch_scaled_one(const ScanArgs &a, const PrefillGeom &g, size_t smem, cudaStream_t stream)
+{
+    const bool exact = (a.N / 4) == LANES * VPL;
+    const int threads = g.rows_per_cta * LANES;
+    const dim3 grid((unsigned)((long long)a.n_seqs * a.G * g.runs_per_group));
+    auto kern = exact ? prefill_scaled_kernel<LANES, VPL, true> : prefill_scaled_kernel<LANES, VPL, false>;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess)
+            return e;
+    }
+    kern<<<grid, threads, smem, stream>>>(a, g);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+#define SSM_SCALED_SHAPES(X) \
+    X(1, 1) X(1, 2) X(1, 4) X(1, 8) X(2, 8) X(4, 8) X(8, 8) X(16, 8) X(32, 8) \
+    X(8, 4) X(16, 2) X(32, 1) X(4, 4) X(8, 2)
+
+bool prefill_scaled_supported(int lanes, int vpl, int rpt)
+{
+    if (rpt != 1)
+        return false;
+#define X(L, V) if (lanes == L && vpl == V) return true;
+    SSM_SCALED_SHAPES(X)
+#undef X
+    return false;
+}
+
+cudaError_t launch_prefill_scaled(const ScanArgs &a, const PrefillGeom &g, int lanes, int vpl,
+                                  size_t smem, cudaStream_t stream)
+{
+#define X(L, V) if (lanes == L && vpl == V) return launch_scaled_one<L, V>(a, g, smem, stream);
+    SSM_SCALED_SHAPES(X)
+#undef X
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace ssm

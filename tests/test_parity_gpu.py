@@ -27,7 +27,8 @@ def _tuning(path=0, lanes=0, rpt=0, rows=0, chunk=0, ctas=0):
 
 
 PATHS = [("auto", None), ("decode", _tuning(path=bd.PATH_DECODE)),
-         ("prefill", _tuning(path=bd.PATH_PREFILL))]
+         ("prefill", _tuning(path=bd.PATH_PREFILL)),
+         ("prefill_direct", _tuning(path=bd.PATH_PREFILL_DIRECT))]
 
 
 @pytest.mark.parametrize("name", ["tiny", "edge_p96_n100"])
@@ -105,11 +106,39 @@ PREFILL_SHAPES = [
 
 
 @pytest.mark.parametrize("lanes,rpt,rows,chunk", PREFILL_SHAPES)
-def test_parity_prefill_launch_shapes(lanes, rpt, rows, chunk):
+def test_parity_prefill_direct_launch_shapes(lanes, rpt, rows, chunk):
     inp = workload("tiny")
     y_ref, s_ref = oracle.scan_inputs(inp)
-    t = _tuning(path=bd.PATH_PREFILL, lanes=lanes, rpt=rpt, rows=rows, chunk=chunk)
+    t = _tuning(path=bd.PATH_PREFILL_DIRECT, lanes=lanes, rpt=rpt, rows=rows, chunk=chunk)
     y, s = run_gpu(inp, tuning=t)
+    assert_parity(inp, y, s, y_ref, s_ref)
+
+
+SCALED_SHAPES = [(4, 8, 32), (4, 32, 7), (4, 64, 32), (8, 32, 16), (16, 16, 5), (32, 8, 1),
+                 (8, 16, 32), (1, 32, 32), (2, 16, 3)]
+
+
+@pytest.mark.parametrize("lanes,rows,chunk", SCALED_SHAPES)
+def test_parity_prefill_launch_shapes(lanes, rows, chunk):
+    inp = workload("tiny")
+    y_ref, s_ref = oracle.scan_inputs(inp)
+    t = _tuning(path=bd.PATH_PREFILL, lanes=lanes, rows=rows, chunk=chunk)
+    y, s = run_gpu(inp, tuning=t)
+    assert_parity(inp, y, s, y_ref, s_ref)
+
+
+@pytest.mark.parametrize("dt_scale,a_value", [(1.0, -16.0), (8.0, -16.0), (60.0, -16.0),
+                                              (1.0, 0.0), (0.5, 0.05)],
+                         ids=["strong", "anchor_every_few", "underflow", "no_decay", "growth"])
+@pytest.mark.parametrize("path", PATHS[2:], ids=[p[0] for p in PATHS[2:]])
+def test_parity_extreme_decay(dt_scale, a_value, path):
+    """Decay far outside the drawn range: re-anchoring of the rescaled state
+    every few tokens, dA underflowing to zero, no decay at all, and growth."""
+    inp = make_inputs(Geometry(4, 16, 32, 2), [150, 77], [0, 1], seed=31)
+    inp.dt.mul_(dt_scale)
+    inp.A.fill_(a_value)
+    y_ref, s_ref = oracle.scan_inputs(inp)
+    y, s = run_gpu(inp, tuning=path[1])
     assert_parity(inp, y, s, y_ref, s_ref)
 
 
