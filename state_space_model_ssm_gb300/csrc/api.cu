@@ -162,20 +162,26 @@ int scan_impl(float *state, const float *x, const float *dt, const float *A, con
 
     if (path == SSM_PATH_DECODE) {
         const int lanes = t.lanes_per_row ? t.lanes_per_row : std::min(32, pow2ceil(N4));
-        const int rpt = t.rows_per_thread ? t.rows_per_thread
-                                          : ((lanes == 32 && N4 <= 32) ? 2 : 1);
+        int rpt = t.rows_per_thread;
+        if (!rpt) {     // up to 4 rows in flight per lane, a divisor of P
+            rpt = (lanes == 32 && N4 <= 32) ? 4 : 1;
+            while (P % rpt)
+                rpt >>= 1;
+        }
         const int vpl = pick_vpl(N4, lanes, rpt, ssm::decode_supported);
-        if (rpt > lanes || vpl == 0)
+        if (rpt > lanes || vpl == 0 || P % rpt != 0)
             return SSM_ERR_INVALID_ARG;
         ssm::DecodeGeom g;
         g.rows_per_warp = (32 / lanes) * rpt;
         g.tasks_per_seq = (H * P + g.rows_per_warp - 1) / g.rows_per_warp;
-        g.n_tasks = (long long)n_seqs * g.tasks_per_seq;
-        long long grid = (g.n_tasks + ssm::kDecodeWarps - 1) / ssm::kDecodeWarps;
+        const long long blocks_per_seq = (g.tasks_per_seq + ssm::kDecodeWarps - 1) / ssm::kDecodeWarps;
+        long long grid_seqs = std::min<long long>(n_seqs, 65535);
         if (t.ctas_per_sm > 0)
-            grid = std::min<long long>(grid, (long long)t.ctas_per_sm * dev.sms);
-        grid = std::min<long long>(grid, INT_MAX);
-        if (ssm::launch_decode(a, g, lanes, vpl, rpt, (int)grid, stream) != cudaSuccess)
+            grid_seqs = std::max<long long>(1, std::min<long long>(
+                grid_seqs, (long long)t.ctas_per_sm * dev.sms / std::max<long long>(1, blocks_per_seq)));
+        if (blocks_per_seq > INT_MAX)
+            return SSM_ERR_UNSUPPORTED;
+        if (ssm::launch_decode(a, g, lanes, vpl, rpt, (int)grid_seqs, stream) != cudaSuccess)
             return SSM_ERR_CUDA;
         return SSM_OK;
     }

@@ -13,8 +13,9 @@
 //   - B and C (shared by the heads of a group) and the per-row scalars come
 //     through the read-only path and hit in L1/L2 after the first warp.
 // A warp's rows always belong to one sequence, so the token loop is uniform
-// per warp.  The kernel is correct for any sequence lengths; it is meant for
-// length 1.
+// per warp, and a lane group's RPT rows to one head, so dt, dA, B and C are
+// loaded once per lane group and token.  The kernel is correct for any
+// sequence lengths; it is meant for length 1.
 #include "scan_common.cuh"
 
 namespace ssm {
@@ -25,75 +26,75 @@ decode_kernel(const ScanArgs a, const DecodeGeom geo)
 {
     const int N = a.N, N4 = a.N >> 2, P = a.P, H = a.H;
     const int HP = H * P;
-    const int heads_per_group = H / a.G;
     const int lane = threadIdx.x & 31;
     const int j = lane % LANES;
     const int lg = lane / LANES;
-    const long long warp_id = (long long)blockIdx.x * kDecodeWarps + (threadIdx.x >> 5);
-    const long long warp_stride = (long long)gridDim.x * kDecodeWarps;
+    const int task = blockIdx.x * kDecodeWarps + (threadIdx.x >> 5);   // warp within a sequence
+    if (task >= geo.tasks_per_seq)
+        return;                                                       // whole warp
+    // The RPT rows of a lane group are consecutive and, because RPT divides P
+    // (checked by the host), belong to one head and so to one group.
+    const int row0 = task * geo.rows_per_warp + lg * RPT;
+    const bool valid = row0 < HP;                                     // all RPT rows or none
+    const int r0 = valid ? row0 : HP - RPT;
+    const int head = r0 / P;
+    const int grp = head / (H / a.G);
+    const float Ah = __ldg(a.A + head);
+    const float Dh = __ldg(a.D + head);
 
-    for (long long task = warp_id; task < geo.n_tasks; task += warp_stride) {
-        const int seq = (int)(task / geo.tasks_per_seq);
-        const int tr = (int)(task - (long long)seq * geo.tasks_per_seq);
+    for (int seq = blockIdx.y; seq < a.n_seqs; seq += gridDim.y) {
         const int len = a.seq_lens[seq];
         const int tok_start = a.seq_starts[seq];
         const bool resume = a.resume[seq] != 0;
+        float *slot = a.state + ((long long)seq * HP + r0) * N;
 
-        int row[RPT], head[RPT];
-        bool rvalid[RPT];
-#pragma unroll
-        for (int q = 0; q < RPT; ++q) {
-            const int r = tr * geo.rows_per_warp + lg * RPT + q;
-            rvalid[q] = r < HP;
-            row[q] = rvalid[q] ? r : HP - 1;
-            head[q] = row[q] / P;
-        }
-
-        // A2: all slot loads of this lane first (RPT*VPL float4 in flight).
+        // A2: every slot load of this lane first (RPT*VPL float4 in flight).
         float4 s[RPT][VPL];
 #pragma unroll
-        for (int q = 0; q < RPT; ++q) {
-            const float *slot = a.state + ((long long)seq * HP + row[q]) * N;
+        for (int q = 0; q < RPT; ++q)
 #pragma unroll
             for (int k = 0; k < VPL; ++k) {
                 const int c = k * LANES + j;
                 s[q][k] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (resume && rvalid[q] && (EXACT || c < N4))
-                    s[q][k] = *reinterpret_cast<const float4 *>(slot + 4 * c);
+                if (resume && valid && (EXACT || c < N4))
+                    s[q][k] = __ldcs(reinterpret_cast<const float4 *>(slot + (long long)q * N + 4 * c));
             }
-        }
 
         for (int t = 0; t < len; ++t) {
             const long long tok = (long long)tok_start + t;
-            float dA[RPT], xdt[RPT], xv[RPT], part[RPT];
+            const float dtv = __ldg(a.dt + tok * H + head);
+            const float dA = expf(dtv * Ah);                               // A4
+            const float4 *bt = reinterpret_cast<const float4 *>(a.B + (tok * a.G + grp) * N);
+            const float4 *ct = reinterpret_cast<const float4 *>(a.C + (tok * a.G + grp) * N);
+            float xv[RPT], part[RPT];
 #pragma unroll
-            for (int q = 0; q < RPT; ++q) {
-                const float dtv = __ldg(a.dt + tok * H + head[q]);
-                dA[q] = expf(dtv * __ldg(a.A + head[q]));          // A4
-                xv[q] = __ldg(a.x + tok * HP + row[q]);
-                xdt[q] = dtv * xv[q];
-                part[q] = 0.f;
+            for (int q = 0; q < RPT; ++q)
+                xv[q] = __ldg(a.x + tok * HP + r0 + q);
+            float4 b[VPL], cc[VPL];
+#pragma unroll
+            for (int k = 0; k < VPL; ++k) {
+                const int c = k * LANES + j;
+                if (EXACT || c < N4) {
+                    b[k] = __ldg(bt + c);
+                    cc[k] = __ldg(ct + c);
+                }
             }
 #pragma unroll
             for (int q = 0; q < RPT; ++q) {
-                const int g = head[q] / heads_per_group;
-                const float *bt = a.B + (tok * a.G + g) * N;
-                const float *ct = a.C + (tok * a.G + g) * N;
+                const float xdt = dtv * xv[q];
                 float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
 #pragma unroll
                 for (int k = 0; k < VPL; ++k) {
                     const int c = k * LANES + j;
                     if (EXACT || c < N4) {
-                        const float4 b = __ldg(reinterpret_cast<const float4 *>(bt) + c);
-                        const float4 cc = __ldg(reinterpret_cast<const float4 *>(ct) + c);
-                        s[q][k].x = fmaf(s[q][k].x, dA[q], xdt[q] * b.x);     // A5
-                        s[q][k].y = fmaf(s[q][k].y, dA[q], xdt[q] * b.y);
-                        s[q][k].z = fmaf(s[q][k].z, dA[q], xdt[q] * b.z);
-                        s[q][k].w = fmaf(s[q][k].w, dA[q], xdt[q] * b.w);
-                        acc0 = fmaf(s[q][k].x, cc.x, acc0);                  // A6
-                        acc1 = fmaf(s[q][k].y, cc.y, acc1);
-                        acc2 = fmaf(s[q][k].z, cc.z, acc2);
-                        acc3 = fmaf(s[q][k].w, cc.w, acc3);
+                        s[q][k].x = fmaf(s[q][k].x, dA, xdt * b[k].x);          // A5
+                        s[q][k].y = fmaf(s[q][k].y, dA, xdt * b[k].y);
+                        s[q][k].z = fmaf(s[q][k].z, dA, xdt * b[k].z);
+                        s[q][k].w = fmaf(s[q][k].w, dA, xdt * b[k].w);
+                        acc0 = fmaf(s[q][k].x, cc[k].x, acc0);                  // A6
+                        acc1 = fmaf(s[q][k].y, cc[k].y, acc1);
+                        acc2 = fmaf(s[q][k].z, cc[k].z, acc2);
+                        acc3 = fmaf(s[q][k].w, cc[k].w, acc3);
                     }
                 }
                 part[q] = (acc0 + acc1) + (acc2 + acc3);
@@ -101,27 +102,23 @@ decode_kernel(const ScanArgs a, const DecodeGeom geo)
             const float ysum = reduce_rows<LANES, RPT>(part, j);
             const int qy = reduced_row<LANES, RPT>(j);
             float dxv = xv[0];
-            int hy = head[0], ry = row[0];
-            bool vy = rvalid[0];
 #pragma unroll
             for (int q = 1; q < RPT; ++q)
-                if (q == qy) { dxv = xv[q]; hy = head[q]; ry = row[q]; vy = rvalid[q]; }
-            if (reduced_writer<LANES, RPT>(j) && vy)
-                a.y[tok * HP + ry] = fmaf(__ldg(a.D + hy), dxv, ysum);
+                if (q == qy) dxv = xv[q];
+            if (reduced_writer<LANES, RPT>(j) && valid)
+                a.y[tok * HP + r0 + qy] = fmaf(Dh, dxv, ysum);
         }
 
         // A7: registers -> slot (coalesced 128-bit stores).
+        if (valid) {
 #pragma unroll
-        for (int q = 0; q < RPT; ++q) {
-            if (!rvalid[q])
-                continue;
-            float *slot = a.state + ((long long)seq * HP + row[q]) * N;
+            for (int q = 0; q < RPT; ++q)
 #pragma unroll
-            for (int k = 0; k < VPL; ++k) {
-                const int c = k * LANES + j;
-                if (EXACT || c < N4)
-                    *reinterpret_cast<float4 *>(slot + 4 * c) = s[q][k];
-            }
+                for (int k = 0; k < VPL; ++k) {
+                    const int c = k * LANES + j;
+                    if (EXACT || c < N4)
+                        __stcs(reinterpret_cast<float4 *>(slot + (long long)q * N + 4 * c), s[q][k]);
+                }
         }
     }
 }
@@ -129,10 +126,11 @@ decode_kernel(const ScanArgs a, const DecodeGeom geo)
 namespace {
 
 template <int LANES, int VPL, int RPT>
-cudaError_t launch_one(const ScanArgs &a, const DecodeGeom &g, int grid, cudaStream_t stream)
+cudaError_t launch_one(const ScanArgs &a, const DecodeGeom &g, int grid_seqs, cudaStream_t stream)
 {
     const bool exact = (a.N / 4) == LANES * VPL;
     auto kern = exact ? decode_kernel<LANES, VPL, RPT, true> : decode_kernel<LANES, VPL, RPT, false>;
+    const dim3 grid((unsigned)((g.tasks_per_seq + kDecodeWarps - 1) / kDecodeWarps), (unsigned)grid_seqs);
     kern<<<grid, kDecodeWarps * 32, 0, stream>>>(a, g);
     return cudaGetLastError();
 }
@@ -143,7 +141,7 @@ cudaError_t launch_one(const ScanArgs &a, const DecodeGeom &g, int grid, cudaStr
     X(1, 1, 1) X(2, 1, 1) X(4, 1, 1) X(8, 1, 1) X(16, 1, 1) X(32, 1, 1) \
     X(32, 2, 1) X(32, 4, 1) X(32, 8, 1) \
     X(32, 1, 2) X(32, 1, 4) X(16, 1, 2) X(32, 2, 2) X(8, 1, 2) X(4, 1, 2) \
-    X(16, 2, 1) X(16, 2, 2) X(8, 4, 1)
+    X(16, 2, 1) X(16, 2, 2) X(8, 4, 1) X(32, 1, 8)
 
 bool decode_supported(int lanes, int vpl, int rpt)
 {
@@ -154,9 +152,9 @@ bool decode_supported(int lanes, int vpl, int rpt)
 }
 
 cudaError_t launch_decode(const ScanArgs &a, const DecodeGeom &g, int lanes, int vpl, int rpt,
-                          int grid, cudaStream_t stream)
+                          int grid_seqs, cudaStream_t stream)
 {
-#define X(L, V, R) if (lanes == L && vpl == V && rpt == R) return launch_one<L, V, R>(a, g, grid, stream);
+#define X(L, V, R) if (lanes == L && vpl == V && rpt == R) return launch_one<L, V, R>(a, g, grid_seqs, stream);
     SSM_DECODE_SHAPES(X)
 #undef X
     return cudaErrorInvalidValue;

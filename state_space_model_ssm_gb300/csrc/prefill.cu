@@ -208,6 +208,7 @@ prefill_kernel(const ScanArgs a, const PrefillGeom geo)
         const int cnt = min(geo.chunk, len - c * geo.chunk);
         const float *sB = sm.B(buf), *sC = sm.C(buf), *sX = sm.X(buf);
         const float *sDt = sm.Dt(buf), *sDA = sm.DA(buf);
+#pragma unroll 4
         for (int tt = 0; tt < cnt; ++tt) {
             float dA[RPT], xdt[RPT], xv[RPT];
 #pragma unroll

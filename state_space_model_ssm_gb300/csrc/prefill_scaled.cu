@@ -38,7 +38,8 @@ constexpr int kDtPerWarp = 4;     // heads per warp whose next-chunk dt is prefe
 
 struct ScaledSmem {
     float *base;
-    int cb, cx, cc;     // floats per buffer: B (= C), x, coefficients (float4 per token and head)
+    int cb, cx, cc, cm; // floats per buffer: B (= C), x, coefficients (float4 per token and
+                        // head), anchor masks (one word per head)
     __device__ __forceinline__ float *B(int b) const { return base + b * cb; }
     __device__ __forceinline__ float *C(int b) const { return base + 2 * cb + b * cb; }
     __device__ __forceinline__ float *X(int b) const { return base + 4 * cb + b * cx; }
@@ -46,15 +47,20 @@ struct ScaledSmem {
     {
         return reinterpret_cast<float4 *>(base + 4 * cb + 2 * cx + b * cc);
     }
-    __device__ __forceinline__ float *Y() const { return base + 4 * cb + 2 * cx + 2 * cc; }
+    __device__ __forceinline__ unsigned *Mask(int b) const
+    {
+        return reinterpret_cast<unsigned *>(base + 4 * cb + 2 * cx + 2 * cc + b * cm);
+    }
+    __device__ __forceinline__ float *Y() const { return base + 4 * cb + 2 * cx + 2 * cc + 2 * cm; }
 };
 
 __device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
 
 // Coefficients of one head for one chunk of n <= 32 tokens; lane = token.
-// out[t * stride] = {dt_t / Lambda_t, Lambda_t, r_t, 0}.
+// out[t * stride] = {dt_t / Lambda_t, Lambda_t, r_t, 0}; *mask = bit t set for
+// every anchor token t.
 __device__ __forceinline__ void chunk_coefficients(float dt, float A, int n, int lane,
-                                                   float4 *out, int stride)
+                                                   float4 *out, int stride, unsigned *mask)
 {
     const bool live = lane < n;
     const float a = live ? dt * A : 0.f;
@@ -85,6 +91,9 @@ __device__ __forceinline__ void chunk_coefficients(float dt, float A, int n, int
     const float r = anchor ? (lane == 0 ? dA : lam_prev * dA) : 1.f;
     if (live)
         out[lane * stride] = make_float4(dt / lam, lam, r, 0.f);
+    const unsigned m = __ballot_sync(kFullMask, anchor && live);
+    if (lane == 0)
+        *mask = m;
 }
 
 }  // namespace
@@ -92,7 +101,7 @@ __device__ __forceinline__ void chunk_coefficients(float dt, float A, int n, int
 size_t prefill_scaled_smem_bytes(const PrefillGeom &g, int N)
 {
     const size_t cx = ((size_t)g.chunk * g.rows_per_cta + 3) & ~(size_t)3;
-    const size_t per_buf = (size_t)g.chunk * (2 * (size_t)N + 4 * (size_t)g.heads_cap) + cx;
+    const size_t per_buf = (size_t)g.chunk * (2 * (size_t)N + 4 * (size_t)g.heads_cap) + cx + g.heads_cap;
     return (2 * per_buf + (size_t)g.chunk * g.rows_per_cta) * sizeof(float);
 }
 
@@ -108,6 +117,7 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
     sm.cb = geo.chunk * N;
     sm.cx = (geo.chunk * geo.rows_per_cta + 3) & ~3;     // keeps the float4 coefficients 16-byte aligned
     sm.cc = geo.chunk * geo.heads_cap * 4;
+    sm.cm = geo.heads_cap;
 
     // ---- A1 work mapping: (sequence, group, run of rows) ----
     const int ctas_per_seq = a.G * geo.runs_per_group;
@@ -212,7 +222,8 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
             } else {
                 dtv = lane < cnt ? a.dt[((long long)tok_start + t0 + lane) * H + h0 + hh] : 0.f;
             }
-            chunk_coefficients(dtv, a.A[h0 + hh], cnt, lane, sm.Coef(buf) + hh, geo.heads_cap);
+            chunk_coefficients(dtv, a.A[h0 + hh], cnt, lane, sm.Coef(buf) + hh, geo.heads_cap,
+                               sm.Mask(buf) + hh);
         }
     };
 
@@ -239,16 +250,11 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
         const float *sB = sm.B(buf), *sC = sm.C(buf), *sX = sm.X(buf);
         const float4 *sCf = sm.Coef(buf) + hl;
         float *sY = sm.Y();
-        for (int tt = 0; tt < cnt; ++tt) {
+        // One token: U += (x dt / Lambda) B, y = Lambda (U . C) + D x.  No branch, so
+        // the unrolled loop below can overlap one token's reduction with the next
+        // token's updates.
+        auto token = [&](int tt) {
             const float4 cf = sCf[tt * geo.heads_cap];      // {dt/Lambda, Lambda, r, -}
-            if (cf.z != 1.f) {                              // re-anchor: U <- r U
-                const float2 r2 = f2(cf.z, cf.z);
-#pragma unroll
-                for (int k = 0; k < VPL; ++k) {
-                    u[k][0] = __fmul2_rn(u[k][0], r2);
-                    u[k][1] = __fmul2_rn(u[k][1], r2);
-                }
-            }
             const float xv = sX[tt * geo.rows_per_cta + rl];
             const float alpha = xv * cf.x;
             const float2 a2 = f2(alpha, alpha);
@@ -277,6 +283,30 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
             const float ysum = reduce_rows<LANES, 1>(part, j);
             if (ywriter)
                 sY[tt * geo.rows_per_cta + rl] = fmaf(cf.y, ysum, Dv * xv);
+        };
+        // Anchor tokens of any head of the block split the chunk into segments;
+        // a head that does not anchor at a split has r = 1 there (exact no-op).
+        unsigned amask = 0;
+        for (int hh = 0; hh < nheads; ++hh)
+            amask |= sm.Mask(buf)[hh];
+        int tt = 0;
+        while (tt < cnt) {
+            {   // re-anchor: U <- r U
+                const float r = sCf[tt * geo.heads_cap].z;
+                const float2 r2 = f2(r, r);
+#pragma unroll
+                for (int k = 0; k < VPL; ++k) {
+                    u[k][0] = __fmul2_rn(u[k][0], r2);
+                    u[k][1] = __fmul2_rn(u[k][1], r2);
+                }
+            }
+            token(tt);
+            const unsigned rest = (tt + 1 < 32) ? (amask >> (tt + 1)) : 0u;
+            const int next = rest ? min(cnt, tt + __ffs(rest)) : cnt;
+#pragma unroll 4
+            for (int t2 = tt + 1; t2 < next; ++t2)
+                token(t2);
+            tt = next;
         }
         {   // back to S at the chunk end: U <- Lambda_last U
             const float lam = sCf[(cnt - 1) * geo.heads_cap].y;

@@ -41,11 +41,11 @@ struct PrefillGeom {
     int heads_cap;       // most heads one block's rows can touch
 };
 
-// Launch geometry of the warp-per-row decode kernel.
+// Launch geometry of the warp-per-row decode kernel: grid.x covers the warps
+// of one sequence, grid.y the sequences (blocks loop when n_seqs > grid.y).
 struct DecodeGeom {
     int rows_per_warp;   // (32/LANES)*RPT
-    int tasks_per_seq;   // ceil(H*P / rows_per_warp)
-    long long n_tasks;   // n_seqs * tasks_per_seq
+    int tasks_per_seq;   // warps per sequence: ceil(H*P / rows_per_warp)
 };
 
 constexpr unsigned kFullMask = 0xffffffffu;
@@ -141,7 +141,7 @@ size_t prefill_scaled_smem_bytes(const PrefillGeom &g, int N);
 constexpr int kScaledMaxChunk = 32;    // one warp lane per token in the coefficient pass
 
 cudaError_t launch_decode(const ScanArgs &a, const DecodeGeom &g, int lanes,
-                          int vpl, int rpt, int grid, cudaStream_t stream);
+                          int vpl, int rpt, int grid_seqs, cudaStream_t stream);
 bool decode_supported(int lanes, int vpl, int rpt);
 constexpr int kDecodeWarps = 8;
 

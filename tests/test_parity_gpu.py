@@ -142,7 +142,7 @@ def test_parity_extreme_decay(dt_scale, a_value, path):
     assert_parity(inp, y, s, y_ref, s_ref)
 
 
-DECODE_SHAPES = [(32, 1, 0), (32, 2, 0), (32, 4, 0), (16, 2, 0), (16, 1, 0), (8, 1, 0), (32, 2, 1)]
+DECODE_SHAPES = [(32, 1, 0), (32, 2, 0), (32, 4, 0), (32, 8, 0), (16, 2, 0), (16, 1, 0), (8, 1, 0), (32, 2, 1)]
 
 
 @pytest.mark.parametrize("lanes,rpt,ctas", DECODE_SHAPES)
