@@ -188,9 +188,28 @@ int scan_impl(float *state, const float *x, const float *dt, const float *A, con
 
     // ---- prefill ----
     const bool scaled = (path == SSM_PATH_PREFILL);
-    const int lanes = t.lanes_per_row ? t.lanes_per_row : std::min(32, pow2ceil((N + 31) / 32));
-    const int rpt = t.rows_per_thread ? t.rows_per_thread : 1;
-    const int vpl = pick_vpl(N4, lanes, rpt, scaled ? ssm::prefill_scaled_supported : ssm::prefill_supported);
+    auto supported = scaled ? ssm::prefill_scaled_supported : ssm::prefill_supported;
+    int lanes, rpt, vpl;
+    if (scaled) {
+        // About 8 state elements of a row per lane, and up to 4 rows per lane
+        // (32 state registers) so that each B/C value read from shared memory
+        // feeds several rows.  The rows of a lane must share a head: RPT | P.
+        lanes = t.lanes_per_row ? t.lanes_per_row : std::min(32, pow2ceil((N + 7) / 8));
+        rpt = t.rows_per_thread;
+        if (!rpt) {
+            rpt = 4;
+            while (rpt > 1 && (P % rpt != 0 || rpt > lanes ||
+                               pick_vpl(N4, lanes, rpt, supported) * 4 * rpt > 32 ||
+                               pick_vpl(N4, lanes, rpt, supported) == 0))
+                rpt >>= 1;
+        }
+        if (P % rpt != 0)
+            return SSM_ERR_INVALID_ARG;
+    } else {
+        lanes = t.lanes_per_row ? t.lanes_per_row : std::min(32, pow2ceil((N + 31) / 32));
+        rpt = t.rows_per_thread ? t.rows_per_thread : 1;
+    }
+    vpl = pick_vpl(N4, lanes, rpt, supported);
     if (rpt > lanes || vpl == 0)
         return SSM_ERR_INVALID_ARG;
     if (scaled && t.chunk_tokens > ssm::kScaledMaxChunk)
@@ -237,7 +256,7 @@ int scan_impl(float *state, const float *x, const float *dt, const float *A, con
             return SSM_ERR_UNSUPPORTED;
     }
     const size_t smem = smem_of(g);
-    const cudaError_t e = scaled ? ssm::launch_prefill_scaled(a, g, lanes, vpl, smem, stream)
+    const cudaError_t e = scaled ? ssm::launch_prefill_scaled(a, g, lanes, vpl, rpt, smem, stream)
                                  : ssm::launch_prefill(a, g, lanes, vpl, rpt, smem, dev.sms, stream);
     if (e != cudaSuccess)
         return SSM_ERR_CUDA;

@@ -56,6 +56,26 @@ struct ScaledSmem {
 
 __device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
 
+// R consecutive floats from shared memory (16-byte aligned when R = 4, 8 bytes when R = 2).
+template <int R>
+__device__ __forceinline__ void load_rows(float (&v)[R], const float *p)
+{
+    if constexpr (R % 4 == 0) {
+#pragma unroll
+        for (int i = 0; i < R; i += 4) {
+            const float4 t = *reinterpret_cast<const float4 *>(p + i);
+            v[i] = t.x; v[i + 1] = t.y; v[i + 2] = t.z; v[i + 3] = t.w;
+        }
+    } else if constexpr (R == 2) {
+        const float2 t = *reinterpret_cast<const float2 *>(p);
+        v[0] = t.x; v[1] = t.y;
+    } else {
+#pragma unroll
+        for (int i = 0; i < R; ++i)
+            v[i] = p[i];
+    }
+}
+
 // Coefficients of one head for one chunk of n <= 32 tokens; lane = token.
 // out[t * stride] = {dt_t / Lambda_t, Lambda_t, r_t, 0}; *mask = bit t set for
 // every anchor token t.
@@ -105,7 +125,7 @@ size_t prefill_scaled_smem_bytes(const PrefillGeom &g, int N)
     return (2 * per_buf + (size_t)g.chunk * g.rows_per_cta) * sizeof(float);
 }
 
-template <int LANES, int VPL, bool EXACT>
+template <int LANES, int VPL, int RPT, bool EXACT>
 __global__ void __launch_bounds__(256, 1)
 prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
 {
@@ -137,25 +157,30 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
     const int tid = threadIdx.x, nthr = blockDim.x;
     const int lane = tid & 31, warp = tid >> 5, nwarps = nthr >> 5;
     const int j = lane % LANES;
-    const int row_raw = warp * (32 / LANES) + lane / LANES;
+    // A lane group (LANES lanes) holds RPT consecutive rows.  RPT divides P and
+    // the rows per block (checked by the host), so the group's rows are all
+    // valid or all padding, and they share one head.
+    const int row_raw = (warp * (32 / LANES) + lane / LANES) * RPT;
     const bool rvalid = row_raw < nrows;
-    const int rl = rvalid ? row_raw : nrows - 1;
+    const int rl = rvalid ? row_raw : nrows - RPT;          // first of the RPT rows
     const int hl = (r0 + rl) / P - h0;
     const float Dv = a.D[h0 + hl];
-    const bool ywriter = (j == 0) && rvalid;
+    const int yq = reduced_row<LANES, RPT>(j);               // row of this lane's reduced sum
+    const bool ywriter = reduced_writer<LANES, RPT>(j) && rvalid;
 
     // ---- A2 state load: U = S at the start ----
-    float2 u[VPL][2];
-    {
-        const float *slot = a.state + ((long long)seq * HP + r0 + rl) * N;
+    float2 u[RPT][VPL][2];
+#pragma unroll
+    for (int q = 0; q < RPT; ++q) {
+        const float *slot = a.state + ((long long)seq * HP + r0 + rl + q) * N;
 #pragma unroll
         for (int k = 0; k < VPL; ++k) {
             const int c = k * LANES + j;
             float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
             if (resume && rvalid && (EXACT || c < N4))
                 v = *reinterpret_cast<const float4 *>(slot + 4 * c);
-            u[k][0] = f2(v.x, v.y);
-            u[k][1] = f2(v.z, v.w);
+            u[q][k][0] = f2(v.x, v.y);
+            u[q][k][1] = f2(v.z, v.w);
         }
     }
 
@@ -255,10 +280,15 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
         // token's updates.
         auto token = [&](int tt) {
             const float4 cf = sCf[tt * geo.heads_cap];      // {dt/Lambda, Lambda, r, -}
-            const float xv = sX[tt * geo.rows_per_cta + rl];
-            const float alpha = xv * cf.x;
-            const float2 a2 = f2(alpha, alpha);
-            float2 acc0 = f2(0.f, 0.f), acc1 = acc0, acc2 = acc0, acc3 = acc0;
+            float xv[RPT];
+            load_rows<RPT>(xv, sX + tt * geo.rows_per_cta + rl);
+            float2 a2[RPT], acc[RPT][2];
+#pragma unroll
+            for (int q = 0; q < RPT; ++q) {
+                const float alpha = xv[q] * cf.x;
+                a2[q] = f2(alpha, alpha);
+                acc[q][0] = acc[q][1] = f2(0.f, 0.f);
+            }
             const float *bt = sB + tt * N;
             const float *ct = sC + tt * N;
 #pragma unroll
@@ -267,22 +297,28 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
                 if (EXACT || cidx < N4) {
                     const float4 b = *reinterpret_cast<const float4 *>(bt + 4 * cidx);
                     const float4 cc = *reinterpret_cast<const float4 *>(ct + 4 * cidx);
-                    u[k][0] = __ffma2_rn(a2, f2(b.x, b.y), u[k][0]);        // A5
-                    u[k][1] = __ffma2_rn(a2, f2(b.z, b.w), u[k][1]);
-                    if (k & 1) {                                             // A6
-                        acc2 = __ffma2_rn(u[k][0], f2(cc.x, cc.y), acc2);
-                        acc3 = __ffma2_rn(u[k][1], f2(cc.z, cc.w), acc3);
-                    } else {
-                        acc0 = __ffma2_rn(u[k][0], f2(cc.x, cc.y), acc0);
-                        acc1 = __ffma2_rn(u[k][1], f2(cc.z, cc.w), acc1);
+#pragma unroll
+                    for (int q = 0; q < RPT; ++q) {
+                        u[q][k][0] = __ffma2_rn(a2[q], f2(b.x, b.y), u[q][k][0]);      // A5
+                        u[q][k][1] = __ffma2_rn(a2[q], f2(b.z, b.w), u[q][k][1]);
+                        acc[q][k & 1] = __ffma2_rn(u[q][k][0], f2(cc.x, cc.y), acc[q][k & 1]);   // A6
+                        acc[q][k & 1] = __ffma2_rn(u[q][k][1], f2(cc.z, cc.w), acc[q][k & 1]);
                     }
                 }
             }
-            const float2 s2 = __fadd2_rn(__fadd2_rn(acc0, acc2), __fadd2_rn(acc1, acc3));
-            float part[1] = {s2.x + s2.y};
-            const float ysum = reduce_rows<LANES, 1>(part, j);
+            float part[RPT];
+#pragma unroll
+            for (int q = 0; q < RPT; ++q) {
+                const float2 s2 = __fadd2_rn(acc[q][0], acc[q][1]);
+                part[q] = s2.x + s2.y;
+            }
+            const float ysum = reduce_rows<LANES, RPT>(part, j);
+            float xy = xv[0];
+#pragma unroll
+            for (int q = 1; q < RPT; ++q)
+                if (q == yq) xy = xv[q];
             if (ywriter)
-                sY[tt * geo.rows_per_cta + rl] = fmaf(cf.y, ysum, Dv * xv);
+                sY[tt * geo.rows_per_cta + rl + yq] = fmaf(cf.y, ysum, Dv * xy);
         };
         // Anchor tokens of any head of the block split the chunk into segments;
         // a head that does not anchor at a split has r = 1 there (exact no-op).
@@ -295,10 +331,12 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
                 const float r = sCf[tt * geo.heads_cap].z;
                 const float2 r2 = f2(r, r);
 #pragma unroll
-                for (int k = 0; k < VPL; ++k) {
-                    u[k][0] = __fmul2_rn(u[k][0], r2);
-                    u[k][1] = __fmul2_rn(u[k][1], r2);
-                }
+                for (int q = 0; q < RPT; ++q)
+#pragma unroll
+                    for (int k = 0; k < VPL; ++k) {
+                        u[q][k][0] = __fmul2_rn(u[q][k][0], r2);
+                        u[q][k][1] = __fmul2_rn(u[q][k][1], r2);
+                    }
             }
             token(tt);
             const unsigned rest = (tt + 1 < 32) ? (amask >> (tt + 1)) : 0u;
@@ -312,10 +350,12 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
             const float lam = sCf[(cnt - 1) * geo.heads_cap].y;
             const float2 l2 = f2(lam, lam);
 #pragma unroll
-            for (int k = 0; k < VPL; ++k) {
-                u[k][0] = __fmul2_rn(u[k][0], l2);
-                u[k][1] = __fmul2_rn(u[k][1], l2);
-            }
+            for (int q = 0; q < RPT; ++q)
+#pragma unroll
+                for (int k = 0; k < VPL; ++k) {
+                    u[q][k][0] = __fmul2_rn(u[q][k][0], l2);
+                    u[q][k][1] = __fmul2_rn(u[q][k][1], l2);
+                }
         }
         if (more)
             coefficients(c + 1, buf ^ 1);
@@ -336,26 +376,30 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
 
     // ---- A7 state store ----
     if (rvalid) {
-        float *slot = a.state + ((long long)seq * HP + r0 + rl) * N;
 #pragma unroll
-        for (int k = 0; k < VPL; ++k) {
-            const int c = k * LANES + j;
-            if (EXACT || c < N4)
-                *reinterpret_cast<float4 *>(slot + 4 * c) =
-                    make_float4(u[k][0].x, u[k][0].y, u[k][1].x, u[k][1].y);
+        for (int q = 0; q < RPT; ++q) {
+            float *slot = a.state + ((long long)seq * HP + r0 + rl + q) * N;
+#pragma unroll
+            for (int k = 0; k < VPL; ++k) {
+                const int c = k * LANES + j;
+                if (EXACT || c < N4)
+                    *reinterpret_cast<float4 *>(slot + 4 * c) =
+                        make_float4(u[q][k][0].x, u[q][k][0].y, u[q][k][1].x, u[q][k][1].y);
+            }
         }
     }
 }
 
 namespace {
 
-template <int LANES, int VPL>
+template <int LANES, int VPL, int RPT>
 cudaError_t launch_scaled_one(const ScanArgs &a, const PrefillGeom &g, size_t smem, cudaStream_t stream)
 {
     const bool exact = (a.N / 4) == LANES * VPL;
-    const int threads = g.rows_per_cta * LANES;
+    const int threads = (g.rows_per_cta / RPT) * LANES;
     const dim3 grid((unsigned)((long long)a.n_seqs * a.G * g.runs_per_group));
-    auto kern = exact ? prefill_scaled_kernel<LANES, VPL, true> : prefill_scaled_kernel<LANES, VPL, false>;
+    auto kern = exact ? prefill_scaled_kernel<LANES, VPL, RPT, true>
+                      : prefill_scaled_kernel<LANES, VPL, RPT, false>;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess)
@@ -367,24 +411,25 @@ cudaError_t launch_scaled_one(const ScanArgs &a, const PrefillGeom &g, size_t sm
 
 }  // namespace
 
+// (lanes per row, float4 per lane and row, rows per lane)
 #define SSM_SCALED_SHAPES(X) \
-    X(1, 1) X(1, 2) X(1, 4) X(1, 8) X(2, 8) X(4, 8) X(8, 8) X(16, 8) X(32, 8) \
-    X(8, 4) X(16, 2) X(32, 1) X(4, 4) X(8, 2)
+    X(16, 2, 4) X(16, 2, 2) X(16, 2, 1) X(8, 2, 4) X(8, 2, 2) X(8, 2, 1) \
+    X(4, 2, 4) X(4, 2, 2) X(4, 2, 1) X(2, 2, 2) X(2, 2, 1) X(1, 2, 1) X(1, 1, 1) X(1, 4, 1) X(2, 4, 1) \
+    X(32, 2, 4) X(32, 2, 1) X(32, 4, 2) X(32, 4, 1) X(32, 8, 1) X(32, 1, 8) X(32, 1, 4) X(32, 1, 1) \
+    X(4, 8, 1) X(8, 4, 1) X(8, 4, 2) X(16, 4, 1)
 
 bool prefill_scaled_supported(int lanes, int vpl, int rpt)
 {
-    if (rpt != 1)
-        return false;
-#define X(L, V) if (lanes == L && vpl == V) return true;
+#define X(L, V, R) if (lanes == L && vpl == V && rpt == R) return true;
     SSM_SCALED_SHAPES(X)
 #undef X
     return false;
 }
 
-cudaError_t launch_prefill_scaled(const ScanArgs &a, const PrefillGeom &g, int lanes, int vpl,
+cudaError_t launch_prefill_scaled(const ScanArgs &a, const PrefillGeom &g, int lanes, int vpl, int rpt,
                                   size_t smem, cudaStream_t stream)
 {
-#define X(L, V) if (lanes == L && vpl == V) return launch_scaled_one<L, V>(a, g, smem, stream);
+#define X(L, V, R) if (lanes == L && vpl == V && rpt == R) return launch_scaled_one<L, V, R>(a, g, smem, stream);
     SSM_SCALED_SHAPES(X)
 #undef X
     return cudaErrorInvalidValue;

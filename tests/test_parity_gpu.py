@@ -114,15 +114,15 @@ def test_parity_prefill_direct_launch_shapes(lanes, rpt, rows, chunk):
     assert_parity(inp, y, s, y_ref, s_ref)
 
 
-SCALED_SHAPES = [(4, 8, 32), (4, 32, 7), (4, 64, 32), (8, 32, 16), (16, 16, 5), (32, 8, 1),
-                 (8, 16, 32), (1, 32, 32), (2, 16, 3)]
+SCALED_SHAPES = [(16, 4, 32, 32), (8, 2, 16, 32), (4, 4, 32, 7), (32, 8, 8, 1), (4, 1, 8, 32),
+                 (2, 1, 16, 3), (16, 1, 16, 5), (8, 4, 32, 32), (4, 2, 64, 32), (16, 2, 64, 17)]
 
 
-@pytest.mark.parametrize("lanes,rows,chunk", SCALED_SHAPES)
-def test_parity_prefill_launch_shapes(lanes, rows, chunk):
+@pytest.mark.parametrize("lanes,rpt,rows,chunk", SCALED_SHAPES)
+def test_parity_prefill_launch_shapes(lanes, rpt, rows, chunk):
     inp = workload("tiny")
     y_ref, s_ref = oracle.scan_inputs(inp)
-    t = _tuning(path=bd.PATH_PREFILL, lanes=lanes, rows=rows, chunk=chunk)
+    t = _tuning(path=bd.PATH_PREFILL, lanes=lanes, rpt=rpt, rows=rows, chunk=chunk)
     y, s = run_gpu(inp, tuning=t)
     assert_parity(inp, y, s, y_ref, s_ref)
 
