@@ -215,7 +215,7 @@ int scan_impl(float *state, const float *x, const float *dt, const float *A, con
     if (scaled && t.chunk_tokens > ssm::kScaledMaxChunk)
         return SSM_ERR_INVALID_ARG;
     auto smem_of = [&](const ssm::PrefillGeom &gg) {
-        return scaled ? ssm::prefill_scaled_smem_bytes(gg, N) : ssm::prefill_smem_bytes(gg, N);
+        return scaled ? ssm::prefill_scaled_smem_bytes(gg, N, lanes) : ssm::prefill_smem_bytes(gg, N);
     };
     const int rows_per_warp = (32 / lanes) * rpt;
     ssm::PrefillGeom g;
@@ -243,7 +243,8 @@ int scan_impl(float *state, const float *x, const float *dt, const float *A, con
         return SSM_ERR_UNSUPPORTED;
     // The direct kernel carries one chunk's dt in 4 registers per thread.
     const int dt_cap = scaled ? INT_MAX : 4 * threads;
-    const size_t smem_cap = (size_t)(N > 256 ? dev.smem_optin : std::min(dev.smem_optin, 112 * 1024));
+    // Two blocks per SM fit in the 228 KB of shared memory (1 KB per block is reserved).
+    const size_t smem_cap = (size_t)(N > 256 ? dev.smem_optin : std::min(dev.smem_optin, 113 * 1024));
     if (t.chunk_tokens) {
         g.chunk = t.chunk_tokens;
         if ((long long)g.chunk * g.heads_cap > dt_cap || smem_of(g) > (size_t)dev.smem_optin)

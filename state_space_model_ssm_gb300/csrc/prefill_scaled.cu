@@ -40,6 +40,7 @@ struct ScaledSmem {
     float *base;
     int cb, cx, cc, cm; // floats per buffer: B (= C), x, coefficients (float4 per token and
                         // head), anchor masks (one word per head)
+    int ps;             // floats between the partial-sum rows of two lanes (see Part())
     __device__ __forceinline__ float *B(int b) const { return base + b * cb; }
     __device__ __forceinline__ float *C(int b) const { return base + 2 * cb + b * cb; }
     __device__ __forceinline__ float *X(int b) const { return base + 4 * cb + b * cx; }
@@ -51,10 +52,32 @@ struct ScaledSmem {
     {
         return reinterpret_cast<unsigned *>(base + 4 * cb + 2 * cx + 2 * cc + b * cm);
     }
-    __device__ __forceinline__ float *Y() const { return base + 4 * cb + 2 * cx + 2 * cc + 2 * cm; }
+    // Per-lane partial dot products of one chunk: [token][lane in row][ps] with
+    // the block's rows contiguous; ps = rows rounded up to 4, plus 4, so the 16-byte
+    // stores of eight lanes fall on eight different bank quads.
+    __device__ __forceinline__ float *Part() const { return base + 4 * cb + 2 * cx + 2 * cc + 2 * cm; }
 };
 
 __device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
+
+__host__ __device__ __forceinline__ int part_stride(int rows) { return ((rows + 3) & ~3) + 4; }
+
+// R consecutive floats to shared memory (aligned like load_rows).
+template <int R>
+__device__ __forceinline__ void store_rows(float *p, const float (&v)[R])
+{
+    if constexpr (R % 4 == 0) {
+#pragma unroll
+        for (int i = 0; i < R; i += 4)
+            *reinterpret_cast<float4 *>(p + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+    } else if constexpr (R == 2) {
+        *reinterpret_cast<float2 *>(p) = make_float2(v[0], v[1]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < R; ++i)
+            p[i] = v[i];
+    }
+}
 
 // R consecutive floats from shared memory (16-byte aligned when R = 4, 8 bytes when R = 2).
 template <int R>
@@ -118,11 +141,12 @@ __device__ __forceinline__ void chunk_coefficients(float dt, float A, int n, int
 
 }  // namespace
 
-size_t prefill_scaled_smem_bytes(const PrefillGeom &g, int N)
+size_t prefill_scaled_smem_bytes(const PrefillGeom &g, int N, int lanes)
 {
     const size_t cx = ((size_t)g.chunk * g.rows_per_cta + 3) & ~(size_t)3;
     const size_t per_buf = (size_t)g.chunk * (2 * (size_t)N + 4 * (size_t)g.heads_cap) + cx + g.heads_cap;
-    return (2 * per_buf + (size_t)g.chunk * g.rows_per_cta) * sizeof(float);
+    const size_t part = (size_t)g.chunk * lanes * (size_t)part_stride(g.rows_per_cta);
+    return (2 * per_buf + part) * sizeof(float);
 }
 
 template <int LANES, int VPL, int RPT, bool EXACT>
@@ -138,6 +162,7 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
     sm.cx = (geo.chunk * geo.rows_per_cta + 3) & ~3;     // keeps the float4 coefficients 16-byte aligned
     sm.cc = geo.chunk * geo.heads_cap * 4;
     sm.cm = geo.heads_cap;
+    sm.ps = part_stride(geo.rows_per_cta);
 
     // ---- A1 work mapping: (sequence, group, run of rows) ----
     const int ctas_per_seq = a.G * geo.runs_per_group;
@@ -164,9 +189,6 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
     const bool rvalid = row_raw < nrows;
     const int rl = rvalid ? row_raw : nrows - RPT;          // first of the RPT rows
     const int hl = (r0 + rl) / P - h0;
-    const float Dv = a.D[h0 + hl];
-    const int yq = reduced_row<LANES, RPT>(j);               // row of this lane's reduced sum
-    const bool ywriter = reduced_writer<LANES, RPT>(j) && rvalid;
 
     // ---- A2 state load: U = S at the start ----
     float2 u[RPT][VPL][2];
@@ -274,10 +296,10 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
         const int cnt = min(geo.chunk, len - c * geo.chunk);
         const float *sB = sm.B(buf), *sC = sm.C(buf), *sX = sm.X(buf);
         const float4 *sCf = sm.Coef(buf) + hl;
-        float *sY = sm.Y();
-        // One token: U += (x dt / Lambda) B, y = Lambda (U . C) + D x.  No branch, so
-        // the unrolled loop below can overlap one token's reduction with the next
-        // token's updates.
+        float *sPart = sm.Part() + j * sm.ps + row_raw;
+        // One token: U += (x dt / Lambda) B and this lane's part of U . C.  No
+        // branch and no cross-lane step, so the unrolled loop below overlaps
+        // consecutive tokens; the lanes' parts are summed once per chunk.
         auto token = [&](int tt) {
             const float4 cf = sCf[tt * geo.heads_cap];      // {dt/Lambda, Lambda, r, -}
             float xv[RPT];
@@ -312,13 +334,7 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
                 const float2 s2 = __fadd2_rn(acc[q][0], acc[q][1]);
                 part[q] = s2.x + s2.y;
             }
-            const float ysum = reduce_rows<LANES, RPT>(part, j);
-            float xy = xv[0];
-#pragma unroll
-            for (int q = 1; q < RPT; ++q)
-                if (q == yq) xy = xv[q];
-            if (ywriter)
-                sY[tt * geo.rows_per_cta + rl + yq] = fmaf(cf.y, ysum, Dv * xy);
+            store_rows<RPT>(sPart + tt * LANES * sm.ps, part);
         };
         // Anchor tokens of any head of the block split the chunk into segments;
         // a head that does not anchor at a split has r = 1 there (exact no-op).
@@ -361,15 +377,34 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
             coefficients(c + 1, buf ^ 1);
         __syncthreads();
 
-        const long long tok0 = (long long)tok_start + c * geo.chunk;
+        // A6 readout for the chunk: y = Lambda_t * (sum of the lanes' parts) + D x,
+        // four rows per thread and pass, stored coalesced along the rows.
         {
-            int t = tid / nrows, r = tid - (tid / nrows) * nrows;
-            const int dt_ = nthr / nrows, dr = nthr - dt_ * nrows;
-            for (; t < cnt;) {
-                a.y[(tok0 + t) * HP + r0 + r] = sY[t * geo.rows_per_cta + r];
-                t += dt_;
-                r += dr;
-                if (r >= nrows) { r -= nrows; ++t; }
+            const long long tok0 = (long long)tok_start + c * geo.chunk;
+            const int nq = (nrows + 3) >> 2;
+            const float *part = sm.Part();
+            const float4 *cfb = sm.Coef(buf);
+            for (int idx = tid; idx < cnt * nq; idx += nthr) {
+                const int t = idx / nq, q4 = idx - t * nq;
+                const float *pp = part + t * LANES * sm.ps + 4 * q4;
+                float2 s01 = f2(0.f, 0.f), s23 = s01;
+#pragma unroll 8
+                for (int l = 0; l < LANES; ++l) {
+                    const float4 v = *reinterpret_cast<const float4 *>(pp + l * sm.ps);
+                    s01 = __fadd2_rn(s01, f2(v.x, v.y));
+                    s23 = __fadd2_rn(s23, f2(v.z, v.w));
+                }
+                const float sum[4] = {s01.x, s01.y, s23.x, s23.y};
+                const long long yrow = (tok0 + t) * HP + r0;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int r = 4 * q4 + e;
+                    if (r < nrows) {
+                        const int hh = (r0 + r) / P - h0;
+                        const float lam = cfb[t * geo.heads_cap + hh].y;
+                        a.y[yrow + r] = fmaf(lam, sum[e], a.D[h0 + hh] * a.x[yrow + r]);
+                    }
+                }
             }
         }
     }

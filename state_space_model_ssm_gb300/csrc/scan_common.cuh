@@ -137,7 +137,7 @@ size_t prefill_smem_bytes(const PrefillGeom &g, int N);
 cudaError_t launch_prefill_scaled(const ScanArgs &a, const PrefillGeom &g, int lanes, int vpl,
                                   int rpt, size_t smem_bytes, cudaStream_t stream);
 bool prefill_scaled_supported(int lanes, int vpl, int rpt);
-size_t prefill_scaled_smem_bytes(const PrefillGeom &g, int N);
+size_t prefill_scaled_smem_bytes(const PrefillGeom &g, int N, int lanes);
 constexpr int kScaledMaxChunk = 32;    // one warp lane per token in the coefficient pass
 
 cudaError_t launch_decode(const ScanArgs &a, const DecodeGeom &g, int lanes,
