@@ -144,7 +144,8 @@ __device__ __forceinline__ void chunk_coefficients(float dt, float A, int n, int
 size_t prefill_scaled_smem_bytes(const PrefillGeom &g, int N, int lanes)
 {
     const size_t cx = ((size_t)g.chunk * g.rows_per_cta + 3) & ~(size_t)3;
-    const size_t per_buf = (size_t)g.chunk * (2 * (size_t)N + 4 * (size_t)g.heads_cap) + cx + g.heads_cap;
+    const size_t cm = ((size_t)g.heads_cap + 3) & ~(size_t)3;
+    const size_t per_buf = (size_t)g.chunk * (2 * (size_t)N + 4 * (size_t)g.heads_cap) + cx + cm;
     const size_t part = (size_t)g.chunk * lanes * (size_t)part_stride(g.rows_per_cta);
     return (2 * per_buf + part) * sizeof(float);
 }
@@ -161,7 +162,7 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
     sm.cb = geo.chunk * N;
     sm.cx = (geo.chunk * geo.rows_per_cta + 3) & ~3;     // keeps the float4 coefficients 16-byte aligned
     sm.cc = geo.chunk * geo.heads_cap * 4;
-    sm.cm = geo.heads_cap;
+    sm.cm = (geo.heads_cap + 3) & ~3;        // keeps the partial sums after it 16-byte aligned
     sm.ps = part_stride(geo.rows_per_cta);
 
     // ---- A1 work mapping: (sequence, group, run of rows) ----
@@ -294,31 +295,47 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
         __syncthreads();
 
         const int cnt = min(geo.chunk, len - c * geo.chunk);
-        const float *sB = sm.B(buf), *sC = sm.C(buf), *sX = sm.X(buf);
-        const float4 *sCf = sm.Coef(buf) + hl;
-        float *sPart = sm.Part() + j * sm.ps + row_raw;
-        // One token: U += (x dt / Lambda) B and this lane's part of U . C.  No
-        // branch and no cross-lane step, so the unrolled loop below overlaps
-        // consecutive tokens; the lanes' parts are summed once per chunk.
-        auto token = [&](int tt) {
-            const float4 cf = sCf[tt * geo.heads_cap];      // {dt/Lambda, Lambda, r, -}
+        const float *__restrict__ sB = sm.B(buf);
+        const float *__restrict__ sC = sm.C(buf);
+        const float *__restrict__ sX = sm.X(buf);
+        const float4 *__restrict__ sCf = sm.Coef(buf) + hl;
+        float *__restrict__ sPart = sm.Part() + j * sm.ps + row_raw;
+
+        // Shared-memory operands of one token.
+        struct TokenIn {
+            float4 cf;          // {dt/Lambda, Lambda, r, -}
             float xv[RPT];
-            load_rows<RPT>(xv, sX + tt * geo.rows_per_cta + rl);
-            float2 a2[RPT], acc[RPT][2];
-#pragma unroll
-            for (int q = 0; q < RPT; ++q) {
-                const float alpha = xv[q] * cf.x;
-                a2[q] = f2(alpha, alpha);
-                acc[q][0] = acc[q][1] = f2(0.f, 0.f);
-            }
+            float4 b[VPL], c[VPL];
+        };
+        auto load_token = [&](int tt, TokenIn &in) {
+            in.cf = sCf[tt * geo.heads_cap];
+            load_rows<RPT>(in.xv, sX + tt * geo.rows_per_cta + rl);
             const float *bt = sB + tt * N;
             const float *ct = sC + tt * N;
 #pragma unroll
             for (int k = 0; k < VPL; ++k) {
                 const int cidx = k * LANES + j;
                 if (EXACT || cidx < N4) {
-                    const float4 b = *reinterpret_cast<const float4 *>(bt + 4 * cidx);
-                    const float4 cc = *reinterpret_cast<const float4 *>(ct + 4 * cidx);
+                    in.b[k] = *reinterpret_cast<const float4 *>(bt + 4 * cidx);
+                    in.c[k] = *reinterpret_cast<const float4 *>(ct + 4 * cidx);
+                }
+            }
+        };
+        // One token: U += (x dt / Lambda) B and this lane's part of U . C.  No
+        // cross-lane step: the lanes' parts are summed once per chunk.
+        auto compute_token = [&](const TokenIn &in, int tt) {
+            float2 a2[RPT], acc[RPT][2];
+#pragma unroll
+            for (int q = 0; q < RPT; ++q) {
+                const float alpha = in.xv[q] * in.cf.x;
+                a2[q] = f2(alpha, alpha);
+                acc[q][0] = acc[q][1] = f2(0.f, 0.f);
+            }
+#pragma unroll
+            for (int k = 0; k < VPL; ++k) {
+                const int cidx = k * LANES + j;
+                if (EXACT || cidx < N4) {
+                    const float4 b = in.b[k], cc = in.c[k];
 #pragma unroll
                     for (int q = 0; q < RPT; ++q) {
                         u[q][k][0] = __ffma2_rn(a2[q], f2(b.x, b.y), u[q][k][0]);      // A5
@@ -338,14 +355,17 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
         };
         // Anchor tokens of any head of the block split the chunk into segments;
         // a head that does not anchor at a split has r = 1 there (exact no-op).
+        // Within a segment the loop is software-pipelined: the operands of token
+        // t+1 are read before token t is computed and its partial sums stored.
         unsigned amask = 0;
         for (int hh = 0; hh < nheads; ++hh)
             amask |= sm.Mask(buf)[hh];
+        TokenIn cur;
+        load_token(0, cur);
         int tt = 0;
         while (tt < cnt) {
             {   // re-anchor: U <- r U
-                const float r = sCf[tt * geo.heads_cap].z;
-                const float2 r2 = f2(r, r);
+                const float2 r2 = f2(cur.cf.z, cur.cf.z);
 #pragma unroll
                 for (int q = 0; q < RPT; ++q)
 #pragma unroll
@@ -354,12 +374,15 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
                         u[q][k][1] = __fmul2_rn(u[q][k][1], r2);
                     }
             }
-            token(tt);
             const unsigned rest = (tt + 1 < 32) ? (amask >> (tt + 1)) : 0u;
             const int next = rest ? min(cnt, tt + __ffs(rest)) : cnt;
-#pragma unroll 4
-            for (int t2 = tt + 1; t2 < next; ++t2)
-                token(t2);
+#pragma unroll 2
+            for (int t2 = tt; t2 < next; ++t2) {
+                TokenIn nx;
+                load_token(min(t2 + 1, cnt - 1), nx);
+                compute_token(cur, t2);
+                cur = nx;
+            }
             tt = next;
         }
         {   // back to S at the chunk end: U <- Lambda_last U
