@@ -99,7 +99,8 @@ enum {
  *   rows_per_thread  state rows each lane holds (1, 2 or 4; <= lanes_per_row;
  *                    1 on SSM_PATH_PREFILL)
  *   rows_per_cta     prefill: state rows per thread block (a multiple of the
- *                    rows one warp holds, at most 256 threads); decode: ignored
+ *                    rows one warp holds, at most 256 threads, 224 on
+ *                    SSM_PATH_PREFILL which adds a producer warp); decode: ignored
  *   chunk_tokens     prefill: tokens staged in shared memory per chunk (1..256;
  *                    at most 32 on SSM_PATH_PREFILL)
  *   ctas_per_sm      decode: if > 0, the grid is capped at this many blocks

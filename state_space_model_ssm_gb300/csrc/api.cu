@@ -221,7 +221,8 @@ int scan_impl(float *state, const float *x, const float *dt, const float *A, con
     ssm::PrefillGeom g;
     g.rows_per_group = (H / G) * P;
     if (t.rows_per_cta) {
-        if (t.rows_per_cta % rows_per_warp != 0 || (t.rows_per_cta / rpt) * lanes > 256)
+        // the rescaled kernel adds one producer warp to the block's 256 threads
+        if (t.rows_per_cta % rows_per_warp != 0 || (t.rows_per_cta / rpt) * lanes > (scaled ? 224 : 256))
             return SSM_ERR_INVALID_ARG;
         g.rows_per_cta = t.rows_per_cta;
     } else {
@@ -250,7 +251,7 @@ int scan_impl(float *state, const float *x, const float *dt, const float *A, con
         if ((long long)g.chunk * g.heads_cap > dt_cap || smem_of(g) > (size_t)dev.smem_optin)
             return SSM_ERR_INVALID_ARG;
     } else {
-        g.chunk = 32;
+        g.chunk = scaled ? 16 : 32;
         while (g.chunk > 1 && ((long long)g.chunk * g.heads_cap > dt_cap || smem_of(g) > smem_cap))
             g.chunk >>= 1;
         if (smem_of(g) > (size_t)dev.smem_optin)

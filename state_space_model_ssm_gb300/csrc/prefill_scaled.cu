@@ -1,28 +1,34 @@
 // Prefill kernel of the Mamba2 scan with a decay-rescaled state (sm_103a).
 //
-// Same work mapping, register layout and chunk staging as prefill.cu, but the
-// registers hold U = S / Lambda instead of S, where Lambda is the decay
-// accumulated since an anchor token.  Because Lambda_t = dA_t * Lambda_{t-1},
+// Work mapping and register layout follow prefill.cu (a block owns one
+// sequence and a run of rows inside one group; a row's state lives in the
+// registers of LANES lanes as interleaved float4 chunks), with two changes.
 //
-//     S_t = dA_t S_{t-1} + dt_t x_t B_t   <=>   U_t = U_{t-1} + (dt_t / Lambda_t) x_t B_t
-//     y_t = S_t . C_t + D x_t             =    Lambda_t (U_t . C_t) + D x_t
+// 1. Rescaled state.  The registers hold U = S / Lambda, where Lambda is the
+//    decay accumulated since an anchor token.  Because Lambda_t = dA_t Lambda_{t-1},
 //
-// so each state element costs one multiply-add for the update and one for the
-// readout (the decay multiply of the direct form disappears), and both run as
-// packed fp32x2 FMAs (two lanes of work per instruction on sm_100-class SMs).
+//        S_t = dA_t S_{t-1} + dt_t x_t B_t  <=>  U_t = U_{t-1} + (dt_t / Lambda_t) x_t B_t
+//        y_t = S_t . C_t + D x_t            =    Lambda_t (U_t . C_t) + D x_t
 //
-// Lambda must stay inside the fp32 range, so the reference is re-anchored:
-// at the first token of every chunk and whenever the running log-decay
-// sum(dt*A) of the chunk crosses a multiple of kAnchorSpan, U is multiplied by
-// the decay since the previous anchor and Lambda restarts at 1.  Between
-// anchors |log Lambda| < kAnchorSpan, so 1/Lambda < e^40.  At the end of each
-// chunk U is scaled back to S, which makes every chunk's coefficients
-// independent of the previous chunk.
+//    so a state element costs one multiply-add for the update and one for the
+//    readout (the decay multiply of the direct form disappears); both run as
+//    packed fp32x2 FMAs.  Lambda must stay inside the fp32 range, so the
+//    reference is re-anchored at the first token of every chunk and whenever the
+//    chunk's running log-decay sum(dt*A) crosses a multiple of kAnchorSpan: U is
+//    multiplied by the decay since the previous anchor and Lambda restarts at 1
+//    (between anchors 1/Lambda < e^40).  At the end of each chunk U is scaled
+//    back to S, so every chunk's coefficients are independent.
 //
-// Per chunk and head one warp computes, lane = token, the coefficients
-//     c_t = dt_t / Lambda_t,   Lambda_t,   r_t (anchor multiplier, 1 elsewhere)
-// with a warp prefix sum (anchor placement) and a segmented prefix product of
-// dA = exp(dt*A) (Lambda, ~1 ulp per factor; no exp of long sums).
+// 2. Warp specialisation.  The block has one producer warp and (rows/RPT)*LANES/32
+//    consumer warps.  Consumers only run the token loop: per token, U += alpha B
+//    and each lane's partial of U . C, stored to shared memory.  The producer,
+//    one chunk ahead, stages B, C and x with cp.async, computes the chunk's
+//    coefficients (lane = token: a warp prefix sum places the anchors, a
+//    segmented prefix product of dA = exp(dt*A) gives Lambda, ~1 ulp per
+//    factor), and, one chunk behind, sums the lanes' partials into y.  The two
+//    sides meet at named barriers (bar.arrive / bar.sync, hardware barriers with
+//    no spin loop): FULL[b] when a chunk's inputs are staged, DONE[b] when its
+//    partials are written; buffers alternate between two slots b.
 //
 // The rescaling is an algebraic identity of the recurrence defined by "The
 // llama journey", Day 14 (decay exp(dt*A), input dt*x*B, y from the updated
@@ -34,7 +40,18 @@ namespace ssm {
 namespace {
 
 constexpr float kAnchorSpan = 40.f;
-constexpr int kDtPerWarp = 4;     // heads per warp whose next-chunk dt is prefetched
+constexpr int kBarFull = 1;       // named barriers kBarFull + b: inputs of slot b staged
+constexpr int kBarDone = 3;       // named barriers kBarDone + b: partials of slot b written
+
+__device__ __forceinline__ void bar_sync(int id, int nthreads)
+{
+    asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ void bar_arrive(int id, int nthreads)
+{
+    asm volatile("bar.arrive %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
+}
 
 struct ScaledSmem {
     float *base;
@@ -54,8 +71,12 @@ struct ScaledSmem {
     }
     // Per-lane partial dot products of one chunk: [token][lane in row][ps] with
     // the block's rows contiguous; ps = rows rounded up to 4, plus 4, so the 16-byte
-    // stores of eight lanes fall on eight different bank quads.
-    __device__ __forceinline__ float *Part() const { return base + 4 * cb + 2 * cx + 2 * cc + 2 * cm; }
+    // stores of eight lanes fall on eight different bank quads.  cp floats per slot.
+    int cp;
+    __device__ __forceinline__ float *Part(int b) const
+    {
+        return base + 4 * cb + 2 * cx + 2 * cc + 2 * cm + b * cp;
+    }
 };
 
 __device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
@@ -147,7 +168,7 @@ size_t prefill_scaled_smem_bytes(const PrefillGeom &g, int N, int lanes)
     const size_t cm = ((size_t)g.heads_cap + 3) & ~(size_t)3;
     const size_t per_buf = (size_t)g.chunk * (2 * (size_t)N + 4 * (size_t)g.heads_cap) + cx + cm;
     const size_t part = (size_t)g.chunk * lanes * (size_t)part_stride(g.rows_per_cta);
-    return (2 * per_buf + part) * sizeof(float);
+    return (2 * per_buf + 2 * part) * sizeof(float);
 }
 
 template <int LANES, int VPL, int RPT, bool EXACT>
@@ -162,8 +183,9 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
     sm.cb = geo.chunk * N;
     sm.cx = (geo.chunk * geo.rows_per_cta + 3) & ~3;     // keeps the float4 coefficients 16-byte aligned
     sm.cc = geo.chunk * geo.heads_cap * 4;
-    sm.cm = (geo.heads_cap + 3) & ~3;        // keeps the partial sums after it 16-byte aligned
+    sm.cm = (geo.heads_cap + 3) & ~3;                    // keeps the partial sums 16-byte aligned
     sm.ps = part_stride(geo.rows_per_cta);
+    sm.cp = geo.chunk * LANES * sm.ps;
 
     // ---- A1 work mapping: (sequence, group, run of rows) ----
     const int ctas_per_seq = a.G * geo.runs_per_group;
@@ -179,9 +201,103 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
     const int tok_start = a.seq_starts[seq];
     const int len = a.seq_lens[seq];
     const bool resume = a.resume[seq] != 0;
+    const int n_chunks = (len + geo.chunk - 1) / geo.chunk;
 
     const int tid = threadIdx.x, nthr = blockDim.x;
-    const int lane = tid & 31, warp = tid >> 5, nwarps = nthr >> 5;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int producer = (nthr >> 5) - 1;               // the last warp
+
+    if (warp == producer) {
+        // ================= producer warp =================
+        const float *Bg = a.B + (long long)grp * N;
+        const float *Cg = a.C + (long long)grp * N;
+        const long long tokN = (long long)a.G * N;
+        // A3: stage B, C and x of chunk c0 into slot b (cp.async, this warp only)
+        auto stage = [&](int c0, int b) {
+            const int t0 = c0 * geo.chunk;
+            const int cnt = min(geo.chunk, len - t0);
+            const long long tok0 = (long long)tok_start + t0;
+            float *sB = sm.B(b), *sC = sm.C(b), *sX = sm.X(b);
+            for (int idx = lane; idx < cnt * N4; idx += 32) {
+                const int t = idx / N4, v = idx - t * N4;
+                const long long goff = (tok0 + t) * tokN + 4 * v;
+                cp_async16(sB + t * N + 4 * v, Bg + goff);
+                cp_async16(sC + t * N + 4 * v, Cg + goff);
+            }
+            for (int idx = lane; idx < cnt * nrows; idx += 32) {
+                const int t = idx / nrows, r = idx - t * nrows;
+                cp_async4(sX + t * geo.rows_per_cta + r, a.x + (tok0 + t) * HP + r0 + r);
+            }
+            cp_async_commit();
+        };
+        // A4: coefficients of chunk c0 for every head of the block
+        auto coefficients = [&](int c0, int b) {
+            const int t0 = c0 * geo.chunk;
+            const int cnt = min(geo.chunk, len - t0);
+            for (int hh = 0; hh < nheads; ++hh) {
+                const float dtv = lane < cnt ? a.dt[((long long)tok_start + t0 + lane) * H + h0 + hh] : 0.f;
+                chunk_coefficients(dtv, a.A[h0 + hh], cnt, lane, sm.Coef(b) + hh, geo.heads_cap,
+                                   sm.Mask(b) + hh);
+            }
+        };
+        // A6 readout of chunk c0: y = Lambda_t * (sum of the lanes' parts) + D x,
+        // four rows per lane and pass.
+        const int nq = (nrows + 3) >> 2;
+        auto readout = [&](int c0, int b) {
+            const int t0 = c0 * geo.chunk;
+            const int cnt = min(geo.chunk, len - t0);
+            const long long tok0 = (long long)tok_start + t0;
+            const float *part = sm.Part(b);
+            const float4 *cf = sm.Coef(b);
+            const float *sX = sm.X(b);
+            for (int idx = lane; idx < cnt * nq; idx += 32) {
+                const int t = idx / nq, q4 = idx - t * nq;
+                const float *pp = part + t * LANES * sm.ps + 4 * q4;
+                float2 s01 = f2(0.f, 0.f), s23 = s01;
+#pragma unroll 8
+                for (int l = 0; l < LANES; ++l) {
+                    const float4 v = *reinterpret_cast<const float4 *>(pp + l * sm.ps);
+                    s01 = __fadd2_rn(s01, f2(v.x, v.y));
+                    s23 = __fadd2_rn(s23, f2(v.z, v.w));
+                }
+                const float sum[4] = {s01.x, s01.y, s23.x, s23.y};
+                float *yrow = a.y + (tok0 + t) * HP + r0;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int r = 4 * q4 + e;
+                    if (r < nrows) {
+                        const int hh = (r0 + r) / P - h0;
+                        const float lam = cf[t * geo.heads_cap + hh].y;
+                        yrow[r] = fmaf(lam, sum[e], __ldg(a.D + h0 + hh) * sX[t * geo.rows_per_cta + r]);
+                    }
+                }
+            }
+        };
+
+        if (n_chunks > 0) {
+            stage(0, 0);
+            coefficients(0, 0);
+            cp_async_wait<0>();
+            __syncwarp();
+            bar_arrive(kBarFull + 0, nthr);
+        }
+        for (int c = 0; c < n_chunks; ++c) {
+            if (c + 1 < n_chunks) {       // slot (c+1)&1 was released by DONE of chunk c-1
+                const int b = (c + 1) & 1;
+                stage(c + 1, b);
+                coefficients(c + 1, b);
+                cp_async_wait<0>();
+                __syncwarp();
+                bar_arrive(kBarFull + b, nthr);
+            }
+            bar_sync(kBarDone + (c & 1), nthr);
+            readout(c, c & 1);
+            __syncwarp();
+        }
+        return;
+    }
+
+    // ================= consumer warps =================
     const int j = lane % LANES;
     // A lane group (LANES lanes) holds RPT consecutive rows.  RPT divides P and
     // the rows per block (checked by the host), so the group's rows are all
@@ -207,99 +323,15 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
         }
     }
 
-    const float *Bg = a.B + (long long)grp * N;
-    const float *Cg = a.C + (long long)grp * N;
-    const long long tokN = (long long)a.G * N;
-
-    // ---- A3 staging of B, C and x for chunk c0 into buffer buf ----
-    auto stage = [&](int c0, int buf) {
-        const int t0 = c0 * geo.chunk;
-        const int cnt = min(geo.chunk, len - t0);
-        const long long tok0 = (long long)tok_start + t0;
-        {
-            int t = tid / N4, v = tid - (tid / N4) * N4;
-            const int dt_ = nthr / N4, dv = nthr - dt_ * N4;
-            for (; t < cnt;) {
-                const long long goff = (tok0 + t) * tokN + 4 * v;
-                cp_async16(sm.B(buf) + t * N + 4 * v, Bg + goff);
-                cp_async16(sm.C(buf) + t * N + 4 * v, Cg + goff);
-                t += dt_;
-                v += dv;
-                if (v >= N4) { v -= N4; ++t; }
-            }
-        }
-        {
-            int t = tid / nrows, r = tid - (tid / nrows) * nrows;
-            const int dt_ = nthr / nrows, dr = nthr - dt_ * nrows;
-            for (; t < cnt;) {
-                cp_async4(sm.X(buf) + t * geo.rows_per_cta + r, a.x + (tok0 + t) * HP + r0 + r);
-                t += dt_;
-                r += dr;
-                if (r >= nrows) { r -= nrows; ++t; }
-            }
-        }
-        cp_async_commit();
-    };
-
-    // ---- A4: dt of chunk c0 for this warp's heads (head hh goes to warp (hh + c0) % nwarps) ----
-    float dtp[kDtPerWarp];
-    auto load_dt = [&](int c0) {
-        const int t0 = c0 * geo.chunk;
-        const int cnt = min(geo.chunk, len - t0);
-        const int first = ((warp - c0) % nwarps + nwarps) % nwarps;
-#pragma unroll
-        for (int q = 0; q < kDtPerWarp; ++q) {
-            const int hh = first + q * nwarps;
-            dtp[q] = 0.f;
-            if (hh < nheads && lane < cnt)
-                dtp[q] = a.dt[((long long)tok_start + t0 + lane) * H + h0 + hh];
-        }
-    };
-    auto coefficients = [&](int c0, int buf) {
-        const int t0 = c0 * geo.chunk;
-        const int cnt = min(geo.chunk, len - t0);
-        const int first = ((warp - c0) % nwarps + nwarps) % nwarps;
-        int q = 0;
-        for (int hh = first; hh < nheads; hh += nwarps, ++q) {
-            float dtv;
-            if (q < kDtPerWarp) {
-                dtv = dtp[0];
-#pragma unroll
-                for (int qq = 1; qq < kDtPerWarp; ++qq)
-                    if (qq == q) dtv = dtp[qq];
-            } else {
-                dtv = lane < cnt ? a.dt[((long long)tok_start + t0 + lane) * H + h0 + hh] : 0.f;
-            }
-            chunk_coefficients(dtv, a.A[h0 + hh], cnt, lane, sm.Coef(buf) + hh, geo.heads_cap,
-                               sm.Mask(buf) + hh);
-        }
-    };
-
-    const int n_chunks = (len + geo.chunk - 1) / geo.chunk;
-    if (n_chunks > 0) {
-        stage(0, 0);
-        load_dt(0);
-        coefficients(0, 0);
-    }
-
     for (int c = 0; c < n_chunks; ++c) {
-        const int buf = c & 1;
-        const bool more = (c + 1) < n_chunks;
-        if (more) {
-            stage(c + 1, buf ^ 1);
-            load_dt(c + 1);
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
-        }
-        __syncthreads();
-
+        const int b = c & 1;
+        bar_sync(kBarFull + b, nthr);
         const int cnt = min(geo.chunk, len - c * geo.chunk);
-        const float *__restrict__ sB = sm.B(buf);
-        const float *__restrict__ sC = sm.C(buf);
-        const float *__restrict__ sX = sm.X(buf);
-        const float4 *__restrict__ sCf = sm.Coef(buf) + hl;
-        float *__restrict__ sPart = sm.Part() + j * sm.ps + row_raw;
+        const float *__restrict__ sB = sm.B(b);
+        const float *__restrict__ sC = sm.C(b);
+        const float *__restrict__ sX = sm.X(b);
+        const float4 *__restrict__ sCf = sm.Coef(b) + hl;
+        float *__restrict__ sPart = sm.Part(b) + j * sm.ps + row_raw;
 
         // Shared-memory operands of one token.
         struct TokenIn {
@@ -321,8 +353,7 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
                 }
             }
         };
-        // One token: U += (x dt / Lambda) B and this lane's part of U . C.  No
-        // cross-lane step: the lanes' parts are summed once per chunk.
+        // One token: U += (x dt / Lambda) B and this lane's part of U . C.
         auto compute_token = [&](const TokenIn &in, int tt) {
             float2 a2[RPT], acc[RPT][2];
 #pragma unroll
@@ -335,11 +366,11 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
             for (int k = 0; k < VPL; ++k) {
                 const int cidx = k * LANES + j;
                 if (EXACT || cidx < N4) {
-                    const float4 b = in.b[k], cc = in.c[k];
+                    const float4 bb = in.b[k], cc = in.c[k];
 #pragma unroll
                     for (int q = 0; q < RPT; ++q) {
-                        u[q][k][0] = __ffma2_rn(a2[q], f2(b.x, b.y), u[q][k][0]);      // A5
-                        u[q][k][1] = __ffma2_rn(a2[q], f2(b.z, b.w), u[q][k][1]);
+                        u[q][k][0] = __ffma2_rn(a2[q], f2(bb.x, bb.y), u[q][k][0]);      // A5
+                        u[q][k][1] = __ffma2_rn(a2[q], f2(bb.z, bb.w), u[q][k][1]);
                         acc[q][k & 1] = __ffma2_rn(u[q][k][0], f2(cc.x, cc.y), acc[q][k & 1]);   // A6
                         acc[q][k & 1] = __ffma2_rn(u[q][k][1], f2(cc.z, cc.w), acc[q][k & 1]);
                     }
@@ -359,7 +390,7 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
         // t+1 are read before token t is computed and its partial sums stored.
         unsigned amask = 0;
         for (int hh = 0; hh < nheads; ++hh)
-            amask |= sm.Mask(buf)[hh];
+            amask |= sm.Mask(b)[hh];
         TokenIn cur;
         load_token(0, cur);
         int tt = 0;
@@ -396,40 +427,7 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
                     u[q][k][1] = __fmul2_rn(u[q][k][1], l2);
                 }
         }
-        if (more)
-            coefficients(c + 1, buf ^ 1);
-        __syncthreads();
-
-        // A6 readout for the chunk: y = Lambda_t * (sum of the lanes' parts) + D x,
-        // four rows per thread and pass, stored coalesced along the rows.
-        {
-            const long long tok0 = (long long)tok_start + c * geo.chunk;
-            const int nq = (nrows + 3) >> 2;
-            const float *part = sm.Part();
-            const float4 *cfb = sm.Coef(buf);
-            for (int idx = tid; idx < cnt * nq; idx += nthr) {
-                const int t = idx / nq, q4 = idx - t * nq;
-                const float *pp = part + t * LANES * sm.ps + 4 * q4;
-                float2 s01 = f2(0.f, 0.f), s23 = s01;
-#pragma unroll 8
-                for (int l = 0; l < LANES; ++l) {
-                    const float4 v = *reinterpret_cast<const float4 *>(pp + l * sm.ps);
-                    s01 = __fadd2_rn(s01, f2(v.x, v.y));
-                    s23 = __fadd2_rn(s23, f2(v.z, v.w));
-                }
-                const float sum[4] = {s01.x, s01.y, s23.x, s23.y};
-                const long long yrow = (tok0 + t) * HP + r0;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int r = 4 * q4 + e;
-                    if (r < nrows) {
-                        const int hh = (r0 + r) / P - h0;
-                        const float lam = cfb[t * geo.heads_cap + hh].y;
-                        a.y[yrow + r] = fmaf(lam, sum[e], a.D[h0 + hh] * a.x[yrow + r]);
-                    }
-                }
-            }
-        }
+        bar_arrive(kBarDone + b, nthr);
     }
 
     // ---- A7 state store ----
@@ -454,7 +452,7 @@ template <int LANES, int VPL, int RPT>
 cudaError_t launch_scaled_one(const ScanArgs &a, const PrefillGeom &g, size_t smem, cudaStream_t stream)
 {
     const bool exact = (a.N / 4) == LANES * VPL;
-    const int threads = (g.rows_per_cta / RPT) * LANES;
+    const int threads = (g.rows_per_cta / RPT) * LANES + 32;     // consumers + one producer warp
     const dim3 grid((unsigned)((long long)a.n_seqs * a.G * g.runs_per_group));
     auto kern = exact ? prefill_scaled_kernel<LANES, VPL, RPT, true>
                       : prefill_scaled_kernel<LANES, VPL, RPT, false>;
