@@ -20,15 +20,15 @@
 //    back to S, so every chunk's coefficients are independent.
 //
 // 2. Warp specialisation.  The block has one producer warp and (rows/RPT)*LANES/32
-//    consumer warps.  Consumers only run the token loop: per token, U += alpha B
-//    and each lane's partial of U . C, stored to shared memory.  The producer,
-//    one chunk ahead, stages B, C and x with cp.async, computes the chunk's
-//    coefficients (lane = token: a warp prefix sum places the anchors, a
-//    segmented prefix product of dA = exp(dt*A) gives Lambda, ~1 ulp per
-//    factor), and, one chunk behind, sums the lanes' partials into y.  The two
-//    sides meet at named barriers (bar.arrive / bar.sync, hardware barriers with
-//    no spin loop): FULL[b] when a chunk's inputs are staged, DONE[b] when its
-//    partials are written; buffers alternate between two slots b.
+//    consumer warps.  The producer keeps two chunks of B, C and x in flight
+//    (cp.async into three slots) and computes each chunk's coefficients (lane =
+//    token: a warp prefix sum places the anchors, a segmented prefix product of
+//    dA = exp(dt*A) gives Lambda, ~1 ulp per factor).  Consumers run the token
+//    loop (per token U += alpha B and each lane's partial of U . C, stored to
+//    shared memory) and then sum their own rows' partials into y, which needs
+//    only the warp itself.  The two sides meet at named barriers (bar.arrive /
+//    bar.sync: hardware barriers, no spin loop): FULL[s] when slot s holds a
+//    staged chunk, EMPTY[s] when the consumers are done with it.
 //
 // The rescaling is an algebraic identity of the recurrence defined by "The
 // llama journey", Day 14 (decay exp(dt*A), input dt*x*B, y from the updated
@@ -40,8 +40,9 @@ namespace ssm {
 namespace {
 
 constexpr float kAnchorSpan = 40.f;
-constexpr int kBarFull = 1;       // named barriers kBarFull + b: inputs of slot b staged
-constexpr int kBarDone = 3;       // named barriers kBarDone + b: partials of slot b written
+constexpr int kSlots = 3;         // staging slots: two chunks in flight while one is consumed
+constexpr int kBarFull = 1;       // named barriers kBarFull + s: slot s staged
+constexpr int kBarEmpty = 4;      // named barriers kBarEmpty + s: slot s consumed
 
 __device__ __forceinline__ void bar_sync(int id, int nthreads)
 {
@@ -58,24 +59,26 @@ struct ScaledSmem {
     int cb, cx, cc, cm; // floats per buffer: B (= C), x, coefficients (float4 per token and
                         // head), anchor masks (one word per head)
     int ps;             // floats between the partial-sum rows of two lanes (see Part())
-    __device__ __forceinline__ float *B(int b) const { return base + b * cb; }
-    __device__ __forceinline__ float *C(int b) const { return base + 2 * cb + b * cb; }
-    __device__ __forceinline__ float *X(int b) const { return base + 4 * cb + b * cx; }
-    __device__ __forceinline__ float4 *Coef(int b) const
+    // slot s: [B | C | x | coefficients | anchor masks], each 16-byte aligned
+    __device__ __forceinline__ float *slot(int s) const { return base + s * (2 * cb + cx + cc + cm); }
+    __device__ __forceinline__ float *B(int s) const { return slot(s); }
+    __device__ __forceinline__ float *C(int s) const { return slot(s) + cb; }
+    __device__ __forceinline__ float *X(int s) const { return slot(s) + 2 * cb; }
+    __device__ __forceinline__ float4 *Coef(int s) const
     {
-        return reinterpret_cast<float4 *>(base + 4 * cb + 2 * cx + b * cc);
+        return reinterpret_cast<float4 *>(slot(s) + 2 * cb + cx);
     }
-    __device__ __forceinline__ unsigned *Mask(int b) const
+    __device__ __forceinline__ unsigned *Mask(int s) const
     {
-        return reinterpret_cast<unsigned *>(base + 4 * cb + 2 * cx + 2 * cc + b * cm);
+        return reinterpret_cast<unsigned *>(slot(s) + 2 * cb + cx + cc);
     }
     // Per-lane partial dot products of one chunk: [token][lane in row][ps] with
-    // the block's rows contiguous; ps = rows rounded up to 4, plus 4, so the 16-byte
-    // stores of eight lanes fall on eight different bank quads.  cp floats per slot.
-    int cp;
-    __device__ __forceinline__ float *Part(int b) const
+    // the block's rows contiguous (each consumer warp uses only its own rows);
+    // ps = rows rounded up to 4, plus 4, so the 16-byte stores of eight lanes fall
+    // on eight different bank quads.
+    __device__ __forceinline__ float *Part() const
     {
-        return base + 4 * cb + 2 * cx + 2 * cc + 2 * cm + b * cp;
+        return base + kSlots * (2 * cb + cx + cc + cm);
     }
 };
 
@@ -166,9 +169,9 @@ size_t prefill_scaled_smem_bytes(const PrefillGeom &g, int N, int lanes)
 {
     const size_t cx = ((size_t)g.chunk * g.rows_per_cta + 3) & ~(size_t)3;
     const size_t cm = ((size_t)g.heads_cap + 3) & ~(size_t)3;
-    const size_t per_buf = (size_t)g.chunk * (2 * (size_t)N + 4 * (size_t)g.heads_cap) + cx + cm;
+    const size_t per_slot = (size_t)g.chunk * (2 * (size_t)N + 4 * (size_t)g.heads_cap) + cx + cm;
     const size_t part = (size_t)g.chunk * lanes * (size_t)part_stride(g.rows_per_cta);
-    return (2 * per_buf + 2 * part) * sizeof(float);
+    return (kSlots * per_slot + part) * sizeof(float);
 }
 
 template <int LANES, int VPL, int RPT, bool EXACT>
@@ -185,7 +188,6 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
     sm.cc = geo.chunk * geo.heads_cap * 4;
     sm.cm = (geo.heads_cap + 3) & ~3;                    // keeps the partial sums 16-byte aligned
     sm.ps = part_stride(geo.rows_per_cta);
-    sm.cp = geo.chunk * LANES * sm.ps;
 
     // ---- A1 work mapping: (sequence, group, run of rows) ----
     const int ctas_per_seq = a.G * geo.runs_per_group;
@@ -240,59 +242,28 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
                                    sm.Mask(b) + hh);
             }
         };
-        // A6 readout of chunk c0: y = Lambda_t * (sum of the lanes' parts) + D x,
-        // four rows per lane and pass.
-        const int nq = (nrows + 3) >> 2;
-        auto readout = [&](int c0, int b) {
-            const int t0 = c0 * geo.chunk;
-            const int cnt = min(geo.chunk, len - t0);
-            const long long tok0 = (long long)tok_start + t0;
-            const float *part = sm.Part(b);
-            const float4 *cf = sm.Coef(b);
-            const float *sX = sm.X(b);
-            for (int idx = lane; idx < cnt * nq; idx += 32) {
-                const int t = idx / nq, q4 = idx - t * nq;
-                const float *pp = part + t * LANES * sm.ps + 4 * q4;
-                float2 s01 = f2(0.f, 0.f), s23 = s01;
-#pragma unroll 8
-                for (int l = 0; l < LANES; ++l) {
-                    const float4 v = *reinterpret_cast<const float4 *>(pp + l * sm.ps);
-                    s01 = __fadd2_rn(s01, f2(v.x, v.y));
-                    s23 = __fadd2_rn(s23, f2(v.z, v.w));
-                }
-                const float sum[4] = {s01.x, s01.y, s23.x, s23.y};
-                float *yrow = a.y + (tok0 + t) * HP + r0;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int r = 4 * q4 + e;
-                    if (r < nrows) {
-                        const int hh = (r0 + r) / P - h0;
-                        const float lam = cf[t * geo.heads_cap + hh].y;
-                        yrow[r] = fmaf(lam, sum[e], __ldg(a.D + h0 + hh) * sX[t * geo.rows_per_cta + r]);
-                    }
-                }
-            }
-        };
-
-        if (n_chunks > 0) {
+        // Staging runs two chunks ahead: chunks k and k+1 are in flight while the
+        // consumers work on chunk k-1.  A slot is refilled only after EMPTY says
+        // the consumers are done with the chunk three back.
+        if (n_chunks > 0)
             stage(0, 0);
-            coefficients(0, 0);
-            cp_async_wait<0>();
-            __syncwarp();
-            bar_arrive(kBarFull + 0, nthr);
-        }
-        for (int c = 0; c < n_chunks; ++c) {
-            if (c + 1 < n_chunks) {       // slot (c+1)&1 was released by DONE of chunk c-1
-                const int b = (c + 1) & 1;
-                stage(c + 1, b);
-                coefficients(c + 1, b);
+        if (n_chunks > 1)
+            stage(1, 1);
+        for (int k = 0; k < n_chunks; ++k) {
+            const int s = k % kSlots;
+            coefficients(k, s);
+            if (k + 1 < n_chunks)
+                cp_async_wait<1>();          // chunk k landed, chunk k+1 may still fly
+            else
                 cp_async_wait<0>();
-                __syncwarp();
-                bar_arrive(kBarFull + b, nthr);
-            }
-            bar_sync(kBarDone + (c & 1), nthr);
-            readout(c, c & 1);
             __syncwarp();
+            bar_arrive(kBarFull + s, nthr);
+            if (k + 2 < n_chunks) {
+                const int s2 = (k + 2) % kSlots;
+                if (k >= 1)                   // chunk k-1 used slot s2
+                    bar_sync(kBarEmpty + s2, nthr);
+                stage(k + 2, s2);
+            }
         }
         return;
     }
@@ -323,15 +294,34 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
         }
     }
 
+    // Readout geometry of this warp: its rows [wr0, wr0 + kRowsPerWarp).  With
+    // four or more rows a lane sums a fixed quad of rows (16-byte reads), else a
+    // fixed single row; either way its heads and D are fixed too.
+    constexpr int kRowsPerWarp = (32 / LANES) * RPT;
+    constexpr int kVec = (kRowsPerWarp % 4 == 0) ? 4 : 1;
+    constexpr int kItems = kRowsPerWarp / kVec;          // row groups per token
+    static_assert(kItems <= 32 && (32 % kItems) == 0, "readout mapping");
+    const int wr0 = warp * kRowsPerWarp;
+    const int my_item = lane % kItems;
+    const int rq = wr0 + kVec * my_item;                 // first row of this lane's group
+    int q_head[kVec];
+    float q_D[kVec];
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) {
+        const int r = min(rq + e, nrows - 1);
+        q_head[e] = (r0 + r) / P - h0;
+        q_D[e] = __ldg(a.D + h0 + q_head[e]);
+    }
+
     for (int c = 0; c < n_chunks; ++c) {
-        const int b = c & 1;
+        const int b = c % kSlots;
         bar_sync(kBarFull + b, nthr);
         const int cnt = min(geo.chunk, len - c * geo.chunk);
         const float *__restrict__ sB = sm.B(b);
         const float *__restrict__ sC = sm.C(b);
         const float *__restrict__ sX = sm.X(b);
         const float4 *__restrict__ sCf = sm.Coef(b) + hl;
-        float *__restrict__ sPart = sm.Part(b) + j * sm.ps + row_raw;
+        float *__restrict__ sPart = sm.Part() + j * sm.ps + row_raw;
 
         // Shared-memory operands of one token.
         struct TokenIn {
@@ -427,7 +417,45 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
                     u[q][k][1] = __fmul2_rn(u[q][k][1], l2);
                 }
         }
-        bar_arrive(kBarDone + b, nthr);
+        // A6 readout of this warp's rows: y = Lambda_t (sum of the lanes' parts) + D x.
+        __syncwarp();
+        {
+            const long long tok0 = (long long)tok_start + c * geo.chunk;
+            const float *part = sm.Part() + rq;
+            const float4 *cfb = sm.Coef(b);
+            for (int t = lane / kItems; t < cnt; t += 32 / kItems) {
+                const float *pp = part + t * LANES * sm.ps;
+                float sum[kVec];
+                if constexpr (kVec == 4) {
+                    float2 s01 = f2(0.f, 0.f), s23 = s01;
+#pragma unroll
+                    for (int l = 0; l < LANES; ++l) {
+                        const float4 v = *reinterpret_cast<const float4 *>(pp + l * sm.ps);
+                        s01 = __fadd2_rn(s01, f2(v.x, v.y));
+                        s23 = __fadd2_rn(s23, f2(v.z, v.w));
+                    }
+                    sum[0] = s01.x; sum[1] = s01.y; sum[2] = s23.x; sum[3] = s23.y;
+                } else {
+                    float acc = 0.f;
+#pragma unroll
+                    for (int l = 0; l < LANES; ++l)
+                        acc += pp[l * sm.ps];
+                    sum[0] = acc;
+                }
+                float *yrow = a.y + (tok0 + t) * HP + r0;
+#pragma unroll
+                for (int e = 0; e < kVec; ++e) {
+                    const int r = rq + e;
+                    if (r < nrows) {
+                        const float lam = cfb[t * geo.heads_cap + q_head[e]].y;
+                        yrow[r] = fmaf(lam, sum[e], q_D[e] * sX[t * geo.rows_per_cta + r]);
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (c + kSlots < n_chunks)          // the producer refills this slot with chunk c+3
+            bar_arrive(kBarEmpty + b, nthr);
     }
 
     // ---- A7 state store ----
