@@ -215,29 +215,51 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
         const float *Cg = a.C + (long long)grp * N;
         const long long tokN = (long long)a.G * N;
         // A3: stage B, C and x of chunk c0 into slot b (cp.async, this warp only)
+        // Per-lane walk over (token, column) items in steps of 32 without
+        // divisions: start at (lane / width, lane % width), step (32 / width, 32 % width).
+        const int bt0 = lane / N4, bv0 = lane - bt0 * N4, bdt = 32 / N4, bdv = 32 - bdt * N4;
+        const int xt0 = lane / nrows, xv0 = lane - xt0 * nrows, xdt = 32 / nrows, xdv = 32 - xdt * nrows;
         auto stage = [&](int c0, int b) {
             const int t0 = c0 * geo.chunk;
             const int cnt = min(geo.chunk, len - t0);
             const long long tok0 = (long long)tok_start + t0;
             float *sB = sm.B(b), *sC = sm.C(b), *sX = sm.X(b);
-            for (int idx = lane; idx < cnt * N4; idx += 32) {
-                const int t = idx / N4, v = idx - t * N4;
+            for (int t = bt0, v = bv0; t < cnt;) {
                 const long long goff = (tok0 + t) * tokN + 4 * v;
                 cp_async16(sB + t * N + 4 * v, Bg + goff);
                 cp_async16(sC + t * N + 4 * v, Cg + goff);
+                t += bdt;
+                v += bdv;
+                if (v >= N4) { v -= N4; ++t; }
             }
-            for (int idx = lane; idx < cnt * nrows; idx += 32) {
-                const int t = idx / nrows, r = idx - t * nrows;
+            for (int t = xt0, r = xv0; t < cnt;) {
                 cp_async4(sX + t * geo.rows_per_cta + r, a.x + (tok0 + t) * HP + r0 + r);
+                t += xdt;
+                r += xdv;
+                if (r >= nrows) { r -= nrows; ++t; }
             }
             cp_async_commit();
         };
-        // A4: coefficients of chunk c0 for every head of the block
-        auto coefficients = [&](int c0, int b) {
+        // A4: dt of chunk c0 (lane = token) for the first kDtHeads heads, read two
+        // chunks before its coefficients are needed.
+        constexpr int kDtHeads = 4;
+        auto load_dt = [&](int c0, float (&d)[kDtHeads]) {
+            const int t0 = c0 * geo.chunk;
+            const int cnt = min(geo.chunk, len - t0);
+#pragma unroll
+            for (int q = 0; q < kDtHeads; ++q)
+                d[q] = (q < nheads && lane < cnt) ? a.dt[((long long)tok_start + t0 + lane) * H + h0 + q] : 0.f;
+        };
+        auto coefficients = [&](int c0, int b, const float (&d)[kDtHeads]) {
             const int t0 = c0 * geo.chunk;
             const int cnt = min(geo.chunk, len - t0);
             for (int hh = 0; hh < nheads; ++hh) {
-                const float dtv = lane < cnt ? a.dt[((long long)tok_start + t0 + lane) * H + h0 + hh] : 0.f;
+                float dtv = d[0];
+#pragma unroll
+                for (int q = 1; q < kDtHeads; ++q)
+                    if (hh == q) dtv = d[q];
+                if (hh >= kDtHeads)
+                    dtv = lane < cnt ? a.dt[((long long)tok_start + t0 + lane) * H + h0 + hh] : 0.f;
                 chunk_coefficients(dtv, a.A[h0 + hh], cnt, lane, sm.Coef(b) + hh, geo.heads_cap,
                                    sm.Mask(b) + hh);
             }
@@ -245,13 +267,20 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
         // Staging runs two chunks ahead: chunks k and k+1 are in flight while the
         // consumers work on chunk k-1.  A slot is refilled only after EMPTY says
         // the consumers are done with the chunk three back.
-        if (n_chunks > 0)
+        float dt0[kDtHeads], dt1[kDtHeads], dt2[kDtHeads];
+        if (n_chunks > 0) {
             stage(0, 0);
-        if (n_chunks > 1)
+            load_dt(0, dt0);
+        }
+        if (n_chunks > 1) {
             stage(1, 1);
+            load_dt(1, dt1);
+        }
         for (int k = 0; k < n_chunks; ++k) {
             const int s = k % kSlots;
-            coefficients(k, s);
+            if (k + 2 < n_chunks)
+                load_dt(k + 2, dt2);
+            coefficients(k, s, dt0);
             if (k + 1 < n_chunks)
                 cp_async_wait<1>();          // chunk k landed, chunk k+1 may still fly
             else
@@ -263,6 +292,11 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
                 if (k >= 1)                   // chunk k-1 used slot s2
                     bar_sync(kBarEmpty + s2, nthr);
                 stage(k + 2, s2);
+            }
+#pragma unroll
+            for (int q = 0; q < kDtHeads; ++q) {
+                dt0[q] = dt1[q];
+                dt1[q] = dt2[q];
             }
         }
         return;
