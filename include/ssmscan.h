@@ -105,6 +105,9 @@ enum {
  *                    at most 32 on SSM_PATH_PREFILL)
  *   ctas_per_sm      decode: if > 0, the grid is capped at this many blocks
  *                    per SM and warps loop over the remaining rows
+ *   segment_tokens   SSM_PATH_PREFILL with a workspace (ssm_scan_ws): length of
+ *                    the time segments long sequences are cut into (a multiple
+ *                    of the chunk); 0 = automatic, < 0 = never segment
  */
 typedef struct {
     int path;
@@ -113,6 +116,7 @@ typedef struct {
     int rows_per_cta;
     int chunk_tokens;
     int ctas_per_sm;
+    int segment_tokens;
 } ssm_scan_tuning;
 
 /*
@@ -135,6 +139,38 @@ int ssm_scan_tuned(float *state_slots, const float *x, const float *dt,
                    int n_seqs, int n_tokens, int n_heads, int head_dim,
                    int d_state, int n_groups, const ssm_scan_tuning *tuning,
                    void *stream);
+
+/*
+ * The scan with a caller-owned device workspace.  With a workspace the
+ * prefill path may cut long sequences into time segments and run them in
+ * parallel: a state-only pass per segment, a combine of the segment states
+ * (S_in[k+1] = d_k S_in[k] + L_k, d_k the segment's decay prod exp(dt*A)),
+ * then the full pass from each segment's incoming state.  This is the same
+ * recurrence applied to whole segments; only float association changes.
+ *   tuning          may be NULL
+ *   workspace       device memory, 256-byte aligned, at least
+ *                   ssm_scan_workspace_bytes(...) bytes for the same arguments
+ *                   and tuning; NULL or too small: runs without segments
+ *                   (SSM_ERR_INVALID_ARG if tuning->segment_tokens > 0)
+ * The workspace is scratch: its contents are undefined afterwards and two
+ * calls that overlap on the GPU must not share it.
+ */
+int ssm_scan_ws(float *state_slots, const float *x, const float *dt,
+                const float *A, const float *B, const float *C, const float *D,
+                float *y, const int32_t *seq_starts, const int32_t *seq_lens,
+                const int32_t *resume_flags, int n_seqs, int n_tokens,
+                int n_heads, int head_dim, int d_state, int n_groups,
+                const ssm_scan_tuning *tuning, void *workspace,
+                size_t workspace_bytes, void *stream);
+
+/*
+ * Bytes of workspace ssm_scan_ws uses for these sizes and tuning (NULL =
+ * automatic) on the current device; 0 when it would not cut any sequence into
+ * segments (for example decode batches) or the arguments are invalid.
+ */
+size_t ssm_scan_workspace_bytes(int n_seqs, int n_tokens, int n_heads,
+                                int head_dim, int d_state, int n_groups,
+                                const ssm_scan_tuning *tuning);
 
 /* Text for a status code (static storage; never NULL). */
 const char *ssm_status_string(int status);

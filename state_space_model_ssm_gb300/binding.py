@@ -40,7 +40,8 @@ class Tuning(ctypes.Structure):
     """Launch-shape overrides (``ssm_scan_tuning``); zero fields mean automatic."""
     _fields_ = [("path", ctypes.c_int), ("lanes_per_row", ctypes.c_int),
                 ("rows_per_thread", ctypes.c_int), ("rows_per_cta", ctypes.c_int),
-                ("chunk_tokens", ctypes.c_int), ("ctas_per_sm", ctypes.c_int)]
+                ("chunk_tokens", ctypes.c_int), ("ctas_per_sm", ctypes.c_int),
+                ("segment_tokens", ctypes.c_int)]
 
 
 _P = ctypes.c_void_p
@@ -62,6 +63,10 @@ def load():
             lib.ssm_scan.argtypes = _SCAN_ARGS + [_P]
             lib.ssm_scan_tuned.restype = _I
             lib.ssm_scan_tuned.argtypes = _SCAN_ARGS + [ctypes.POINTER(Tuning), _P]
+            lib.ssm_scan_ws.restype = _I
+            lib.ssm_scan_ws.argtypes = _SCAN_ARGS + [ctypes.POINTER(Tuning), _P, ctypes.c_size_t, _P]
+            lib.ssm_scan_workspace_bytes.restype = ctypes.c_size_t
+            lib.ssm_scan_workspace_bytes.argtypes = [_I] * 6 + [ctypes.POINTER(Tuning)]
             lib.ssm_status_string.restype = ctypes.c_char_p
             lib.ssm_status_string.argtypes = [_I]
             _lib = lib
@@ -85,15 +90,29 @@ def declared_functions(header: str = HEADER):
 
 def scan_raw(state, x, dt, A, B, C, D, y, seq_starts, seq_lens, resume,
              n_seqs, n_tokens, n_heads, head_dim, d_state, n_groups,
-             stream=0, tuning: Tuning | None = None) -> int:
-    """Call the C ABI with integer pointers; returns the status code."""
+             stream=0, tuning: Tuning | None = None, workspace=None, workspace_bytes=0) -> int:
+    """Call the C ABI with integer pointers; returns the status code.
+    With `workspace` (a device pointer) the call goes through ssm_scan_ws."""
     lib = load()
     args = [_P(int(p) if p else None) for p in
             (state, x, dt, A, B, C, D, y, seq_starts, seq_lens, resume)]
     args += [int(n_seqs), int(n_tokens), int(n_heads), int(head_dim), int(d_state), int(n_groups)]
+    st = _P(int(stream) if stream else None)
+    if workspace is not None:
+        tp = ctypes.byref(tuning) if tuning is not None else None
+        return lib.ssm_scan_ws(*args, tp, _P(int(workspace) if workspace else None),
+                               ctypes.c_size_t(int(workspace_bytes)), st)
     if tuning is None:
-        return lib.ssm_scan(*args, _P(int(stream) if stream else None))
-    return lib.ssm_scan_tuned(*args, ctypes.byref(tuning), _P(int(stream) if stream else None))
+        return lib.ssm_scan(*args, st)
+    return lib.ssm_scan_tuned(*args, ctypes.byref(tuning), st)
+
+
+def workspace_bytes(n_seqs, n_tokens, n_heads, head_dim, d_state, n_groups,
+                    tuning: Tuning | None = None) -> int:
+    """Bytes of workspace ssm_scan_ws uses for these sizes on the current device."""
+    tp = ctypes.byref(tuning) if tuning is not None else None
+    return int(load().ssm_scan_workspace_bytes(int(n_seqs), int(n_tokens), int(n_heads),
+                                               int(head_dim), int(d_state), int(n_groups), tp))
 
 
 def _check(t, name, dtype, device, shape=None):
@@ -110,12 +129,14 @@ def _check(t, name, dtype, device, shape=None):
 
 
 def ssm_scan(state_slots, x, dt, A, B, C, D, seq_starts, seq_lens, resume_flags,
-             y=None, *, tuning: Tuning | None = None, stream=None):
+             y=None, *, tuning: Tuning | None = None, stream=None, workspace=None):
     """Run the scan on the current CUDA stream (or ``stream``).
 
     state_slots [n,H,P,N] fp32 (updated in place), x [T,H,P], dt [T,H], A [H],
     B/C [T,G,N], D [H] fp32; seq_starts/seq_lens/resume_flags [n] int32; all on
     one CUDA device.  Returns y [T,H,P] (allocated if not given).
+    workspace: optional uint8 CUDA tensor (see ``workspace_bytes``); lets long
+    sequences run as parallel time segments.
     """
     dev = state_slots.device
     if dev.type != "cuda":
@@ -139,11 +160,17 @@ def ssm_scan(state_slots, x, dt, A, B, C, D, seq_starts, seq_lens, resume_flags,
     if stream is None:
         stream = torch.cuda.current_stream(dev)
     handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        if workspace.device != dev or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous tensor on the scan's device")
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
     with torch.cuda.device(dev):
         rc = scan_raw(state_slots.data_ptr(), x.data_ptr(), dt.data_ptr(), A.data_ptr(),
                       B.data_ptr(), C.data_ptr(), D.data_ptr(), y.data_ptr(),
                       seq_starts.data_ptr(), seq_lens.data_ptr(), resume_flags.data_ptr(),
-                      n, T, H, P, N, G, stream=handle, tuning=tuning)
+                      n, T, H, P, N, G, stream=handle, tuning=tuning,
+                      workspace=ws_ptr, workspace_bytes=ws_bytes)
     if rc != SSM_OK:
         raise SsmScanError(rc, "ssm_scan")
     return y

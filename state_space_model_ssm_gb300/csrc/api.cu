@@ -99,10 +99,143 @@ int check_metadata(const ssm::ScanArgs &a, cudaStream_t stream)
     return SSM_OK;
 }
 
+// Launch shape and segment plan of the prefill path.
+struct PrefillPlan {
+    bool scaled = true;
+    int lanes = 0, rpt = 0, vpl = 0;
+    ssm::PrefillGeom g{};
+    size_t smem = 0;
+    int seg_len = 0;              // 0: no time segments
+    long long max_units = 0;      // upper bound of (sequence, segment) units
+    size_t ws_bytes = 0;          // workspace the segment plan needs
+    // workspace offsets (bytes)
+    size_t off_units = 0, off_n_units = 0, off_unit_base = 0, off_decay = 0, off_state = 0;
+};
+
+size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+// Shapes for the prefill kernels; also the time-segment plan when segments
+// are allowed.  Returns SSM_OK or an error status (no launch happens here).
+int plan_prefill(const ssm_scan_tuning &t, bool scaled, int n_seqs, int n_tokens, int H, int P, int N,
+                 int G, const DeviceInfo &dev, bool allow_segments, PrefillPlan *out)
+{
+    PrefillPlan pl;
+    pl.scaled = scaled;
+    const int N4 = N / 4;
+    auto supported = scaled ? ssm::prefill_scaled_supported : ssm::prefill_supported;
+    int lanes, rpt;
+    if (scaled) {
+        // About 8 state elements of a row per lane, and up to 4 rows per lane
+        // (32 state registers) so that each B/C value read from shared memory
+        // feeds several rows.  The rows of a lane must share a head: RPT | P.
+        lanes = t.lanes_per_row ? t.lanes_per_row : std::min(32, pow2ceil((N + 7) / 8));
+        rpt = t.rows_per_thread;
+        if (!rpt) {
+            rpt = 4;
+            while (rpt > 1 && (P % rpt != 0 || rpt > lanes ||
+                               pick_vpl(N4, lanes, rpt, supported) * 4 * rpt > 32 ||
+                               pick_vpl(N4, lanes, rpt, supported) == 0))
+                rpt >>= 1;
+        }
+        if (P % rpt != 0)
+            return SSM_ERR_INVALID_ARG;
+    } else {
+        lanes = t.lanes_per_row ? t.lanes_per_row : std::min(32, pow2ceil((N + 31) / 32));
+        rpt = t.rows_per_thread ? t.rows_per_thread : 1;
+    }
+    const int vpl = pick_vpl(N4, lanes, rpt, supported);
+    if (rpt > lanes || vpl == 0)
+        return SSM_ERR_INVALID_ARG;
+    if (scaled && t.chunk_tokens > ssm::kScaledMaxChunk)
+        return SSM_ERR_INVALID_ARG;
+    auto smem_of = [&](const ssm::PrefillGeom &gg) {
+        return scaled ? ssm::prefill_scaled_smem_bytes(gg, N, lanes) : ssm::prefill_smem_bytes(gg, N);
+    };
+    const int rows_per_warp = (32 / lanes) * rpt;
+    ssm::PrefillGeom &g = pl.g;
+    g.rows_per_group = (H / G) * P;
+    if (t.rows_per_cta) {
+        // the rescaled kernel adds one producer warp to the block's 256 threads
+        if (t.rows_per_cta % rows_per_warp != 0 || (t.rows_per_cta / rpt) * lanes > (scaled ? 224 : 256))
+            return SSM_ERR_INVALID_ARG;
+        g.rows_per_cta = t.rows_per_cta;
+    } else {
+        // Largest block (up to 4 warps) that still gives every SM a block.
+        int warps = 4;
+        while (warps > 1) {
+            const long long runs = (g.rows_per_group + warps * rows_per_warp - 1) / (warps * rows_per_warp);
+            if ((long long)n_seqs * G * runs >= dev.sms)
+                break;
+            warps >>= 1;
+        }
+        g.rows_per_cta = warps * rows_per_warp;
+    }
+    const int threads = (g.rows_per_cta / rpt) * lanes;
+    g.runs_per_group = (g.rows_per_group + g.rows_per_cta - 1) / g.rows_per_cta;
+    g.heads_cap = (P + g.rows_per_cta - 2) / P + 1;
+    // The direct kernel carries one chunk's dt in 4 registers per thread.
+    const int dt_cap = scaled ? INT_MAX : 4 * threads;
+    // Two blocks per SM fit in the 228 KB of shared memory (1 KB per block is reserved).
+    const size_t smem_cap = (size_t)(N > 256 ? dev.smem_optin : std::min(dev.smem_optin, 113 * 1024));
+    if (t.chunk_tokens) {
+        g.chunk = t.chunk_tokens;
+        if ((long long)g.chunk * g.heads_cap > dt_cap || smem_of(g) > (size_t)dev.smem_optin)
+            return SSM_ERR_INVALID_ARG;
+    } else {
+        g.chunk = scaled ? 16 : 32;
+        while (g.chunk > 1 && ((long long)g.chunk * g.heads_cap > dt_cap || smem_of(g) > smem_cap))
+            g.chunk >>= 1;
+        if (smem_of(g) > (size_t)dev.smem_optin)
+            return SSM_ERR_UNSUPPORTED;
+    }
+    pl.smem = smem_of(g);
+    pl.lanes = lanes;
+    pl.rpt = rpt;
+    pl.vpl = vpl;
+
+    // Time segments: only the rescaled kernel has the state pass.  Automatic
+    // choice: enough (sequence, segment) units for about three consumer warps
+    // per SM sub-partition.
+    if (scaled && allow_segments && t.segment_tokens >= 0 && n_tokens > 0) {
+        int seg = 0;
+        if (t.segment_tokens > 0) {
+            if (t.segment_tokens % g.chunk != 0)
+                return SSM_ERR_INVALID_ARG;
+            seg = t.segment_tokens;
+        } else {
+            const long long warps_per_unit = (long long)G * g.runs_per_group * (threads / 32);
+            const long long target = 3LL * 4 * dev.sms;
+            if ((long long)n_seqs * warps_per_unit < target) {
+                const long long want = (target + warps_per_unit - 1) / warps_per_unit;
+                long long L = ((long long)n_tokens + want - 1) / want;
+                L = std::max<long long>(L, 4LL * g.chunk);
+                seg = (int)(((L + g.chunk - 1) / g.chunk) * g.chunk);
+                if (seg >= n_tokens)
+                    seg = 0;
+            }
+        }
+        if (seg > 0) {
+            pl.seg_len = seg;
+            pl.max_units = (long long)n_seqs + ((long long)n_tokens + seg - 1) / seg;
+            const size_t slot = (size_t)H * P * N * sizeof(float);
+            size_t off = 0;
+            pl.off_units = off;      off = align256(off + (size_t)pl.max_units * sizeof(int2));
+            pl.off_n_units = off;    off = align256(off + sizeof(int));
+            pl.off_unit_base = off;  off = align256(off + ((size_t)n_seqs + 1) * sizeof(int));
+            pl.off_decay = off;      off = align256(off + (size_t)pl.max_units * H * sizeof(float));
+            pl.off_state = off;      off = align256(off + (size_t)pl.max_units * slot);
+            pl.ws_bytes = off;
+        }
+    }
+    *out = pl;
+    return SSM_OK;
+}
+
 int scan_impl(float *state, const float *x, const float *dt, const float *A, const float *B,
               const float *C, const float *D, float *y, const int32_t *seq_starts,
               const int32_t *seq_lens, const int32_t *resume, int n_seqs, int n_tokens,
-              int H, int P, int N, int G, const ssm_scan_tuning *tun, void *stream_v)
+              int H, int P, int N, int G, const ssm_scan_tuning *tun, void *workspace,
+              size_t workspace_bytes, void *stream_v)
 {
     // ---- host-checkable arguments ----
     if (n_seqs < 0 || n_tokens < 0 || H <= 0 || P <= 0 || N <= 0 || G <= 0)
@@ -188,79 +321,43 @@ int scan_impl(float *state, const float *x, const float *dt, const float *A, con
 
     // ---- prefill ----
     const bool scaled = (path == SSM_PATH_PREFILL);
-    auto supported = scaled ? ssm::prefill_scaled_supported : ssm::prefill_supported;
-    int lanes, rpt, vpl;
-    if (scaled) {
-        // About 8 state elements of a row per lane, and up to 4 rows per lane
-        // (32 state registers) so that each B/C value read from shared memory
-        // feeds several rows.  The rows of a lane must share a head: RPT | P.
-        lanes = t.lanes_per_row ? t.lanes_per_row : std::min(32, pow2ceil((N + 7) / 8));
-        rpt = t.rows_per_thread;
-        if (!rpt) {
-            rpt = 4;
-            while (rpt > 1 && (P % rpt != 0 || rpt > lanes ||
-                               pick_vpl(N4, lanes, rpt, supported) * 4 * rpt > 32 ||
-                               pick_vpl(N4, lanes, rpt, supported) == 0))
-                rpt >>= 1;
-        }
-        if (P % rpt != 0)
-            return SSM_ERR_INVALID_ARG;
-    } else {
-        lanes = t.lanes_per_row ? t.lanes_per_row : std::min(32, pow2ceil((N + 31) / 32));
-        rpt = t.rows_per_thread ? t.rows_per_thread : 1;
+    PrefillPlan pl;
+    rc = plan_prefill(t, scaled, n_seqs, n_tokens, H, P, N, G, dev, workspace != nullptr, &pl);
+    if (rc != SSM_OK)
+        return rc;
+    if (pl.seg_len > 0 && (workspace_bytes < pl.ws_bytes || !aligned(workspace, 256))) {
+        if (t.segment_tokens > 0)
+            return SSM_ERR_INVALID_ARG;     // explicit segments need the workspace
+        pl.seg_len = 0;                     // automatic: run without segments
     }
-    vpl = pick_vpl(N4, lanes, rpt, supported);
-    if (rpt > lanes || vpl == 0)
-        return SSM_ERR_INVALID_ARG;
-    if (scaled && t.chunk_tokens > ssm::kScaledMaxChunk)
-        return SSM_ERR_INVALID_ARG;
-    auto smem_of = [&](const ssm::PrefillGeom &gg) {
-        return scaled ? ssm::prefill_scaled_smem_bytes(gg, N, lanes) : ssm::prefill_smem_bytes(gg, N);
-    };
-    const int rows_per_warp = (32 / lanes) * rpt;
-    ssm::PrefillGeom g;
-    g.rows_per_group = (H / G) * P;
-    if (t.rows_per_cta) {
-        // the rescaled kernel adds one producer warp to the block's 256 threads
-        if (t.rows_per_cta % rows_per_warp != 0 || (t.rows_per_cta / rpt) * lanes > (scaled ? 224 : 256))
-            return SSM_ERR_INVALID_ARG;
-        g.rows_per_cta = t.rows_per_cta;
-    } else {
-        // Largest block (up to 4 warps) that still gives every SM a block.
-        int warps = 4;
-        while (warps > 1) {
-            const long long runs = (g.rows_per_group + warps * rows_per_warp - 1) / (warps * rows_per_warp);
-            if ((long long)n_seqs * G * runs >= dev.sms)
-                break;
-            warps >>= 1;
-        }
-        g.rows_per_cta = warps * rows_per_warp;
-    }
-    const int threads = (g.rows_per_cta / rpt) * lanes;
-    g.runs_per_group = (g.rows_per_group + g.rows_per_cta - 1) / g.rows_per_cta;
-    g.heads_cap = (P + g.rows_per_cta - 2) / P + 1;
-    const long long n_ctas = (long long)n_seqs * G * g.runs_per_group;
-    if (n_ctas > INT_MAX)
+    if (pl.max_units * G * pl.g.runs_per_group > INT_MAX || (long long)n_seqs * G * pl.g.runs_per_group > INT_MAX)
         return SSM_ERR_UNSUPPORTED;
-    // The direct kernel carries one chunk's dt in 4 registers per thread.
-    const int dt_cap = scaled ? INT_MAX : 4 * threads;
-    // Two blocks per SM fit in the 228 KB of shared memory (1 KB per block is reserved).
-    const size_t smem_cap = (size_t)(N > 256 ? dev.smem_optin : std::min(dev.smem_optin, 113 * 1024));
-    if (t.chunk_tokens) {
-        g.chunk = t.chunk_tokens;
-        if ((long long)g.chunk * g.heads_cap > dt_cap || smem_of(g) > (size_t)dev.smem_optin)
-            return SSM_ERR_INVALID_ARG;
-    } else {
-        g.chunk = scaled ? 16 : 32;
-        while (g.chunk > 1 && ((long long)g.chunk * g.heads_cap > dt_cap || smem_of(g) > smem_cap))
-            g.chunk >>= 1;
-        if (smem_of(g) > (size_t)dev.smem_optin)
-            return SSM_ERR_UNSUPPORTED;
+    if (!scaled) {
+        if (ssm::launch_prefill(a, pl.g, pl.lanes, pl.vpl, pl.rpt, pl.smem, dev.sms, stream) != cudaSuccess)
+            return SSM_ERR_CUDA;
+        return SSM_OK;
     }
-    const size_t smem = smem_of(g);
-    const cudaError_t e = scaled ? ssm::launch_prefill_scaled(a, g, lanes, vpl, rpt, smem, stream)
-                                 : ssm::launch_prefill(a, g, lanes, vpl, rpt, smem, dev.sms, stream);
-    if (e != cudaSuccess)
+    ssm::SegmentPlan plan{};
+    if (pl.seg_len == 0) {
+        if (ssm::launch_prefill_scaled(a, pl.g, pl.lanes, pl.vpl, pl.rpt, plan, ssm::kScanFull, n_seqs,
+                                       pl.smem, stream) != cudaSuccess)
+            return SSM_ERR_CUDA;
+        return SSM_OK;
+    }
+    char *ws = static_cast<char *>(workspace);
+    plan.units = reinterpret_cast<const int2 *>(ws + pl.off_units);
+    plan.n_units = reinterpret_cast<const int *>(ws + pl.off_n_units);
+    plan.unit_base = reinterpret_cast<const int *>(ws + pl.off_unit_base);
+    plan.seg_len = pl.seg_len;
+    plan.seg_decay = reinterpret_cast<float *>(ws + pl.off_decay);
+    plan.seg_state = reinterpret_cast<float *>(ws + pl.off_state);
+    const int mu = (int)pl.max_units;
+    if (ssm::launch_segment_plan(a, plan, mu, stream) != cudaSuccess ||
+        ssm::launch_prefill_scaled(a, pl.g, pl.lanes, pl.vpl, pl.rpt, plan, ssm::kScanStateOnly, mu, pl.smem,
+                                   stream) != cudaSuccess ||
+        ssm::launch_segment_combine(a, plan, mu, stream) != cudaSuccess ||
+        ssm::launch_prefill_scaled(a, pl.g, pl.lanes, pl.vpl, pl.rpt, plan, ssm::kScanFull, mu, pl.smem,
+                                   stream) != cudaSuccess)
         return SSM_ERR_CUDA;
     return SSM_OK;
 }
@@ -275,7 +372,7 @@ int ssm_scan(float *state_slots, const float *x, const float *dt, const float *A
              int n_heads, int head_dim, int d_state, int n_groups, void *stream)
 {
     return scan_impl(state_slots, x, dt, A, B, C, D, y, seq_starts, seq_lens, resume_flags, n_seqs,
-                     n_tokens, n_heads, head_dim, d_state, n_groups, nullptr, stream);
+                     n_tokens, n_heads, head_dim, d_state, n_groups, nullptr, nullptr, 0, stream);
 }
 
 int ssm_scan_tuned(float *state_slots, const float *x, const float *dt, const float *A,
@@ -285,7 +382,42 @@ int ssm_scan_tuned(float *state_slots, const float *x, const float *dt, const fl
                    const ssm_scan_tuning *tuning, void *stream)
 {
     return scan_impl(state_slots, x, dt, A, B, C, D, y, seq_starts, seq_lens, resume_flags, n_seqs,
-                     n_tokens, n_heads, head_dim, d_state, n_groups, tuning, stream);
+                     n_tokens, n_heads, head_dim, d_state, n_groups, tuning, nullptr, 0, stream);
+}
+
+int ssm_scan_ws(float *state_slots, const float *x, const float *dt, const float *A, const float *B,
+                const float *C, const float *D, float *y, const int32_t *seq_starts,
+                const int32_t *seq_lens, const int32_t *resume_flags, int n_seqs, int n_tokens,
+                int n_heads, int head_dim, int d_state, int n_groups, const ssm_scan_tuning *tuning,
+                void *workspace, size_t workspace_bytes, void *stream)
+{
+    return scan_impl(state_slots, x, dt, A, B, C, D, y, seq_starts, seq_lens, resume_flags, n_seqs,
+                     n_tokens, n_heads, head_dim, d_state, n_groups, tuning, workspace, workspace_bytes,
+                     stream);
+}
+
+size_t ssm_scan_workspace_bytes(int n_seqs, int n_tokens, int n_heads, int head_dim, int d_state,
+                                int n_groups, const ssm_scan_tuning *tuning)
+{
+    if (n_seqs <= 0 || n_tokens < 0 || n_heads <= 0 || head_dim <= 0 || d_state <= 0 || n_groups <= 0 ||
+        n_heads % n_groups != 0 || d_state % 4 != 0 || d_state > kMaxDState)
+        return 0;
+    ssm_scan_tuning t;
+    std::memset(&t, 0, sizeof t);
+    if (tuning)
+        t = *tuning;
+    int path = t.path;
+    if (path == SSM_PATH_AUTO)
+        path = (n_tokens == n_seqs) ? SSM_PATH_DECODE : SSM_PATH_PREFILL;
+    if (path != SSM_PATH_PREFILL)
+        return 0;
+    DeviceInfo dev;
+    if (device_info(&dev) != SSM_OK)
+        return 0;
+    PrefillPlan pl;
+    if (plan_prefill(t, true, n_seqs, n_tokens, n_heads, head_dim, d_state, n_groups, dev, true, &pl) != SSM_OK)
+        return 0;
+    return pl.seg_len > 0 ? pl.ws_bytes : 0;
 }
 
 const char *ssm_status_string(int status)

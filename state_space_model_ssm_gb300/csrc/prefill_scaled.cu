@@ -80,6 +80,9 @@ struct ScaledSmem {
     {
         return base + kSlots * (2 * cb + cx + cc + cm);
     }
+    int cpart;          // floats of Part()
+    // per-head running decay of a time segment (state pass only), cm floats
+    __device__ __forceinline__ float *Dec() const { return Part() + cpart; }
 };
 
 __device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
@@ -126,8 +129,8 @@ __device__ __forceinline__ void load_rows(float (&v)[R], const float *p)
 // Coefficients of one head for one chunk of n <= 32 tokens; lane = token.
 // out[t * stride] = {dt_t / Lambda_t, Lambda_t, r_t, 0}; *mask = bit t set for
 // every anchor token t.
-__device__ __forceinline__ void chunk_coefficients(float dt, float A, int n, int lane,
-                                                   float4 *out, int stride, unsigned *mask)
+__device__ __forceinline__ float chunk_coefficients(float dt, float A, int n, int lane,
+                                                    float4 *out, int stride, unsigned *mask)
 {
     const bool live = lane < n;
     const float a = live ? dt * A : 0.f;
@@ -161,6 +164,12 @@ __device__ __forceinline__ void chunk_coefficients(float dt, float A, int n, int
     const unsigned m = __ballot_sync(kFullMask, anchor && live);
     if (lane == 0)
         *mask = m;
+    // total decay of the chunk, prod dA (lanes past n contribute exp(0) = 1)
+    float prod = dA;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1)
+        prod *= __shfl_xor_sync(kFullMask, prod, off);
+    return prod;
 }
 
 }  // namespace
@@ -171,13 +180,16 @@ size_t prefill_scaled_smem_bytes(const PrefillGeom &g, int N, int lanes)
     const size_t cm = ((size_t)g.heads_cap + 3) & ~(size_t)3;
     const size_t per_slot = (size_t)g.chunk * (2 * (size_t)N + 4 * (size_t)g.heads_cap) + cx + cm;
     const size_t part = (size_t)g.chunk * lanes * (size_t)part_stride(g.rows_per_cta);
-    return (kSlots * per_slot + part) * sizeof(float);
+    return (kSlots * per_slot + part + cm) * sizeof(float);
 }
 
-template <int LANES, int VPL, int RPT, bool EXACT>
+// MODE kScanFull: the scan with y.  MODE kScanStateOnly: one time segment's
+// state from zero (no C, no y), for the segment pass of long sequences.
+template <int LANES, int VPL, int RPT, bool EXACT, int MODE>
 __global__ void __launch_bounds__(256, 1)
-prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
+prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan plan)
 {
+    constexpr bool kFull = (MODE == kScanFull);
     extern __shared__ __align__(16) float smem[];
     const int N = a.N, N4 = a.N >> 2, P = a.P, H = a.H;
     const long long HP = (long long)H * P;
@@ -188,11 +200,14 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
     sm.cc = geo.chunk * geo.heads_cap * 4;
     sm.cm = (geo.heads_cap + 3) & ~3;                    // keeps the partial sums 16-byte aligned
     sm.ps = part_stride(geo.rows_per_cta);
+    sm.cpart = geo.chunk * LANES * sm.ps;
 
-    // ---- A1 work mapping: (sequence, group, run of rows) ----
-    const int ctas_per_seq = a.G * geo.runs_per_group;
-    const int seq = blockIdx.x / ctas_per_seq;
-    const int rem = blockIdx.x - seq * ctas_per_seq;
+    // ---- A1 work mapping: (work unit, group, run of rows) ----
+    // A work unit is a whole sequence, or with a segment plan one time segment
+    // (seq, seg) of it: tokens [seg * seg_len, (seg + 1) * seg_len).
+    const int ctas_per_unit = a.G * geo.runs_per_group;
+    const int unit = blockIdx.x / ctas_per_unit;
+    const int rem = blockIdx.x - unit * ctas_per_unit;
     const int grp = rem / geo.runs_per_group;
     const int run = rem - grp * geo.runs_per_group;
     const int r0 = grp * geo.rows_per_group + run * geo.rows_per_cta;
@@ -200,9 +215,28 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
     const int h0 = r0 / P;
     const int nheads = (r0 + nrows - 1) / P - h0 + 1;
 
-    const int tok_start = a.seq_starts[seq];
-    const int len = a.seq_lens[seq];
+    int seq = unit, seg = 0, nseg = 1;
+    if (plan.units) {
+        if (unit >= *plan.n_units)
+            return;                                      // whole block: beyond the plan
+        const int2 us = plan.units[unit];
+        seq = us.x;
+        seg = us.y;
+    }
+    const int seq_len = a.seq_lens[seq];
+    int seg_off = 0, len = seq_len;
+    if (plan.units) {
+        nseg = max(1, (seq_len + plan.seg_len - 1) / plan.seg_len);
+        seg_off = seg * plan.seg_len;
+        len = min(plan.seg_len, seq_len - seg_off);
+    }
+    if (!kFull && seg == nseg - 1)
+        return;                                          // the last segment needs no state pass
+    const int tok_start = a.seq_starts[seq] + seg_off;
     const bool resume = a.resume[seq] != 0;
+    const bool from_slot = (seg == 0) && resume;                 // initial state from the slot
+    const bool from_plan = kFull && seg > 0;                     // incoming state of the segment
+    const bool to_slot = kFull && seg == nseg - 1;               // final state to the slot
     const int n_chunks = (len + geo.chunk - 1) / geo.chunk;
 
     const int tid = threadIdx.x, nthr = blockDim.x;
@@ -215,6 +249,7 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
         const float *Cg = a.C + (long long)grp * N;
         const long long tokN = (long long)a.G * N;
         // A3: stage B, C and x of chunk c0 into slot b (cp.async, this warp only)
+        float *seg_decay = sm.Dec();     // state pass: running decay of the segment per head
         // Per-lane walk over (token, column) items in steps of 32 without
         // divisions: start at (lane / width, lane % width), step (32 / width, 32 % width).
         const int bt0 = lane / N4, bv0 = lane - bt0 * N4, bdt = 32 / N4, bdv = 32 - bdt * N4;
@@ -227,7 +262,8 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
             for (int t = bt0, v = bv0; t < cnt;) {
                 const long long goff = (tok0 + t) * tokN + 4 * v;
                 cp_async16(sB + t * N + 4 * v, Bg + goff);
-                cp_async16(sC + t * N + 4 * v, Cg + goff);
+                if (kFull)
+                    cp_async16(sC + t * N + 4 * v, Cg + goff);
                 t += bdt;
                 v += bdv;
                 if (v >= N4) { v -= N4; ++t; }
@@ -260,8 +296,10 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
                     if (hh == q) dtv = d[q];
                 if (hh >= kDtHeads)
                     dtv = lane < cnt ? a.dt[((long long)tok_start + t0 + lane) * H + h0 + hh] : 0.f;
-                chunk_coefficients(dtv, a.A[h0 + hh], cnt, lane, sm.Coef(b) + hh, geo.heads_cap,
-                                   sm.Mask(b) + hh);
+                const float dec = chunk_coefficients(dtv, a.A[h0 + hh], cnt, lane, sm.Coef(b) + hh,
+                                                     geo.heads_cap, sm.Mask(b) + hh);
+                if (!kFull && lane == 0)
+                    seg_decay[hh] = (c0 == 0 ? 1.f : seg_decay[hh]) * dec;
             }
         };
         // Staging runs two chunks ahead: chunks k and k+1 are in flight while the
@@ -299,6 +337,12 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
                 dt1[q] = dt2[q];
             }
         }
+        if (!kFull && lane == 0) {
+            // the segment's decay per head, written by the block holding the head's first row
+            for (int hh = 0; hh < nheads; ++hh)
+                if ((h0 + hh) * P >= r0)
+                    plan.seg_decay[(long long)unit * H + h0 + hh] = n_chunks > 0 ? seg_decay[hh] : 1.f;
+        }
         return;
     }
 
@@ -312,19 +356,26 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
     const int rl = rvalid ? row_raw : nrows - RPT;          // first of the RPT rows
     const int hl = (r0 + rl) / P - h0;
 
-    // ---- A2 state load: U = S at the start ----
+    // ---- A2 state load: U = S at the start (slot, segment plan, or zero) ----
     float2 u[RPT][VPL][2];
+    {
+        const float *src = nullptr;
+        if (from_slot)
+            src = a.state + (long long)seq * HP * N;
+        else if (from_plan)          // the combine pass left S_in[seg] in unit-1's scratch
+            src = plan.seg_state + (long long)(unit - 1) * HP * N;
 #pragma unroll
-    for (int q = 0; q < RPT; ++q) {
-        const float *slot = a.state + ((long long)seq * HP + r0 + rl + q) * N;
+        for (int q = 0; q < RPT; ++q) {
+            const float *row = src + ((long long)r0 + rl + q) * N;
 #pragma unroll
-        for (int k = 0; k < VPL; ++k) {
-            const int c = k * LANES + j;
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (resume && rvalid && (EXACT || c < N4))
-                v = *reinterpret_cast<const float4 *>(slot + 4 * c);
-            u[q][k][0] = f2(v.x, v.y);
-            u[q][k][1] = f2(v.z, v.w);
+            for (int k = 0; k < VPL; ++k) {
+                const int c = k * LANES + j;
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (src && rvalid && (EXACT || c < N4))
+                    v = *reinterpret_cast<const float4 *>(row + 4 * c);
+                u[q][k][0] = f2(v.x, v.y);
+                u[q][k][1] = f2(v.z, v.w);
+            }
         }
     }
 
@@ -373,7 +424,8 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
                 const int cidx = k * LANES + j;
                 if (EXACT || cidx < N4) {
                     in.b[k] = *reinterpret_cast<const float4 *>(bt + 4 * cidx);
-                    in.c[k] = *reinterpret_cast<const float4 *>(ct + 4 * cidx);
+                    if constexpr (kFull)
+                        in.c[k] = *reinterpret_cast<const float4 *>(ct + 4 * cidx);
                 }
             }
         };
@@ -395,18 +447,22 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
                     for (int q = 0; q < RPT; ++q) {
                         u[q][k][0] = __ffma2_rn(a2[q], f2(bb.x, bb.y), u[q][k][0]);      // A5
                         u[q][k][1] = __ffma2_rn(a2[q], f2(bb.z, bb.w), u[q][k][1]);
-                        acc[q][k & 1] = __ffma2_rn(u[q][k][0], f2(cc.x, cc.y), acc[q][k & 1]);   // A6
-                        acc[q][k & 1] = __ffma2_rn(u[q][k][1], f2(cc.z, cc.w), acc[q][k & 1]);
+                        if constexpr (kFull) {                                           // A6
+                            acc[q][k & 1] = __ffma2_rn(u[q][k][0], f2(cc.x, cc.y), acc[q][k & 1]);
+                            acc[q][k & 1] = __ffma2_rn(u[q][k][1], f2(cc.z, cc.w), acc[q][k & 1]);
+                        }
                     }
                 }
             }
-            float part[RPT];
+            if constexpr (kFull) {
+                float part[RPT];
 #pragma unroll
-            for (int q = 0; q < RPT; ++q) {
-                const float2 s2 = __fadd2_rn(acc[q][0], acc[q][1]);
-                part[q] = s2.x + s2.y;
+                for (int q = 0; q < RPT; ++q) {
+                    const float2 s2 = __fadd2_rn(acc[q][0], acc[q][1]);
+                    part[q] = s2.x + s2.y;
+                }
+                store_rows<RPT>(sPart + tt * LANES * sm.ps, part);
             }
-            store_rows<RPT>(sPart + tt * LANES * sm.ps, part);
         };
         // Anchor tokens of any head of the block split the chunk into segments;
         // a head that does not anchor at a split has r = 1 there (exact no-op).
@@ -453,7 +509,7 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
         }
         // A6 readout of this warp's rows: y = Lambda_t (sum of the lanes' parts) + D x.
         __syncwarp();
-        {
+        if constexpr (kFull) {
             const long long tok0 = (long long)tok_start + c * geo.chunk;
             const float *part = sm.Part() + rq;
             const float4 *cfb = sm.Coef(b);
@@ -492,11 +548,16 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
             bar_arrive(kBarEmpty + b, nthr);
     }
 
-    // ---- A7 state store ----
-    if (rvalid) {
+    // ---- A7 state store: slot (last segment) or the unit's scratch (state pass) ----
+    float *dst = nullptr;
+    if (to_slot)
+        dst = a.state + (long long)seq * HP * N;
+    else if (!kFull)
+        dst = plan.seg_state + (long long)unit * HP * N;
+    if (dst && rvalid) {
 #pragma unroll
         for (int q = 0; q < RPT; ++q) {
-            float *slot = a.state + ((long long)seq * HP + r0 + rl + q) * N;
+            float *slot = dst + ((long long)r0 + rl + q) * N;
 #pragma unroll
             for (int k = 0; k < VPL; ++k) {
                 const int c = k * LANES + j;
@@ -511,19 +572,25 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo)
 namespace {
 
 template <int LANES, int VPL, int RPT>
-cudaError_t launch_scaled_one(const ScanArgs &a, const PrefillGeom &g, size_t smem, cudaStream_t stream)
+cudaError_t launch_scaled_one(const ScanArgs &a, const PrefillGeom &g, const SegmentPlan &plan, int mode,
+                              long long n_units, size_t smem, cudaStream_t stream)
 {
     const bool exact = (a.N / 4) == LANES * VPL;
     const int threads = (g.rows_per_cta / RPT) * LANES + 32;     // consumers + one producer warp
-    const dim3 grid((unsigned)((long long)a.n_seqs * a.G * g.runs_per_group));
-    auto kern = exact ? prefill_scaled_kernel<LANES, VPL, RPT, true>
-                      : prefill_scaled_kernel<LANES, VPL, RPT, false>;
+    const dim3 grid((unsigned)(n_units * a.G * g.runs_per_group));
+    void (*kern)(const ScanArgs, const PrefillGeom, const SegmentPlan);
+    if (mode == kScanFull)
+        kern = exact ? prefill_scaled_kernel<LANES, VPL, RPT, true, kScanFull>
+                     : prefill_scaled_kernel<LANES, VPL, RPT, false, kScanFull>;
+    else
+        kern = exact ? prefill_scaled_kernel<LANES, VPL, RPT, true, kScanStateOnly>
+                     : prefill_scaled_kernel<LANES, VPL, RPT, false, kScanStateOnly>;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess)
             return e;
     }
-    kern<<<grid, threads, smem, stream>>>(a, g);
+    kern<<<grid, threads, smem, stream>>>(a, g, plan);
     return cudaGetLastError();
 }
 
@@ -545,9 +612,11 @@ bool prefill_scaled_supported(int lanes, int vpl, int rpt)
 }
 
 cudaError_t launch_prefill_scaled(const ScanArgs &a, const PrefillGeom &g, int lanes, int vpl, int rpt,
-                                  size_t smem, cudaStream_t stream)
+                                  const SegmentPlan &plan, int mode, long long n_units, size_t smem,
+                                  cudaStream_t stream)
 {
-#define X(L, V, R) if (lanes == L && vpl == V && rpt == R) return launch_scaled_one<L, V, R>(a, g, smem, stream);
+#define X(L, V, R) \
+    if (lanes == L && vpl == V && rpt == R) return launch_scaled_one<L, V, R>(a, g, plan, mode, n_units, smem, stream);
     SSM_SCALED_SHAPES(X)
 #undef X
     return cudaErrorInvalidValue;

@@ -134,8 +134,27 @@ cudaError_t launch_prefill(const ScanArgs &a, const PrefillGeom &g, int lanes,
 bool prefill_supported(int lanes, int vpl, int rpt);
 size_t prefill_smem_bytes(const PrefillGeom &g, int N);
 
+// Time segments of long sequences (the segment pass): work unit u is time
+// segment units[u] = (sequence, segment) covering tokens [seg*seg_len,
+// (seg+1)*seg_len) of the sequence.  units == nullptr: one unit per sequence.
+struct SegmentPlan {
+    const int2 *units;        // [max_units] (device), filled by the plan kernel
+    const int *n_units;       // device count of valid units
+    const int *unit_base;     // [n_seqs + 1] first unit of each sequence
+    int seg_len;              // tokens per segment (a multiple of the chunk)
+    float *seg_state;         // [max_units][H][P][N]: state pass output, then S_in of seg+1
+    float *seg_decay;         // [max_units][H]: prod dA over the segment
+};
+constexpr int kScanFull = 0;        // the scan with y
+constexpr int kScanStateOnly = 1;   // one segment's state from zero, no y
+
 cudaError_t launch_prefill_scaled(const ScanArgs &a, const PrefillGeom &g, int lanes, int vpl,
-                                  int rpt, size_t smem_bytes, cudaStream_t stream);
+                                  int rpt, const SegmentPlan &plan, int mode, long long n_units,
+                                  size_t smem_bytes, cudaStream_t stream);
+cudaError_t launch_segment_plan(const ScanArgs &a, const SegmentPlan &plan, int max_units,
+                                cudaStream_t stream);
+cudaError_t launch_segment_combine(const ScanArgs &a, const SegmentPlan &plan, int max_units,
+                                   cudaStream_t stream);
 bool prefill_scaled_supported(int lanes, int vpl, int rpt);
 size_t prefill_scaled_smem_bytes(const PrefillGeom &g, int N, int lanes);
 constexpr int kScaledMaxChunk = 32;    // one warp lane per token in the coefficient pass

@@ -18,16 +18,23 @@ def _guarded(shape, fill, device):
     return buf, buf[GUARD:GUARD + numel].view(*shape)
 
 
-def run_gpu(inp, tuning=None, device="cuda", stream=None, y_fill=float("nan")):
+def run_gpu(inp, tuning=None, device="cuda", stream=None, y_fill=float("nan"), workspace=False):
     """Run libssmscan on a ScanInputs bundle; returns (y, state) as float64
     numpy arrays.  Checks that the NaN guard bands around y and the state are
-    intact afterwards."""
+    intact afterwards.  workspace=True calls ssm_scan_ws with a workspace of
+    the size the library asks for (NaN-filled, so stale reads show)."""
     d = inp.to(device)
     sbuf, state = _guarded(tuple(inp.state.shape), float("nan"), device)
     state.copy_(d.state)
     ybuf, y = _guarded(tuple(inp.x.shape), y_fill, device)
+    ws = None
+    if workspace:
+        g = inp.geom
+        nbytes = bd.workspace_bytes(inp.n_seqs, inp.n_tokens, g.n_heads, g.head_dim, g.d_state,
+                                    g.n_groups, tuning)
+        ws = torch.full((max(nbytes, 256) // 4,), float("nan"), dtype=torch.float32, device=device)
     bd.ssm_scan(state, d.x, d.dt, d.A, d.B, d.C, d.D, d.seq_starts, d.seq_lens, d.resume,
-                y=y, tuning=tuning, stream=stream)
+                y=y, tuning=tuning, stream=stream, workspace=ws)
     torch.cuda.synchronize()
     for buf in (sbuf, ybuf):
         head, tail = buf[:GUARD], buf[-GUARD:]

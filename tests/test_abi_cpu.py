@@ -30,7 +30,14 @@ def _call(lib, tuning=None, **over):
 
 def test_header_declares_the_scan_entry_points():
     names = bd.declared_functions()
-    assert {"ssm_scan", "ssm_scan_tuned", "ssm_status_string"} <= set(names)
+    assert {"ssm_scan", "ssm_scan_tuned", "ssm_scan_ws", "ssm_scan_workspace_bytes",
+            "ssm_status_string"} <= set(names)
+
+
+def test_workspace_bytes_is_zero_for_invalid_sizes(lib):
+    assert bd.workspace_bytes(0, 8, 4, 16, 32, 2) == 0
+    assert bd.workspace_bytes(2, 8, 4, 16, 30, 2) == 0
+    assert bd.workspace_bytes(2, 8, 4, 16, 32, 3) == 0
 
 
 def test_library_exports_every_declared_symbol(lib):

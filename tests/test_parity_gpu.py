@@ -22,8 +22,8 @@ def built():
     bd.load()
 
 
-def _tuning(path=0, lanes=0, rpt=0, rows=0, chunk=0, ctas=0):
-    return bd.Tuning(path, lanes, rpt, rows, chunk, ctas)
+def _tuning(path=0, lanes=0, rpt=0, rows=0, chunk=0, ctas=0, seg=0):
+    return bd.Tuning(path, lanes, rpt, rows, chunk, ctas, seg)
 
 
 PATHS = [("auto", None), ("decode", _tuning(path=bd.PATH_DECODE)),
@@ -217,3 +217,43 @@ def test_bad_arguments_raise_before_launch():
     with pytest.raises(TypeError):
         bd.ssm_scan(inp.state.double(), inp.x, inp.dt, inp.A, inp.B, inp.C, inp.D,
                     inp.seq_starts, inp.seq_lens, inp.resume)
+
+
+# Time segments (ssm_scan_ws): long sequences cut into segments that run in
+# parallel, then combined.  Short segments make many segments per sequence.
+SEGMENT_CASES = [("tiny", 16), ("tiny", 32), ("edge_p96_n100", 64), ("ragged_12", 256),
+                 ("edge_n1024", 512), ("prefill_1x4096", 0), ("ragged_12", 0)]
+
+
+@pytest.mark.parametrize("name,seg", SEGMENT_CASES, ids=[f"{n}-{s}" for n, s in SEGMENT_CASES])
+def test_parity_time_segments(name, seg):
+    inp = workload(name)
+    y_ref, s_ref = oracle.scan_inputs(inp)
+    t = _tuning(path=bd.PATH_PREFILL, seg=seg)
+    if seg > 0:
+        g = inp.geom
+        assert bd.workspace_bytes(inp.n_seqs, inp.n_tokens, g.n_heads, g.head_dim, g.d_state,
+                                  g.n_groups, t) > 0
+    y, s = run_gpu(inp, tuning=t, workspace=True)
+    assert_parity(inp, y, s, y_ref, s_ref)
+
+
+@pytest.mark.parametrize("dt_scale,a_value", [(8.0, -16.0), (60.0, -16.0), (1.0, 0.0), (0.5, 0.05)],
+                         ids=["anchor_every_few", "underflow", "no_decay", "growth"])
+def test_parity_time_segments_extreme_decay(dt_scale, a_value):
+    inp = make_inputs(Geometry(4, 16, 32, 2), [150, 77, 0, 33], [0, 1, 1, 0], seed=32)
+    inp.dt.mul_(dt_scale)
+    inp.A.fill_(a_value)
+    y_ref, s_ref = oracle.scan_inputs(inp)
+    y, s = run_gpu(inp, tuning=_tuning(path=bd.PATH_PREFILL, seg=16), workspace=True)
+    assert_parity(inp, y, s, y_ref, s_ref)
+
+
+def test_time_segments_need_their_workspace():
+    inp = workload("tiny").to("cuda")
+    t = _tuning(path=bd.PATH_PREFILL, seg=16)
+    small = torch.empty(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(bd.SsmScanError) as e:
+        bd.ssm_scan(inp.state, inp.x, inp.dt, inp.A, inp.B, inp.C, inp.D, inp.seq_starts,
+                    inp.seq_lens, inp.resume, tuning=t, workspace=small)
+    assert e.value.status == bd.SSM_ERR_INVALID_ARG
