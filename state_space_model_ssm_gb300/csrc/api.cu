@@ -125,15 +125,15 @@ int plan_prefill(const ssm_scan_tuning &t, bool scaled, int n_seqs, int n_tokens
     auto supported = scaled ? ssm::prefill_scaled_supported : ssm::prefill_supported;
     int lanes, rpt;
     if (scaled) {
-        // About 8 state elements of a row per lane, and up to 4 rows per lane
-        // (32 state registers) so that each B/C value read from shared memory
+        // About 8 state elements of a row per lane, and up to 8 rows per lane
+        // (64 state registers) so that each B/C value read from shared memory
         // feeds several rows.  The rows of a lane must share a head: RPT | P.
         lanes = t.lanes_per_row ? t.lanes_per_row : std::min(32, pow2ceil((N + 7) / 8));
         rpt = t.rows_per_thread;
         if (!rpt) {
-            rpt = 4;
+            rpt = 8;
             while (rpt > 1 && (P % rpt != 0 || rpt > lanes ||
-                               pick_vpl(N4, lanes, rpt, supported) * 4 * rpt > 32 ||
+                               pick_vpl(N4, lanes, rpt, supported) * 4 * rpt > 64 ||
                                pick_vpl(N4, lanes, rpt, supported) == 0))
                 rpt >>= 1;
         }

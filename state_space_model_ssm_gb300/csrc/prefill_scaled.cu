@@ -24,11 +24,13 @@
 //    (cp.async into three slots) and computes each chunk's coefficients (lane =
 //    token: a warp prefix sum places the anchors, a segmented prefix product of
 //    dA = exp(dt*A) gives Lambda, ~1 ulp per factor).  Consumers run the token
-//    loop (per token U += alpha B and each lane's partial of U . C, stored to
-//    shared memory) and then sum their own rows' partials into y, which needs
-//    only the warp itself.  The two sides meet at named barriers (bar.arrive /
-//    bar.sync: hardware barriers, no spin loop): FULL[s] when slot s holds a
-//    staged chunk, EMPTY[s] when the consumers are done with it.
+//    loop: per token U += alpha B, each lane's part of U . C, a shuffle
+//    reduction over the row's lanes and the y store.  A lane holds RPT rows so
+//    that each B/C value read from shared memory (128-bit reads cost four
+//    wavefronts even when broadcast) feeds RPT rows.  The two sides meet at
+//    named barriers (bar.arrive / bar.sync: hardware barriers, no spin loop):
+//    FULL[s] when slot s holds a staged chunk, EMPTY[s] when the consumers are
+//    done with it.
 //
 // The rescaling is an algebraic identity of the recurrence defined by "The
 // llama journey", Day 14 (decay exp(dt*A), input dt*x*B, y from the updated
@@ -58,7 +60,6 @@ struct ScaledSmem {
     float *base;
     int cb, cx, cc, cm; // floats per buffer: B (= C), x, coefficients (float4 per token and
                         // head), anchor masks (one word per head)
-    int ps;             // floats between the partial-sum rows of two lanes (see Part())
     // slot s: [B | C | x | coefficients | anchor masks], each 16-byte aligned
     __device__ __forceinline__ float *slot(int s) const { return base + s * (2 * cb + cx + cc + cm); }
     __device__ __forceinline__ float *B(int s) const { return slot(s); }
@@ -72,39 +73,10 @@ struct ScaledSmem {
     {
         return reinterpret_cast<unsigned *>(slot(s) + 2 * cb + cx + cc);
     }
-    // Per-lane partial dot products of one chunk: [token][lane in row][ps] with
-    // the block's rows contiguous (each consumer warp uses only its own rows);
-    // ps = rows rounded up to 4, plus 4, so the 16-byte stores of eight lanes fall
-    // on eight different bank quads.
-    __device__ __forceinline__ float *Part() const
-    {
-        return base + kSlots * (2 * cb + cx + cc + cm);
-    }
-    int cpart;          // floats of Part()
-    // per-head running decay of a time segment (state pass only), cm floats
-    __device__ __forceinline__ float *Dec() const { return Part() + cpart; }
+    __device__ __forceinline__ float *Dec() const { return base + kSlots * (2 * cb + cx + cc + cm); }
 };
 
 __device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
-
-__host__ __device__ __forceinline__ int part_stride(int rows) { return ((rows + 3) & ~3) + 4; }
-
-// R consecutive floats to shared memory (aligned like load_rows).
-template <int R>
-__device__ __forceinline__ void store_rows(float *p, const float (&v)[R])
-{
-    if constexpr (R % 4 == 0) {
-#pragma unroll
-        for (int i = 0; i < R; i += 4)
-            *reinterpret_cast<float4 *>(p + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-    } else if constexpr (R == 2) {
-        *reinterpret_cast<float2 *>(p) = make_float2(v[0], v[1]);
-    } else {
-#pragma unroll
-        for (int i = 0; i < R; ++i)
-            p[i] = v[i];
-    }
-}
 
 // R consecutive floats from shared memory (16-byte aligned when R = 4, 8 bytes when R = 2).
 template <int R>
@@ -179,8 +151,8 @@ size_t prefill_scaled_smem_bytes(const PrefillGeom &g, int N, int lanes)
     const size_t cx = ((size_t)g.chunk * g.rows_per_cta + 3) & ~(size_t)3;
     const size_t cm = ((size_t)g.heads_cap + 3) & ~(size_t)3;
     const size_t per_slot = (size_t)g.chunk * (2 * (size_t)N + 4 * (size_t)g.heads_cap) + cx + cm;
-    const size_t part = (size_t)g.chunk * lanes * (size_t)part_stride(g.rows_per_cta);
-    return (kSlots * per_slot + part + cm) * sizeof(float);
+    (void)lanes;
+    return (kSlots * per_slot + cm) * sizeof(float);
 }
 
 // MODE kScanFull: the scan with y.  MODE kScanStateOnly: one time segment's
@@ -198,9 +170,7 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan
     sm.cb = geo.chunk * N;
     sm.cx = (geo.chunk * geo.rows_per_cta + 3) & ~3;     // keeps the float4 coefficients 16-byte aligned
     sm.cc = geo.chunk * geo.heads_cap * 4;
-    sm.cm = (geo.heads_cap + 3) & ~3;                    // keeps the partial sums 16-byte aligned
-    sm.ps = part_stride(geo.rows_per_cta);
-    sm.cpart = geo.chunk * LANES * sm.ps;
+    sm.cm = (geo.heads_cap + 3) & ~3;                    // keeps the next slot 16-byte aligned
 
     // ---- A1 work mapping: (work unit, group, run of rows) ----
     // A work unit is a whole sequence, or with a segment plan one time segment
@@ -355,6 +325,9 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan
     const bool rvalid = row_raw < nrows;
     const int rl = rvalid ? row_raw : nrows - RPT;          // first of the RPT rows
     const int hl = (r0 + rl) / P - h0;
+    const float Dv = __ldg(a.D + h0 + hl);
+    const int yq = reduced_row<LANES, RPT>(j);               // row of this lane's reduced sum
+    const bool ywriter = kFull && reduced_writer<LANES, RPT>(j) && rvalid;
 
     // ---- A2 state load: U = S at the start (slot, segment plan, or zero) ----
     float2 u[RPT][VPL][2];
@@ -379,25 +352,6 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan
         }
     }
 
-    // Readout geometry of this warp: its rows [wr0, wr0 + kRowsPerWarp).  With
-    // four or more rows a lane sums a fixed quad of rows (16-byte reads), else a
-    // fixed single row; either way its heads and D are fixed too.
-    constexpr int kRowsPerWarp = (32 / LANES) * RPT;
-    constexpr int kVec = (kRowsPerWarp % 4 == 0) ? 4 : 1;
-    constexpr int kItems = kRowsPerWarp / kVec;          // row groups per token
-    static_assert(kItems <= 32 && (32 % kItems) == 0, "readout mapping");
-    const int wr0 = warp * kRowsPerWarp;
-    const int my_item = lane % kItems;
-    const int rq = wr0 + kVec * my_item;                 // first row of this lane's group
-    int q_head[kVec];
-    float q_D[kVec];
-#pragma unroll
-    for (int e = 0; e < kVec; ++e) {
-        const int r = min(rq + e, nrows - 1);
-        q_head[e] = (r0 + r) / P - h0;
-        q_D[e] = __ldg(a.D + h0 + q_head[e]);
-    }
-
     for (int c = 0; c < n_chunks; ++c) {
         const int b = c % kSlots;
         bar_sync(kBarFull + b, nthr);
@@ -406,7 +360,7 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan
         const float *__restrict__ sC = sm.C(b);
         const float *__restrict__ sX = sm.X(b);
         const float4 *__restrict__ sCf = sm.Coef(b) + hl;
-        float *__restrict__ sPart = sm.Part() + j * sm.ps + row_raw;
+        float *yrow = a.y + ((long long)tok_start + c * geo.chunk) * HP + r0 + rl + yq;
 
         // Shared-memory operands of one token.
         struct TokenIn {
@@ -429,7 +383,9 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan
                 }
             }
         };
-        // One token: U += (x dt / Lambda) B and this lane's part of U . C.
+        // One token: U += (x dt / Lambda) B; with y: the lanes' parts of U . C
+        // summed by shuffles (transposing over the RPT rows), then
+        // y = Lambda (U . C) + D x from the lane that holds the row's sum.
         auto compute_token = [&](const TokenIn &in, int tt) {
             float2 a2[RPT], acc[RPT][2];
 #pragma unroll
@@ -461,13 +417,15 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan
                     const float2 s2 = __fadd2_rn(acc[q][0], acc[q][1]);
                     part[q] = s2.x + s2.y;
                 }
-                store_rows<RPT>(sPart + tt * LANES * sm.ps, part);
+                const float ysum = reduce_rows<LANES, RPT>(part, j);
+                if (ywriter)
+                    yrow[(long long)tt * HP] = fmaf(in.cf.y, ysum, Dv * sX[tt * geo.rows_per_cta + rl + yq]);
             }
         };
         // Anchor tokens of any head of the block split the chunk into segments;
         // a head that does not anchor at a split has r = 1 there (exact no-op).
         // Within a segment the loop is software-pipelined: the operands of token
-        // t+1 are read before token t is computed and its partial sums stored.
+        // t+1 are read before token t is computed.
         unsigned amask = 0;
         for (int hh = 0; hh < nheads; ++hh)
             amask |= sm.Mask(b)[hh];
@@ -506,42 +464,6 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan
                     u[q][k][0] = __fmul2_rn(u[q][k][0], l2);
                     u[q][k][1] = __fmul2_rn(u[q][k][1], l2);
                 }
-        }
-        // A6 readout of this warp's rows: y = Lambda_t (sum of the lanes' parts) + D x.
-        __syncwarp();
-        if constexpr (kFull) {
-            const long long tok0 = (long long)tok_start + c * geo.chunk;
-            const float *part = sm.Part() + rq;
-            const float4 *cfb = sm.Coef(b);
-            for (int t = lane / kItems; t < cnt; t += 32 / kItems) {
-                const float *pp = part + t * LANES * sm.ps;
-                float sum[kVec];
-                if constexpr (kVec == 4) {
-                    float2 s01 = f2(0.f, 0.f), s23 = s01;
-#pragma unroll
-                    for (int l = 0; l < LANES; ++l) {
-                        const float4 v = *reinterpret_cast<const float4 *>(pp + l * sm.ps);
-                        s01 = __fadd2_rn(s01, f2(v.x, v.y));
-                        s23 = __fadd2_rn(s23, f2(v.z, v.w));
-                    }
-                    sum[0] = s01.x; sum[1] = s01.y; sum[2] = s23.x; sum[3] = s23.y;
-                } else {
-                    float acc = 0.f;
-#pragma unroll
-                    for (int l = 0; l < LANES; ++l)
-                        acc += pp[l * sm.ps];
-                    sum[0] = acc;
-                }
-                float *yrow = a.y + (tok0 + t) * HP + r0;
-#pragma unroll
-                for (int e = 0; e < kVec; ++e) {
-                    const int r = rq + e;
-                    if (r < nrows) {
-                        const float lam = cfb[t * geo.heads_cap + q_head[e]].y;
-                        yrow[r] = fmaf(lam, sum[e], q_D[e] * sX[t * geo.rows_per_cta + r]);
-                    }
-                }
-            }
         }
         __syncwarp();
         if (c + kSlots < n_chunks)          // the producer refills this slot with chunk c+3
@@ -598,10 +520,10 @@ cudaError_t launch_scaled_one(const ScanArgs &a, const PrefillGeom &g, const Seg
 
 // (lanes per row, float4 per lane and row, rows per lane)
 #define SSM_SCALED_SHAPES(X) \
-    X(16, 2, 4) X(16, 2, 2) X(16, 2, 1) X(8, 2, 4) X(8, 2, 2) X(8, 2, 1) \
-    X(4, 2, 4) X(4, 2, 2) X(4, 2, 1) X(2, 2, 2) X(2, 2, 1) X(1, 2, 1) X(1, 1, 1) X(1, 4, 1) X(2, 4, 1) \
-    X(32, 2, 4) X(32, 2, 1) X(32, 4, 2) X(32, 4, 1) X(32, 8, 1) X(32, 1, 8) X(32, 1, 4) X(32, 1, 1) \
-    X(4, 8, 1) X(8, 4, 1) X(8, 4, 2) X(16, 4, 1)
+    X(16, 2, 8) X(16, 2, 4) X(16, 2, 2) X(16, 2, 1) X(32, 1, 8) X(32, 1, 4) X(8, 4, 4) \
+    X(8, 2, 8) X(8, 2, 4) X(8, 2, 2) X(8, 2, 1) X(4, 2, 4) X(4, 2, 2) X(4, 2, 1) \
+    X(2, 2, 2) X(2, 2, 1) X(1, 2, 1) X(1, 1, 1) \
+    X(32, 2, 8) X(32, 2, 4) X(32, 2, 1) X(32, 4, 4) X(32, 4, 2) X(32, 4, 1) X(32, 8, 2) X(32, 8, 1)
 
 bool prefill_scaled_supported(int lanes, int vpl, int rpt)
 {

@@ -115,8 +115,8 @@ def test_parity_prefill_direct_launch_shapes(lanes, rpt, rows, chunk):
 
 
 SCALED_SHAPES = [(16, 4, 32, 32), (8, 2, 16, 32), (4, 4, 32, 7), (32, 8, 8, 1), (4, 1, 8, 32),
-                 (2, 1, 16, 3), (16, 1, 8, 5), (8, 4, 32, 32), (4, 2, 64, 32), (16, 2, 16, 17),
-                 (16, 4, 24, 16), (32, 1, 7, 9)]
+                 (4, 2, 16, 3), (16, 1, 8, 5), (8, 4, 32, 32), (4, 2, 64, 32), (16, 2, 16, 17),
+                 (16, 4, 24, 16), (32, 8, 16, 9), (16, 8, 16, 16), (8, 8, 32, 16)]
 
 
 @pytest.mark.parametrize("lanes,rpt,rows,chunk", SCALED_SHAPES)
