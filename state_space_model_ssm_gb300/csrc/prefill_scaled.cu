@@ -392,7 +392,6 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan
             for (int q = 0; q < RPT; ++q) {
                 const float alpha = in.xv[q] * in.cf.x;
                 a2[q] = f2(alpha, alpha);
-                acc[q][0] = acc[q][1] = f2(0.f, 0.f);
             }
 #pragma unroll
             for (int k = 0; k < VPL; ++k) {
@@ -404,17 +403,27 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan
                         u[q][k][0] = __ffma2_rn(a2[q], f2(bb.x, bb.y), u[q][k][0]);      // A5
                         u[q][k][1] = __ffma2_rn(a2[q], f2(bb.z, bb.w), u[q][k][1]);
                         if constexpr (kFull) {                                           // A6
-                            acc[q][k & 1] = __ffma2_rn(u[q][k][0], f2(cc.x, cc.y), acc[q][k & 1]);
-                            acc[q][k & 1] = __ffma2_rn(u[q][k][1], f2(cc.z, cc.w), acc[q][k & 1]);
+                            // two accumulators per row; the first product of each
+                            // starts it (no zero fill)
+                            float2 &ac = acc[q][k & 1];
+                            if (k < 2 && (EXACT || cidx < N4))
+                                ac = __fmul2_rn(u[q][k][0], f2(cc.x, cc.y));
+                            else
+                                ac = __ffma2_rn(u[q][k][0], f2(cc.x, cc.y), ac);
+                            ac = __ffma2_rn(u[q][k][1], f2(cc.z, cc.w), ac);
                         }
                     }
+                } else if (kFull && k < 2) {
+#pragma unroll
+                    for (int q = 0; q < RPT; ++q)
+                        acc[q][k & 1] = f2(0.f, 0.f);
                 }
             }
             if constexpr (kFull) {
                 float part[RPT];
 #pragma unroll
                 for (int q = 0; q < RPT; ++q) {
-                    const float2 s2 = __fadd2_rn(acc[q][0], acc[q][1]);
+                    const float2 s2 = VPL > 1 ? __fadd2_rn(acc[q][0], acc[q][1]) : acc[q][0];
                     part[q] = s2.x + s2.y;
                 }
                 const float ysum = reduce_rows<LANES, RPT>(part, j);
@@ -424,17 +433,19 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan
         };
         // Anchor tokens of any head of the block split the chunk into segments;
         // a head that does not anchor at a split has r = 1 there (exact no-op).
-        // Within a segment the loop is software-pipelined: the operands of token
-        // t+1 are read before token t is computed.
+        // Within a segment the loop is software-pipelined over two operand
+        // buffers: the operands of token t+1 are read before token t is computed.
         unsigned amask = 0;
         for (int hh = 0; hh < nheads; ++hh)
             amask |= sm.Mask(b)[hh];
-        TokenIn cur;
-        load_token(0, cur);
         int tt = 0;
         while (tt < cnt) {
+            const unsigned rest = (tt + 1 < 32) ? (amask >> (tt + 1)) : 0u;
+            const int next = rest ? min(cnt, tt + __ffs(rest)) : cnt;
+            TokenIn ta, tb;
+            load_token(tt, ta);
             {   // re-anchor: U <- r U
-                const float2 r2 = f2(cur.cf.z, cur.cf.z);
+                const float2 r2 = f2(ta.cf.z, ta.cf.z);
 #pragma unroll
                 for (int q = 0; q < RPT; ++q)
 #pragma unroll
@@ -443,15 +454,15 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan
                         u[q][k][1] = __fmul2_rn(u[q][k][1], r2);
                     }
             }
-            const unsigned rest = (tt + 1 < 32) ? (amask >> (tt + 1)) : 0u;
-            const int next = rest ? min(cnt, tt + __ffs(rest)) : cnt;
-#pragma unroll 2
-            for (int t2 = tt; t2 < next; ++t2) {
-                TokenIn nx;
-                load_token(min(t2 + 1, cnt - 1), nx);
-                compute_token(cur, t2);
-                cur = nx;
+            int t2 = tt;
+            for (; t2 + 1 < next; t2 += 2) {
+                load_token(t2 + 1, tb);
+                compute_token(ta, t2);
+                load_token(min(t2 + 2, cnt - 1), ta);
+                compute_token(tb, t2 + 1);
             }
+            if (t2 < next)
+                compute_token(ta, t2);
             tt = next;
         }
         {   // back to S at the chunk end: U <- Lambda_last U
