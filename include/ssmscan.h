@@ -172,6 +172,40 @@ size_t ssm_scan_workspace_bytes(int n_seqs, int n_tokens, int n_heads,
                                 int head_dim, int d_state, int n_groups,
                                 const ssm_scan_tuning *tuning);
 
+/*
+ * Size of the scratch that ssm_scan_static keeps in device memory (32 MiB per
+ * device, held from the library's load on that device until process exit).
+ */
+#define SSM_SCAN_STATIC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * The scan for callers that cannot allocate device memory (the pages have no
+ * counterpart: it is a packaging choice of this library).  Some callers never
+ * get to hand the library a workspace: a runtime without a device allocator,
+ * a plugin whose host owns every allocation, a path that must not enter
+ * cudaMalloc.  ssm_scan_static takes the same arguments as ssm_scan and runs
+ * what ssm_scan_ws runs with an automatic plan, using instead a fixed scratch
+ * array of SSM_SCAN_STATIC_SCRATCH_BYTES in device global memory that the
+ * library owns.  It allocates nothing.
+ *   - The first call on a device looks up the scratch's device address (a
+ *     cudaGetSymbolAddress with that device current) and caches it; make that
+ *     first call before any stream capture.
+ *   - Calls whose plan needs more scratch than SSM_SCAN_STATIC_SCRATCH_BYTES
+ *     (very long or many long sequences) return SSM_ERR_UNSUPPORTED before any
+ *     launch; ssm_scan_ws with a caller workspace has no such limit.
+ *   - Every call in the process shares the scratch, which keeps the last
+ *     call's contents (nothing in it needs to start at zero).  Calls whose GPU
+ *     work overlaps, on two streams or from two threads, race on it: the
+ *     caller must serialise them.
+ * Errors otherwise as for ssm_scan.
+ */
+int ssm_scan_static(float *state_slots, const float *x, const float *dt,
+                    const float *A, const float *B, const float *C,
+                    const float *D, float *y, const int32_t *seq_starts,
+                    const int32_t *seq_lens, const int32_t *resume_flags,
+                    int n_seqs, int n_tokens, int n_heads, int head_dim,
+                    int d_state, int n_groups, void *stream);
+
 /* Text for a status code (static storage; never NULL). */
 const char *ssm_status_string(int status);
 

@@ -1,0 +1,105 @@
+"""ssm_scan_static, the entry point for callers that cannot allocate device
+memory (a runtime without a device allocator, a plugin whose host owns every
+allocation, a path that must not enter cudaMalloc).  It runs the segmented
+prefill with the library's own fixed device scratch instead of a caller
+workspace, so it must give what ssm_scan_ws gives with a workspace the caller
+allocated.  This file is collected last on purpose: if it fails, a run that
+stops at the first failure has already run every other test."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from state_space_model_ssm_gb300 import binding as bd
+from state_space_model_ssm_gb300.workloads import workload
+from tests.gpu_helpers import TOL
+
+pytestmark = pytest.mark.gpu
+
+STATIC_SCRATCH_BYTES = 32 << 20     # SSM_SCAN_STATIC_SCRATCH_BYTES in include/ssmscan.h
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from state_space_model_ssm_gb300 import build
+    build.build()
+    lib = bd.load()
+    f = lib.ssm_scan_static
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p] * 11 + [ctypes.c_int] * 6 + [ctypes.c_void_p]
+    return lib
+
+
+def _ptrs(state, d, y):
+    return [state.data_ptr(), d.x.data_ptr(), d.dt.data_ptr(), d.A.data_ptr(), d.B.data_ptr(),
+            d.C.data_ptr(), d.D.data_ptr(), y.data_ptr(), d.seq_starts.data_ptr(),
+            d.seq_lens.data_ptr(), d.resume.data_ptr()]
+
+
+def _sizes(inp):
+    g = inp.geom
+    return [inp.n_seqs, inp.n_tokens, g.n_heads, g.head_dim, g.d_state, g.n_groups]
+
+
+def _close(got, ref):
+    got, ref = got.double().cpu().numpy(), ref.double().cpu().numpy()
+    assert np.isfinite(got).all()
+    err = np.abs(got - ref)
+    assert np.all(err <= TOL * (1.0 + np.abs(ref))), f"max err {err.max():.3e}"
+
+
+@pytest.mark.parametrize("first,second,segmented", [("prefill_1x4096", 7, True), ("ragged_12", 8, False)])
+def test_static_scratch_matches_caller_workspace(lib, first, second, segmented):
+    """Two calls in a row (the second resumes every sequence from the first's
+    slots): ssm_scan_static against ssm_scan_ws with a torch workspace."""
+    a = workload(first)
+    b = workload(first, seed=second)
+    b.resume.fill_(1)
+    need = bd.workspace_bytes(*_sizes(a))
+    assert need <= STATIC_SCRATCH_BYTES
+    if segmented:
+        assert need > 0                         # the time-segmented path is the one exercised
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
+    da, db = a.to("cuda"), b.to("cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+
+    state_ref = da.state.clone()
+    state_new = da.state.clone()
+    for d in (da, db):
+        y_ref = torch.full_like(d.x, float("nan"))
+        y_new = torch.full_like(d.x, float("nan"))
+        bd.ssm_scan(state_ref, d.x, d.dt, d.A, d.B, d.C, d.D, d.seq_starts, d.seq_lens,
+                    d.resume, y=y_ref, workspace=ws)
+        rc = lib.ssm_scan_static(*_ptrs(state_new, d, y_new), *_sizes(a), stream)
+        assert rc == bd.SSM_OK, bd.status_string(rc)
+        torch.cuda.synchronize()
+        _close(y_new, y_ref)
+        _close(state_new, state_ref)
+
+
+def test_static_scratch_without_segments(lib):
+    """A decode batch needs no scratch; the entry point still runs it."""
+    inp = workload("decode_16x1")
+    d = inp.to("cuda")
+    state_ref, state_new = d.state.clone(), d.state.clone()
+    y_ref, y_new = torch.empty_like(d.x), torch.empty_like(d.x)
+    bd.ssm_scan(state_ref, d.x, d.dt, d.A, d.B, d.C, d.D, d.seq_starts, d.seq_lens, d.resume, y=y_ref)
+    rc = lib.ssm_scan_static(*_ptrs(state_new, d, y_new), *_sizes(inp),
+                             torch.cuda.current_stream().cuda_stream)
+    assert rc == bd.SSM_OK
+    torch.cuda.synchronize()
+    _close(y_new, y_ref)
+    _close(state_new, state_ref)
+
+
+def test_static_scratch_rejects_oversized_plans(lib):
+    """A plan that needs more scratch than the static array is refused before
+    any launch (so the pointers below are never used)."""
+    sizes = [1, 8192, 24, 128, 1024, 24]          # one sequence, 12 MiB state slots
+    need = bd.workspace_bytes(*sizes)
+    if need <= STATIC_SCRATCH_BYTES:
+        pytest.skip("on this device the plan fits the static scratch")
+    fake = 1 << 20                                  # aligned, never dereferenced
+    rc = lib.ssm_scan_static(*([fake] * 11), *sizes, 0)
+    assert rc == bd.SSM_ERR_UNSUPPORTED
