@@ -44,7 +44,8 @@ L2_FLUSH_BYTES = 256 << 20
 DECODE_STEPS = 300
 DECODE_SLOT_SETS = 8          # 8 x 32 MiB of slots rotate, 2x the 129 MB L2
 KERNEL_SOURCES = {
-    "prefill_kernel": ["state_space_model_ssm_gb300/csrc/prefill.cu",
+    "prefill_kernel": ["state_space_model_ssm_gb300/csrc/prefill_scaled.cu",
+                       "state_space_model_ssm_gb300/csrc/segments.cu",
                        "state_space_model_ssm_gb300/csrc/scan_common.cuh"],
     "decode_kernel": ["state_space_model_ssm_gb300/csrc/decode.cu",
                       "state_space_model_ssm_gb300/csrc/scan_common.cuh"],
@@ -175,6 +176,14 @@ def event_pair():
 
 # ---------------------------------------------------------------- our arm
 
+def prefill_workspace(inp, dev):
+    """The workspace ssm_scan_ws asks for (time segments of the long sequence)."""
+    from state_space_model_ssm_gb300 import binding as bd
+    g = inp.geom
+    nbytes = bd.workspace_bytes(inp.n_seqs, inp.n_tokens, g.n_heads, g.head_dim, g.d_state, g.n_groups)
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+
+
 def run_prefill(args, world, rank, dev):
     from state_space_model_ssm_gb300 import binding as bd
 
@@ -184,9 +193,11 @@ def run_prefill(args, world, rank, dev):
     y = torch.empty_like(d.x)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    ws = prefill_workspace(inp, dev)
 
     def step():
-        bd.ssm_scan(state, d.x, d.dt, d.A, d.B, d.C, d.D, d.seq_starts, d.seq_lens, d.resume, y=y)
+        bd.ssm_scan(state, d.x, d.dt, d.A, d.B, d.C, d.D, d.seq_starts, d.seq_lens, d.resume, y=y,
+                    workspace=ws)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -224,11 +235,14 @@ def run_prefill_e2e(args, dev, inp):
     d2h = y.numel() * 4 + inp.state.numel() * 4
     stream = torch.cuda.current_stream(dev)
 
+    ws = prefill_workspace(inp, dev)
+
     def step():
         for k in in_keys:
             dbuf[k].copy_(host_in[k], non_blocking=True)
         bd.ssm_scan(dbuf["state"], dbuf["x"], dbuf["dt"], dbuf["A"], dbuf["B"], dbuf["C"],
-                    dbuf["D"], dbuf["seq_starts"], dbuf["seq_lens"], dbuf["resume"], y=y)
+                    dbuf["D"], dbuf["seq_starts"], dbuf["seq_lens"], dbuf["resume"], y=y,
+                    workspace=ws)
         y_host.copy_(y, non_blocking=True)
         s_host.copy_(dbuf["state"], non_blocking=True)
 
@@ -390,6 +404,8 @@ def ours(args):
         "config": {"workload": "prefill_1x4096", "what": WORKLOADS["prefill_1x4096"]["what"],
                    "n_seqs": 1, "tokens_per_rank": T, "geometry": "H=64 P=64 N=128 G=8",
                    "l2": "flushed between timed steps (256 MiB write)",
+                   "path": "ssm_scan_ws: rescaled prefill kernel, time segments (workspace %.1f MiB)"
+                           % (bd.workspace_bytes(1, T, 64, 64, 128, 8) / 2**20),
                    "parallelism": f"dp{world} (independent sequences per GPU)",
                    "vs_baseline_ref": "gllm PR 90: 3.5 ms on RTX PRO 6000 (context, another machine)"},
         "roofline": {"bound": "alu", "achieved": achieved / 1e12, "peak": peak_ops / 1e12,

@@ -125,15 +125,15 @@ int plan_prefill(const ssm_scan_tuning &t, bool scaled, int n_seqs, int n_tokens
     auto supported = scaled ? ssm::prefill_scaled_supported : ssm::prefill_supported;
     int lanes, rpt;
     if (scaled) {
-        // About 8 state elements of a row per lane, and up to 8 rows per lane
-        // (64 state registers) so that each B/C value read from shared memory
+        // About 8 state elements of a row per lane, and up to 4 rows per lane
+        // (32 state registers) so that each B/C value read from shared memory
         // feeds several rows.  The rows of a lane must share a head: RPT | P.
         lanes = t.lanes_per_row ? t.lanes_per_row : std::min(32, pow2ceil((N + 7) / 8));
         rpt = t.rows_per_thread;
         if (!rpt) {
-            rpt = 8;
+            rpt = 4;
             while (rpt > 1 && (P % rpt != 0 || rpt > lanes ||
-                               pick_vpl(N4, lanes, rpt, supported) * 4 * rpt > 64 ||
+                               pick_vpl(N4, lanes, rpt, supported) * 4 * rpt > 32 ||
                                pick_vpl(N4, lanes, rpt, supported) == 0))
                 rpt >>= 1;
         }
@@ -160,9 +160,10 @@ int plan_prefill(const ssm_scan_tuning &t, bool scaled, int n_seqs, int n_tokens
             return SSM_ERR_INVALID_ARG;
         g.rows_per_cta = t.rows_per_cta;
     } else {
-        // Largest block (up to 4 warps) that still gives every SM a block.
+        // Largest block (up to 4 warps) that still gives every SM a block; with
+        // time segments the segments supply the blocks.
         int warps = 4;
-        while (warps > 1) {
+        while (warps > 1 && !(scaled && allow_segments)) {
             const long long runs = (g.rows_per_group + warps * rows_per_warp - 1) / (warps * rows_per_warp);
             if ((long long)n_seqs * G * runs >= dev.sms)
                 break;
@@ -194,7 +195,7 @@ int plan_prefill(const ssm_scan_tuning &t, bool scaled, int n_seqs, int n_tokens
     pl.vpl = vpl;
 
     // Time segments: only the rescaled kernel has the state pass.  Automatic
-    // choice: enough (sequence, segment) units for about three consumer warps
+    // choice: enough (sequence, segment) units for about six consumer warps
     // per SM sub-partition.
     if (scaled && allow_segments && t.segment_tokens >= 0 && n_tokens > 0) {
         int seg = 0;
@@ -204,7 +205,7 @@ int plan_prefill(const ssm_scan_tuning &t, bool scaled, int n_seqs, int n_tokens
             seg = t.segment_tokens;
         } else {
             const long long warps_per_unit = (long long)G * g.runs_per_group * (threads / 32);
-            const long long target = 3LL * 4 * dev.sms;
+            const long long target = 6LL * 4 * dev.sms;      // consumer warps to keep resident
             if ((long long)n_seqs * warps_per_unit < target) {
                 const long long want = (target + warps_per_unit - 1) / warps_per_unit;
                 long long L = ((long long)n_tokens + want - 1) / want;

@@ -386,6 +386,7 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan
         // One token: U += (x dt / Lambda) B; with y: the lanes' parts of U . C
         // summed by shuffles (transposing over the RPT rows), then
         // y = Lambda (U . C) + D x from the lane that holds the row's sum.
+        float *yp = yrow;                   // y of the next token computed
         auto compute_token = [&](const TokenIn &in, int tt) {
             float2 a2[RPT], acc[RPT][2];
 #pragma unroll
@@ -393,30 +394,39 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan
                 const float alpha = in.xv[q] * in.cf.x;
                 a2[q] = f2(alpha, alpha);
             }
+            // all state updates first, then the dot products, so no FMA waits
+            // on the one issued just before it
 #pragma unroll
             for (int k = 0; k < VPL; ++k) {
                 const int cidx = k * LANES + j;
                 if (EXACT || cidx < N4) {
-                    const float4 bb = in.b[k], cc = in.c[k];
+                    const float4 bb = in.b[k];
 #pragma unroll
                     for (int q = 0; q < RPT; ++q) {
                         u[q][k][0] = __ffma2_rn(a2[q], f2(bb.x, bb.y), u[q][k][0]);      // A5
                         u[q][k][1] = __ffma2_rn(a2[q], f2(bb.z, bb.w), u[q][k][1]);
-                        if constexpr (kFull) {                                           // A6
-                            // two accumulators per row; the first product of each
-                            // starts it (no zero fill)
-                            float2 &ac = acc[q][k & 1];
-                            if (k < 2 && (EXACT || cidx < N4))
+                    }
+                }
+            }
+            if constexpr (kFull) {                                                       // A6
+                // two accumulators per row; the first product of each starts it
+#pragma unroll
+                for (int k = 0; k < VPL; ++k) {
+                    const int cidx = k * LANES + j;
+                    const float4 cc = in.c[k];
+#pragma unroll
+                    for (int q = 0; q < RPT; ++q) {
+                        float2 &ac = acc[q][k & 1];
+                        if (EXACT || cidx < N4) {
+                            if (k < 2)
                                 ac = __fmul2_rn(u[q][k][0], f2(cc.x, cc.y));
                             else
                                 ac = __ffma2_rn(u[q][k][0], f2(cc.x, cc.y), ac);
                             ac = __ffma2_rn(u[q][k][1], f2(cc.z, cc.w), ac);
+                        } else if (k < 2) {
+                            ac = f2(0.f, 0.f);
                         }
                     }
-                } else if (kFull && k < 2) {
-#pragma unroll
-                    for (int q = 0; q < RPT; ++q)
-                        acc[q][k & 1] = f2(0.f, 0.f);
                 }
             }
             if constexpr (kFull) {
@@ -428,7 +438,8 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan
                 }
                 const float ysum = reduce_rows<LANES, RPT>(part, j);
                 if (ywriter)
-                    yrow[(long long)tt * HP] = fmaf(in.cf.y, ysum, Dv * sX[tt * geo.rows_per_cta + rl + yq]);
+                    *yp = fmaf(in.cf.y, ysum, Dv * sX[tt * geo.rows_per_cta + rl + yq]);
+                yp += HP;
             }
         };
         // Anchor tokens of any head of the block split the chunk into segments;
