@@ -11,7 +11,11 @@ Two independent forms are provided:
                      independent (sequence, head) units only);
 * ``matrix_form`` -- the same map written out as a sum over earlier tokens with
                      explicit decay factors (``matrix_form.py``, NumPy float64),
-                     for tiny inputs.  It is used to pin the loop form.
+                     for tiny inputs.  It is used to pin the loop form;
+* ``chunked_form`` -- the recurrence unrolled over chunks of tokens (the SSD
+                     chunked matrix form with state passing between chunks,
+                     ``chunked_form.py``, NumPy float64): the decomposition the
+                     tensor-core kernels evaluate, checked against ``scan``.
 """
 from __future__ import annotations
 
@@ -22,6 +26,7 @@ import threading
 
 import numpy as np
 
+from .chunked_form import chunked_form  # noqa: F401
 from .matrix_form import matrix_form  # noqa: F401
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
