@@ -7,7 +7,9 @@ One step is one scan call over the 1 x 4096-token prefill workload at
 Nemotron-H geometry (64 heads x 64 x 128 state, 8 groups, fp32): state
 load, chunk staging, discretisation, state update, y readout and state store,
 all in the prefill kernel.  The same run also times the 16 x 1 decode step
-(300 steps over rotating slot sets) and reports it under "decode".
+(300 steps over rotating slot sets) and reports it under "decode", and the
+chunked matrix form on the TF32 tensor cores (ssm_scan_ssd, chunk 128) on the
+same prefill input under "ssd" (a lower-precision variant, not the headline).
 
 Prints one JSON line (rank 0).  Under torchrun every rank scans its own
 batch (weak scaling, no collective on the data path); the step time is the
@@ -40,6 +42,7 @@ METRIC = "scan tokens/s (1×4096 prefill), decode µs (16×1); % of HBM/FP32 roo
 PAGE_PREFILL_MS = 3.5
 PAGE_DECODE_US = 32.0
 FP32_LANES_PER_SM = 128
+TF32_PER_BF16 = 1.1 / 2.25    # nominal dense TF32 / BF16 tensor rate
 L2_FLUSH_BYTES = 256 << 20
 DECODE_STEPS = 300
 DECODE_SLOT_SETS = 8          # 8 x 32 MiB of slots rotate, 2x the 129 MB L2
@@ -61,6 +64,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-ssd", action="store_true")
     return ap.parse_args()
 
 
@@ -315,6 +319,49 @@ def run_decode(dev, rank):
     return dict(cold_us=cold, warm_graph_us=warm)
 
 
+def run_ssd(args, dev, inp, d, chunk=128):
+    """ssm_scan_ssd (the chunked form on the TF32 tensor cores) on the same
+    prefill input, timed like the prefill step (L2 flushed between steps)."""
+    from state_space_model_ssm_gb300 import binding as bd
+    g = inp.geom
+    nbytes = bd.ssd_workspace_bytes(inp.n_seqs, inp.n_tokens, g.n_heads, g.head_dim, g.d_state,
+                                    g.n_groups, chunk)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    state = d.state.clone()
+    y = torch.empty_like(d.x)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        bd.ssm_scan_ssd(state, d.x, d.dt, d.A, d.B, d.C, d.D, d.seq_starts, d.seq_lens, d.resume,
+                        y=y, chunk=chunk, workspace=ws)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    evs = [event_pair() for _ in range(args.steps)]
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    times = [e0.elapsed_time(e1) for e0, e1 in evs]
+    return sum(times) / len(times), nbytes
+
+
+def ssd_algorithmic_flops(inp, chunk):
+    """Dense FLOPs of the chunked form per call: per chunk, G groups x 2 Q^2 N
+    (C B^T) plus H heads x (2 Q^2 P (masked product with x) + 2 Q N P (C S_in^T)
+    + 2 Q N P (x^T B)), with Q = chunk (the causal half is not subtracted)."""
+    g = inp.geom
+    H, P, N, G = g.n_heads, g.head_dim, g.d_state, g.n_groups
+    chunks = sum((int(L) + chunk - 1) // chunk for L in inp.seq_lens.tolist())
+    Q = chunk
+    return chunks * (G * 2 * Q * Q * N + H * (2 * Q * Q * P + 4 * Q * N * P))
+
+
 def prefill_algorithmic(inp):
     T = int(inp.seq_lens.sum())
     H, P, N, G = inp.geom.n_heads, inp.geom.head_dim, inp.geom.d_state, inp.geom.n_groups
@@ -445,6 +492,27 @@ def ours(args):
                          "timing": "graph replay / 300 (includes the gaps between kernels)",
                          "algorithmic": f"{dbytes} bytes per launch ({sbytes} of state)"},
             "vs_page": PAGE_DECODE_US / dec["cold_us"],
+        }
+    if not args.no_ssd:
+        ssd_ms, ssd_ws = run_ssd(args, dev, inp, d)
+        flops = ssd_algorithmic_flops(inp, 128)
+        tf32_peak = peaks["bf16_tflops"] * TF32_PER_BF16
+        line["ssd"] = {
+            "what": ("ssm_scan_ssd: chunked matrix form, chunk 128, TF32 operands (rounded to nearest), "
+                     "fp32 accumulation and fp32 state pass; parity bound 5e-3 (1 + |ref|)"),
+            "ms_per_step": ssd_ms,
+            "value": T / (ssd_ms * 1e-3),
+            "unit": "tokens/s",
+            "dtype": "tf32",
+            "workspace_mib": ssd_ws / 2**20,
+            "launches_per_step": 4,
+            "roofline": {"bound": "tensor", "achieved": flops / (ssd_ms * 1e-3) / 1e12,
+                         "peak": tf32_peak, "unit": "TFLOP/s",
+                         "frac": flops / (ssd_ms * 1e-3) / 1e12 / tf32_peak,
+                         "peak_basis": "measured bf16 burst x 1.1/2.25 (nominal dense TF32/BF16)",
+                         "algorithmic": f"{flops} dense FLOPs per call",
+                         "hbm_frac": (alg_bytes / (ssd_ms * 1e-3)) / (peaks["hbm_gbs"] * 1e9),
+                         "traffic": None},
         }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_prefill(inp)

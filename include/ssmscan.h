@@ -173,6 +173,53 @@ size_t ssm_scan_workspace_bytes(int n_seqs, int n_tokens, int n_heads,
                                 const ssm_scan_tuning *tuning);
 
 /*
+ * The scan in chunked matrix form ("SSD") on the TF32 tensor cores.  The
+ * gllm PR 90 page ("keep the Mamba2 scan state in registers, stage tokens by
+ * chunk", "What changes" and "Not in this PR") names Mamba2's SSD
+ * chunked-matmul algorithm as the way to parallelise prefill over time and
+ * gives no algorithm; this form is the recurrence above unrolled over chunks
+ * of `chunk` tokens of each sequence.  With a_t = sum_{s<=t in the chunk}
+ * dt[s,h] A[h]:
+ *     y_t   = exp(a_t) S_in.C_t + sum_{s<=t} exp(a_t - a_s) dt_s (C_t.B_s) x_s + D x_t
+ *     S_out = exp(a_last) S_in + sum_s exp(a_last - a_s) dt_s x_s (x) B_s
+ * and S_in of chunk k+1 is S_out of chunk k.  In exact arithmetic it equals
+ * ssm_scan.  The contractions C B^T, (masked decay-weighted C B^T) x, S_in C^T
+ * and x^T B round their operands to TF32 (10-bit mantissa, round to nearest)
+ * and accumulate in fp32; the pass over chunks is fp32.  Expect
+ * |y - y_exact| <= 5e-3 (1 + |y_exact|), not the 1e-4 of ssm_scan.
+ *   chunk         tokens per chunk: 64 or 128 (0 = 128)
+ *   workspace     device memory, 256-byte aligned, at least
+ *                 ssm_scan_ssd_workspace_bytes(...) bytes for the same sizes
+ *                 and chunk (chunk states [units][n_heads][head_dim][d_state]
+ *                 fp32, units <= n_seqs + ceil(n_tokens / chunk)); scratch:
+ *                 undefined afterwards, not shared by calls that overlap on
+ *                 the GPU
+ * Same arguments, layouts and metadata rules as ssm_scan, and also:
+ *   - x and y 16-byte aligned;
+ *   - head_dim a multiple of 16 and at most 128 (else SSM_ERR_UNSUPPORTED);
+ *   - the chunk's shared-memory tiles must fit one block: SSM_ERR_UNSUPPORTED
+ *     otherwise (for example d_state 1024; d_state up to 256 fits with
+ *     chunk 64, up to 128 with chunk 128).
+ * SSM_ERR_INVALID_ARG for a missing, misaligned or too small workspace or a
+ * chunk other than 0, 64 or 128.
+ */
+int ssm_scan_ssd(float *state_slots, const float *x, const float *dt,
+                 const float *A, const float *B, const float *C, const float *D,
+                 float *y, const int32_t *seq_starts, const int32_t *seq_lens,
+                 const int32_t *resume_flags, int n_seqs, int n_tokens,
+                 int n_heads, int head_dim, int d_state, int n_groups,
+                 int chunk, void *workspace, size_t workspace_bytes,
+                 void *stream);
+
+/*
+ * Bytes of workspace ssm_scan_ssd needs for these sizes and chunk (the same on
+ * every device); 0 for invalid or unsupported arguments.
+ */
+size_t ssm_scan_ssd_workspace_bytes(int n_seqs, int n_tokens, int n_heads,
+                                    int head_dim, int d_state, int n_groups,
+                                    int chunk);
+
+/*
  * Size of the scratch that ssm_scan_static keeps in device memory (32 MiB per
  * device, held from the library's load on that device until process exit).
  */

@@ -8,7 +8,8 @@ ctypes.  ``workloads`` draws the seeded synthetic inputs.
 """
 from .binding import (PATH_AUTO, PATH_DECODE, PATH_PREFILL, PATH_PREFILL_DIRECT,  # noqa: F401
                       SsmScanError, Tuning,
-                      load, ssm_scan, status_string)
+                      load, ssd_workspace_bytes, ssm_scan, ssm_scan_ssd,
+                      status_string)
 
-__all__ = ["ssm_scan", "Tuning", "SsmScanError", "PATH_AUTO", "PATH_DECODE",
+__all__ = ["ssm_scan", "ssm_scan_ssd", "ssd_workspace_bytes", "Tuning", "SsmScanError", "PATH_AUTO", "PATH_DECODE",
            "PATH_PREFILL", "PATH_PREFILL_DIRECT", "load", "status_string"]

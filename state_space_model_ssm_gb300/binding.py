@@ -67,6 +67,10 @@ def load():
             lib.ssm_scan_ws.argtypes = _SCAN_ARGS + [ctypes.POINTER(Tuning), _P, ctypes.c_size_t, _P]
             lib.ssm_scan_workspace_bytes.restype = ctypes.c_size_t
             lib.ssm_scan_workspace_bytes.argtypes = [_I] * 6 + [ctypes.POINTER(Tuning)]
+            lib.ssm_scan_ssd.restype = _I
+            lib.ssm_scan_ssd.argtypes = _SCAN_ARGS + [_I, _P, ctypes.c_size_t, _P]
+            lib.ssm_scan_ssd_workspace_bytes.restype = ctypes.c_size_t
+            lib.ssm_scan_ssd_workspace_bytes.argtypes = [_I] * 7
             lib.ssm_status_string.restype = ctypes.c_char_p
             lib.ssm_status_string.argtypes = [_I]
             _lib = lib
@@ -113,6 +117,24 @@ def workspace_bytes(n_seqs, n_tokens, n_heads, head_dim, d_state, n_groups,
     tp = ctypes.byref(tuning) if tuning is not None else None
     return int(load().ssm_scan_workspace_bytes(int(n_seqs), int(n_tokens), int(n_heads),
                                                int(head_dim), int(d_state), int(n_groups), tp))
+
+
+def ssd_raw(state, x, dt, A, B, C, D, y, seq_starts, seq_lens, resume,
+            n_seqs, n_tokens, n_heads, head_dim, d_state, n_groups, chunk,
+            workspace, workspace_bytes, stream=0) -> int:
+    """ssm_scan_ssd with integer pointers; returns the status code."""
+    args = [_P(int(p) if p else None) for p in
+            (state, x, dt, A, B, C, D, y, seq_starts, seq_lens, resume)]
+    args += [int(n_seqs), int(n_tokens), int(n_heads), int(head_dim), int(d_state), int(n_groups)]
+    return load().ssm_scan_ssd(*args, int(chunk), _P(int(workspace) if workspace else None),
+                               ctypes.c_size_t(int(workspace_bytes)), _P(int(stream) if stream else None))
+
+
+def ssd_workspace_bytes(n_seqs, n_tokens, n_heads, head_dim, d_state, n_groups, chunk=0) -> int:
+    """Bytes of workspace ssm_scan_ssd needs (0 for unsupported arguments)."""
+    return int(load().ssm_scan_ssd_workspace_bytes(int(n_seqs), int(n_tokens), int(n_heads),
+                                                   int(head_dim), int(d_state), int(n_groups),
+                                                   int(chunk)))
 
 
 def _check(t, name, dtype, device, shape=None):
@@ -173,4 +195,51 @@ def ssm_scan(state_slots, x, dt, A, B, C, D, seq_starts, seq_lens, resume_flags,
                       workspace=ws_ptr, workspace_bytes=ws_bytes)
     if rc != SSM_OK:
         raise SsmScanError(rc, "ssm_scan")
+    return y
+
+
+def ssm_scan_ssd(state_slots, x, dt, A, B, C, D, seq_starts, seq_lens, resume_flags,
+                 y=None, *, chunk: int = 0, workspace=None, stream=None):
+    """The scan in chunked matrix form on the TF32 tensor cores (``ssm_scan_ssd``).
+
+    Same tensors as ``ssm_scan``; y matches the exact scan to about
+    5e-3 * (1 + |y|).  ``workspace`` is a contiguous CUDA tensor of at least
+    ``ssd_workspace_bytes(...)`` bytes; if omitted one is allocated with torch
+    for this call.
+    """
+    dev = state_slots.device
+    if dev.type != "cuda":
+        raise ValueError("the scan runs on CUDA tensors only")
+    n, H, P, N = state_slots.shape
+    T = x.shape[0]
+    G = B.shape[1]
+    f32, i32 = torch.float32, torch.int32
+    _check(state_slots, "state_slots", f32, dev)
+    _check(x, "x", f32, dev, (T, H, P))
+    _check(dt, "dt", f32, dev, (T, H))
+    _check(A, "A", f32, dev, (H,))
+    _check(B, "B", f32, dev, (T, G, N))
+    _check(C, "C", f32, dev, (T, G, N))
+    _check(D, "D", f32, dev, (H,))
+    for nm, t in (("seq_starts", seq_starts), ("seq_lens", seq_lens), ("resume_flags", resume_flags)):
+        _check(t, nm, i32, dev, (n,))
+    if y is None:
+        y = torch.empty((T, H, P), dtype=f32, device=dev)
+    _check(y, "y", f32, dev, (T, H, P))
+    need = ssd_workspace_bytes(n, T, H, P, N, G, chunk)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    if workspace.device != dev or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous tensor on the scan's device")
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    with torch.cuda.device(dev):
+        rc = ssd_raw(state_slots.data_ptr(), x.data_ptr(), dt.data_ptr(), A.data_ptr(),
+                     B.data_ptr(), C.data_ptr(), D.data_ptr(), y.data_ptr(),
+                     seq_starts.data_ptr(), seq_lens.data_ptr(), resume_flags.data_ptr(),
+                     n, T, H, P, N, G, chunk, workspace.data_ptr(),
+                     workspace.numel() * workspace.element_size(), stream=handle)
+    if rc != SSM_OK:
+        raise SsmScanError(rc, "ssm_scan_ssd")
     return y

@@ -363,6 +363,153 @@ int scan_impl(float *state, const float *x, const float *dt, const float *A, con
     return SSM_OK;
 }
 
+// Layout of the SSD workspace and launch shape of its kernels.
+struct SsdLayout {
+    int chunk = 0;
+    long long max_units = 0;
+    size_t off_units = 0, off_n_units = 0, off_unit_base = 0, off_decay = 0, off_state = 0, bytes = 0;
+    ssm::SsdGeom g{};
+};
+
+// Shared-memory row stride (floats) of at least `width` that is == `residue`
+// (mod 32), so the fragment loads of a warp hit 32 distinct banks.
+int bank_stride(int width, int residue) { return width + ((residue - width % 32) + 64) % 32; }
+
+// Arguments the SSD form accepts, its workspace layout and (with dev) its
+// launch shape.  Host only; returns SSM_OK or an error status.
+int plan_ssd(int n_seqs, int n_tokens, int H, int P, int N, int G, int chunk, const DeviceInfo *dev,
+             SsdLayout *out)
+{
+    SsdLayout L;
+    L.chunk = chunk ? chunk : 128;
+    if (!ssm::ssd_supported_chunk(L.chunk))
+        return SSM_ERR_INVALID_ARG;
+    if (P % 16 != 0 || P > ssm::ssd_max_head_dim())
+        return SSM_ERR_UNSUPPORTED;
+    const int Q = L.chunk;
+    ssm::SsdGeom &g = L.g;
+    g.n_pad = (N + 7) & ~7;
+    g.bs_stride = bank_stride(g.n_pad, 8);
+    g.xw_stride = bank_stride(P, 8);
+    g.cs_stride = bank_stride(g.n_pad, 4);
+    g.xs_stride = bank_stride(P, 4);
+    // Shared memory of each kernel with `nb` tiles in flight (see ssd.cu).
+    auto smem_state = [&](int nb) {
+        return sizeof(float) * ((size_t)Q * g.bs_stride + (size_t)nb * Q * g.xw_stride + 2 * (size_t)Q);
+    };
+    const size_t out_buf = (size_t)Q * g.xs_stride + (size_t)P * g.cs_stride;
+    auto smem_out = [&](int nb) {
+        return sizeof(float) * ((size_t)Q * g.cs_stride + std::max((size_t)Q * g.cs_stride, out_buf) +
+                                (nb == 2 ? out_buf : 0) + 4 * (size_t)Q);
+    };
+    g.state_buffers = g.out_buffers = 2;
+    g.smem_state = smem_state(2);
+    g.smem_out = smem_out(2);
+    L.max_units = (long long)n_seqs + ((long long)n_tokens + Q - 1) / Q;
+    if (L.max_units > INT_MAX || G > 65535)
+        return SSM_ERR_UNSUPPORTED;
+    const size_t slot = (size_t)H * P * N * sizeof(float);
+    size_t off = 0;
+    L.off_units = off;      off = align256(off + (size_t)L.max_units * sizeof(int2));
+    L.off_n_units = off;    off = align256(off + sizeof(int));
+    L.off_unit_base = off;  off = align256(off + ((size_t)n_seqs + 1) * sizeof(int));
+    L.off_decay = off;      off = align256(off + (size_t)L.max_units * H * sizeof(float));
+    L.off_state = off;      off = align256(off + (size_t)L.max_units * slot);
+    L.bytes = off;
+    if (dev) {
+        const size_t cap = (size_t)dev->smem_optin;
+        if (g.smem_state > cap) {               // one x tile at a time
+            g.state_buffers = 1;
+            g.smem_state = smem_state(1);
+        }
+        if (g.smem_out > cap) {                 // one (x, S_in) tile pair at a time
+            g.out_buffers = 1;
+            g.smem_out = smem_out(1);
+        }
+        if (g.smem_state > cap || g.smem_out > cap)
+            return SSM_ERR_UNSUPPORTED;
+        // Split a group's heads over blocks until there are about four
+        // blocks per SM (C B^T is formed once per block).
+        const int hpg = H / G;
+        const long long blocks = L.max_units * G;
+        const long long want = 4LL * dev->sms;
+        const int split = (int)std::min<long long>(hpg, std::max<long long>(1, (want + blocks - 1) / blocks));
+        g.heads_per_cta = (hpg + split - 1) / split;
+    }
+    *out = L;
+    return SSM_OK;
+}
+
+int ssd_impl(float *state, const float *x, const float *dt, const float *A, const float *B,
+             const float *C, const float *D, float *y, const int32_t *seq_starts,
+             const int32_t *seq_lens, const int32_t *resume, int n_seqs, int n_tokens, int H, int P,
+             int N, int G, int chunk, void *workspace, size_t workspace_bytes, void *stream_v)
+{
+    if (n_seqs < 0 || n_tokens < 0 || H <= 0 || P <= 0 || N <= 0 || G <= 0 || chunk < 0)
+        return SSM_ERR_INVALID_ARG;
+    if (H % G != 0)
+        return SSM_ERR_INVALID_ARG;
+    if (N % 4 != 0 || N > kMaxDState)
+        return SSM_ERR_UNSUPPORTED;
+    if ((long long)H * P > INT_MAX / 2)
+        return SSM_ERR_UNSUPPORTED;
+    SsdLayout L;
+    int rc = plan_ssd(n_seqs, n_tokens, H, P, N, G, chunk, nullptr, &L);
+    if (rc != SSM_OK)
+        return rc;
+    if (n_seqs == 0)
+        return SSM_OK;
+    if (!state || !A || !D || !seq_starts || !seq_lens || !resume)
+        return SSM_ERR_INVALID_ARG;
+    if (n_tokens > 0 && (!x || !dt || !B || !C || !y))
+        return SSM_ERR_INVALID_ARG;
+    if (!aligned(state, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(x, 16) || !aligned(y, 16))
+        return SSM_ERR_INVALID_ARG;
+    if (!aligned(dt, 4) || !aligned(A, 4) || !aligned(D, 4) || !aligned(seq_starts, 4) ||
+        !aligned(seq_lens, 4) || !aligned(resume, 4))
+        return SSM_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.bytes)
+        return SSM_ERR_INVALID_ARG;
+
+    DeviceInfo dev;
+    rc = device_info(&dev);
+    if (rc != SSM_OK)
+        return rc;
+    rc = plan_ssd(n_seqs, n_tokens, H, P, N, G, chunk, &dev, &L);
+    if (rc != SSM_OK)
+        return rc;
+
+    ssm::ScanArgs a;
+    a.state = state; a.x = x; a.dt = dt; a.A = A; a.B = B; a.C = C; a.D = D; a.y = y;
+    a.seq_starts = seq_starts; a.seq_lens = seq_lens; a.resume = resume;
+    a.n_seqs = n_seqs; a.n_tokens = n_tokens; a.H = H; a.P = P; a.N = N; a.G = G;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_v);
+    if (check_env()) {
+        rc = check_metadata(a, stream);
+        if (rc != SSM_OK)
+            return rc;
+    }
+
+    char *ws = static_cast<char *>(workspace);
+    ssm::SegmentPlan seg{};
+    seg.units = reinterpret_cast<const int2 *>(ws + L.off_units);
+    seg.n_units = reinterpret_cast<const int *>(ws + L.off_n_units);
+    seg.unit_base = reinterpret_cast<const int *>(ws + L.off_unit_base);
+    seg.seg_len = L.chunk;
+    ssm::SsdPlan plan;
+    plan.units = seg.units;
+    plan.n_units = seg.n_units;
+    plan.unit_base = seg.unit_base;
+    plan.chunk = L.chunk;
+    plan.chunk_logdecay = reinterpret_cast<float *>(ws + L.off_decay);
+    plan.chunk_state = reinterpret_cast<float *>(ws + L.off_state);
+    const int mu = (int)L.max_units;
+    if (ssm::launch_segment_plan(a, seg, mu, stream) != cudaSuccess ||
+        ssm::launch_ssd(a, plan, L.g, mu, stream) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    return SSM_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -419,6 +566,29 @@ size_t ssm_scan_workspace_bytes(int n_seqs, int n_tokens, int n_heads, int head_
     if (plan_prefill(t, true, n_seqs, n_tokens, n_heads, head_dim, d_state, n_groups, dev, true, &pl) != SSM_OK)
         return 0;
     return pl.seg_len > 0 ? pl.ws_bytes : 0;
+}
+
+int ssm_scan_ssd(float *state_slots, const float *x, const float *dt, const float *A, const float *B,
+                 const float *C, const float *D, float *y, const int32_t *seq_starts,
+                 const int32_t *seq_lens, const int32_t *resume_flags, int n_seqs, int n_tokens,
+                 int n_heads, int head_dim, int d_state, int n_groups, int chunk, void *workspace,
+                 size_t workspace_bytes, void *stream)
+{
+    return ssd_impl(state_slots, x, dt, A, B, C, D, y, seq_starts, seq_lens, resume_flags, n_seqs,
+                    n_tokens, n_heads, head_dim, d_state, n_groups, chunk, workspace, workspace_bytes,
+                    stream);
+}
+
+size_t ssm_scan_ssd_workspace_bytes(int n_seqs, int n_tokens, int n_heads, int head_dim, int d_state,
+                                    int n_groups, int chunk)
+{
+    if (n_seqs <= 0 || n_tokens < 0 || n_heads <= 0 || head_dim <= 0 || d_state <= 0 || n_groups <= 0 ||
+        chunk < 0 || n_heads % n_groups != 0 || d_state % 4 != 0 || d_state > kMaxDState)
+        return 0;
+    SsdLayout L;
+    if (plan_ssd(n_seqs, n_tokens, n_heads, head_dim, d_state, n_groups, chunk, nullptr, &L) != SSM_OK)
+        return 0;
+    return L.bytes;
 }
 
 const char *ssm_status_string(int status)

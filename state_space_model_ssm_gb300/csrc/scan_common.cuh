@@ -159,6 +159,35 @@ bool prefill_scaled_supported(int lanes, int vpl, int rpt);
 size_t prefill_scaled_smem_bytes(const PrefillGeom &g, int N, int lanes);
 constexpr int kScaledMaxChunk = 32;    // one warp lane per token in the coefficient pass
 
+// The SSD chunked form (ssd.cu): work unit u is chunk units[u] = (sequence,
+// k) covering tokens [k*chunk, (k+1)*chunk) of the sequence.
+struct SsdPlan {
+    const int2 *units;        // [max_units] (device), filled by the plan kernel
+    const int *n_units;       // device count of valid units
+    const int *unit_base;     // [n_seqs + 1] first unit of each sequence
+    int chunk;                // tokens per chunk (64 or 128)
+    float *chunk_state;       // [max_units][H][P][N]: chunk state, then the chunk's incoming state
+    float *chunk_logdecay;    // [max_units][H]: sum of dt*A over the chunk
+};
+
+// Shared-memory strides (floats) and launch shape of the SSD kernels.
+struct SsdGeom {
+    int n_pad;                // d_state rounded up to a multiple of 8
+    int bs_stride;            // chunk-state kernel: B rows (== 8 mod 32)
+    int xw_stride;            // chunk-state kernel: weighted x rows (== 8 mod 32)
+    int cs_stride;            // output kernel: C, B and state rows (== 4 mod 32)
+    int xs_stride;            // output kernel: x rows (== 4 mod 32)
+    int heads_per_cta;        // heads of one group a block handles
+    int state_buffers;        // chunk-state kernel: x tiles in flight (1 or 2)
+    int out_buffers;          // output kernel: (x, S_in) tile pairs in flight (1 or 2)
+    size_t smem_state, smem_out;
+};
+
+cudaError_t launch_ssd(const ScanArgs &a, const SsdPlan &plan, const SsdGeom &g, int max_units,
+                       cudaStream_t stream);
+bool ssd_supported_chunk(int chunk);
+int ssd_max_head_dim();
+
 cudaError_t launch_decode(const ScanArgs &a, const DecodeGeom &g, int lanes,
                           int vpl, int rpt, int grid_seqs, cudaStream_t stream);
 bool decode_supported(int lanes, int vpl, int rpt);

@@ -74,3 +74,30 @@ def assert_parity(inp, y_gpu, s_gpu, y_ref, s_ref, heads=None, tol=TOL):
     sbound = tol * (1.0 + np.abs(sr))
     assert np.all(serr <= sbound), f"state parity: max err {serr.max():.3e}"
     return float(err.max() if err.size else 0.0), float(serr.max() if serr.size else 0.0)
+
+
+# SSD chunked form with TF32 operands: max |gpu - ref| <= SSD_TOL * (1 + |ref|).
+SSD_TOL = 5e-3
+
+
+def run_gpu_ssd(inp, chunk=0, device="cuda", stream=None, y_fill=float("nan")):
+    """ssm_scan_ssd on a ScanInputs bundle with NaN guard bands around y and the
+    state and a NaN-filled workspace of exactly the size the library asks for
+    (so a read of a word the call did not write shows up).  Returns (y, state)
+    as float64 numpy arrays."""
+    d = inp.to(device)
+    g = inp.geom
+    sbuf, state = _guarded(tuple(inp.state.shape), float("nan"), device)
+    state.copy_(d.state)
+    ybuf, y = _guarded(tuple(inp.x.shape), y_fill, device)
+    need = bd.ssd_workspace_bytes(inp.n_seqs, inp.n_tokens, g.n_heads, g.head_dim, g.d_state,
+                                  g.n_groups, chunk)
+    assert need > 0
+    ws = torch.full((need // 4,), float("nan"), dtype=torch.float32, device=device)
+    bd.ssm_scan_ssd(state, d.x, d.dt, d.A, d.B, d.C, d.D, d.seq_starts, d.seq_lens, d.resume,
+                    y=y, chunk=chunk, workspace=ws, stream=stream)
+    torch.cuda.synchronize()
+    for buf in (sbuf, ybuf):
+        head, tail = buf[:GUARD], buf[-GUARD:]
+        assert torch.isnan(head).all() and torch.isnan(tail).all(), "guard band overwritten"
+    return y.double().cpu().numpy(), state.double().cpu().numpy()

@@ -104,3 +104,62 @@ def test_binding_refuses_cpu_tensors():
     z = torch.zeros(1, 1, 1, 4)
     with pytest.raises(ValueError):
         bd.ssm_scan(z, z, z, z, z, z, z, z, z, z)
+
+
+# ---- ssm_scan_ssd: host checks (never reach the device) ----
+SSD_GOOD = dict(n_seqs=2, n_tokens=100, n_heads=4, head_dim=16, d_state=32, n_groups=2)
+
+
+def _ssd_call(lib, chunk=64, ws=PTR, ws_bytes=None, **over):
+    ptrs = dict(state=PTR, x=PTR, dt=PTR, A=PTR, B=PTR, C=PTR, D=PTR, y=PTR,
+                seq_starts=PTR, seq_lens=PTR, resume=PTR)
+    sizes = dict(SSD_GOOD)
+    for k, v in over.items():
+        (ptrs if k in ptrs else sizes)[k] = v
+    if ws_bytes is None:
+        ws_bytes = bd.ssd_workspace_bytes(**sizes, chunk=chunk)
+    return bd.ssd_raw(**ptrs, **sizes, chunk=chunk, workspace=ws, workspace_bytes=ws_bytes)
+
+
+def test_header_declares_the_ssd_entry_points():
+    assert {"ssm_scan_ssd", "ssm_scan_ssd_workspace_bytes"} <= set(bd.declared_functions())
+
+
+def test_ssd_workspace_bytes(lib):
+    # units <= n_seqs + ceil(n_tokens / chunk); one fp32 state per unit and head
+    for chunk, units in ((64, 2 + 2), (128, 2 + 1), (0, 2 + 1)):
+        nbytes = bd.ssd_workspace_bytes(**SSD_GOOD, chunk=chunk)
+        state_bytes = units * 4 * 16 * 32 * 4
+        assert state_bytes < nbytes <= state_bytes + 5 * 256 + units * (8 + 4 * 4) + 3 * 4
+        assert nbytes % 256 == 0
+    # 1 x 4096 tokens at 64 heads x 64 x 128: 33 units of 2 MiB
+    big = bd.ssd_workspace_bytes(1, 4096, 64, 64, 128, 8, 128)
+    assert 33 * (2 << 20) < big < 33 * (2 << 20) + 16384
+    for bad in (dict(chunk=32), dict(chunk=-1), dict(head_dim=24), dict(head_dim=144),
+                dict(d_state=30), dict(n_groups=3), dict(n_seqs=0)):
+        args = dict(SSD_GOOD, chunk=64)
+        args.update(bad)
+        assert bd.ssd_workspace_bytes(**args) == 0, bad
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(chunk=32), bd.SSM_ERR_INVALID_ARG),
+    (dict(chunk=-1), bd.SSM_ERR_INVALID_ARG),
+    (dict(head_dim=24), bd.SSM_ERR_UNSUPPORTED),         # not a multiple of 16
+    (dict(head_dim=144), bd.SSM_ERR_UNSUPPORTED),        # above 128
+    (dict(d_state=30), bd.SSM_ERR_UNSUPPORTED),
+    (dict(n_groups=3), bd.SSM_ERR_INVALID_ARG),
+    (dict(ws=0), bd.SSM_ERR_INVALID_ARG),                # no workspace
+    (dict(ws=PTR + 16), bd.SSM_ERR_INVALID_ARG),         # workspace not 256-byte aligned
+    (dict(ws_bytes=4096), bd.SSM_ERR_INVALID_ARG),       # workspace too small
+    (dict(x=PTR + 4), bd.SSM_ERR_INVALID_ARG),           # x and y must be 16-byte aligned here
+    (dict(y=PTR + 8), bd.SSM_ERR_INVALID_ARG),
+    (dict(state=0), bd.SSM_ERR_INVALID_ARG),
+    (dict(B=PTR + 4), bd.SSM_ERR_INVALID_ARG),
+])
+def test_ssd_host_rejects_bad_arguments(lib, over, expect):
+    assert _ssd_call(lib, **over) == expect
+
+
+def test_ssd_empty_batch_is_a_noop(lib):
+    assert _ssd_call(lib, n_seqs=0, state=0, x=0, y=0, ws=0, ws_bytes=0) == bd.SSM_OK
