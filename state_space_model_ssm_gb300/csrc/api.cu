@@ -43,7 +43,8 @@ int pick_vpl(int N4, int lanes, int rpt, bool (*supported)(int, int, int))
 
 struct DeviceInfo {
     int sms = 0;
-    int smem_optin = 0;
+    int smem_optin = 0;        // largest dynamic shared memory of one block
+    int smem_per_sm = 0;       // shared memory of one SM
 };
 
 int device_info(DeviceInfo *out)
@@ -59,6 +60,8 @@ int device_info(DeviceInfo *out)
         if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return SSM_ERR_CUDA;
         if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return SSM_ERR_CUDA;
+        if (cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess)
             return SSM_ERR_CUDA;
         cache[dev] = d;
     }
@@ -367,7 +370,8 @@ int scan_impl(float *state, const float *x, const float *dt, const float *A, con
 struct SsdLayout {
     int chunk = 0;
     long long max_units = 0;
-    size_t off_units = 0, off_n_units = 0, off_unit_base = 0, off_decay = 0, off_state = 0, bytes = 0;
+    size_t off_units = 0, off_n_units = 0, off_status = 0, off_unit_base = 0, off_decay = 0, off_state = 0;
+    size_t bytes = 0;
     ssm::SsdGeom g{};
 };
 
@@ -412,19 +416,33 @@ int plan_ssd(int n_seqs, int n_tokens, int H, int P, int N, int G, int chunk, co
     size_t off = 0;
     L.off_units = off;      off = align256(off + (size_t)L.max_units * sizeof(int2));
     L.off_n_units = off;    off = align256(off + sizeof(int));
+    L.off_status = off;     off = align256(off + sizeof(int));
     L.off_unit_base = off;  off = align256(off + ((size_t)n_seqs + 1) * sizeof(int));
     L.off_decay = off;      off = align256(off + (size_t)L.max_units * H * sizeof(float));
     L.off_state = off;      off = align256(off + (size_t)L.max_units * slot);
     L.bytes = off;
     if (dev) {
         const size_t cap = (size_t)dev->smem_optin;
-        if (g.smem_state > cap) {               // one x tile at a time
+        // Blocks of `bytes` dynamic shared memory that fit one SM (1 KiB per
+        // block is reserved by the runtime).
+        auto per_sm = [&](size_t bytes) { return (size_t)dev->smem_per_sm / (bytes + 1024); };
+        // One x tile at a time when two tiles do not fit, or when one tile lets
+        // more blocks share an SM (their copies then overlap across blocks).
+        if (g.smem_state > cap || per_sm(smem_state(1)) > per_sm(smem_state(2))) {
             g.state_buffers = 1;
             g.smem_state = smem_state(1);
         }
         if (g.smem_out > cap) {                 // one (x, S_in) tile pair at a time
             g.out_buffers = 1;
             g.smem_out = smem_out(1);
+        }
+        // The output kernel on tcgen05 where its tiles fit, else on mma.sync.
+        const int tc_buffers = ssm::ssd_tc_buffers(Q, g.n_pad, P, cap);
+        g.use_tc = tc_buffers > 0 ? 1 : 0;
+        if (g.use_tc) {
+            g.out_buffers = tc_buffers;
+            g.smem_out = ssm::ssd_tc_smem_bytes(g.n_pad, P, tc_buffers);
+            g.tmem_cols = ssm::ssd_tc_tmem_cols(g.n_pad, P);
         }
         if (g.smem_state > cap || g.smem_out > cap)
             return SSM_ERR_UNSUPPORTED;
@@ -503,10 +521,21 @@ int ssd_impl(float *state, const float *x, const float *dt, const float *A, cons
     plan.chunk = L.chunk;
     plan.chunk_logdecay = reinterpret_cast<float *>(ws + L.off_decay);
     plan.chunk_state = reinterpret_cast<float *>(ws + L.off_state);
+    plan.status = reinterpret_cast<int *>(ws + L.off_status);
     const int mu = (int)L.max_units;
+    if (cudaMemsetAsync(plan.status, 0, sizeof(int), stream) != cudaSuccess)
+        return SSM_ERR_CUDA;
     if (ssm::launch_segment_plan(a, seg, mu, stream) != cudaSuccess ||
         ssm::launch_ssd(a, plan, L.g, mu, stream) != cudaSuccess)
         return SSM_ERR_CUDA;
+    if (check_env()) {                      // debug: report a bounded wait that gave up
+        int st = 0;
+        if (cudaMemcpyAsync(&st, plan.status, sizeof(int), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+            cudaStreamSynchronize(stream) != cudaSuccess)
+            return SSM_ERR_CUDA;
+        if (st != 0)
+            return SSM_ERR_TIMEOUT;
+    }
     return SSM_OK;
 }
 

@@ -168,6 +168,7 @@ struct SsdPlan {
     int chunk;                // tokens per chunk (64 or 128)
     float *chunk_state;       // [max_units][H][P][N]: chunk state, then the chunk's incoming state
     float *chunk_logdecay;    // [max_units][H]: sum of dt*A over the chunk
+    int *status;              // device word: nonzero when a kernel's bounded wait gave up
 };
 
 // Shared-memory strides (floats) and launch shape of the SSD kernels.
@@ -178,6 +179,8 @@ struct SsdGeom {
     int cs_stride;            // output kernel: C, B and state rows (== 4 mod 32)
     int xs_stride;            // output kernel: x rows (== 4 mod 32)
     int heads_per_cta;        // heads of one group a block handles
+    int use_tc;               // output kernel on tcgen05 (ssd_tc.cu) instead of mma.sync
+    int tmem_cols;            // TMEM columns the tcgen05 output kernel allocates
     int state_buffers;        // chunk-state kernel: x tiles in flight (1 or 2)
     int out_buffers;          // output kernel: (x, S_in) tile pairs in flight (1 or 2)
     size_t smem_state, smem_out;
@@ -186,6 +189,11 @@ struct SsdGeom {
 cudaError_t launch_ssd(const ScanArgs &a, const SsdPlan &plan, const SsdGeom &g, int max_units,
                        cudaStream_t stream);
 bool ssd_supported_chunk(int chunk);
+int ssd_tc_buffers(int chunk, int n_pad, int P, size_t smem_optin);   // 0: not supported
+int ssd_tc_tmem_cols(int n_pad, int P);
+size_t ssd_tc_smem_bytes(int n_pad, int P, int nbuf);
+cudaError_t launch_ssd_output_tc(const ScanArgs &a, const SsdPlan &plan, const SsdGeom &g, int max_units,
+                                 cudaStream_t stream);
 int ssd_max_head_dim();
 
 cudaError_t launch_decode(const ScanArgs &a, const DecodeGeom &g, int lanes,

@@ -24,195 +24,15 @@
 // A block of the chunk-state and output kernels handles one chunk, one group
 // and a run of that group's heads, so B and C are staged (and C B^T formed)
 // once for all of those heads.
-#include "scan_common.cuh"
+#include "ssd_common.cuh"
 
 namespace ssm {
 
 namespace {
 
+using namespace ssd;
+
 constexpr int kStateThreads = 256;
-
-// Round a finite float to TF32 (10 mantissa bits), to nearest with ties away
-// from zero: add half a unit of the 11th mantissa bit to the magnitude, then
-// clear the 13 bits below the TF32 mantissa.  (Infinities stay infinite.)
-__device__ __forceinline__ uint32_t tf32_bits(float v)
-{
-    return (__float_as_uint(v) + 0x1000u) & 0xffffe000u;
-}
-
-// 2^x with the special-function unit (relative error about 2^-22; results
-// below the normal range flush to zero).
-__device__ __forceinline__ float ex2(float x)
-{
-    float r;
-    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(r) : "f"(x));
-    return r;
-}
-
-__device__ __forceinline__ float tf32_round(float v) { return __uint_as_float(tf32_bits(v)); }
-
-__device__ __forceinline__ float4 tf32_round4(float4 v)
-{
-    return make_float4(tf32_round(v.x), tf32_round(v.y), tf32_round(v.z), tf32_round(v.w));
-}
-
-__device__ __forceinline__ uint32_t fb(float v) { return __float_as_uint(v); }
-
-// d += A * B for one m16n8k8 tile: A 16x8 row-major fragment (a0..a3),
-// B 8x8 column fragment (b0, b1), fp32 accumulators d0..d3.
-__device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1)
-{
-    asm("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};\n"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// 16-byte cp.async; src_bytes == 0 writes 16 zero bytes and reads nothing.
-__device__ __forceinline__ void cp_async16_zfill(void *smem, const void *gmem, int src_bytes)
-{
-    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem), "r"(src_bytes)
-                 : "memory");
-}
-
-// Four 8x8 tiles of 32-bit words (each row 16 bytes) from shared memory; lane
-// l gives the row address of tile l/8, row l%8, and receives word (l%4) of
-// row (l/4) of each tile: the m16n8k8 TF32 fragment layout.
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const float *p)
-{
-    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(p));
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(s)
-                 : "memory");
-}
-
-// Lane layout for row tiles `w4` float4 cells wide: `lanes` (a power of two,
-// at least w4 unless w4 > 32) lanes share a row, so one warp instruction
-// covers 32/lanes rows and a thread keeps a fixed column; no division per cell.
-struct RowMap {
-    int row0;    // first row of this thread
-    int col;     // first float4 column of this thread
-    int lanes;   // lanes per row (column step)
-    int step;    // rows per pass of the block
-};
-
-__device__ __forceinline__ RowMap row_map(int w4, int lane, int warp, int nwarps)
-{
-    int lg = 0;
-    while ((1 << lg) < w4 && lg < 5)
-        ++lg;
-    RowMap m;
-    m.lanes = 1 << lg;
-    const int rpi = 32 >> lg;                         // rows per warp instruction
-    m.row0 = warp * rpi + (lane >> lg);
-    m.col = lane & (m.lanes - 1);
-    m.step = nwarps * rpi;
-    return m;
-}
-
-// Asynchronous copy of a rows x w4 float4 tile: global row r at g + r*gstride
-// floats, shared row r at s + r*sstride.  Cells with r >= vrows or column
-// >= v4 are zero-filled without a global read (vrows >= 1, so g is a valid
-// address).
-__device__ __forceinline__ void rows_copy(float *s, int sstride, const float *g, size_t gstride, int rows,
-                                          int w4, int vrows, int v4, const RowMap &m)
-{
-    for (int r = m.row0; r < rows; r += m.step) {
-        const float *grow = g + (size_t)r * gstride;
-        float *srow = s + r * sstride;
-        for (int c = m.col; c < w4; c += m.lanes) {
-            const bool ok = r < vrows && c < v4;
-            cp_async16_zfill(srow + 4 * c, ok ? grow + 4 * c : g, ok ? 16 : 0);
-        }
-    }
-}
-
-// In place TF32 rounding of the cells this thread copied with the same map.
-__device__ __forceinline__ void rows_round(float *s, int sstride, int rows, int w4, const RowMap &m)
-{
-    for (int r = m.row0; r < rows; r += m.step) {
-        float *srow = s + r * sstride;
-        for (int c = m.col; c < w4; c += m.lanes) {
-            float4 *q = reinterpret_cast<float4 *>(srow + 4 * c);
-            *q = tf32_round4(*q);
-        }
-    }
-}
-
-// In place: row r scaled by w[r], then rounded to TF32.
-__device__ __forceinline__ void rows_scale_round(float *s, int sstride, int rows, int w4, const RowMap &m,
-                                                 const float *w)
-{
-    for (int r = m.row0; r < rows; r += m.step) {
-        float *srow = s + r * sstride;
-        const float f = w[r];
-        for (int c = m.col; c < w4; c += m.lanes) {
-            float4 *q = reinterpret_cast<float4 *>(srow + 4 * c);
-            const float4 v = *q;
-            *q = tf32_round4(make_float4(f * v.x, f * v.y, f * v.z, f * v.w));
-        }
-    }
-}
-
-struct ChunkRange {
-    int seq, t0, len;     // packed token range [t0, t0 + len)
-};
-
-__device__ __forceinline__ bool chunk_of(const ScanArgs &a, const SsdPlan &p, int u, ChunkRange &c)
-{
-    if (u >= *p.n_units)
-        return false;
-    const int2 sk = p.units[u];
-    const int L = a.seq_lens[sk.x];
-    c.seq = sk.x;
-    c.t0 = a.seq_starts[sk.x] + sk.y * p.chunk;
-    c.len = max(0, min(p.chunk, L - sk.y * p.chunk));
-    return true;
-}
-
-// One warp: the chunk-local cumulative log decay a_t = sum_{s<=t} dt_s A[h]
-// for t = lane*R .. lane*R+R-1 (dt = 0 past the chunk's end, so a_t stays at
-// a_last there), with each lane's dt values.
-template <int Q>
-struct ChunkDecay {
-    static constexpr int R = Q / 32;
-    float a[R];
-    float d[R];
-    float last;
-};
-
-template <int Q>
-__device__ __forceinline__ void chunk_decay(const ScanArgs &a, const ChunkRange &c, int h, int lane,
-                                            ChunkDecay<Q> &cd)
-{
-    constexpr int R = ChunkDecay<Q>::R;
-    const float Ah = a.A[h];
-    float run = 0.f;
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-        const int t = lane * R + r;
-        cd.d[r] = t < c.len ? a.dt[(size_t)(c.t0 + t) * a.H + h] : 0.f;
-        run += cd.d[r] * Ah;
-        cd.a[r] = run;
-    }
-    float incl = run;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const float v = __shfl_up_sync(kFullMask, incl, off);
-        if (lane >= off)
-            incl += v;
-    }
-    float excl = __shfl_up_sync(kFullMask, incl, 1);
-    if (lane == 0)
-        excl = 0.f;
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-        cd.a[r] += excl;
-    cd.last = __shfl_sync(kFullMask, incl, 31);
-}
 
 // The chunk-state product for the items (16 head-dim rows x 4 column blocks)
 // of one warp: dS[p][n] = sum_s Xw[s][p] Bs[s][n].  FULL: every item has its 4
@@ -345,20 +165,26 @@ ssd_chunk_state_kernel(const ScanArgs a, const SsdPlan p, const SsdGeom sg)
 // State pass, in place over the units of each sequence:
 //   S = slot (resume) or 0;  for k: tmp = dS_k; W_k = S; S = exp(a_last,k) S + tmp;
 //   slot = S.
-// One thread per float4 of a state slot; the loads of a batch of chunks are
-// issued before any of its stores, so the chain waits on one load latency per
-// batch, not per chunk.
-__global__ void __launch_bounds__(256)
+// One thread per float4 of a state slot.  The chain is serial in k but its
+// loads are not: a thread copies the dS_k of up to kPassBatch chunks into its
+// own column of shared memory with cp.async (no registers held while they fly)
+// and only then runs the chain, so a sequence of 32 chunks waits on one memory
+// latency, not 32.
+constexpr int kPassThreads = 128;
+constexpr int kPassBatch = 32;
+
+__global__ void __launch_bounds__(kPassThreads)
 ssd_state_pass_kernel(const ScanArgs a, const SsdPlan p, int max_units)
 {
-    constexpr int kBatch = 8;
+    extern __shared__ float4 pass_buf[];               // [kPassBatch][kPassThreads]
     const int N4 = a.N >> 2;
     const long long slot4 = (long long)a.H * a.P * N4;
-    const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long e = (long long)blockIdx.x * kPassThreads + threadIdx.x;
     if (e >= slot4)
         return;
     const int head = (int)((e / N4) / a.P);
     float4 *W = reinterpret_cast<float4 *>(p.chunk_state);
+    float4 *mine = pass_buf + threadIdx.x;
     for (int seq = blockIdx.y; seq < a.n_seqs; seq += gridDim.y) {
         const int b = p.unit_base[seq];
         const int nu = p.unit_base[seq + 1] - b;
@@ -366,25 +192,23 @@ ssd_state_pass_kernel(const ScanArgs a, const SsdPlan p, int max_units)
             continue;
         float4 *slot = reinterpret_cast<float4 *>(a.state) + (long long)seq * slot4 + e;
         float4 S = a.resume[seq] ? *slot : make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int k0 = 0; k0 < nu; k0 += kBatch) {
-            float4 d[kBatch];
-            float ld[kBatch];
+        for (int k0 = 0; k0 < nu; k0 += kPassBatch) {
+            const int n = min(kPassBatch, nu - k0);
+            for (int j = 0; j < n; ++j)
+                cp_async16(mine + j * kPassThreads, W + (long long)(b + k0 + j) * slot4 + e);
+            cp_async_commit();
+            float ld[kPassBatch];
 #pragma unroll
-            for (int j = 0; j < kBatch; ++j) {
-                d[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-                ld[j] = 0.f;
-                if (k0 + j < nu) {
-                    d[j] = W[(long long)(b + k0 + j) * slot4 + e];
-                    ld[j] = p.chunk_logdecay[(long long)(b + k0 + j) * a.H + head];
-                }
-            }
+            for (int j = 0; j < kPassBatch; ++j)
+                ld[j] = j < n ? p.chunk_logdecay[(long long)(b + k0 + j) * a.H + head] : 0.f;
+            cp_async_wait<0>();
 #pragma unroll
-            for (int j = 0; j < kBatch; ++j) {
-                if (k0 + j < nu) {
+            for (int j = 0; j < kPassBatch; ++j) {
+                if (j < n) {
+                    const float4 d = mine[j * kPassThreads];
                     W[(long long)(b + k0 + j) * slot4 + e] = S;
                     const float f = expf(ld[j]);
-                    S = make_float4(fmaf(f, S.x, d[j].x), fmaf(f, S.y, d[j].y), fmaf(f, S.z, d[j].z),
-                                    fmaf(f, S.w, d[j].w));
+                    S = make_float4(fmaf(f, S.x, d.x), fmaf(f, S.y, d.y), fmaf(f, S.z, d.z), fmaf(f, S.w, d.w));
                 }
             }
         }
@@ -695,11 +519,18 @@ cudaError_t launch_ssd_q(const ScanArgs &a, const SsdPlan &plan, const SsdGeom &
         return e;
 
     const long long slot4 = (long long)a.H * a.P * (a.N >> 2);
-    const dim3 pgrid((unsigned)((slot4 + 255) / 256), (unsigned)(a.n_seqs < 65535 ? a.n_seqs : 65535));
-    ssd_state_pass_kernel<<<pgrid, 256, 0, stream>>>(a, plan, max_units);
+    const dim3 pgrid((unsigned)((slot4 + kPassThreads - 1) / kPassThreads),
+                     (unsigned)(a.n_seqs < 65535 ? a.n_seqs : 65535));
+    const int pass_smem = kPassBatch * kPassThreads * (int)sizeof(float4);
+    e = cudaFuncSetAttribute(ssd_state_pass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, pass_smem);
+    if (e != cudaSuccess)
+        return e;
+    ssd_state_pass_kernel<<<pgrid, kPassThreads, pass_smem, stream>>>(a, plan, max_units);
     if ((e = cudaGetLastError()) != cudaSuccess)
         return e;
 
+    if (g.use_tc)
+        return launch_ssd_output_tc(a, plan, g, max_units, stream);
     void (*out_k)(const ScanArgs, const SsdPlan, const SsdGeom) = nullptr;
     switch (a.P / 8) {
     case 2: out_k = ssd_output_kernel<Q, 2>; break;

@@ -53,9 +53,10 @@ def test_ssd_long_4x16384_sampled_heads():
     (Geometry(2, 16, 4, 1), 64),          # d_state padded from 4 to 8
     (Geometry(6, 32, 12, 3), 128),        # padded from 12 to 16, 3 groups
     (Geometry(3, 48, 36, 3), 64),         # head_dim 48: 6 column blocks
-    (Geometry(4, 128, 128, 2), 128),      # the widest head_dim
+    (Geometry(4, 128, 128, 2), 128),      # the widest head_dim (mma.sync: tiles exceed one block)
+    (Geometry(8, 96, 100, 2), 128),       # tcgen05 with d_state padded to 104
     (Geometry(4, 64, 256, 2), 64),        # the widest d_state that fits chunk 64
-], ids=["n4", "n12_g3", "p48", "p128", "n256"])
+], ids=["n4", "n12_g3", "p48", "p128", "p96_n100", "n256"])
 def test_ssd_odd_geometries(geom, chunk):
     inp = make_inputs(geom, [1, 70, 200, 129], [0, 1, 0, 1], seed=21)
     y_ref, s_ref = oracle.scan_inputs(inp)
@@ -63,12 +64,16 @@ def test_ssd_odd_geometries(geom, chunk):
     assert_parity(inp, y, s, y_ref, s_ref, tol=SSD_TOL)
 
 
+# head_dim 16 runs the output kernel on mma.sync; head_dim 32 and 64 at chunk
+# 128 run it on tcgen05 (chunk 64 stays on mma.sync).
+@pytest.mark.parametrize("geom", [Geometry(4, 16, 32, 2), Geometry(4, 32, 32, 2), Geometry(2, 64, 128, 1)],
+                         ids=["p16", "p32", "p64"])
 @pytest.mark.parametrize("dt_scale,a_value", [(1.0, -16.0), (60.0, -16.0), (1.0, 0.0), (0.5, 0.05)],
                          ids=["strong", "underflow", "no_decay", "growth"])
-def test_ssd_extreme_decay(dt_scale, a_value):
+def test_ssd_extreme_decay(dt_scale, a_value, geom):
     """exp(a_t - a_s) only for s <= t: steep decay underflows to zero and never
     overflows; no decay and slow growth stay finite."""
-    inp = make_inputs(Geometry(4, 16, 32, 2), [150, 77, 256], [0, 1, 1], seed=31)
+    inp = make_inputs(geom, [150, 77, 256], [0, 1, 1], seed=31)
     inp.dt.mul_(dt_scale)
     inp.A.fill_(a_value)
     y_ref, s_ref = oracle.scan_inputs(inp)
@@ -77,19 +82,21 @@ def test_ssd_extreme_decay(dt_scale, a_value):
         assert_parity(inp, y, s, y_ref, s_ref, tol=SSD_TOL)
 
 
-def test_ssd_zero_length_and_unowned_tokens():
+@pytest.mark.parametrize("head_dim,chunk", [(16, 64), (32, 128)], ids=["mma_sync", "tcgen05"])
+def test_ssd_zero_length_and_unowned_tokens(head_dim, chunk):
     """Zero-length sequences (fresh -> zero slot, resumed -> unchanged) and
     token rows owned by no sequence (never written)."""
-    inp = make_inputs(Geometry(4, 16, 32, 2), [0, 0, 9, 4, 130], [0, 1, 0, 1, 1], seed=12,
+    inp = make_inputs(Geometry(4, head_dim, 32, 2), [0, 0, 9, 4, 130], [0, 1, 0, 1, 1], seed=12,
                       starts=[0, 0, 3, 14, 20], n_tokens=160)
     y_ref, s_ref = oracle.scan_inputs(inp)
-    y, s = run_gpu_ssd(inp, chunk=64)
+    y, s = run_gpu_ssd(inp, chunk=chunk)
     assert_parity(inp, y, s, y_ref, s_ref, tol=SSD_TOL)
     assert np.array_equal(s[0], np.zeros_like(s[0]))
     assert np.array_equal(s[1], inp.state[1].double().numpy())
 
 
-def test_ssd_split_resume_equals_one_call():
+@pytest.mark.parametrize("chunk", [64, 128])
+def test_ssd_split_resume_equals_one_call(chunk):
     """A sequence run as two SSD calls (the second resuming from the slot the
     first left) matches one call and the oracle."""
     geom = Geometry(8, 32, 64, 2)
@@ -98,12 +105,12 @@ def test_ssd_split_resume_equals_one_call():
     a = make_inputs(geom, [k], [1], seed=13)
     a.x, a.dt, a.B, a.C = inp.x[:k], inp.dt[:k], inp.B[:k], inp.C[:k]
     a.A, a.D, a.state = inp.A, inp.D, inp.state
-    y1, s1 = run_gpu_ssd(a, chunk=64)
+    y1, s1 = run_gpu_ssd(a, chunk=chunk)
     b = make_inputs(geom, [300 - k], [1], seed=13)
     b.x, b.dt, b.B, b.C = inp.x[k:], inp.dt[k:], inp.B[k:], inp.C[k:]
     b.A, b.D = inp.A, inp.D
     b.state = torch.from_numpy(s1).float()
-    y2, s2 = run_gpu_ssd(b, chunk=64)
+    y2, s2 = run_gpu_ssd(b, chunk=chunk)
     y_ref, s_ref = oracle.scan_inputs(inp)
     assert_parity(inp, np.concatenate([y1, y2]), s2, y_ref, s_ref, tol=SSD_TOL)
 
