@@ -52,6 +52,9 @@ KERNEL_SOURCES = {
                        "state_space_model_ssm_gb300/csrc/scan_common.cuh"],
     "decode_kernel": ["state_space_model_ssm_gb300/csrc/decode.cu",
                       "state_space_model_ssm_gb300/csrc/scan_common.cuh"],
+    "ssd_output_kernel": ["state_space_model_ssm_gb300/csrc/ssd_tc.cu",
+                          "state_space_model_ssm_gb300/csrc/ssd_common.cuh",
+                          "state_space_model_ssm_gb300/csrc/scan_common.cuh"],
 }
 
 
@@ -512,7 +515,9 @@ def ours(args):
                          "peak_basis": "measured bf16 burst x 1.1/2.25 (nominal dense TF32/BF16)",
                          "algorithmic": f"{flops} dense FLOPs per call",
                          "hbm_frac": (alg_bytes / (ssd_ms * 1e-3)) / (peaks["hbm_gbs"] * 1e9),
-                         "traffic": None},
+                         "timing": "whole call (plan, chunk states, state pass, output)",
+                         "traffic": ncu_traffic("ssd_output_kernel", "prefill_1x4096"),
+                         "traffic_kernel": "the output kernel (tcgen05), DRAM bytes per launch"},
         }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_prefill(inp)
