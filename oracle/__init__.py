@@ -15,7 +15,9 @@ Two independent forms are provided:
 * ``chunked_form`` -- the recurrence unrolled over chunks of tokens (the SSD
                      chunked matrix form with state passing between chunks,
                      ``chunked_form.py``, NumPy float64): the decomposition the
-                     tensor-core kernels evaluate, checked against ``scan``.
+                     tensor-core kernels evaluate, checked against ``scan``;
+* ``extensions``   -- the steps around the scan (dt discretisation, gated
+                     RMSNorm, per-token state snapshots, causal conv1d + SiLU).
 """
 from __future__ import annotations
 
@@ -27,6 +29,7 @@ import threading
 import numpy as np
 
 from .chunked_form import chunked_form  # noqa: F401
+from .extensions import conv1d_silu, discretize_dt, gated_rmsnorm, scan_with_snapshots  # noqa: F401
 from .matrix_form import matrix_form  # noqa: F401
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -84,7 +87,7 @@ def _ptr(a):
 
 
 def scan(x, dt, A, B, C, D, state, seq_starts, seq_lens, resume, *,
-         heads=None, n_threads=None, y_fill=np.nan, lib=None):
+         heads=None, n_threads=None, y_fill=np.nan, lib=None, dt_bias=None, dt_softplus=False):
     """Run the oracle.  Inputs may be torch tensors or arrays (any float type;
     they are widened to float64 exactly).  Shapes: x [T,H,P], dt [T,H], A [H],
     B/C [T,G,N], D [H], state [n,H,P,N] (read for resuming sequences only),
@@ -92,8 +95,11 @@ def scan(x, dt, A, B, C, D, state, seq_starts, seq_lens, resume, *,
 
     heads: optional iterable of head indices to compute (others stay NaN).
     lib: an already opened oracle library (default: the one built here).
+    dt_bias [H], dt_softplus: discretise dt first (``extensions.discretize_dt``).
     Returns (y [T,H,P], state_out [n,H,P,N]) as float64 arrays.
     """
+    if dt_bias is not None or dt_softplus:
+        dt = discretize_dt(dt, dt_bias, dt_softplus)
     x, dt, A, B, C, D = map(_f64, (x, dt, A, B, C, D))
     state = _f64(state)
     seq_starts, seq_lens, resume = map(_i32, (seq_starts, seq_lens, resume))
