@@ -141,6 +141,54 @@ int ssm_scan_tuned(float *state_slots, const float *x, const float *dt,
                    void *stream);
 
 /*
+ * Optional steps around the scan (all NULL / 0 = the plain scan).
+ *   dt_bias, dt_softplus  Mamba2's discretisation of dt, fused into the scan's
+ *       own loads of dt ("The llama journey", Day 14 kernel body; the decay-gate
+ *       kernel of "ssm_gated_delta.cu"): v = dt[t,h] + dt_bias[h] (dt_bias NULL:
+ *       no bias), then with dt_softplus nonzero the step is v for v > 20 and
+ *       log1p(exp(v)) otherwise; that step replaces dt[t,h] everywhere in the
+ *       recurrence above.  dt_bias: device, [n_heads] fp32, 4-byte aligned.
+ *   state_snapshots  device, [n_tokens][n_heads][head_dim][d_state] fp32, out:
+ *       row t receives the state right after token t for every token owned by a
+ *       sequence, so accepting the first M tokens of a speculative run restores
+ *       one contiguous [n_heads][head_dim][d_state] image (the rows of tokens
+ *       owned by no sequence are not written).  16-byte aligned.
+ *   gated_y, gate_z, norm_weight, norm_eps  Mamba2's gated RMSNorm after the
+ *       scan, per (token, head) row of head_dim values:
+ *       gated_y[t,h,p] = y[t,h,p] / sqrt(mean_p(y[t,h,:]^2) + norm_eps)
+ *                        * norm_weight[p] * silu(gate_z[t,h,p]),
+ *       silu(z) = z / (1 + exp(-z)), the weight shared by all heads (kernel 3
+ *       of "ssm_gated_delta.cu").  gated_y, gate_z: device [n_tokens][n_heads]
+ *       [head_dim] fp32; norm_weight: device [head_dim]; norm_eps > 0.  y is
+ *       still written.  gated_y NULL: off (the other three are then ignored).
+ */
+typedef struct {
+    const float *dt_bias;
+    int dt_softplus;
+    float *state_snapshots;
+    const float *gate_z;
+    const float *norm_weight;
+    float norm_eps;
+    float *gated_y;
+} ssm_scan_options;
+
+/*
+ * The scan with tuning, options and workspace (each may be NULL / 0):
+ * ssm_scan_ws plus the optional steps of ssm_scan_options.  State snapshots
+ * run the direct prefill kernel (one sequence token by token, no time
+ * segments) or the decode kernel.  Errors as for ssm_scan_ws, and
+ * SSM_ERR_INVALID_ARG for a misaligned option pointer or norm_eps <= 0 with
+ * gated_y set.
+ */
+int ssm_scan_ex(float *state_slots, const float *x, const float *dt,
+                const float *A, const float *B, const float *C, const float *D,
+                float *y, const int32_t *seq_starts, const int32_t *seq_lens,
+                const int32_t *resume_flags, int n_seqs, int n_tokens,
+                int n_heads, int head_dim, int d_state, int n_groups,
+                const ssm_scan_tuning *tuning, const ssm_scan_options *options,
+                void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * The scan with a caller-owned device workspace.  With a workspace the
  * prefill path may cut long sequences into time segments and run them in
  * parallel: a state-only pass per segment, a combine of the segment states
@@ -200,6 +248,8 @@ size_t ssm_scan_workspace_bytes(int n_seqs, int n_tokens, int n_heads,
  *   - the chunk's shared-memory tiles must fit one block: SSM_ERR_UNSUPPORTED
  *     otherwise (for example d_state 1024; d_state up to 256 fits with
  *     chunk 64, up to 128 with chunk 128).
+ * options: as for ssm_scan_ex (NULL = none); state snapshots are not
+ * available in this form (SSM_ERR_UNSUPPORTED).
  * SSM_ERR_INVALID_ARG for a missing, misaligned or too small workspace or a
  * chunk other than 0, 64 or 128.
  */
@@ -208,8 +258,8 @@ int ssm_scan_ssd(float *state_slots, const float *x, const float *dt,
                  float *y, const int32_t *seq_starts, const int32_t *seq_lens,
                  const int32_t *resume_flags, int n_seqs, int n_tokens,
                  int n_heads, int head_dim, int d_state, int n_groups,
-                 int chunk, void *workspace, size_t workspace_bytes,
-                 void *stream);
+                 int chunk, const ssm_scan_options *options, void *workspace,
+                 size_t workspace_bytes, void *stream);
 
 /*
  * Bytes of workspace ssm_scan_ssd needs for these sizes and chunk (the same on

@@ -44,6 +44,14 @@ class Tuning(ctypes.Structure):
                 ("segment_tokens", ctypes.c_int)]
 
 
+class Options(ctypes.Structure):
+    """Optional steps around the scan (``ssm_scan_options``); zero fields mean off."""
+    _fields_ = [("dt_bias", ctypes.c_void_p), ("dt_softplus", ctypes.c_int),
+                ("state_snapshots", ctypes.c_void_p), ("gate_z", ctypes.c_void_p),
+                ("norm_weight", ctypes.c_void_p), ("norm_eps", ctypes.c_float),
+                ("gated_y", ctypes.c_void_p)]
+
+
 _P = ctypes.c_void_p
 _I = ctypes.c_int
 _SCAN_ARGS = [_P] * 11 + [_I] * 6
@@ -67,8 +75,11 @@ def load():
             lib.ssm_scan_ws.argtypes = _SCAN_ARGS + [ctypes.POINTER(Tuning), _P, ctypes.c_size_t, _P]
             lib.ssm_scan_workspace_bytes.restype = ctypes.c_size_t
             lib.ssm_scan_workspace_bytes.argtypes = [_I] * 6 + [ctypes.POINTER(Tuning)]
+            lib.ssm_scan_ex.restype = _I
+            lib.ssm_scan_ex.argtypes = _SCAN_ARGS + [ctypes.POINTER(Tuning), ctypes.POINTER(Options), _P,
+                                                     ctypes.c_size_t, _P]
             lib.ssm_scan_ssd.restype = _I
-            lib.ssm_scan_ssd.argtypes = _SCAN_ARGS + [_I, _P, ctypes.c_size_t, _P]
+            lib.ssm_scan_ssd.argtypes = _SCAN_ARGS + [_I, ctypes.POINTER(Options), _P, ctypes.c_size_t, _P]
             lib.ssm_scan_ssd_workspace_bytes.restype = ctypes.c_size_t
             lib.ssm_scan_ssd_workspace_bytes.argtypes = [_I] * 7
             lib.ssm_status_string.restype = ctypes.c_char_p
@@ -94,14 +105,20 @@ def declared_functions(header: str = HEADER):
 
 def scan_raw(state, x, dt, A, B, C, D, y, seq_starts, seq_lens, resume,
              n_seqs, n_tokens, n_heads, head_dim, d_state, n_groups,
-             stream=0, tuning: Tuning | None = None, workspace=None, workspace_bytes=0) -> int:
+             stream=0, tuning: Tuning | None = None, workspace=None, workspace_bytes=0,
+             options: Options | None = None) -> int:
     """Call the C ABI with integer pointers; returns the status code.
-    With `workspace` (a device pointer) the call goes through ssm_scan_ws."""
+    With `options` the call goes through ssm_scan_ex, else with `workspace`
+    (a device pointer) through ssm_scan_ws."""
     lib = load()
     args = [_P(int(p) if p else None) for p in
             (state, x, dt, A, B, C, D, y, seq_starts, seq_lens, resume)]
     args += [int(n_seqs), int(n_tokens), int(n_heads), int(head_dim), int(d_state), int(n_groups)]
     st = _P(int(stream) if stream else None)
+    if options is not None:
+        tp = ctypes.byref(tuning) if tuning is not None else None
+        return lib.ssm_scan_ex(*args, tp, ctypes.byref(options), _P(int(workspace) if workspace else None),
+                               ctypes.c_size_t(int(workspace_bytes)), st)
     if workspace is not None:
         tp = ctypes.byref(tuning) if tuning is not None else None
         return lib.ssm_scan_ws(*args, tp, _P(int(workspace) if workspace else None),
@@ -121,13 +138,41 @@ def workspace_bytes(n_seqs, n_tokens, n_heads, head_dim, d_state, n_groups,
 
 def ssd_raw(state, x, dt, A, B, C, D, y, seq_starts, seq_lens, resume,
             n_seqs, n_tokens, n_heads, head_dim, d_state, n_groups, chunk,
-            workspace, workspace_bytes, stream=0) -> int:
+            workspace, workspace_bytes, stream=0, options: Options | None = None) -> int:
     """ssm_scan_ssd with integer pointers; returns the status code."""
     args = [_P(int(p) if p else None) for p in
             (state, x, dt, A, B, C, D, y, seq_starts, seq_lens, resume)]
     args += [int(n_seqs), int(n_tokens), int(n_heads), int(head_dim), int(d_state), int(n_groups)]
-    return load().ssm_scan_ssd(*args, int(chunk), _P(int(workspace) if workspace else None),
+    op = ctypes.byref(options) if options is not None else None
+    return load().ssm_scan_ssd(*args, int(chunk), op, _P(int(workspace) if workspace else None),
                                ctypes.c_size_t(int(workspace_bytes)), _P(int(stream) if stream else None))
+
+
+def make_options(dev, H, P, T, *, dt_bias=None, dt_softplus=False, snapshots=None, gate_z=None,
+                 norm_weight=None, norm_eps=1e-6, gated_y=None):
+    """Options from tensors (checked for dtype, device and shape); None when all are off."""
+    f32 = torch.float32
+    if dt_bias is None and not dt_softplus and snapshots is None and gated_y is None:
+        return None
+    o = Options()
+    if dt_bias is not None:
+        _check(dt_bias, "dt_bias", f32, dev, (H,))
+        o.dt_bias = dt_bias.data_ptr()
+    o.dt_softplus = 1 if dt_softplus else 0
+    if snapshots is not None:
+        _check(snapshots, "snapshots", f32, dev)
+        if snapshots.shape[0] != T or snapshots.shape[1:3] != (H, P):
+            raise ValueError("snapshots must be [n_tokens, n_heads, head_dim, d_state]")
+        o.state_snapshots = snapshots.data_ptr()
+    if gated_y is not None:
+        for nm, t, shp in (("gated_y", gated_y, (T, H, P)), ("gate_z", gate_z, (T, H, P)),
+                           ("norm_weight", norm_weight, (P,))):
+            if t is None:
+                raise ValueError(f"{nm} is required for the gated output")
+            _check(t, nm, f32, dev, shp)
+        o.gated_y, o.gate_z, o.norm_weight = gated_y.data_ptr(), gate_z.data_ptr(), norm_weight.data_ptr()
+        o.norm_eps = float(norm_eps)
+    return o
 
 
 def ssd_workspace_bytes(n_seqs, n_tokens, n_heads, head_dim, d_state, n_groups, chunk=0) -> int:
@@ -151,7 +196,9 @@ def _check(t, name, dtype, device, shape=None):
 
 
 def ssm_scan(state_slots, x, dt, A, B, C, D, seq_starts, seq_lens, resume_flags,
-             y=None, *, tuning: Tuning | None = None, stream=None, workspace=None):
+             y=None, *, tuning: Tuning | None = None, stream=None, workspace=None,
+             dt_bias=None, dt_softplus=False, snapshots=None, gate_z=None, norm_weight=None,
+             norm_eps=1e-6, gated_y=None):
     """Run the scan on the current CUDA stream (or ``stream``).
 
     state_slots [n,H,P,N] fp32 (updated in place), x [T,H,P], dt [T,H], A [H],
@@ -159,6 +206,10 @@ def ssm_scan(state_slots, x, dt, A, B, C, D, seq_starts, seq_lens, resume_flags,
     one CUDA device.  Returns y [T,H,P] (allocated if not given).
     workspace: optional uint8 CUDA tensor (see ``workspace_bytes``); lets long
     sequences run as parallel time segments.
+    dt_bias [H] / dt_softplus: discretise dt inside the scan; snapshots
+    [T,H,P,N]: the state after every token; gated_y [T,H,P] with gate_z
+    [T,H,P], norm_weight [P], norm_eps: the gated RMSNorm of y (see
+    ``ssm_scan_options`` in the C header).
     """
     dev = state_slots.device
     if dev.type != "cuda":
@@ -187,19 +238,22 @@ def ssm_scan(state_slots, x, dt, A, B, C, D, seq_starts, seq_lens, resume_flags,
         if workspace.device != dev or not workspace.is_contiguous():
             raise ValueError("workspace must be a contiguous tensor on the scan's device")
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    opts = make_options(dev, H, P, T, dt_bias=dt_bias, dt_softplus=dt_softplus, snapshots=snapshots,
+                        gate_z=gate_z, norm_weight=norm_weight, norm_eps=norm_eps, gated_y=gated_y)
     with torch.cuda.device(dev):
         rc = scan_raw(state_slots.data_ptr(), x.data_ptr(), dt.data_ptr(), A.data_ptr(),
                       B.data_ptr(), C.data_ptr(), D.data_ptr(), y.data_ptr(),
                       seq_starts.data_ptr(), seq_lens.data_ptr(), resume_flags.data_ptr(),
                       n, T, H, P, N, G, stream=handle, tuning=tuning,
-                      workspace=ws_ptr, workspace_bytes=ws_bytes)
+                      workspace=ws_ptr, workspace_bytes=ws_bytes, options=opts)
     if rc != SSM_OK:
         raise SsmScanError(rc, "ssm_scan")
     return y
 
 
 def ssm_scan_ssd(state_slots, x, dt, A, B, C, D, seq_starts, seq_lens, resume_flags,
-                 y=None, *, chunk: int = 0, workspace=None, stream=None):
+                 y=None, *, chunk: int = 0, workspace=None, stream=None, dt_bias=None,
+                 dt_softplus=False, gate_z=None, norm_weight=None, norm_eps=1e-6, gated_y=None):
     """The scan in chunked matrix form on the TF32 tensor cores (``ssm_scan_ssd``).
 
     Same tensors as ``ssm_scan``; y matches the exact scan to about
@@ -234,12 +288,14 @@ def ssm_scan_ssd(state_slots, x, dt, A, B, C, D, seq_starts, seq_lens, resume_fl
     if stream is None:
         stream = torch.cuda.current_stream(dev)
     handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    opts = make_options(dev, H, P, T, dt_bias=dt_bias, dt_softplus=dt_softplus, gate_z=gate_z,
+                        norm_weight=norm_weight, norm_eps=norm_eps, gated_y=gated_y)
     with torch.cuda.device(dev):
         rc = ssd_raw(state_slots.data_ptr(), x.data_ptr(), dt.data_ptr(), A.data_ptr(),
                      B.data_ptr(), C.data_ptr(), D.data_ptr(), y.data_ptr(),
                      seq_starts.data_ptr(), seq_lens.data_ptr(), resume_flags.data_ptr(),
                      n, T, H, P, N, G, chunk, workspace.data_ptr(),
-                     workspace.numel() * workspace.element_size(), stream=handle)
+                     workspace.numel() * workspace.element_size(), stream=handle, options=opts)
     if rc != SSM_OK:
         raise SsmScanError(rc, "ssm_scan_ssd")
     return y

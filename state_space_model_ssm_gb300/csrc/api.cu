@@ -235,11 +235,29 @@ int plan_prefill(const ssm_scan_tuning &t, bool scaled, int n_seqs, int n_tokens
     return SSM_OK;
 }
 
+// Copy the caller's options (NULL = all off) and check their pointers.
+int read_options(const ssm_scan_options *opts, ssm_scan_options *out)
+{
+    std::memset(out, 0, sizeof *out);
+    if (!opts)
+        return SSM_OK;
+    *out = *opts;
+    if (!aligned(out->dt_bias, 4) || !aligned(out->state_snapshots, 16))
+        return SSM_ERR_INVALID_ARG;
+    if (out->gated_y) {
+        if (!out->gate_z || !out->norm_weight || !(out->norm_eps > 0.f))
+            return SSM_ERR_INVALID_ARG;
+        if (!aligned(out->gated_y, 16) || !aligned(out->gate_z, 16) || !aligned(out->norm_weight, 16))
+            return SSM_ERR_INVALID_ARG;
+    }
+    return SSM_OK;
+}
+
 int scan_impl(float *state, const float *x, const float *dt, const float *A, const float *B,
               const float *C, const float *D, float *y, const int32_t *seq_starts,
               const int32_t *seq_lens, const int32_t *resume, int n_seqs, int n_tokens,
-              int H, int P, int N, int G, const ssm_scan_tuning *tun, void *workspace,
-              size_t workspace_bytes, void *stream_v)
+              int H, int P, int N, int G, const ssm_scan_tuning *tun, const ssm_scan_options *opts,
+              void *workspace, size_t workspace_bytes, void *stream_v)
 {
     // ---- host-checkable arguments ----
     if (n_seqs < 0 || n_tokens < 0 || H <= 0 || P <= 0 || N <= 0 || G <= 0)
@@ -262,6 +280,13 @@ int scan_impl(float *state, const float *x, const float *dt, const float *A, con
         !aligned(seq_starts, 4) || !aligned(seq_lens, 4) || !aligned(resume, 4))
         return SSM_ERR_INVALID_ARG;
 
+    ssm_scan_options o;
+    int rc = read_options(opts, &o);
+    if (rc != SSM_OK)
+        return rc;
+    if (o.state_snapshots || o.gated_y)
+        return SSM_ERR_UNSUPPORTED;
+
     ssm_scan_tuning t;
     std::memset(&t, 0, sizeof t);
     if (tun)
@@ -276,7 +301,7 @@ int scan_impl(float *state, const float *x, const float *dt, const float *A, con
         return SSM_ERR_INVALID_ARG;
 
     DeviceInfo dev;
-    int rc = device_info(&dev);
+    rc = device_info(&dev);
     if (rc != SSM_OK)
         return rc;
 
@@ -284,6 +309,7 @@ int scan_impl(float *state, const float *x, const float *dt, const float *A, con
     a.state = state; a.x = x; a.dt = dt; a.A = A; a.B = B; a.C = C; a.D = D; a.y = y;
     a.seq_starts = seq_starts; a.seq_lens = seq_lens; a.resume = resume;
     a.n_seqs = n_seqs; a.n_tokens = n_tokens; a.H = H; a.P = P; a.N = N; a.G = G;
+    a.dt_bias = o.dt_bias; a.dt_softplus = o.dt_softplus;
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_v);
 
     if (check_env()) {
@@ -461,7 +487,8 @@ int plan_ssd(int n_seqs, int n_tokens, int H, int P, int N, int G, int chunk, co
 int ssd_impl(float *state, const float *x, const float *dt, const float *A, const float *B,
              const float *C, const float *D, float *y, const int32_t *seq_starts,
              const int32_t *seq_lens, const int32_t *resume, int n_seqs, int n_tokens, int H, int P,
-             int N, int G, int chunk, void *workspace, size_t workspace_bytes, void *stream_v)
+             int N, int G, int chunk, const ssm_scan_options *opts, void *workspace, size_t workspace_bytes,
+             void *stream_v)
 {
     if (n_seqs < 0 || n_tokens < 0 || H <= 0 || P <= 0 || N <= 0 || G <= 0 || chunk < 0)
         return SSM_ERR_INVALID_ARG;
@@ -488,6 +515,12 @@ int ssd_impl(float *state, const float *x, const float *dt, const float *A, cons
         return SSM_ERR_INVALID_ARG;
     if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.bytes)
         return SSM_ERR_INVALID_ARG;
+    ssm_scan_options o;
+    rc = read_options(opts, &o);
+    if (rc != SSM_OK)
+        return rc;
+    if (o.state_snapshots || o.gated_y)
+        return SSM_ERR_UNSUPPORTED;
 
     DeviceInfo dev;
     rc = device_info(&dev);
@@ -501,6 +534,7 @@ int ssd_impl(float *state, const float *x, const float *dt, const float *A, cons
     a.state = state; a.x = x; a.dt = dt; a.A = A; a.B = B; a.C = C; a.D = D; a.y = y;
     a.seq_starts = seq_starts; a.seq_lens = seq_lens; a.resume = resume;
     a.n_seqs = n_seqs; a.n_tokens = n_tokens; a.H = H; a.P = P; a.N = N; a.G = G;
+    a.dt_bias = o.dt_bias; a.dt_softplus = o.dt_softplus;
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_v);
     if (check_env()) {
         rc = check_metadata(a, stream);
@@ -549,7 +583,7 @@ int ssm_scan(float *state_slots, const float *x, const float *dt, const float *A
              int n_heads, int head_dim, int d_state, int n_groups, void *stream)
 {
     return scan_impl(state_slots, x, dt, A, B, C, D, y, seq_starts, seq_lens, resume_flags, n_seqs,
-                     n_tokens, n_heads, head_dim, d_state, n_groups, nullptr, nullptr, 0, stream);
+                     n_tokens, n_heads, head_dim, d_state, n_groups, nullptr, nullptr, nullptr, 0, stream);
 }
 
 int ssm_scan_tuned(float *state_slots, const float *x, const float *dt, const float *A,
@@ -559,7 +593,7 @@ int ssm_scan_tuned(float *state_slots, const float *x, const float *dt, const fl
                    const ssm_scan_tuning *tuning, void *stream)
 {
     return scan_impl(state_slots, x, dt, A, B, C, D, y, seq_starts, seq_lens, resume_flags, n_seqs,
-                     n_tokens, n_heads, head_dim, d_state, n_groups, tuning, nullptr, 0, stream);
+                     n_tokens, n_heads, head_dim, d_state, n_groups, tuning, nullptr, nullptr, 0, stream);
 }
 
 int ssm_scan_ws(float *state_slots, const float *x, const float *dt, const float *A, const float *B,
@@ -569,8 +603,19 @@ int ssm_scan_ws(float *state_slots, const float *x, const float *dt, const float
                 void *workspace, size_t workspace_bytes, void *stream)
 {
     return scan_impl(state_slots, x, dt, A, B, C, D, y, seq_starts, seq_lens, resume_flags, n_seqs,
-                     n_tokens, n_heads, head_dim, d_state, n_groups, tuning, workspace, workspace_bytes,
+                     n_tokens, n_heads, head_dim, d_state, n_groups, tuning, nullptr, workspace, workspace_bytes,
                      stream);
+}
+
+int ssm_scan_ex(float *state_slots, const float *x, const float *dt, const float *A, const float *B,
+                const float *C, const float *D, float *y, const int32_t *seq_starts,
+                const int32_t *seq_lens, const int32_t *resume_flags, int n_seqs, int n_tokens,
+                int n_heads, int head_dim, int d_state, int n_groups, const ssm_scan_tuning *tuning,
+                const ssm_scan_options *options, void *workspace, size_t workspace_bytes, void *stream)
+{
+    return scan_impl(state_slots, x, dt, A, B, C, D, y, seq_starts, seq_lens, resume_flags, n_seqs,
+                     n_tokens, n_heads, head_dim, d_state, n_groups, tuning, options, workspace,
+                     workspace_bytes, stream);
 }
 
 size_t ssm_scan_workspace_bytes(int n_seqs, int n_tokens, int n_heads, int head_dim, int d_state,
@@ -600,12 +645,12 @@ size_t ssm_scan_workspace_bytes(int n_seqs, int n_tokens, int n_heads, int head_
 int ssm_scan_ssd(float *state_slots, const float *x, const float *dt, const float *A, const float *B,
                  const float *C, const float *D, float *y, const int32_t *seq_starts,
                  const int32_t *seq_lens, const int32_t *resume_flags, int n_seqs, int n_tokens,
-                 int n_heads, int head_dim, int d_state, int n_groups, int chunk, void *workspace,
-                 size_t workspace_bytes, void *stream)
+                 int n_heads, int head_dim, int d_state, int n_groups, int chunk,
+                 const ssm_scan_options *options, void *workspace, size_t workspace_bytes, void *stream)
 {
     return ssd_impl(state_slots, x, dt, A, B, C, D, y, seq_starts, seq_lens, resume_flags, n_seqs,
-                    n_tokens, n_heads, head_dim, d_state, n_groups, chunk, workspace, workspace_bytes,
-                    stream);
+                    n_tokens, n_heads, head_dim, d_state, n_groups, chunk, options, workspace,
+                    workspace_bytes, stream);
 }
 
 size_t ssm_scan_ssd_workspace_bytes(int n_seqs, int n_tokens, int n_heads, int head_dim, int d_state,

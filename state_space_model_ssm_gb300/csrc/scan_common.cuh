@@ -30,7 +30,21 @@ struct ScanArgs {
     const int32_t *seq_lens;   // [n]
     const int32_t *resume;     // [n]
     int n_seqs, n_tokens, H, P, N, G;
+    const float *dt_bias;      // [H] added to dt before use, or null
+    int dt_softplus;           // nonzero: dt_eff = softplus(dt + dt_bias) (identity above 20)
 };
+
+// The step size the recurrence uses for raw value `v` of head h: v as given,
+// or softplus(v + dt_bias[h]) with the identity above 20 ("The llama journey",
+// Day 14 kernel body; the decay-gate kernel of "ssm_gated_delta.cu").
+__device__ __forceinline__ float dt_eff(const ScanArgs &a, float v, int h)
+{
+    if (a.dt_bias)
+        v += __ldg(a.dt_bias + h);
+    if (a.dt_softplus && v <= 20.f)
+        v = log1pf(expf(v));
+    return v;
+}
 
 // Launch geometry of the chunk-staged prefill kernel.
 struct PrefillGeom {

@@ -18,7 +18,12 @@ def _guarded(shape, fill, device):
     return buf, buf[GUARD:GUARD + numel].view(*shape)
 
 
-def run_gpu(inp, tuning=None, device="cuda", stream=None, y_fill=float("nan"), workspace=False):
+def _opt_tensors(device, kw):
+    """Move tensor-valued scan options to the device."""
+    return {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in kw.items()}
+
+
+def run_gpu(inp, tuning=None, device="cuda", stream=None, y_fill=float("nan"), workspace=False, **opts):
     """Run libssmscan on a ScanInputs bundle; returns (y, state) as float64
     numpy arrays.  Checks that the NaN guard bands around y and the state are
     intact afterwards.  workspace=True calls ssm_scan_ws with a workspace of
@@ -34,7 +39,7 @@ def run_gpu(inp, tuning=None, device="cuda", stream=None, y_fill=float("nan"), w
                                     g.n_groups, tuning)
         ws = torch.full((max(nbytes, 256) // 4,), float("nan"), dtype=torch.float32, device=device)
     bd.ssm_scan(state, d.x, d.dt, d.A, d.B, d.C, d.D, d.seq_starts, d.seq_lens, d.resume,
-                y=y, tuning=tuning, stream=stream, workspace=ws)
+                y=y, tuning=tuning, stream=stream, workspace=ws, **_opt_tensors(device, opts))
     torch.cuda.synchronize()
     for buf in (sbuf, ybuf):
         head, tail = buf[:GUARD], buf[-GUARD:]
@@ -80,7 +85,7 @@ def assert_parity(inp, y_gpu, s_gpu, y_ref, s_ref, heads=None, tol=TOL):
 SSD_TOL = 5e-3
 
 
-def run_gpu_ssd(inp, chunk=0, device="cuda", stream=None, y_fill=float("nan")):
+def run_gpu_ssd(inp, chunk=0, device="cuda", stream=None, y_fill=float("nan"), **opts):
     """ssm_scan_ssd on a ScanInputs bundle with NaN guard bands around y and the
     state and a NaN-filled workspace of exactly the size the library asks for
     (so a read of a word the call did not write shows up).  Returns (y, state)
@@ -95,7 +100,7 @@ def run_gpu_ssd(inp, chunk=0, device="cuda", stream=None, y_fill=float("nan")):
     assert need > 0
     ws = torch.full((need // 4,), float("nan"), dtype=torch.float32, device=device)
     bd.ssm_scan_ssd(state, d.x, d.dt, d.A, d.B, d.C, d.D, d.seq_starts, d.seq_lens, d.resume,
-                    y=y, chunk=chunk, workspace=ws, stream=stream)
+                    y=y, chunk=chunk, workspace=ws, stream=stream, **_opt_tensors(device, opts))
     torch.cuda.synchronize()
     for buf in (sbuf, ybuf):
         head, tail = buf[:GUARD], buf[-GUARD:]

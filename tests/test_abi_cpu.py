@@ -163,3 +163,32 @@ def test_ssd_host_rejects_bad_arguments(lib, over, expect):
 
 def test_ssd_empty_batch_is_a_noop(lib):
     assert _ssd_call(lib, n_seqs=0, state=0, x=0, y=0, ws=0, ws_bytes=0) == bd.SSM_OK
+
+
+# ---- ssm_scan_ex options: host checks ----
+
+def _ex_call(lib, options):
+    ptrs = dict(state=PTR, x=PTR, dt=PTR, A=PTR, B=PTR, C=PTR, D=PTR, y=PTR,
+                seq_starts=PTR, seq_lens=PTR, resume=PTR)
+    return bd.scan_raw(**ptrs, **GOOD, options=options)
+
+
+def test_header_declares_the_options_entry_point_and_struct():
+    import re
+    assert "ssm_scan_ex" in bd.declared_functions()
+    text = open(bd.HEADER).read()
+    body = re.search(r"typedef struct \{([^{}]*?)\} ssm_scan_options;", text, re.S).group(1)
+    fields = re.findall(r"\b(\w+);", body)
+    assert fields == [f[0] for f in bd.Options._fields_]
+
+
+@pytest.mark.parametrize("opts,expect", [
+    (dict(dt_bias=PTR + 2), bd.SSM_ERR_INVALID_ARG),                   # 4-byte alignment
+    (dict(state_snapshots=PTR + 8), bd.SSM_ERR_INVALID_ARG),           # 16-byte alignment
+    (dict(gated_y=PTR), bd.SSM_ERR_INVALID_ARG),                       # no gate, no weight
+    (dict(gated_y=PTR, gate_z=PTR, norm_weight=PTR, norm_eps=0.0), bd.SSM_ERR_INVALID_ARG),
+    (dict(gated_y=PTR, gate_z=PTR + 4, norm_weight=PTR, norm_eps=1e-5), bd.SSM_ERR_INVALID_ARG),
+])
+def test_options_rejected_on_the_host(lib, opts, expect):
+    o = bd.Options(**opts)
+    assert _ex_call(lib, o) == expect

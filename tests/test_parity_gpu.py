@@ -257,3 +257,38 @@ def test_time_segments_need_their_workspace():
         bd.ssm_scan(inp.state, inp.x, inp.dt, inp.A, inp.B, inp.C, inp.D, inp.seq_starts,
                     inp.seq_lens, inp.resume, tuning=t, workspace=small)
     assert e.value.status == bd.SSM_ERR_INVALID_ARG
+
+
+# ---- fused dt discretisation (dt + bias, softplus with the identity above 20) ----
+
+def _raw_dt_case(geom, lens, resume, seed):
+    inp = make_inputs(geom, lens, resume, seed=seed)
+    g = torch.Generator().manual_seed(seed + 500)
+    inp.dt = torch.randn(inp.dt.shape, generator=g) * 0.5 - 2.0          # pre-activation values
+    inp.dt[::7] += 23.0                                                  # some rows above the threshold
+    bias = torch.rand(geom.n_heads, generator=g) - 0.5
+    return inp, bias
+
+
+@pytest.mark.parametrize("path", PATHS, ids=[p[0] for p in PATHS])
+@pytest.mark.parametrize("softplus", [True, False], ids=["softplus", "bias_only"])
+def test_parity_fused_dt(path, softplus):
+    inp, bias = _raw_dt_case(Geometry(4, 16, 32, 2), [1, 40, 77], [0, 1, 0], seed=41)
+    if not softplus:                                                     # steps dt + bias stay small and positive
+        inp.dt = inp.dt.abs() * 0.05
+        bias = bias.abs() * 0.1
+    y_ref, s_ref = oracle.scan_inputs(inp, dt_bias=bias, dt_softplus=softplus)
+    if path[0] == "decode":
+        dec = make_inputs(Geometry(4, 16, 32, 2), [1, 1, 1], [1, 0, 1], seed=42)
+        dec.dt = inp.dt[:3].clone()
+        y_ref, s_ref = oracle.scan_inputs(dec, dt_bias=bias, dt_softplus=softplus)
+        inp = dec
+    y, s = run_gpu(inp, tuning=path[1], dt_bias=bias, dt_softplus=softplus)
+    assert_parity(inp, y, s, y_ref, s_ref)
+
+
+def test_parity_fused_dt_time_segments():
+    inp, bias = _raw_dt_case(Geometry(8, 64, 128, 2), [3000], [1], seed=43)
+    y_ref, s_ref = oracle.scan_inputs(inp, dt_bias=bias, dt_softplus=True)
+    y, s = run_gpu(inp, workspace=True, dt_bias=bias, dt_softplus=True)
+    assert_parity(inp, y, s, y_ref, s_ref)

@@ -152,3 +152,30 @@ def test_ssd_rejections_before_launch():
     assert _raw_call(inp, 128) == bd.SSM_ERR_UNSUPPORTED
     assert _raw_call(inp, 64) == bd.SSM_OK
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("geom,chunk", [(Geometry(4, 16, 32, 2), 64), (Geometry(4, 64, 128, 2), 128)],
+                         ids=["mma_sync", "tcgen05"])
+def test_ssd_fused_dt(geom, chunk):
+    """dt + bias and softplus inside the kernels: against the oracle (a few
+    steps above the softplus threshold), and against the same call on the
+    step discretised on the host in fp32 (the same arithmetic, so far tighter
+    than the TF32 bound)."""
+    inp = make_inputs(geom, [1, 150, 300], [0, 1, 1], seed=44)
+    g = torch.Generator().manual_seed(45)
+    inp.dt = torch.randn(inp.dt.shape, generator=g) * 0.5 - 2.0
+    inp.dt[::97] += 21.5                                                 # a few steps above 20
+    bias = torch.rand(geom.n_heads, generator=g) - 0.5
+    y_ref, s_ref = oracle.scan_inputs(inp, dt_bias=bias, dt_softplus=True)
+    y, s = run_gpu_ssd(inp, chunk=chunk, dt_bias=bias, dt_softplus=True)
+    assert_parity(inp, y, s, y_ref, s_ref, tol=SSD_TOL)
+    host = make_inputs(geom, [1, 150, 300], [0, 1, 1], seed=44)
+    v = inp.dt + bias[None, :]
+    host.dt = torch.where(v > 20.0, v, torch.log1p(torch.exp(v)))      # fp32 on the host
+    y_h, s_h = run_gpu_ssd(host, chunk=chunk)
+    # A one-ulp difference of the step can flip TF32 roundings in the chunk-state
+    # product, so the state agrees to about 1e-3, not to fp32 rounding; a fused
+    # step that dropped the bias or the softplus would differ by percents.
+    ok = ~np.isnan(y_h)
+    assert np.allclose(y[ok], y_h[ok], rtol=1e-3, atol=1e-4)
+    assert np.allclose(s, s_h, rtol=2e-3, atol=1e-4)
