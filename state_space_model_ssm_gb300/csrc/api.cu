@@ -253,6 +253,11 @@ int read_options(const ssm_scan_options *opts, ssm_scan_options *out)
     return SSM_OK;
 }
 
+// Launches the scan kernels for a checked call (everything after the argument
+// checks); the options' post-scan steps run in scan_impl.
+int scan_kernels(const ssm::ScanArgs &a, const ssm_scan_tuning &t, const DeviceInfo &dev, void *workspace,
+                 size_t workspace_bytes, cudaStream_t stream);
+
 int scan_impl(float *state, const float *x, const float *dt, const float *A, const float *B,
               const float *C, const float *D, float *y, const int32_t *seq_starts,
               const int32_t *seq_lens, const int32_t *resume, int n_seqs, int n_tokens,
@@ -284,7 +289,7 @@ int scan_impl(float *state, const float *x, const float *dt, const float *A, con
     int rc = read_options(opts, &o);
     if (rc != SSM_OK)
         return rc;
-    if (o.state_snapshots || o.gated_y)
+    if (o.state_snapshots)
         return SSM_ERR_UNSUPPORTED;
 
     ssm_scan_tuning t;
@@ -317,7 +322,20 @@ int scan_impl(float *state, const float *x, const float *dt, const float *A, con
         if (rc != SSM_OK)
             return rc;
     }
+    rc = scan_kernels(a, t, dev, workspace, workspace_bytes, stream);
+    if (rc != SSM_OK)
+        return rc;
+    if (o.gated_y && n_tokens > 0 &&
+        ssm::launch_gated_norm(a, o.gate_z, o.norm_weight, o.norm_eps, o.gated_y, stream) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    return SSM_OK;
+}
 
+int scan_kernels(const ssm::ScanArgs &a, const ssm_scan_tuning &t, const DeviceInfo &dev, void *workspace,
+                 size_t workspace_bytes, cudaStream_t stream)
+{
+    const int n_seqs = a.n_seqs, n_tokens = a.n_tokens, H = a.H, P = a.P, N = a.N, G = a.G;
+    int rc = SSM_OK;
     const int N4 = N / 4;
     int path = t.path;
     if (path == SSM_PATH_AUTO)
@@ -519,7 +537,7 @@ int ssd_impl(float *state, const float *x, const float *dt, const float *A, cons
     rc = read_options(opts, &o);
     if (rc != SSM_OK)
         return rc;
-    if (o.state_snapshots || o.gated_y)
+    if (o.state_snapshots)
         return SSM_ERR_UNSUPPORTED;
 
     DeviceInfo dev;
@@ -561,6 +579,9 @@ int ssd_impl(float *state, const float *x, const float *dt, const float *A, cons
         return SSM_ERR_CUDA;
     if (ssm::launch_segment_plan(a, seg, mu, stream) != cudaSuccess ||
         ssm::launch_ssd(a, plan, L.g, mu, stream) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    if (o.gated_y && n_tokens > 0 &&
+        ssm::launch_gated_norm(a, o.gate_z, o.norm_weight, o.norm_eps, o.gated_y, stream) != cudaSuccess)
         return SSM_ERR_CUDA;
     if (check_env()) {                      // debug: report a bounded wait that gave up
         int st = 0;

@@ -210,6 +210,10 @@ cudaError_t launch_ssd_output_tc(const ScanArgs &a, const SsdPlan &plan, const S
                                  cudaStream_t stream);
 int ssd_max_head_dim();
 
+// Gated RMSNorm of y per (token, head) row, after the scan (gated_norm.cu).
+cudaError_t launch_gated_norm(const ScanArgs &a, const float *z, const float *w, float eps, float *out,
+                              cudaStream_t stream);
+
 cudaError_t launch_decode(const ScanArgs &a, const DecodeGeom &g, int lanes,
                           int vpl, int rpt, int grid_seqs, cudaStream_t stream);
 bool decode_supported(int lanes, int vpl, int rpt);

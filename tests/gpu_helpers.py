@@ -106,3 +106,47 @@ def run_gpu_ssd(inp, chunk=0, device="cuda", stream=None, y_fill=float("nan"), *
         head, tail = buf[:GUARD], buf[-GUARD:]
         assert torch.isnan(head).all() and torch.isnan(tail).all(), "guard band overwritten"
     return y.double().cpu().numpy(), state.double().cpu().numpy()
+
+
+def run_gpu_gated(inp, eps=1e-5, seed=7, ssd_chunk=None, tuning=None, workspace=False, **opts):
+    """The scan with the gated RMSNorm output (gate z ~ N(0,1), weight ~ U(0.5,1.5));
+    returns (y, state, gated, z, w) as float64 numpy arrays (gated NaN where not written)."""
+    g = torch.Generator().manual_seed(seed)
+    T, H, P = inp.x.shape
+    z = torch.randn((T, H, P), generator=g)
+    w = torch.rand((P,), generator=g) + 0.5
+    d = inp.to("cuda")
+    state = d.state.clone()
+    y = torch.full_like(d.x, float("nan"))
+    gated = torch.full_like(d.x, float("nan"))
+    zc, wc = z.cuda(), w.cuda()
+    kw = dict(gate_z=zc, norm_weight=wc, norm_eps=eps, gated_y=gated, **_opt_tensors("cuda", opts))
+    if ssd_chunk is not None:
+        bd.ssm_scan_ssd(state, d.x, d.dt, d.A, d.B, d.C, d.D, d.seq_starts, d.seq_lens, d.resume,
+                        y=y, chunk=ssd_chunk, **kw)
+    else:
+        ws = None
+        if workspace:
+            gg = inp.geom
+            nbytes = bd.workspace_bytes(inp.n_seqs, inp.n_tokens, gg.n_heads, gg.head_dim, gg.d_state,
+                                        gg.n_groups, tuning)
+            ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device="cuda")
+        bd.ssm_scan(state, d.x, d.dt, d.A, d.B, d.C, d.D, d.seq_starts, d.seq_lens, d.resume,
+                    y=y, tuning=tuning, workspace=ws, **kw)
+    torch.cuda.synchronize()
+    return (y.double().cpu().numpy(), state.double().cpu().numpy(), gated.double().cpu().numpy(),
+            z.double().numpy(), w.double().numpy())
+
+
+def assert_gated(inp, y_gpu, gated_gpu, z, w, eps):
+    """The gated output against the oracle's RMSNorm of the GPU's own y (fp32
+    rounding of the epilogue only), and untouched on unowned token rows."""
+    import oracle
+    mask = covered_tokens(inp)
+    want = oracle.gated_rmsnorm(y_gpu[mask], z[mask], w, eps)
+    got = gated_gpu[mask]
+    assert np.isfinite(got).all()
+    err = np.abs(got - want)
+    assert np.all(err <= 1e-5 * (1.0 + np.abs(want))), f"gated max err {err.max():.3e}"
+    if (~mask).any():
+        assert np.isnan(gated_gpu[~mask]).all()

@@ -292,3 +292,29 @@ def test_parity_fused_dt_time_segments():
     y_ref, s_ref = oracle.scan_inputs(inp, dt_bias=bias, dt_softplus=True)
     y, s = run_gpu(inp, workspace=True, dt_bias=bias, dt_softplus=True)
     assert_parity(inp, y, s, y_ref, s_ref)
+
+
+# ---- gated RMSNorm of y after the scan ----
+
+@pytest.mark.parametrize("path", PATHS, ids=[p[0] for p in PATHS])
+def test_parity_gated_norm(path):
+    from tests.gpu_helpers import assert_gated, run_gpu_gated
+    inp = make_inputs(Geometry(4, 16, 32, 2), [0, 9, 40], [0, 1, 1], seed=46,
+                      starts=[0, 2, 11], n_tokens=60)
+    if path[0] == "decode":
+        inp = make_inputs(Geometry(4, 16, 32, 2), [1, 0, 1], [1, 0, 0], seed=46, starts=[0, 1, 2], n_tokens=4)
+    y_ref, s_ref = oracle.scan_inputs(inp)
+    y, s, gated, z, w = run_gpu_gated(inp, eps=1e-5, tuning=path[1])
+    assert_parity(inp, y, s, y_ref, s_ref)
+    assert_gated(inp, y, gated, z, w, 1e-5)
+
+
+def test_parity_gated_norm_odd_head_dim_and_segments():
+    from tests.gpu_helpers import assert_gated, run_gpu_gated
+    for geom, lens, ws in ((Geometry(3, 37, 12, 3), [5, 64], False),
+                           (Geometry(8, 64, 128, 2), [2500], True)):
+        inp = make_inputs(geom, lens, [1] * len(lens), seed=47)
+        y_ref, s_ref = oracle.scan_inputs(inp)
+        y, s, gated, z, w = run_gpu_gated(inp, eps=1e-6, workspace=ws, dt_softplus=False)
+        assert_parity(inp, y, s, y_ref, s_ref)
+        assert_gated(inp, y, gated, z, w, 1e-6)

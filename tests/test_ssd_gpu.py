@@ -179,3 +179,14 @@ def test_ssd_fused_dt(geom, chunk):
     ok = ~np.isnan(y_h)
     assert np.allclose(y[ok], y_h[ok], rtol=1e-3, atol=1e-4)
     assert np.allclose(s, s_h, rtol=2e-3, atol=1e-4)
+
+
+@pytest.mark.parametrize("geom,chunk", [(Geometry(4, 16, 32, 2), 64), (Geometry(4, 64, 128, 2), 128)],
+                         ids=["mma_sync", "tcgen05"])
+def test_ssd_gated_norm(geom, chunk):
+    from tests.gpu_helpers import assert_gated, run_gpu_gated
+    inp = make_inputs(geom, [3, 0, 200], [0, 1, 1], seed=48, starts=[0, 3, 5], n_tokens=210)
+    y_ref, s_ref = oracle.scan_inputs(inp)
+    y, s, gated, z, w = run_gpu_gated(inp, eps=1e-5, ssd_chunk=chunk)
+    assert_parity(inp, y, s, y_ref, s_ref, tol=SSD_TOL)
+    assert_gated(inp, y, gated, z, w, 1e-5)
