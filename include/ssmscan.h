@@ -174,11 +174,13 @@ typedef struct {
 
 /*
  * The scan with tuning, options and workspace (each may be NULL / 0):
- * ssm_scan_ws plus the optional steps of ssm_scan_options.  State snapshots
- * run the direct prefill kernel (one sequence token by token, no time
- * segments) or the decode kernel.  Errors as for ssm_scan_ws, and
- * SSM_ERR_INVALID_ARG for a misaligned option pointer or norm_eps <= 0 with
- * gated_y set.
+ * ssm_scan_ws plus the optional steps of ssm_scan_options.  With state
+ * snapshots the call runs the decode kernel whatever the lengths (it steps
+ * each sequence token by token with the state in registers and writes every
+ * intermediate state; meant for the few tokens of a speculative verify step);
+ * a tuning that asks for a prefill path then returns SSM_ERR_UNSUPPORTED.
+ * Errors as for ssm_scan_ws, and SSM_ERR_INVALID_ARG for a misaligned option
+ * pointer or norm_eps <= 0 with gated_y set.
  */
 int ssm_scan_ex(float *state_slots, const float *x, const float *dt,
                 const float *A, const float *B, const float *C, const float *D,

@@ -289,9 +289,6 @@ int scan_impl(float *state, const float *x, const float *dt, const float *A, con
     int rc = read_options(opts, &o);
     if (rc != SSM_OK)
         return rc;
-    if (o.state_snapshots)
-        return SSM_ERR_UNSUPPORTED;
-
     ssm_scan_tuning t;
     std::memset(&t, 0, sizeof t);
     if (tun)
@@ -315,7 +312,13 @@ int scan_impl(float *state, const float *x, const float *dt, const float *A, con
     a.seq_starts = seq_starts; a.seq_lens = seq_lens; a.resume = resume;
     a.n_seqs = n_seqs; a.n_tokens = n_tokens; a.H = H; a.P = P; a.N = N; a.G = G;
     a.dt_bias = o.dt_bias; a.dt_softplus = o.dt_softplus;
+    a.snaps = o.state_snapshots;
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_v);
+    if (a.snaps) {                          // the decode kernel steps tokens one by one
+        if (t.path == SSM_PATH_PREFILL || t.path == SSM_PATH_PREFILL_DIRECT)
+            return SSM_ERR_UNSUPPORTED;
+        t.path = SSM_PATH_DECODE;
+    }
 
     if (check_env()) {
         rc = check_metadata(a, stream);
@@ -553,6 +556,7 @@ int ssd_impl(float *state, const float *x, const float *dt, const float *A, cons
     a.seq_starts = seq_starts; a.seq_lens = seq_lens; a.resume = resume;
     a.n_seqs = n_seqs; a.n_tokens = n_tokens; a.H = H; a.P = P; a.N = N; a.G = G;
     a.dt_bias = o.dt_bias; a.dt_softplus = o.dt_softplus;
+    a.snaps = nullptr;
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_v);
     if (check_env()) {
         rc = check_metadata(a, stream);

@@ -15,7 +15,9 @@
 // A warp's rows always belong to one sequence, so the token loop is uniform
 // per warp, and a lane group's RPT rows to one head, so dt, dA, B and C are
 // loaded once per lane group and token.  The kernel is correct for any
-// sequence lengths; it is meant for length 1.
+// sequence lengths; it is meant for length 1, and for the short runs of a
+// speculative verify step, where it can also write the state after every
+// token (snapshots) straight from the registers.
 #include "scan_common.cuh"
 
 namespace ssm {
@@ -107,6 +109,17 @@ decode_kernel(const ScanArgs a, const DecodeGeom geo)
                 if (q == qy) dxv = xv[q];
             if (reduced_writer<LANES, RPT>(j) && valid)
                 a.y[tok * HP + r0 + qy] = fmaf(Dh, dxv, ysum);
+            if (a.snaps && valid) {                                       // state after token t
+                float *sn = a.snaps + (tok * HP + r0) * N;
+#pragma unroll
+                for (int q = 0; q < RPT; ++q)
+#pragma unroll
+                    for (int k = 0; k < VPL; ++k) {
+                        const int c = k * LANES + j;
+                        if (EXACT || c < N4)
+                            __stcs(reinterpret_cast<float4 *>(sn + (long long)q * N + 4 * c), s[q][k]);
+                    }
+            }
         }
 
         // A7: registers -> slot (coalesced 128-bit stores).

@@ -32,6 +32,7 @@ struct ScanArgs {
     int n_seqs, n_tokens, H, P, N, G;
     const float *dt_bias;      // [H] added to dt before use, or null
     int dt_softplus;           // nonzero: dt_eff = softplus(dt + dt_bias) (identity above 20)
+    float *snaps;              // [T][H][P][N]: the state after each owned token, or null (decode kernel)
 };
 
 // The step size the recurrence uses for raw value `v` of head h: v as given,

@@ -318,3 +318,47 @@ def test_parity_gated_norm_odd_head_dim_and_segments():
         y, s, gated, z, w = run_gpu_gated(inp, eps=1e-6, workspace=ws, dt_softplus=False)
         assert_parity(inp, y, s, y_ref, s_ref)
         assert_gated(inp, y, gated, z, w, 1e-6)
+
+
+# ---- per-token state snapshots (speculative verify) ----
+
+@pytest.mark.parametrize("fused_dt", [False, True], ids=["plain", "fused_dt"])
+def test_parity_state_snapshots(fused_dt):
+    """Short multi-token sequences (fresh, resuming, empty, with gaps): every
+    owned token row of the snapshots equals the oracle's state after that
+    token; unowned rows stay untouched; y and the slots as in the scan."""
+    from oracle import extensions as ext
+    geom = Geometry(4, 64, 128, 2)
+    inp = make_inputs(geom, [4, 1, 0, 6, 3], [1, 0, 1, 1, 0], seed=49,
+                      starts=[0, 5, 6, 6, 13], n_tokens=17)
+    kw = {}
+    if fused_dt:
+        g = torch.Generator().manual_seed(50)
+        inp.dt = torch.randn(inp.dt.shape, generator=g) * 0.5 - 2.0
+        kw = dict(dt_bias=torch.rand(geom.n_heads, generator=g) - 0.5, dt_softplus=True)
+    y_ref, s_ref, snaps_ref = ext.scan_with_snapshots(oracle.scan, inp, n_threads=1, **kw)
+    d = inp.to("cuda")
+    state = d.state.clone()
+    y = torch.full_like(d.x, float("nan"))
+    snaps = torch.full((inp.n_tokens, geom.n_heads, geom.head_dim, geom.d_state), float("nan"), device="cuda")
+    bd.ssm_scan(state, d.x, d.dt, d.A, d.B, d.C, d.D, d.seq_starts, d.seq_lens, d.resume, y=y,
+                snapshots=snaps, **{k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in kw.items()})
+    torch.cuda.synchronize()
+    yg, sg, ng = y.double().cpu().numpy(), state.double().cpu().numpy(), snaps.double().cpu().numpy()
+    assert_parity(inp, yg, sg, y_ref, s_ref)
+    from tests.gpu_helpers import covered_tokens
+    mask = covered_tokens(inp)
+    err = np.abs(ng[mask] - snaps_ref[mask])
+    assert np.all(err <= 1e-4 * (1.0 + np.abs(snaps_ref[mask]))), f"snapshot max err {err.max():.3e}"
+    assert np.isnan(ng[~mask]).all()
+
+
+def test_state_snapshots_refuse_prefill_paths():
+    inp = make_inputs(Geometry(2, 16, 32, 1), [3], [0], seed=51)
+    d = inp.to("cuda")
+    snaps = torch.empty((3, 2, 16, 32), device="cuda")
+    for path in (bd.PATH_PREFILL, bd.PATH_PREFILL_DIRECT):
+        with pytest.raises(bd.SsmScanError) as e:
+            bd.ssm_scan(d.state.clone(), d.x, d.dt, d.A, d.B, d.C, d.D, d.seq_starts, d.seq_lens, d.resume,
+                        snapshots=snaps, tuning=_tuning(path=path))
+        assert e.value.status == bd.SSM_ERR_UNSUPPORTED
