@@ -305,6 +305,34 @@ int ssm_scan_static(float *state_slots, const float *x, const float *dt,
                     int n_seqs, int n_tokens, int n_heads, int head_dim,
                     int d_state, int n_groups, void *stream);
 
+/*
+ * Causal depthwise conv1d + SiLU with a rolling conv-state slot, Mamba2's op in
+ * front of the scan ("ssm_gated_delta.cu", kernel 2 and its batched variant;
+ * the pages' kernel has no bias, the optional bias here is added before SiLU).
+ * For sequence i (tokens packed as for ssm_scan) and channel c, the stream of
+ * inputs is the slot's kernel_size-1 remembered inputs (oldest first; zeros
+ * when resume_flags[i] == 0) followed by the sequence's tokens, and
+ *     out[t, c] = silu(bias[c] + sum_{u < K} weight[c, u] * stream[t + u]),
+ * silu(v) = v / (1 + exp(-v)), with stream[K-1+t] = x[t, c] (so weight[c, K-1]
+ * multiplies the current token).  Afterwards slot i holds the stream's last
+ * K-1 entries, and snapshot row t (optional) the slot image right after
+ * token t.
+ *   x, out      [n_tokens][channels] fp32, device (out written for owned tokens)
+ *   weight      [channels][kernel_size] fp32, device
+ *   bias        [channels] fp32, device, or NULL
+ *   conv_state  [n_seqs][channels][kernel_size-1] fp32, device, in/out
+ *   snapshots   [n_tokens][channels][kernel_size-1] fp32, device, or NULL
+ *   kernel_size 1 .. 8
+ * Ownership, metadata, stream and 4-byte alignment rules as for ssm_scan.
+ * Errors: SSM_ERR_INVALID_ARG (sizes, NULL or misaligned pointers),
+ * SSM_ERR_UNSUPPORTED (n_tokens * channels above 2^31), SSM_ERR_CUDA.
+ */
+int ssm_conv1d(const float *x, const float *weight, const float *bias,
+               float *conv_state, float *out, const int32_t *seq_starts,
+               const int32_t *seq_lens, const int32_t *resume_flags,
+               int n_seqs, int n_tokens, int channels, int kernel_size,
+               float *snapshots, void *stream);
+
 /* Text for a status code (static storage; never NULL). */
 const char *ssm_status_string(int status);
 

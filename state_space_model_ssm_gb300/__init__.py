@@ -8,8 +8,8 @@ ctypes.  ``workloads`` draws the seeded synthetic inputs.
 """
 from .binding import (PATH_AUTO, PATH_DECODE, PATH_PREFILL, PATH_PREFILL_DIRECT,  # noqa: F401
                       Options, SsmScanError, Tuning,
-                      load, ssd_workspace_bytes, ssm_scan, ssm_scan_ssd,
+                      load, ssd_workspace_bytes, ssm_conv1d, ssm_scan, ssm_scan_ssd,
                       status_string)
 
-__all__ = ["Options", "ssm_scan", "ssm_scan_ssd", "ssd_workspace_bytes", "Tuning", "SsmScanError", "PATH_AUTO", "PATH_DECODE",
+__all__ = ["Options", "ssm_conv1d", "ssm_scan", "ssm_scan_ssd", "ssd_workspace_bytes", "Tuning", "SsmScanError", "PATH_AUTO", "PATH_DECODE",
            "PATH_PREFILL", "PATH_PREFILL_DIRECT", "load", "status_string"]

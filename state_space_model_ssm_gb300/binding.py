@@ -82,6 +82,8 @@ def load():
             lib.ssm_scan_ssd.argtypes = _SCAN_ARGS + [_I, ctypes.POINTER(Options), _P, ctypes.c_size_t, _P]
             lib.ssm_scan_ssd_workspace_bytes.restype = ctypes.c_size_t
             lib.ssm_scan_ssd_workspace_bytes.argtypes = [_I] * 7
+            lib.ssm_conv1d.restype = _I
+            lib.ssm_conv1d.argtypes = [_P] * 8 + [_I] * 4 + [_P, _P]
             lib.ssm_status_string.restype = ctypes.c_char_p
             lib.ssm_status_string.argtypes = [_I]
             _lib = lib
@@ -299,3 +301,50 @@ def ssm_scan_ssd(state_slots, x, dt, A, B, C, D, seq_starts, seq_lens, resume_fl
     if rc != SSM_OK:
         raise SsmScanError(rc, "ssm_scan_ssd")
     return y
+
+
+def conv1d_raw(x, weight, bias, conv_state, out, seq_starts, seq_lens, resume, n_seqs, n_tokens,
+               channels, kernel_size, snapshots=None, stream=0) -> int:
+    """ssm_conv1d with integer pointers; returns the status code."""
+    ptrs = [_P(int(p) if p else None) for p in
+            (x, weight, bias, conv_state, out, seq_starts, seq_lens, resume)]
+    return load().ssm_conv1d(*ptrs, int(n_seqs), int(n_tokens), int(channels), int(kernel_size),
+                             _P(int(snapshots) if snapshots else None), _P(int(stream) if stream else None))
+
+
+def ssm_conv1d(x, weight, conv_state, seq_starts, seq_lens, resume_flags, out=None, *, bias=None,
+               snapshots=None, stream=None):
+    """Causal depthwise conv1d + SiLU with a rolling conv-state slot (``ssm_conv1d``).
+
+    x [T, C], weight [C, K], conv_state [n, C, K-1] (updated in place), bias [C]
+    or None, snapshots [T, C, K-1] or None; returns out [T, C]."""
+    dev = x.device
+    if dev.type != "cuda":
+        raise ValueError("the convolution runs on CUDA tensors only")
+    T, C = x.shape
+    K = weight.shape[1]
+    n = seq_lens.shape[0]
+    f32, i32 = torch.float32, torch.int32
+    _check(x, "x", f32, dev)
+    _check(weight, "weight", f32, dev, (C, K))
+    _check(conv_state, "conv_state", f32, dev, (n, C, K - 1))
+    if bias is not None:
+        _check(bias, "bias", f32, dev, (C,))
+    if snapshots is not None:
+        _check(snapshots, "snapshots", f32, dev, (T, C, K - 1))
+    for nm, t in (("seq_starts", seq_starts), ("seq_lens", seq_lens), ("resume_flags", resume_flags)):
+        _check(t, nm, i32, dev, (n,))
+    if out is None:
+        out = torch.empty((T, C), dtype=f32, device=dev)
+    _check(out, "out", f32, dev, (T, C))
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    with torch.cuda.device(dev):
+        rc = conv1d_raw(x.data_ptr(), weight.data_ptr(), bias.data_ptr() if bias is not None else None,
+                        conv_state.data_ptr(), out.data_ptr(), seq_starts.data_ptr(), seq_lens.data_ptr(),
+                        resume_flags.data_ptr(), n, T, C, K,
+                        snapshots.data_ptr() if snapshots is not None else None, stream=handle)
+    if rc != SSM_OK:
+        raise SsmScanError(rc, "ssm_conv1d")
+    return out

@@ -16,6 +16,7 @@
 namespace {
 
 constexpr int kMaxDState = 1024;
+constexpr int kMaxConvKernel = 8;
 constexpr int kMaxDevices = 64;
 
 int pow2ceil(int v)
@@ -688,6 +689,38 @@ size_t ssm_scan_ssd_workspace_bytes(int n_seqs, int n_tokens, int n_heads, int h
     if (plan_ssd(n_seqs, n_tokens, n_heads, head_dim, d_state, n_groups, chunk, nullptr, &L) != SSM_OK)
         return 0;
     return L.bytes;
+}
+
+int ssm_conv1d(const float *x, const float *weight, const float *bias, float *conv_state, float *out,
+               const int32_t *seq_starts, const int32_t *seq_lens, const int32_t *resume_flags, int n_seqs,
+               int n_tokens, int channels, int kernel_size, float *snapshots, void *stream)
+{
+    if (n_seqs < 0 || n_tokens < 0 || channels <= 0 || kernel_size < 1 || kernel_size > kMaxConvKernel)
+        return SSM_ERR_INVALID_ARG;
+    if ((long long)n_tokens * channels > INT_MAX || (long long)n_seqs * channels > INT_MAX)
+        return SSM_ERR_UNSUPPORTED;
+    if (n_seqs == 0)
+        return SSM_OK;
+    if (!weight || !seq_starts || !seq_lens || !resume_flags || (kernel_size > 1 && !conv_state))
+        return SSM_ERR_INVALID_ARG;
+    if (n_tokens > 0 && (!x || !out))
+        return SSM_ERR_INVALID_ARG;
+    if (!aligned(x, 4) || !aligned(weight, 4) || !aligned(bias, 4) || !aligned(conv_state, 4) ||
+        !aligned(out, 4) || !aligned(snapshots, 4) || !aligned(seq_starts, 4) || !aligned(seq_lens, 4) ||
+        !aligned(resume_flags, 4))
+        return SSM_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (check_env()) {
+        ssm::ScanArgs m{};
+        m.seq_starts = seq_starts; m.seq_lens = seq_lens; m.n_seqs = n_seqs; m.n_tokens = n_tokens;
+        const int rc = check_metadata(m, st);
+        if (rc != SSM_OK)
+            return rc;
+    }
+    if (ssm::launch_conv1d(x, weight, bias, conv_state, out, snapshots, seq_starts, seq_lens, resume_flags, n_seqs,
+                           n_tokens, channels, kernel_size, st) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    return SSM_OK;
 }
 
 const char *ssm_status_string(int status)

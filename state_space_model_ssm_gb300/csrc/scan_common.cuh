@@ -211,6 +211,11 @@ cudaError_t launch_ssd_output_tc(const ScanArgs &a, const SsdPlan &plan, const S
                                  cudaStream_t stream);
 int ssd_max_head_dim();
 
+// Causal depthwise conv1d + SiLU with a rolling conv-state slot (conv1d.cu).
+cudaError_t launch_conv1d(const float *x, const float *w, const float *bias, float *state, float *out,
+                          float *snaps, const int32_t *seq_starts, const int32_t *seq_lens,
+                          const int32_t *resume, int n_seqs, int n_tokens, int C, int K, cudaStream_t stream);
+
 // Gated RMSNorm of y per (token, head) row, after the scan (gated_norm.cu).
 cudaError_t launch_gated_norm(const ScanArgs &a, const float *z, const float *w, float eps, float *out,
                               cudaStream_t stream);

@@ -192,3 +192,27 @@ def test_header_declares_the_options_entry_point_and_struct():
 def test_options_rejected_on_the_host(lib, opts, expect):
     o = bd.Options(**opts)
     assert _ex_call(lib, o) == expect
+
+
+# ---- ssm_conv1d: host checks ----
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(kernel_size=0), bd.SSM_ERR_INVALID_ARG),
+    (dict(kernel_size=9), bd.SSM_ERR_INVALID_ARG),
+    (dict(channels=0), bd.SSM_ERR_INVALID_ARG),
+    (dict(n_tokens=-1), bd.SSM_ERR_INVALID_ARG),
+    (dict(weight=0), bd.SSM_ERR_INVALID_ARG),
+    (dict(conv_state=0), bd.SSM_ERR_INVALID_ARG),
+    (dict(x=PTR + 2), bd.SSM_ERR_INVALID_ARG),
+    (dict(bias=PTR + 1), bd.SSM_ERR_INVALID_ARG),
+    (dict(n_tokens=1 << 20, channels=1 << 12), bd.SSM_ERR_UNSUPPORTED),
+])
+def test_conv1d_host_rejects(lib, over, expect):
+    args = dict(x=PTR, weight=PTR, bias=None, conv_state=PTR, out=PTR, seq_starts=PTR, seq_lens=PTR,
+                resume=PTR, n_seqs=2, n_tokens=8, channels=16, kernel_size=4, snapshots=None)
+    args.update(over)
+    assert bd.conv1d_raw(**args) == expect
+
+
+def test_conv1d_empty_batch_is_a_noop(lib):
+    assert bd.conv1d_raw(0, 0, 0, 0, 0, 0, 0, 0, 0, 8, 16, 4) == bd.SSM_OK
