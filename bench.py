@@ -68,6 +68,7 @@ def parse_args():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-ssd", action="store_true")
+    ap.add_argument("--no-next", action="store_true")
     return ap.parse_args()
 
 
@@ -365,6 +366,101 @@ def ssd_algorithmic_flops(inp, chunk):
     return chunks * (G * 2 * Q * Q * N + H * (2 * Q * Q * P + 4 * Q * N * P))
 
 
+def _timed(fn, steps, flush=None, warmup=3):
+    """Mean ms of fn() over `steps` runs, CUDA events on the current stream,
+    L2 flushed before each run when `flush` (a large tensor) is given."""
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        if flush is not None:
+            flush.zero_()
+        fn()
+    torch.cuda.synchronize()
+    evs = [event_pair() for _ in range(steps)]
+    for e0, e1 in evs:
+        if flush is not None:
+            flush.zero_()
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return sum(e0.elapsed_time(e1) for e0, e1 in evs) / steps
+
+
+def run_next_rows(dev, inp, d, peaks, steps=10):
+    """The steps around the scan, each timed on its own workload with its HBM
+    roofline (bytes moved per call / time / measured copy bandwidth)."""
+    from state_space_model_ssm_gb300 import binding as bd
+    hbm = peaks["hbm_gbs"] * 1e9
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    g = torch.Generator().manual_seed(77)
+    H, P, N = inp.geom.n_heads, inp.geom.head_dim, inp.geom.d_state
+    T = inp.n_tokens
+    ws = prefill_workspace(inp, dev)
+    state = d.state.clone()
+    y = torch.empty_like(d.x)
+    out = {}
+
+    def prefill(**kw):
+        return lambda: bd.ssm_scan(state, d.x, kw.pop("dt", d.dt), d.A, d.B, d.C, d.D, d.seq_starts,
+                                   d.seq_lens, d.resume, y=y, workspace=ws, **kw)
+    base = _timed(prefill(), steps, flush)
+
+    # 1. fused dt: raw dt + bias with softplus inside the kernels
+    raw = (torch.randn(d.dt.shape, generator=g) * 0.5 - 2.0).to(dev)
+    bias = (torch.rand(H, generator=g) - 0.5).to(dev)
+    fused = _timed(prefill(dt=raw, dt_bias=bias, dt_softplus=True), steps, flush)
+    out["fused_dt"] = {"workload": "prefill_1x4096 with raw dt, dt_bias and softplus",
+                       "ms": fused, "ms_plain": base, "overhead_pct": 100.0 * (fused - base) / base}
+
+    # 2. gated RMSNorm after the scan: y and z read, gated y written
+    z = torch.randn((T, H, P), generator=g).to(dev)
+    wn = (torch.rand(P, generator=g) + 0.5).to(dev)
+    gated = torch.empty_like(d.x)
+    with_norm = _timed(prefill(gate_z=z, norm_weight=wn, norm_eps=1e-5, gated_y=gated), steps, flush)
+    nbytes = 3 * T * H * P * 4
+    extra = max(with_norm - base, 1e-6)
+    out["gated_norm"] = {"workload": "prefill_1x4096, RMSNorm(y) w silu(z) per (token, head) row",
+                         "ms": with_norm, "ms_added": extra, "bytes": nbytes,
+                         "roofline": {"bound": "hbm", "achieved": nbytes / (extra * 1e-3) / 1e9,
+                                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                      "frac": nbytes / (extra * 1e-3) / hbm}}
+
+    # 3. state snapshots: a 16 x 4-token verify step at Nemotron-H geometry
+    from state_space_model_ssm_gb300.workloads import Geometry, make_inputs
+    vin = make_inputs(Geometry(64, 64, 128, 8), [4] * 16, [1] * 16, seed=78)
+    vd = vin.to(dev)
+    vstate = vd.state.clone()
+    vy = torch.empty_like(vd.x)
+    snaps = torch.empty((vin.n_tokens, 64, 64, 128), device=dev)
+    verify = _timed(lambda: bd.ssm_scan(vstate, vd.x, vd.dt, vd.A, vd.B, vd.C, vd.D, vd.seq_starts,
+                                        vd.seq_lens, vd.resume, y=vy, snapshots=snaps), steps, flush)
+    slot = 64 * 64 * 128 * 4
+    sbytes = 2 * 16 * slot + vin.n_tokens * slot
+    out["state_snapshots"] = {"workload": "16 resuming sequences x 4 tokens, state after every token",
+                              "ms": verify, "bytes": sbytes,
+                              "roofline": {"bound": "hbm", "achieved": sbytes / (verify * 1e-3) / 1e9,
+                                           "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                           "frac": sbytes / (verify * 1e-3) / hbm}}
+
+    # 4. conv1d + SiLU: 1 x 4096 tokens over Nemotron-H's conv width 6144, k = 4
+    Cc, K = 6144, 4
+    xc = torch.randn((T, Cc), generator=g).to(dev)
+    wc = (torch.randn((Cc, K), generator=g) * 0.5).to(dev)
+    bc = (torch.randn((Cc,), generator=g) * 0.1).to(dev)
+    cst = torch.randn((1, Cc, K - 1), generator=g).to(dev)
+    oc = torch.empty_like(xc)
+    one = torch.ones(1, dtype=torch.int32, device=dev)
+    conv = _timed(lambda: bd.ssm_conv1d(xc, wc, cst, d.seq_starts, d.seq_lens, one, out=oc, bias=bc),
+                  steps, flush)
+    cbytes = 2 * T * Cc * 4 + Cc * (K + 1) * 4 + 2 * Cc * (K - 1) * 4
+    out["conv1d"] = {"workload": "1 x 4096 tokens x 6144 channels, k = 4, resuming",
+                     "ms": conv, "bytes": cbytes,
+                     "roofline": {"bound": "hbm", "achieved": cbytes / (conv * 1e-3) / 1e9,
+                                  "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                  "frac": cbytes / (conv * 1e-3) / hbm}}
+    return out
+
+
 def prefill_algorithmic(inp):
     T = int(inp.seq_lens.sum())
     H, P, N, G = inp.geom.n_heads, inp.geom.head_dim, inp.geom.d_state, inp.geom.n_groups
@@ -519,6 +615,8 @@ def ours(args):
                          "traffic": ncu_traffic("ssd_output_kernel", "prefill_1x4096"),
                          "traffic_kernel": "the output kernel (tcgen05), DRAM bytes per launch"},
         }
+    if not args.no_next:
+        line["next_rows"] = run_next_rows(dev, inp, d, peaks)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_prefill(inp)
     if rank == 0:

@@ -142,12 +142,15 @@ int ssm_scan_tuned(float *state_slots, const float *x, const float *dt,
 
 /*
  * Optional steps around the scan (all NULL / 0 = the plain scan).
- *   dt_bias, dt_softplus  Mamba2's discretisation of dt, fused into the scan's
- *       own loads of dt ("The llama journey", Day 14 kernel body; the decay-gate
- *       kernel of "ssm_gated_delta.cu"): v = dt[t,h] + dt_bias[h] (dt_bias NULL:
- *       no bias), then with dt_softplus nonzero the step is v for v > 20 and
- *       log1p(exp(v)) otherwise; that step replaces dt[t,h] everywhere in the
- *       recurrence above.  dt_bias: device, [n_heads] fp32, 4-byte aligned.
+ *   dt_bias, dt_softplus  Mamba2's discretisation of dt ("The llama journey",
+ *       Day 14 kernel body; the decay-gate kernel of "ssm_gated_delta.cu"):
+ *       v = dt[t,h] + dt_bias[h] (dt_bias NULL: no bias), then with dt_softplus
+ *       nonzero the step is v for v > 20 and log1p(exp(v)) otherwise; that step
+ *       replaces dt[t,h] everywhere in the recurrence above.  It is computed by
+ *       a pass of its own into the first n_tokens*n_heads floats (rounded up to
+ *       256 bytes) of the workspace, so these options need a workspace (see
+ *       ssm_scan_ex_workspace_bytes); the scan kernels then read it as their
+ *       step.  dt_bias: device, [n_heads] fp32, 4-byte aligned.
  *   state_snapshots  device, [n_tokens][n_heads][head_dim][d_state] fp32, out:
  *       row t receives the state right after token t for every token owned by a
  *       sequence, so accepting the first M tokens of a speculative run restores
@@ -180,7 +183,9 @@ typedef struct {
  * intermediate state; meant for the few tokens of a speculative verify step);
  * a tuning that asks for a prefill path then returns SSM_ERR_UNSUPPORTED.
  * Errors as for ssm_scan_ws, and SSM_ERR_INVALID_ARG for a misaligned option
- * pointer or norm_eps <= 0 with gated_y set.
+ * pointer, norm_eps <= 0 with gated_y set, or dt options without a workspace
+ * of at least the discretised step's bytes.  The workspace is used as by
+ * ssm_scan_ws after that step's bytes.
  */
 int ssm_scan_ex(float *state_slots, const float *x, const float *dt,
                 const float *A, const float *B, const float *C, const float *D,
@@ -241,7 +246,8 @@ size_t ssm_scan_workspace_bytes(int n_seqs, int n_tokens, int n_heads,
  *   workspace     device memory, 256-byte aligned, at least
  *                 ssm_scan_ssd_workspace_bytes(...) bytes for the same sizes
  *                 and chunk (chunk states [units][n_heads][head_dim][d_state]
- *                 fp32, units <= n_seqs + ceil(n_tokens / chunk)); scratch:
+ *                 fp32, units <= n_seqs + ceil(n_tokens / chunk), and room for
+ *                 the discretised step of the dt options); scratch:
  *                 undefined afterwards, not shared by calls that overlap on
  *                 the GPU
  * Same arguments, layouts and metadata rules as ssm_scan, and also:
@@ -262,6 +268,17 @@ int ssm_scan_ssd(float *state_slots, const float *x, const float *dt,
                  int n_heads, int head_dim, int d_state, int n_groups,
                  int chunk, const ssm_scan_options *options, void *workspace,
                  size_t workspace_bytes, void *stream);
+
+/*
+ * Bytes of workspace ssm_scan_ex uses for these sizes, tuning and options
+ * (NULL = none): the discretised step when dt options are set, plus what
+ * ssm_scan_workspace_bytes reports (nothing with state snapshots); 0 for
+ * invalid arguments or when none is needed.
+ */
+size_t ssm_scan_ex_workspace_bytes(int n_seqs, int n_tokens, int n_heads,
+                                   int head_dim, int d_state, int n_groups,
+                                   const ssm_scan_tuning *tuning,
+                                   const ssm_scan_options *options);
 
 /*
  * Bytes of workspace ssm_scan_ssd needs for these sizes and chunk (the same on

@@ -78,6 +78,8 @@ def load():
             lib.ssm_scan_ex.restype = _I
             lib.ssm_scan_ex.argtypes = _SCAN_ARGS + [ctypes.POINTER(Tuning), ctypes.POINTER(Options), _P,
                                                      ctypes.c_size_t, _P]
+            lib.ssm_scan_ex_workspace_bytes.restype = ctypes.c_size_t
+            lib.ssm_scan_ex_workspace_bytes.argtypes = [_I] * 6 + [ctypes.POINTER(Tuning), ctypes.POINTER(Options)]
             lib.ssm_scan_ssd.restype = _I
             lib.ssm_scan_ssd.argtypes = _SCAN_ARGS + [_I, ctypes.POINTER(Options), _P, ctypes.c_size_t, _P]
             lib.ssm_scan_ssd_workspace_bytes.restype = ctypes.c_size_t
@@ -150,6 +152,15 @@ def ssd_raw(state, x, dt, A, B, C, D, y, seq_starts, seq_lens, resume,
                                ctypes.c_size_t(int(workspace_bytes)), _P(int(stream) if stream else None))
 
 
+def ex_workspace_bytes(n_seqs, n_tokens, n_heads, head_dim, d_state, n_groups,
+                       tuning: Tuning | None = None, options: Options | None = None) -> int:
+    """Bytes of workspace ssm_scan_ex uses (the discretised step of the dt options first)."""
+    tp = ctypes.byref(tuning) if tuning is not None else None
+    op = ctypes.byref(options) if options is not None else None
+    return int(load().ssm_scan_ex_workspace_bytes(int(n_seqs), int(n_tokens), int(n_heads), int(head_dim),
+                                                  int(d_state), int(n_groups), tp, op))
+
+
 def make_options(dev, H, P, T, *, dt_bias=None, dt_softplus=False, snapshots=None, gate_z=None,
                  norm_weight=None, norm_eps=1e-6, gated_y=None):
     """Options from tensors (checked for dtype, device and shape); None when all are off."""
@@ -206,8 +217,10 @@ def ssm_scan(state_slots, x, dt, A, B, C, D, seq_starts, seq_lens, resume_flags,
     state_slots [n,H,P,N] fp32 (updated in place), x [T,H,P], dt [T,H], A [H],
     B/C [T,G,N], D [H] fp32; seq_starts/seq_lens/resume_flags [n] int32; all on
     one CUDA device.  Returns y [T,H,P] (allocated if not given).
-    workspace: optional uint8 CUDA tensor (see ``workspace_bytes``); lets long
-    sequences run as parallel time segments.
+    workspace: optional uint8 CUDA tensor (see ``workspace_bytes``, or
+    ``ex_workspace_bytes`` with options); lets long sequences run as parallel
+    time segments.  With the dt options one is allocated when none of the
+    needed size is given.
     dt_bias [H] / dt_softplus: discretise dt inside the scan; snapshots
     [T,H,P,N]: the state after every token; gated_y [T,H,P] with gate_z
     [T,H,P], norm_weight [P], norm_eps: the gated RMSNorm of y (see
@@ -242,6 +255,11 @@ def ssm_scan(state_slots, x, dt, A, B, C, D, seq_starts, seq_lens, resume_flags,
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
     opts = make_options(dev, H, P, T, dt_bias=dt_bias, dt_softplus=dt_softplus, snapshots=snapshots,
                         gate_z=gate_z, norm_weight=norm_weight, norm_eps=norm_eps, gated_y=gated_y)
+    if opts is not None and (dt_bias is not None or dt_softplus):
+        need = ex_workspace_bytes(n, T, H, P, N, G, tuning, opts)
+        if ws_bytes < need:                   # the discretised step needs room in the workspace
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+            ws_ptr, ws_bytes = workspace.data_ptr(), need
     with torch.cuda.device(dev):
         rc = scan_raw(state_slots.data_ptr(), x.data_ptr(), dt.data_ptr(), A.data_ptr(),
                       B.data_ptr(), C.data_ptr(), D.data_ptr(), y.data_ptr(),

@@ -236,6 +236,14 @@ int plan_prefill(const ssm_scan_tuning &t, bool scaled, int n_seqs, int n_tokens
     return SSM_OK;
 }
 
+// Workspace bytes the discretised step takes (0 without the dt options).
+size_t dt_buffer_bytes(const ssm_scan_options &o, int n_tokens, int H)
+{
+    if (!o.dt_bias && !o.dt_softplus)
+        return 0;
+    return align256((size_t)n_tokens * H * sizeof(float));
+}
+
 // Copy the caller's options (NULL = all off) and check their pointers.
 int read_options(const ssm_scan_options *opts, ssm_scan_options *out)
 {
@@ -290,6 +298,11 @@ int scan_impl(float *state, const float *x, const float *dt, const float *A, con
     int rc = read_options(opts, &o);
     if (rc != SSM_OK)
         return rc;
+    // The discretised step goes to the front of the workspace; the rest is
+    // what the segment plan may use.
+    const size_t dtb = dt_buffer_bytes(o, n_tokens, H);
+    if (dtb > 0 && (!workspace || !aligned(workspace, 256) || workspace_bytes < dtb))
+        return SSM_ERR_INVALID_ARG;
     ssm_scan_tuning t;
     std::memset(&t, 0, sizeof t);
     if (tun)
@@ -312,7 +325,6 @@ int scan_impl(float *state, const float *x, const float *dt, const float *A, con
     a.state = state; a.x = x; a.dt = dt; a.A = A; a.B = B; a.C = C; a.D = D; a.y = y;
     a.seq_starts = seq_starts; a.seq_lens = seq_lens; a.resume = resume;
     a.n_seqs = n_seqs; a.n_tokens = n_tokens; a.H = H; a.P = P; a.N = N; a.G = G;
-    a.dt_bias = o.dt_bias; a.dt_softplus = o.dt_softplus;
     a.snaps = o.state_snapshots;
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_v);
     if (a.snaps) {                          // the decode kernel steps tokens one by one
@@ -325,6 +337,14 @@ int scan_impl(float *state, const float *x, const float *dt, const float *A, con
         rc = check_metadata(a, stream);
         if (rc != SSM_OK)
             return rc;
+    }
+    if (dtb > 0) {
+        float *step = static_cast<float *>(workspace);
+        if (ssm::launch_dt_prep(a, o.dt_bias, o.dt_softplus, step, stream) != cudaSuccess)
+            return SSM_ERR_CUDA;
+        a.dt = step;
+        workspace = static_cast<char *>(workspace) + dtb;
+        workspace_bytes -= dtb;
     }
     rc = scan_kernels(a, t, dev, workspace, workspace_bytes, stream);
     if (rc != SSM_OK)
@@ -418,7 +438,8 @@ int scan_kernels(const ssm::ScanArgs &a, const ssm_scan_tuning &t, const DeviceI
 struct SsdLayout {
     int chunk = 0;
     long long max_units = 0;
-    size_t off_units = 0, off_n_units = 0, off_status = 0, off_unit_base = 0, off_decay = 0, off_state = 0;
+    size_t off_step = 0, off_units = 0, off_n_units = 0, off_status = 0, off_unit_base = 0, off_decay = 0,
+           off_state = 0;
     size_t bytes = 0;
     ssm::SsdGeom g{};
 };
@@ -462,6 +483,7 @@ int plan_ssd(int n_seqs, int n_tokens, int H, int P, int N, int G, int chunk, co
         return SSM_ERR_UNSUPPORTED;
     const size_t slot = (size_t)H * P * N * sizeof(float);
     size_t off = 0;
+    L.off_step = off;       off = align256(off + (size_t)n_tokens * H * sizeof(float));
     L.off_units = off;      off = align256(off + (size_t)L.max_units * sizeof(int2));
     L.off_n_units = off;    off = align256(off + sizeof(int));
     L.off_status = off;     off = align256(off + sizeof(int));
@@ -556,13 +578,18 @@ int ssd_impl(float *state, const float *x, const float *dt, const float *A, cons
     a.state = state; a.x = x; a.dt = dt; a.A = A; a.B = B; a.C = C; a.D = D; a.y = y;
     a.seq_starts = seq_starts; a.seq_lens = seq_lens; a.resume = resume;
     a.n_seqs = n_seqs; a.n_tokens = n_tokens; a.H = H; a.P = P; a.N = N; a.G = G;
-    a.dt_bias = o.dt_bias; a.dt_softplus = o.dt_softplus;
     a.snaps = nullptr;
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_v);
     if (check_env()) {
         rc = check_metadata(a, stream);
         if (rc != SSM_OK)
             return rc;
+    }
+    if (dt_buffer_bytes(o, n_tokens, H) > 0) {
+        float *step = reinterpret_cast<float *>(static_cast<char *>(workspace) + L.off_step);
+        if (ssm::launch_dt_prep(a, o.dt_bias, o.dt_softplus, step, stream) != cudaSuccess)
+            return SSM_ERR_CUDA;
+        a.dt = step;
     }
 
     char *ws = static_cast<char *>(workspace);
@@ -721,6 +748,18 @@ int ssm_conv1d(const float *x, const float *weight, const float *bias, float *co
                            n_tokens, channels, kernel_size, st) != cudaSuccess)
         return SSM_ERR_CUDA;
     return SSM_OK;
+}
+
+size_t ssm_scan_ex_workspace_bytes(int n_seqs, int n_tokens, int n_heads, int head_dim, int d_state,
+                                   int n_groups, const ssm_scan_tuning *tuning, const ssm_scan_options *options)
+{
+    ssm_scan_options o;
+    if (n_tokens < 0 || n_heads <= 0 || read_options(options, &o) != SSM_OK)
+        return 0;
+    const size_t dtb = dt_buffer_bytes(o, n_tokens, n_heads);
+    if (o.state_snapshots)                  // the decode kernel: no time segments
+        return dtb;
+    return dtb + ssm_scan_workspace_bytes(n_seqs, n_tokens, n_heads, head_dim, d_state, n_groups, tuning);
 }
 
 const char *ssm_status_string(int status)

@@ -64,7 +64,7 @@ decode_kernel(const ScanArgs a, const DecodeGeom geo)
 
         for (int t = 0; t < len; ++t) {
             const long long tok = (long long)tok_start + t;
-            const float dtv = dt_eff(a, __ldg(a.dt + tok * H + head), head);
+            const float dtv = __ldg(a.dt + tok * H + head);
             const float dA = expf(dtv * Ah);                               // A4
             const float4 *bt = reinterpret_cast<const float4 *>(a.B + (tok * a.G + grp) * N);
             const float4 *ct = reinterpret_cast<const float4 *>(a.C + (tok * a.G + grp) * N);

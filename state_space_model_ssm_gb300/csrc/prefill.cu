@@ -164,7 +164,7 @@ prefill_kernel(const ScanArgs a, const PrefillGeom geo)
             dtr[u] = 0.f;
             if (idx < cnt * nheads) {
                 const int t = idx / nheads, hh = idx - t * nheads;
-                dtr[u] = dt_eff(a, a.dt[((long long)tok_start + t0 + t) * H + h0 + hh], h0 + hh);
+                dtr[u] = a.dt[((long long)tok_start + t0 + t) * H + h0 + hh];
             }
         }
     };

@@ -254,9 +254,7 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan
             const int cnt = min(geo.chunk, len - t0);
 #pragma unroll
             for (int q = 0; q < kDtHeads; ++q)
-                d[q] = (q < nheads && lane < cnt)
-                           ? dt_eff(a, a.dt[((long long)tok_start + t0 + lane) * H + h0 + q], h0 + q)
-                           : 0.f;
+                d[q] = (q < nheads && lane < cnt) ? a.dt[((long long)tok_start + t0 + lane) * H + h0 + q] : 0.f;
         };
         auto coefficients = [&](int c0, int b, const float (&d)[kDtHeads]) {
             const int t0 = c0 * geo.chunk;
@@ -267,8 +265,7 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan
                 for (int q = 1; q < kDtHeads; ++q)
                     if (hh == q) dtv = d[q];
                 if (hh >= kDtHeads)
-                    dtv = lane < cnt ? dt_eff(a, a.dt[((long long)tok_start + t0 + lane) * H + h0 + hh], h0 + hh)
-                                     : 0.f;
+                    dtv = lane < cnt ? a.dt[((long long)tok_start + t0 + lane) * H + h0 + hh] : 0.f;
                 const float dec = chunk_coefficients(dtv, a.A[h0 + hh], cnt, lane, sm.Coef(b) + hh,
                                                      geo.heads_cap, sm.Mask(b) + hh);
                 if (!kFull && lane == 0)

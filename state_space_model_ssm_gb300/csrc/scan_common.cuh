@@ -30,22 +30,8 @@ struct ScanArgs {
     const int32_t *seq_lens;   // [n]
     const int32_t *resume;     // [n]
     int n_seqs, n_tokens, H, P, N, G;
-    const float *dt_bias;      // [H] added to dt before use, or null
-    int dt_softplus;           // nonzero: dt_eff = softplus(dt + dt_bias) (identity above 20)
     float *snaps;              // [T][H][P][N]: the state after each owned token, or null (decode kernel)
 };
-
-// The step size the recurrence uses for raw value `v` of head h: v as given,
-// or softplus(v + dt_bias[h]) with the identity above 20 ("The llama journey",
-// Day 14 kernel body; the decay-gate kernel of "ssm_gated_delta.cu").
-__device__ __forceinline__ float dt_eff(const ScanArgs &a, float v, int h)
-{
-    if (a.dt_bias)
-        v += __ldg(a.dt_bias + h);
-    if (a.dt_softplus && v <= 20.f)
-        v = log1pf(expf(v));
-    return v;
-}
 
 // Launch geometry of the chunk-staged prefill kernel.
 struct PrefillGeom {
@@ -210,6 +196,11 @@ size_t ssd_tc_smem_bytes(int n_pad, int P, int nbuf);
 cudaError_t launch_ssd_output_tc(const ScanArgs &a, const SsdPlan &plan, const SsdGeom &g, int max_units,
                                  cudaStream_t stream);
 int ssd_max_head_dim();
+
+// Mamba2's step for the owned tokens: out[t,h] = softplus(dt[t,h] + bias[h])
+// (identity above 20; bias may be null, softplus optional), written once
+// before the scan so that the scan kernels read a plain step (dt_prep.cu).
+cudaError_t launch_dt_prep(const ScanArgs &a, const float *bias, int softplus, float *out, cudaStream_t stream);
 
 // Causal depthwise conv1d + SiLU with a rolling conv-state slot (conv1d.cu).
 cudaError_t launch_conv1d(const float *x, const float *w, const float *bias, float *state, float *out,

@@ -169,7 +169,7 @@ __device__ __forceinline__ void chunk_decay(const ScanArgs &a, const ChunkRange 
 #pragma unroll
     for (int r = 0; r < R; ++r) {
         const int t = lane * R + r;
-        cd.d[r] = t < c.len ? dt_eff(a, a.dt[(size_t)(c.t0 + t) * a.H + h], h) : 0.f;
+        cd.d[r] = t < c.len ? a.dt[(size_t)(c.t0 + t) * a.H + h] : 0.f;
         run += cd.d[r] * Ah;
         cd.a[r] = run;
     }

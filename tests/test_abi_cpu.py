@@ -130,11 +130,12 @@ def test_ssd_workspace_bytes(lib):
     for chunk, units in ((64, 2 + 2), (128, 2 + 1), (0, 2 + 1)):
         nbytes = bd.ssd_workspace_bytes(**SSD_GOOD, chunk=chunk)
         state_bytes = units * 4 * 16 * 32 * 4
-        assert state_bytes < nbytes <= state_bytes + 5 * 256 + units * (8 + 4 * 4) + 3 * 4
+        step_bytes = -(-100 * 4 * 4 // 256) * 256          # room for the discretised step
+        assert state_bytes + step_bytes < nbytes <= state_bytes + step_bytes + 6 * 256 + units * (8 + 4 * 4) + 3 * 4
         assert nbytes % 256 == 0
     # 1 x 4096 tokens at 64 heads x 64 x 128: 33 units of 2 MiB
     big = bd.ssd_workspace_bytes(1, 4096, 64, 64, 128, 8, 128)
-    assert 33 * (2 << 20) < big < 33 * (2 << 20) + 16384
+    assert 33 * (2 << 20) + 4096 * 64 * 4 < big < 33 * (2 << 20) + 4096 * 64 * 4 + 16384
     for bad in (dict(chunk=32), dict(chunk=-1), dict(head_dim=24), dict(head_dim=144),
                 dict(d_state=30), dict(n_groups=3), dict(n_seqs=0)):
         args = dict(SSD_GOOD, chunk=64)
@@ -216,3 +217,22 @@ def test_conv1d_host_rejects(lib, over, expect):
 
 def test_conv1d_empty_batch_is_a_noop(lib):
     assert bd.conv1d_raw(0, 0, 0, 0, 0, 0, 0, 0, 0, 8, 16, 4) == bd.SSM_OK
+
+
+def test_ex_workspace_bytes_adds_the_discretised_step(lib):
+    sizes = dict(GOOD)
+    plain = bd.workspace_bytes(*sizes.values())
+    assert bd.ex_workspace_bytes(*sizes.values()) == plain
+    step = -(-GOOD["n_tokens"] * GOOD["n_heads"] * 4 // 256) * 256
+    assert bd.ex_workspace_bytes(*sizes.values(), options=bd.Options(dt_softplus=1)) == step + plain
+    assert bd.ex_workspace_bytes(*sizes.values(), options=bd.Options(dt_bias=PTR)) == step + plain
+    assert bd.ex_workspace_bytes(*sizes.values(), options=bd.Options(dt_softplus=1, state_snapshots=PTR)) == step
+
+
+def test_dt_options_need_a_workspace(lib):
+    o = bd.Options(dt_softplus=1)
+    assert _ex_call(lib, o) == bd.SSM_ERR_INVALID_ARG                     # none at all
+    ptrs = dict(state=PTR, x=PTR, dt=PTR, A=PTR, B=PTR, C=PTR, D=PTR, y=PTR,
+                seq_starts=PTR, seq_lens=PTR, resume=PTR)
+    assert bd.scan_raw(**ptrs, **GOOD, options=o, workspace=PTR, workspace_bytes=64) == bd.SSM_ERR_INVALID_ARG
+    assert bd.scan_raw(**ptrs, **GOOD, options=o, workspace=PTR + 16, workspace_bytes=1 << 20) == bd.SSM_ERR_INVALID_ARG
