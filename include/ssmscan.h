@@ -108,7 +108,18 @@ enum {
  *   segment_tokens   SSM_PATH_PREFILL with a workspace (ssm_scan_ws): length of
  *                    the time segments long sequences are cut into (a multiple
  *                    of the chunk); 0 = automatic, < 0 = never segment
+ *   segment_state    how the state pass of the time segments runs
+ *                    (SSM_SEGMENT_STATE_*); ignored without segments
  */
+enum {
+    SSM_SEGMENT_STATE_AUTO = 0,   /* the tensor cores where d_state <= 128 and head_dim <= 256,
+                                     else the sequential kernel */
+    SSM_SEGMENT_STATE_FP32 = 1,   /* the sequential kernel's state-only mode (fp32 FMAs) */
+    SSM_SEGMENT_STATE_TENSOR = 2  /* the segment's state as a matrix product over its tokens on
+                                     the tensor cores, operands split into two TF32 parts
+                                     (hi*hi + hi*lo + lo*hi, fp32 accumulation: fp32-level
+                                     accuracy); SSM_ERR_UNSUPPORTED where the shapes do not fit */
+};
 typedef struct {
     int path;
     int lanes_per_row;
@@ -117,6 +128,7 @@ typedef struct {
     int chunk_tokens;
     int ctas_per_sm;
     int segment_tokens;
+    int segment_state;
 } ssm_scan_tuning;
 
 /*
@@ -201,7 +213,10 @@ int ssm_scan_ex(float *state_slots, const float *x, const float *dt,
  * parallel: a state-only pass per segment, a combine of the segment states
  * (S_in[k+1] = d_k S_in[k] + L_k, d_k the segment's decay prod exp(dt*A)),
  * then the full pass from each segment's incoming state.  This is the same
- * recurrence applied to whole segments; only float association changes.
+ * recurrence applied to whole segments; only float association changes.  The
+ * state pass runs on the tensor cores where the shapes fit (see
+ * tuning->segment_state): L_k unrolled into a sum over the segment's tokens,
+ * sum_s dt_s exp(A sum_{r>s} dt_r) x_s B_s^T, with split TF32 operands.
  *   tuning          may be NULL
  *   workspace       device memory, 256-byte aligned, at least
  *                   ssm_scan_workspace_bytes(...) bytes for the same arguments

@@ -7,9 +7,11 @@ The C ABI is declared in ``include/ssmscan.h``; ``binding`` wraps it with
 ctypes.  ``workloads`` draws the seeded synthetic inputs.
 """
 from .binding import (PATH_AUTO, PATH_DECODE, PATH_PREFILL, PATH_PREFILL_DIRECT,  # noqa: F401
+                      SEGMENT_STATE_AUTO, SEGMENT_STATE_FP32, SEGMENT_STATE_TENSOR,
                       Options, SsmScanError, Tuning,
                       load, ssd_workspace_bytes, ssm_conv1d, ssm_scan, ssm_scan_ssd,
                       status_string)
 
 __all__ = ["Options", "ssm_conv1d", "ssm_scan", "ssm_scan_ssd", "ssd_workspace_bytes", "Tuning", "SsmScanError", "PATH_AUTO", "PATH_DECODE",
-           "PATH_PREFILL", "PATH_PREFILL_DIRECT", "load", "status_string"]
+           "PATH_PREFILL", "PATH_PREFILL_DIRECT", "SEGMENT_STATE_AUTO", "SEGMENT_STATE_FP32",
+           "SEGMENT_STATE_TENSOR", "load", "status_string"]

@@ -25,6 +25,7 @@ SSM_ERR_CUDA = -3
 SSM_ERR_TIMEOUT = -4
 
 PATH_AUTO, PATH_DECODE, PATH_PREFILL, PATH_PREFILL_DIRECT = 0, 1, 2, 3
+SEGMENT_STATE_AUTO, SEGMENT_STATE_FP32, SEGMENT_STATE_TENSOR = 0, 1, 2
 
 _lib = None
 _lock = threading.Lock()
@@ -41,7 +42,7 @@ class Tuning(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("lanes_per_row", ctypes.c_int),
                 ("rows_per_thread", ctypes.c_int), ("rows_per_cta", ctypes.c_int),
                 ("chunk_tokens", ctypes.c_int), ("ctas_per_sm", ctypes.c_int),
-                ("segment_tokens", ctypes.c_int)]
+                ("segment_tokens", ctypes.c_int), ("segment_state", ctypes.c_int)]
 
 
 class Options(ctypes.Structure):

@@ -80,6 +80,17 @@ bool check_env()
     return v == 1;
 }
 
+// Debug mode: SSM_ERR_TIMEOUT when a kernel's bounded wait gave up (the
+// device status word is nonzero); synchronises the stream.
+int read_status(const int *status, cudaStream_t stream)
+{
+    int st = 0;
+    if (cudaMemcpyAsync(&st, status, sizeof(int), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    return st != 0 ? SSM_ERR_TIMEOUT : SSM_OK;
+}
+
 // Debug mode: copy the sequence table to the host and check the ranges.
 int check_metadata(const ssm::ScanArgs &a, cudaStream_t stream)
 {
@@ -112,8 +123,9 @@ struct PrefillPlan {
     int seg_len = 0;              // 0: no time segments
     long long max_units = 0;      // upper bound of (sequence, segment) units
     size_t ws_bytes = 0;          // workspace the segment plan needs
+    bool tc_state = false;        // state pass on the tensor cores (segment_state_tc.cu)
     // workspace offsets (bytes)
-    size_t off_units = 0, off_n_units = 0, off_unit_base = 0, off_decay = 0, off_state = 0;
+    size_t off_units = 0, off_n_units = 0, off_unit_base = 0, off_status = 0, off_decay = 0, off_state = 0;
 };
 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
@@ -220,6 +232,15 @@ int plan_prefill(const ssm_scan_tuning &t, bool scaled, int n_seqs, int n_tokens
             }
         }
         if (seg > 0) {
+            // The state pass: tensor cores where the shapes fit, unless the
+            // caller asks for the sequential kernel's state-only mode.
+            if (t.segment_state == SSM_SEGMENT_STATE_FP32) {
+                pl.tc_state = false;
+            } else {
+                pl.tc_state = ssm::segment_state_tc_supported(N, P, (size_t)dev.smem_optin);
+                if (!pl.tc_state && t.segment_state == SSM_SEGMENT_STATE_TENSOR)
+                    return SSM_ERR_UNSUPPORTED;
+            }
             pl.seg_len = seg;
             pl.max_units = (long long)n_seqs + ((long long)n_tokens + seg - 1) / seg;
             const size_t slot = (size_t)H * P * N * sizeof(float);
@@ -227,6 +248,7 @@ int plan_prefill(const ssm_scan_tuning &t, bool scaled, int n_seqs, int n_tokens
             pl.off_units = off;      off = align256(off + (size_t)pl.max_units * sizeof(int2));
             pl.off_n_units = off;    off = align256(off + sizeof(int));
             pl.off_unit_base = off;  off = align256(off + ((size_t)n_seqs + 1) * sizeof(int));
+            pl.off_status = off;     off = align256(off + sizeof(int));
             pl.off_decay = off;      off = align256(off + (size_t)pl.max_units * H * sizeof(float));
             pl.off_state = off;      off = align256(off + (size_t)pl.max_units * slot);
             pl.ws_bytes = off;
@@ -309,7 +331,7 @@ int scan_impl(float *state, const float *x, const float *dt, const float *A, con
         t = *tun;
     if (t.path < SSM_PATH_AUTO || t.path > SSM_PATH_PREFILL_DIRECT || t.lanes_per_row < 0 ||
         t.rows_per_thread < 0 || t.rows_per_cta < 0 || t.chunk_tokens < 0 || t.chunk_tokens > 256 ||
-        t.ctas_per_sm < 0)
+        t.ctas_per_sm < 0 || t.segment_state < SSM_SEGMENT_STATE_AUTO || t.segment_state > SSM_SEGMENT_STATE_TENSOR)
         return SSM_ERR_INVALID_ARG;
     if (t.lanes_per_row && (!is_pow2(t.lanes_per_row) || t.lanes_per_row > 32))
         return SSM_ERR_INVALID_ARG;
@@ -423,14 +445,20 @@ int scan_kernels(const ssm::ScanArgs &a, const ssm_scan_tuning &t, const DeviceI
     plan.seg_len = pl.seg_len;
     plan.seg_decay = reinterpret_cast<float *>(ws + pl.off_decay);
     plan.seg_state = reinterpret_cast<float *>(ws + pl.off_state);
+    plan.status = reinterpret_cast<int *>(ws + pl.off_status);
     const int mu = (int)pl.max_units;
-    if (ssm::launch_segment_plan(a, plan, mu, stream) != cudaSuccess ||
-        ssm::launch_prefill_scaled(a, pl.g, pl.lanes, pl.vpl, pl.rpt, plan, ssm::kScanStateOnly, mu, pl.smem,
-                                   stream) != cudaSuccess ||
-        ssm::launch_segment_combine(a, plan, mu, stream) != cudaSuccess ||
+    if (ssm::launch_segment_plan(a, plan, mu, stream) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    const cudaError_t e = pl.tc_state
+        ? ssm::launch_segment_state_tc(a, plan, mu, stream)
+        : ssm::launch_prefill_scaled(a, pl.g, pl.lanes, pl.vpl, pl.rpt, plan, ssm::kScanStateOnly, mu, pl.smem,
+                                     stream);
+    if (e != cudaSuccess || ssm::launch_segment_combine(a, plan, mu, stream) != cudaSuccess ||
         ssm::launch_prefill_scaled(a, pl.g, pl.lanes, pl.vpl, pl.rpt, plan, ssm::kScanFull, mu, pl.smem,
                                    stream) != cudaSuccess)
         return SSM_ERR_CUDA;
+    if (pl.tc_state && check_env())         // debug: report a bounded wait that gave up
+        return read_status(plan.status, stream);
     return SSM_OK;
 }
 
@@ -606,23 +634,16 @@ int ssd_impl(float *state, const float *x, const float *dt, const float *A, cons
     plan.chunk_logdecay = reinterpret_cast<float *>(ws + L.off_decay);
     plan.chunk_state = reinterpret_cast<float *>(ws + L.off_state);
     plan.status = reinterpret_cast<int *>(ws + L.off_status);
+    seg.status = plan.status;               // zeroed by the plan kernel
     const int mu = (int)L.max_units;
-    if (cudaMemsetAsync(plan.status, 0, sizeof(int), stream) != cudaSuccess)
-        return SSM_ERR_CUDA;
     if (ssm::launch_segment_plan(a, seg, mu, stream) != cudaSuccess ||
         ssm::launch_ssd(a, plan, L.g, mu, stream) != cudaSuccess)
         return SSM_ERR_CUDA;
     if (o.gated_y && n_tokens > 0 &&
         ssm::launch_gated_norm(a, o.gate_z, o.norm_weight, o.norm_eps, o.gated_y, stream) != cudaSuccess)
         return SSM_ERR_CUDA;
-    if (check_env()) {                      // debug: report a bounded wait that gave up
-        int st = 0;
-        if (cudaMemcpyAsync(&st, plan.status, sizeof(int), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
-            cudaStreamSynchronize(stream) != cudaSuccess)
-            return SSM_ERR_CUDA;
-        if (st != 0)
-            return SSM_ERR_TIMEOUT;
-    }
+    if (check_env())                        // debug: report a bounded wait that gave up
+        return read_status(plan.status, stream);
     return SSM_OK;
 }
 

@@ -145,6 +145,8 @@ struct SegmentPlan {
     int seg_len;              // tokens per segment (a multiple of the chunk)
     float *seg_state;         // [max_units][H][P][N]: state pass output, then S_in of seg+1
     float *seg_decay;         // [max_units][H]: prod dA over the segment
+    int *status;              // device word (may be null): zeroed by the plan kernel, nonzero
+                              // when a bounded wait of the tensor-core state pass gave up
 };
 constexpr int kScanFull = 0;        // the scan with y
 constexpr int kScanStateOnly = 1;   // one segment's state from zero, no y
@@ -156,6 +158,12 @@ cudaError_t launch_segment_plan(const ScanArgs &a, const SegmentPlan &plan, int 
                                 cudaStream_t stream);
 cudaError_t launch_segment_combine(const ScanArgs &a, const SegmentPlan &plan, int max_units,
                                    cudaStream_t stream);
+// The state pass on the tensor cores (segment_state_tc.cu): the same L_k and
+// d_k as the kScanStateOnly mode, as a product over the segment's tokens with
+// fp32 accuracy from split TF32 operands.  Grid (max_units, H).
+bool segment_state_tc_supported(int N, int P, size_t smem_optin);
+cudaError_t launch_segment_state_tc(const ScanArgs &a, const SegmentPlan &plan, int max_units,
+                                    cudaStream_t stream);
 bool prefill_scaled_supported(int lanes, int vpl, int rpt);
 size_t prefill_scaled_smem_bytes(const PrefillGeom &g, int N, int lanes);
 constexpr int kScaledMaxChunk = 32;    // one warp lane per token in the coefficient pass

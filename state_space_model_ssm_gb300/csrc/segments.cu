@@ -29,7 +29,7 @@ namespace {
 // unit list.  Writes stay inside max_units even for inconsistent metadata.
 __global__ void __launch_bounds__(1024)
 segment_plan_kernel(const int32_t *seq_lens, int n_seqs, int seg_len, int max_units,
-                    int2 *units, int *unit_base, int *n_units)
+                    int2 *units, int *unit_base, int *n_units, int *status)
 {
     __shared__ int warp_tot[32];
     __shared__ int carry;
@@ -77,6 +77,8 @@ segment_plan_kernel(const int32_t *seq_lens, int n_seqs, int seg_len, int max_un
     if (tid == 0) {
         unit_base[n_seqs] = carry;
         *n_units = min(carry, max_units);
+        if (status)
+            *status = 0;
     }
     __syncthreads();
     for (int i = tid; i < n_seqs; i += blockDim.x) {
@@ -121,7 +123,7 @@ cudaError_t launch_segment_plan(const ScanArgs &a, const SegmentPlan &plan, int 
     segment_plan_kernel<<<1, 1024, 0, stream>>>(a.seq_lens, a.n_seqs, plan.seg_len, max_units,
                                                 const_cast<int2 *>(plan.units),
                                                 const_cast<int *>(plan.unit_base),
-                                                const_cast<int *>(plan.n_units));
+                                                const_cast<int *>(plan.n_units), plan.status);
     return cudaGetLastError();
 }
 

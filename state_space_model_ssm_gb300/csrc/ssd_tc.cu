@@ -27,93 +27,19 @@
 // before the tensor core reads it.  S_in and the staged x of the next head are
 // copied while the current head computes (two buffers where they fit).
 #include "ssd_common.cuh"
+#include "tc_common.cuh"
 
 namespace ssm {
 
 namespace {
 
 using namespace ssd;
+using namespace tc;
 
 constexpr int kTcQ = 128;
 constexpr int kTcThreads = 256;             // compute warps 0-7 (TMEM rows x column halves)
 constexpr int kTcProducers = 4;             // warps 8-11 issue the global -> shared copies
 constexpr int kTcBlock = kTcThreads + 32 * kTcProducers;
-constexpr long kTcSpinLimit = 1L << 24;     // mbarrier polls before giving up (~seconds)
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p)
-{
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-// Shared-memory matrix descriptor of a K-major tile without swizzle.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo)
-{
-    uint64_t d = (uint64_t)((addr & 0x3FFFF) >> 4);
-    d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
-    d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
-    d |= (uint64_t)1 << 46;                     // descriptor version of tcgen05
-    return d;
-}
-
-// Instruction descriptor, kind::tf32: D fp32, A and B TF32, both K-major, M x N.
-__device__ __forceinline__ uint32_t idesc_tf32(int m, int n)
-{
-    return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
-}
-
-// D (TMEM) += A (TMEM, row r in lane r, K along columns) * B (shared memory).
-__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bd, uint32_t idesc, uint32_t acc)
-{
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}\n"
-                 ::"r"(d_tmem), "r"(a_tmem), "l"(bd), "r"(idesc), "r"(acc) : "memory");
-}
-
-// D (TMEM) += A (shared memory) * B (shared memory).
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t acc)
-{
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}\n"
-                 ::"r"(d_tmem), "l"(ad), "l"(bd), "r"(idesc), "r"(acc) : "memory");
-}
-
-__device__ __forceinline__ void tc_commit(uint64_t *mbar)
-{
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n"
-                 ::"r"(smem_u32(mbar)) : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
-
-// 16 consecutive fp32 TMEM columns of this thread's lane, written.
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16])
-{
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n"
-                 ::"r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-                   "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-                   "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
-                   "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-                   "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-                   "r"(__float_as_uint(v[15]))
-                 : "memory");
-}
-
-// 16 consecutive fp32 TMEM columns of this thread's lane.
-__device__ __forceinline__ void tmem_ld16(float (&v)[16], uint32_t taddr)
-{
-    uint32_t r[16];
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-                 : "r"(taddr)
-                 : "memory");
-    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-        v[i] = __uint_as_float(r[i]);
-}
 
 // Barrier 1 over the 256 compute threads (the producer warp never joins it).
 __device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, 256;\n" ::: "memory"); }
@@ -126,38 +52,6 @@ __device__ __forceinline__ bool compute_sync_or(bool v)
                  "selp.u32 %0, 1, 0, q;\n\t}\n"
                  : "=r"(r) : "r"((uint32_t)v) : "memory");
     return r != 0;
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *mbar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(mbar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *mbar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(mbar)) : "memory");
-}
-
-// Arrive on `mbar` once this thread's earlier cp.async copies have landed.
-__device__ __forceinline__ void cp_async_arrive(uint64_t *mbar)
-{
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(mbar)) : "memory");
-}
-
-// Poll an mbarrier phase; false after kTcSpinLimit polls.
-__device__ __forceinline__ bool mbar_wait(uint64_t *mbar, uint32_t parity)
-{
-    for (long it = 0; it < kTcSpinLimit; ++it) {
-        uint32_t done;
-        asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-                     "selp.u32 %0, 1, 0, p;\n\t}\n"
-                     : "=r"(done) : "r"(smem_u32(mbar)), "r"(parity) : "memory");
-        if (done)
-            return true;
-        if (it > 16)
-            __nanosleep(64);
-    }
-    return false;
 }
 
 // Shared-memory layout (bytes) of the block.
@@ -315,9 +209,7 @@ ssd_output_tc_kernel(const ScanArgs a, const SsdPlan p, const SsdGeom sg)
     const size_t bc_off = ((size_t)c.t0 * a.G + g) * N;
 
     if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n"
-                     ::"r"(smem_u32(tslot)), "r"(sg.tmem_cols) : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+        tmem_alloc(tslot, sg.tmem_cols);
     }
     if (tid == 0) {
         mbar_init(bar_g, 1);
@@ -327,7 +219,7 @@ ssd_output_tc_kernel(const ScanArgs a, const SsdPlan p, const SsdGeom sg)
             mbar_init(full + i, 32 * kTcProducers);
             mbar_init(empty + i, kTcThreads);
         }
-        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+        mbar_init_fence();
     }
     __syncthreads();                                  // barriers and the TMEM address published
 
@@ -355,7 +247,7 @@ ssd_output_tc_kernel(const ScanArgs a, const SsdPlan p, const SsdGeom sg)
     // ---- compute warps ----
     const int quad = warp & 3, half = warp >> 2;
     const int t = 32 * quad + lane;                   // chunk row (TMEM lane) of this thread
-    tc_fence_after();
+    tc::fence_after();
     const uint32_t tmem = *tslot;
     const int ccols = tc_c_cols(sg.n_pad);
     const uint32_t tm_c = tmem, tm_g = tmem + ccols, tm_yi = tm_g + kTcQ, tm_yx = tm_yi + P;
@@ -388,16 +280,16 @@ ssd_output_tc_kernel(const ScanArgs a, const SsdPlan p, const SsdGeom sg)
     if (!compute_sync_or(!ok)) {
         kmajor_round(BMt, L.lc, kTcQ, Np4, warp, lane);
         fence_async_smem();
-        tc_fence_before();
+        tc::fence_before();
         compute_sync();
     }
     const int ksteps_n = sg.n_pad >> 3;
     if (ok && tid == 0) {                             // G = C B^T
-        tc_fence_after();
+        tc::fence_after();
         const uint32_t id = idesc_tf32(kTcQ, kTcQ);
         for (int kk = 0; kk < ksteps_n; ++kk)
-            tc_mma_ts(tm_g, tm_c + 8 * kk, smem_desc(smem_u32(BMt) + 2 * kk * L.lc, L.lc, 128), id, kk > 0);
-        tc_commit(bar_g);
+            tc::mma_ts(tm_g, tm_c + 8 * kk, smem_desc(smem_u32(BMt) + 2 * kk * L.lc, L.lc, 128), id, kk > 0);
+        tc::commit(bar_g);
     }
 
     for (int k = 0; k < nh && ok; ++k) {
@@ -429,10 +321,10 @@ ssd_output_tc_kernel(const ScanArgs a, const SsdPlan p, const SsdGeom sg)
         compute_sync();                               // S_in, x^T, a_t, dt of head k ready
 
         if (tid == 0) {                               // Yi = C S_in^T
-            tc_fence_after();
+            tc::fence_after();
             const uint32_t id = idesc_tf32(kTcQ, P);
             for (int kk = 0; kk < ksteps_n; ++kk)
-                tc_mma_ts(tm_yi, tm_c + 8 * kk, smem_desc(smem_u32(St) + 2 * kk * L.ls, L.ls, 128), id, kk > 0);
+                tc::mma_ts(tm_yi, tm_c + 8 * kk, smem_desc(smem_u32(St) + 2 * kk * L.ls, L.ls, 128), id, kk > 0);
         }
         if (k == 0) {
             wait_bar = bar_g;
@@ -441,7 +333,7 @@ ssd_output_tc_kernel(const ScanArgs a, const SsdPlan p, const SsdGeom sg)
         }
         if (compute_sync_or(!ok))
             break;
-        tc_fence_after();
+        tc::fence_after();
 
         // M = G dt_s exp(a_t - a_s) for s <= t, into the A tile (reusing B's
         // space), in pieces of 16 columns.  A piece wholly left of the warp's
@@ -486,25 +378,25 @@ ssd_output_tc_kernel(const ScanArgs a, const SsdPlan p, const SsdGeom sg)
                 }
             }
         }
-        tc_fence_before();
+        tc::fence_before();
         fence_async_smem();
         compute_sync();                               // M ready
 
         if (tid == 0) {                               // Yx = M x, over the chunk's tokens only
-            tc_fence_after();
+            tc::fence_after();
             const uint32_t id = idesc_tf32(kTcQ, P);
             const int ks = (c.len + 7) >> 3;
             for (int kk = 0; kk < ks; ++kk)
-                tc_mma(tm_yx, smem_desc(smem_u32(BMt) + 2 * kk * L.lc, L.lc, 128),
+                tc::mma(tm_yx, smem_desc(smem_u32(BMt) + 2 * kk * L.lc, L.lc, 128),
                        smem_desc(smem_u32(XTt) + 2 * kk * L.lx, L.lx, 128), id, kk > 0);
-            tc_commit(bar_mma);
+            tc::commit(bar_mma);
         }
         wait_bar = bar_mma;
         wait_par = (uint32_t)(k & 1);
         ok = mbar_wait(bar_mma, wait_par);
         if (compute_sync_or(!ok))
             break;
-        tc_fence_after();
+        tc::fence_after();
 
         // y = exp(a_t) Yi + Yx + D x for this thread's row and column half (every
         // lane takes part in the TMEM loads; rows past the chunk store nothing);
@@ -533,7 +425,7 @@ ssd_output_tc_kernel(const ScanArgs a, const SsdPlan p, const SsdGeom sg)
                 }
             }
         }
-        tc_fence_before();
+        tc::fence_before();
         mbar_arrive(empty + b);                       // buffer b may be refilled
         compute_sync();                               // TMEM accumulators, M and x^T free
     }
@@ -545,8 +437,7 @@ ssd_output_tc_kernel(const ScanArgs a, const SsdPlan p, const SsdGeom sg)
         compute_sync();
     }
     if (warp == 0)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(sg.tmem_cols)
-                     : "memory");
+        tmem_dealloc(tmem, sg.tmem_cols);
 }
 
 }  // namespace

@@ -82,6 +82,7 @@ def test_empty_batch_is_a_noop(lib):
 @pytest.mark.parametrize("field,value", [
     ("path", 4), ("path", -1), ("lanes_per_row", 3), ("lanes_per_row", 64),
     ("rows_per_thread", 3), ("chunk_tokens", 257), ("chunk_tokens", -1), ("ctas_per_sm", -2),
+    ("segment_state", 3), ("segment_state", -1),
 ])
 def test_host_rejects_bad_tuning(lib, field, value):
     t = bd.Tuning()

@@ -22,8 +22,8 @@ def built():
     bd.load()
 
 
-def _tuning(path=0, lanes=0, rpt=0, rows=0, chunk=0, ctas=0, seg=0):
-    return bd.Tuning(path, lanes, rpt, rows, chunk, ctas, seg)
+def _tuning(path=0, lanes=0, rpt=0, rows=0, chunk=0, ctas=0, seg=0, seg_state=0):
+    return bd.Tuning(path, lanes, rpt, rows, chunk, ctas, seg, seg_state)
 
 
 PATHS = [("auto", None), ("decode", _tuning(path=bd.PATH_DECODE)),
@@ -221,15 +221,19 @@ def test_bad_arguments_raise_before_launch():
 
 # Time segments (ssm_scan_ws): long sequences cut into segments that run in
 # parallel, then combined.  Short segments make many segments per sequence.
-SEGMENT_CASES = [("tiny", 16), ("tiny", 32), ("edge_p96_n100", 64), ("ragged_12", 256),
-                 ("edge_n1024", 512), ("prefill_1x4096", 0), ("ragged_12", 0)]
+# The segments' state pass runs on the tensor cores (automatic where d_state <=
+# 128 and head_dim <= 256) or in the sequential kernel (SEGMENT_STATE_FP32).
+SEGMENT_CASES = [("tiny", 16), ("tiny", 32), ("tiny", 48), ("edge_p96_n100", 64), ("edge_p96_n100", 112),
+                 ("ragged_12", 256), ("edge_n1024", 512), ("prefill_1x4096", 0), ("ragged_12", 0)]
+SEGMENT_STATE = [("auto", bd.SEGMENT_STATE_AUTO), ("fp32", bd.SEGMENT_STATE_FP32)]
 
 
+@pytest.mark.parametrize("state_pass", SEGMENT_STATE, ids=[k for k, _ in SEGMENT_STATE])
 @pytest.mark.parametrize("name,seg", SEGMENT_CASES, ids=[f"{n}-{s}" for n, s in SEGMENT_CASES])
-def test_parity_time_segments(name, seg):
+def test_parity_time_segments(name, seg, state_pass):
     inp = workload(name)
     y_ref, s_ref = oracle.scan_inputs(inp)
-    t = _tuning(path=bd.PATH_PREFILL, seg=seg)
+    t = _tuning(path=bd.PATH_PREFILL, seg=seg, seg_state=state_pass[1])
     if seg > 0:
         g = inp.geom
         assert bd.workspace_bytes(inp.n_seqs, inp.n_tokens, g.n_heads, g.head_dim, g.d_state,
@@ -238,15 +242,40 @@ def test_parity_time_segments(name, seg):
     assert_parity(inp, y, s, y_ref, s_ref)
 
 
+@pytest.mark.parametrize("state_pass", SEGMENT_STATE, ids=[k for k, _ in SEGMENT_STATE])
 @pytest.mark.parametrize("dt_scale,a_value", [(8.0, -16.0), (60.0, -16.0), (1.0, 0.0), (0.5, 0.05)],
                          ids=["anchor_every_few", "underflow", "no_decay", "growth"])
-def test_parity_time_segments_extreme_decay(dt_scale, a_value):
+def test_parity_time_segments_extreme_decay(dt_scale, a_value, state_pass):
     inp = make_inputs(Geometry(4, 16, 32, 2), [150, 77, 0, 33], [0, 1, 1, 0], seed=32)
     inp.dt.mul_(dt_scale)
     inp.A.fill_(a_value)
     y_ref, s_ref = oracle.scan_inputs(inp)
-    y, s = run_gpu(inp, tuning=_tuning(path=bd.PATH_PREFILL, seg=16), workspace=True)
+    y, s = run_gpu(inp, tuning=_tuning(path=bd.PATH_PREFILL, seg=16, seg_state=state_pass[1]), workspace=True)
     assert_parity(inp, y, s, y_ref, s_ref)
+
+
+# Head dims across the tensor-core state pass's register shapes (head_dim
+# padded to 32, 64, ..., 256) and d_state below the 128 rows of its product.
+TC_GEOMS = [(4, 32, 64, 2), (2, 160, 128, 1), (2, 256, 48, 2), (6, 224, 16, 3)]
+
+
+@pytest.mark.parametrize("geom", TC_GEOMS, ids=[f"h{g[0]}_p{g[1]}_n{g[2]}" for g in TC_GEOMS])
+def test_parity_tensor_state_pass_geometries(geom):
+    inp = make_inputs(Geometry(*geom), [300, 97, 1, 160], [1, 0, 1, 1], seed=61)
+    y_ref, s_ref = oracle.scan_inputs(inp)
+    t = _tuning(path=bd.PATH_PREFILL, seg=48, seg_state=bd.SEGMENT_STATE_TENSOR)
+    y, s = run_gpu(inp, tuning=t, workspace=True)
+    assert_parity(inp, y, s, y_ref, s_ref)
+
+
+def test_tensor_state_pass_refuses_large_d_state():
+    """d_state 1024 is beyond the 128 rows of the product: an explicit request fails
+    before any launch; the automatic choice takes the sequential kernel."""
+    inp = workload("edge_n1024")
+    t = _tuning(path=bd.PATH_PREFILL, seg=512, seg_state=bd.SEGMENT_STATE_TENSOR)
+    with pytest.raises(bd.SsmScanError) as e:
+        run_gpu(inp, tuning=t, workspace=True)
+    assert e.value.status == bd.SSM_ERR_UNSUPPORTED
 
 
 def test_time_segments_need_their_workspace():
