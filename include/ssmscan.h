@@ -112,8 +112,9 @@ enum {
  *                    (SSM_SEGMENT_STATE_*); ignored without segments
  */
 enum {
-    SSM_SEGMENT_STATE_AUTO = 0,   /* the tensor cores where d_state <= 128 and head_dim <= 256,
-                                     else the sequential kernel */
+    SSM_SEGMENT_STATE_AUTO = 0,   /* the tensor cores where d_state <= 128, head_dim <= 256 and
+                                     a multiple of 4, and x 16-byte aligned; else the sequential
+                                     kernel */
     SSM_SEGMENT_STATE_FP32 = 1,   /* the sequential kernel's state-only mode (fp32 FMAs) */
     SSM_SEGMENT_STATE_TENSOR = 2  /* the segment's state as a matrix product over its tokens on
                                      the tensor cores, operands split into two TF32 parts

@@ -424,6 +424,12 @@ int scan_kernels(const ssm::ScanArgs &a, const ssm_scan_tuning &t, const DeviceI
             return SSM_ERR_INVALID_ARG;     // explicit segments need the workspace
         pl.seg_len = 0;                     // automatic: run without segments
     }
+    ssm::SegStateMaps maps;                 // TMA descriptors of the tensor-core state pass
+    if (pl.seg_len > 0 && pl.tc_state && !(aligned(a.x, 16) && ssm::segment_state_tc_maps(a, &maps))) {
+        if (t.segment_state == SSM_SEGMENT_STATE_TENSOR)
+            return SSM_ERR_UNSUPPORTED;
+        pl.tc_state = false;
+    }
     if (pl.max_units * G * pl.g.runs_per_group > INT_MAX || (long long)n_seqs * G * pl.g.runs_per_group > INT_MAX)
         return SSM_ERR_UNSUPPORTED;
     if (!scaled) {
@@ -450,7 +456,7 @@ int scan_kernels(const ssm::ScanArgs &a, const ssm_scan_tuning &t, const DeviceI
     if (ssm::launch_segment_plan(a, plan, mu, stream) != cudaSuccess)
         return SSM_ERR_CUDA;
     const cudaError_t e = pl.tc_state
-        ? ssm::launch_segment_state_tc(a, plan, mu, stream)
+        ? ssm::launch_segment_state_tc(a, plan, maps, mu, stream)
         : ssm::launch_prefill_scaled(a, pl.g, pl.lanes, pl.vpl, pl.rpt, plan, ssm::kScanStateOnly, mu, pl.smem,
                                      stream);
     if (e != cudaSuccess || ssm::launch_segment_combine(a, plan, mu, stream) != cudaSuccess ||

@@ -161,9 +161,16 @@ cudaError_t launch_segment_combine(const ScanArgs &a, const SegmentPlan &plan, i
 // The state pass on the tensor cores (segment_state_tc.cu): the same L_k and
 // d_k as the kScanStateOnly mode, as a product over the segment's tokens with
 // fp32 accuracy from split TF32 operands.  Grid (max_units, H).
+// Its TMA descriptors of B and x (two CUtensorMap images) are encoded on the
+// host before any launch; false when the driver cannot describe the tensors.
+struct SegStateMaps {
+    alignas(64) unsigned char b[128];
+    alignas(64) unsigned char x[128];
+};
 bool segment_state_tc_supported(int N, int P, size_t smem_optin);
-cudaError_t launch_segment_state_tc(const ScanArgs &a, const SegmentPlan &plan, int max_units,
-                                    cudaStream_t stream);
+bool segment_state_tc_maps(const ScanArgs &a, SegStateMaps *maps);
+cudaError_t launch_segment_state_tc(const ScanArgs &a, const SegmentPlan &plan, const SegStateMaps &maps,
+                                    int max_units, cudaStream_t stream);
 bool prefill_scaled_supported(int lanes, int vpl, int rpt);
 size_t prefill_scaled_smem_bytes(const PrefillGeom &g, int N, int lanes);
 constexpr int kScaledMaxChunk = 32;    // one warp lane per token in the coefficient pass

@@ -10,10 +10,12 @@
 //   d       = exp(A sum_s dt_s),
 //
 // plus d S_slot[p][n] for the first segment of a resuming sequence.  L^T =
-// B^T X_w is a matrix product over the segment's tokens (M = 128 state rows n,
-// d_state padded with zero rows; N = head_dim padded to a multiple of 32;
-// K = tokens), here on tcgen05.mma.  The sequential kernel's state-only mode
-// computes the same values with one multiply-add chain per state element.
+// B^T X_w is a matrix product over the segment's tokens: M = 128 state rows n
+// (d_state padded with zero rows), N = the head dims of HB heads of one group
+// side by side (head_dim padded to a multiple of 32), K = tokens.  B is the
+// group's, so the heads of a block share its operand tile.  The sequential
+// kernel's state-only mode computes the same values with one multiply-add
+// chain per state element.
 //
 // fp32 accuracy from TF32 operands: each operand value v is split into hi =
 // tf32(v) (nearest) and lo = v - hi (exact in fp32), and the products are
@@ -21,18 +23,29 @@
 // dropped lo_a lo_b and the TF32 rounding of lo are each below 2^-21 of the
 // product.
 //
-// A block (8 warps) owns one (segment, head).  It walks the segment's 32-token
-// chunks from the last to the first, so that a token's decay exponent, the sum
-// of dt A over the tokens after it, is a running suffix sum: each warp forms a
-// chunk's weights in registers (lane = token) and carries the chunk's total.
-// Each thread loads its cells of the next chunk's B and x into registers while
-// it writes the current chunk into one of two operand buffers.  The token index
-// is K, so the values of 4 consecutive tokens of one row form a 16-byte cell of
-// the K-major tile, written whole (consecutive rows across a warp: no bank
-// conflicts).  Thread 0 issues the chunk's 12 MMAs (K = 8 each) and commits
-// them to the buffer's mbarrier, which the writers wait on two chunks later.
-// The epilogue reads the accumulator (warp w: state rows 32 (w % 4) .. +31,
-// column half w / 4) and stores L with the state-slot layout, coalesced over n.
+// A block owns one (segment, HB heads) and walks the segment's 16-token chunks
+// from the last to the first, so that a token's decay exponent, the sum of
+// dt A over the tokens after it, is a running suffix sum.  A ninth warp
+// drives the pipeline: it brings the raw rows of B ([16][128] floats, d_state
+// padded by the TMA's zero fill) and x ([16][HB][head_dim padded]) into a
+// ring of three stages with TMA, two chunks ahead, and forms each chunk's
+// weights (lane = head * 16 + token, carrying each head's total) into shared
+// memory one barrier before the chunk is staged.  The 8 staging warps turn
+// their cells of the staged chunk into the operand tiles: the token index is
+// K, so the values of 4 consecutive tokens of one row form a 16-byte cell of a
+// K-major tile, read as four conflict-free 4-byte words from the staged rows
+// and written whole (consecutive rows across a warp).  Two operand buffers
+// alternate.  After the block's barrier the ninth warp issues the chunk's 6
+// MMAs (K = 8 each), commits them to the buffer's mbarrier (which the writers
+// wait on two chunks later) and starts the TMA of the chunk two ahead, while
+// the staging warps go on to the next chunk.  The epilogue reads the
+// accumulator (warp w: state rows 32 (w % 4) .. +31, column half w / 4) and
+// stores L with the state-slot layout, coalesced over n.
+#include <cstring>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "ssd_common.cuh"
 #include "tc_common.cuh"
 
@@ -42,51 +55,52 @@ namespace {
 
 using namespace tc;
 
-constexpr int kSsQ = 32;                   // tokens per chunk (K of a chunk's products)
+constexpr int kSsQ = 16;                   // tokens per chunk (K of a chunk's products)
 constexpr int kSsRows = 128;               // M: state rows n (d_state padded)
-constexpr int kSsThreads = 256;
+constexpr int kSsThreads = 256;           // warps 0-7 stage the operands; warp 8 issues TMA and MMAs
+constexpr int kSsBlock = kSsThreads + 32;
 constexpr int kSsQuads = kSsQ / 4;         // 16-byte K cells per row and chunk
-constexpr int kSsBCells = kSsRows * kSsQuads / kSsThreads;   // B cells per thread: 4
+constexpr int kSsStages = 3;               // staged raw chunks: two in flight while one is used
+constexpr int kSsBCells = kSsRows * kSsQuads / kSsThreads;   // B operand cells per thread: 2
 
-// Shared memory (bytes): two buffers of the four operand tiles, two mbarriers
-// and the TMEM address.
+// Shared memory (bytes), all offsets multiples of 1024: two buffers of the
+// four operand tiles (buffer b at b * buf; A hi at 0), the staged raw chunks
+// (stage s at raw + s * stage; B rows at 0, x rows at rx), mbarriers (full[3]
+// per stage, mma[2] per buffer), the TMEM address, the token weights of two
+// chunks and the heads' decays.
 struct SsLayout {
-    uint32_t a_hi[2], a_lo[2], x_hi[2], x_lo[2], bar, tslot, total;
-    uint32_t la, lx;          // K-cell strides of the B^T tiles (128 rows) and x_w tiles (p_pad rows)
+    uint32_t a_lo, x_hi, x_lo, buf;
+    uint32_t raw, rx, stage;
+    uint32_t bar, tslot, total;
+    uint32_t wts, dec;        // weights of two chunks [2][32] (lane = head * 16 + token), decays [HB]
+    uint32_t la, lx;          // K-cell strides of the B^T tiles (128 rows) and X tiles (nx rows)
 };
 
-__host__ __device__ inline SsLayout ss_layout(int p_pad)
+__host__ __device__ constexpr SsLayout ss_layout(int nx)
 {
-    SsLayout L;
+    SsLayout L{};
     L.la = kSsRows * 16;
-    L.lx = (uint32_t)p_pad * 16;
+    L.lx = (uint32_t)nx * 16;
     const uint32_t ta = L.la * kSsQuads, tx = L.lx * kSsQuads;
-    uint32_t off = 0;
-    for (int b = 0; b < 2; ++b) {
-        L.a_hi[b] = off; off += ta;
-        L.a_lo[b] = off; off += ta;
-        L.x_hi[b] = off; off += tx;
-        L.x_lo[b] = off; off += tx;
-    }
-    L.bar = off;   off += 2 * sizeof(uint64_t);
-    L.tslot = off; off += 16;
-    L.total = off;
+    L.a_lo = ta;
+    L.x_hi = 2 * ta;
+    L.x_lo = 2 * ta + tx;
+    L.buf = 2 * ta + 2 * tx;
+    L.raw = 2 * L.buf;
+    L.rx = kSsQ * kSsRows * 4;
+    L.stage = L.rx + (uint32_t)(kSsQ * nx * 4);
+    L.bar = L.raw + kSsStages * L.stage;
+    L.tslot = L.bar + 8 * sizeof(uint64_t);
+    L.wts = L.tslot + 16;
+    L.dec = L.wts + 2 * 32 * 4;
+    L.total = L.dec + 16;
     return L;
 }
 
-__host__ __device__ inline uint32_t ss_tmem_cols(int p_pad)
+__host__ __device__ constexpr uint32_t ss_tmem_cols(int nx)
 {
-    return p_pad <= 32 ? 32u : p_pad <= 64 ? 64u : p_pad <= 128 ? 128u : 256u;
+    return nx <= 32 ? 32u : nx <= 64 ? 64u : nx <= 128 ? 128u : 256u;
 }
-
-// One chunk's operand values in registers: B cells (row n, 4 tokens) and x
-// cells (row p, 4 tokens) of this thread, and dt of token `lane`.
-template <int XI>
-struct ChunkRegs {
-    float b[kSsBCells][4];
-    float x[XI][4];
-    float dt;
-};
 
 __device__ __forceinline__ float4 split_hi(float4 v, float4 &lo)
 {
@@ -95,13 +109,79 @@ __device__ __forceinline__ float4 split_hi(float4 v, float4 &lo)
     return hi;
 }
 
-// Two blocks per SM where their shared memory fits (head_dim up to 96).
-template <int XI>
-__global__ void __launch_bounds__(kSsThreads, XI <= 3 ? 2 : 1)
-segment_state_tc_kernel(const ScanArgs a, const SegmentPlan plan)
+}  // namespace
+
+namespace {
+
+// X operand cells per staging thread, and whether the last round of them is partial.
+template <int NX>
+struct XCells {
+    static constexpr int count = (NX * kSsQuads + kSsThreads - 1) / kSsThreads;
+    static constexpr bool guard = (NX * kSsQuads) % kSsThreads != 0;
+};
+
+// One staged chunk (stage `raw`) into operand buffer `buf`: this thread's B^T
+// cells (row n, token quads qb + 2i) and X cells (row xr[i] = head * p_pad + p,
+// token quad xq[i]; xq < 0: none), X scaled by the chunk's weights `w`
+// ([head * 16 + token]).  PARTIAL: tokens >= cnt read as zero (only the last
+// chunk of a segment can be short).  No branch inside, so the loads, splits and
+// stores of all cells interleave.
+template <int XI, int HB, bool PARTIAL>
+__device__ __forceinline__ void stage_chunk(const char *raw, char *buf, const float *w, int n, int qb,
+                                            const int (&xr)[XCells<32 * XI * HB>::count],
+                                            const int (&xq)[XCells<32 * XI * HB>::count], int cnt)
 {
+    constexpr int p_pad = 32 * XI, nx = HB * p_pad;
+    constexpr SsLayout L = ss_layout(nx);
+    auto mask = [cnt](float4 v, int q) {
+        if (PARTIAL) {
+            v.x = 4 * q < cnt ? v.x : 0.f;
+            v.y = 4 * q + 1 < cnt ? v.y : 0.f;
+            v.z = 4 * q + 2 < cnt ? v.z : 0.f;
+            v.w = 4 * q + 3 < cnt ? v.w : 0.f;
+        }
+        return v;
+    };
+    const float *rb = reinterpret_cast<const float *>(raw) + n;
+#pragma unroll
+    for (int i = 0; i < kSsBCells; ++i) {
+        const int q = qb + 2 * i;
+        const float4 v = mask(make_float4(rb[(4 * q) * kSsRows], rb[(4 * q + 1) * kSsRows],
+                                          rb[(4 * q + 2) * kSsRows], rb[(4 * q + 3) * kSsRows]), q);
+        float4 lo;
+        const float4 hi = split_hi(v, lo);
+        const uint32_t off = q * L.la + n * 16;
+        *reinterpret_cast<float4 *>(buf + off) = hi;
+        *reinterpret_cast<float4 *>(buf + L.a_lo + off) = lo;
+    }
+#pragma unroll
+    for (int i = 0; i < XCells<nx>::count; ++i) {
+        const int q = xq[i], r = xr[i];
+        if (!XCells<nx>::guard || q >= 0) {
+            const float4 w4 = *reinterpret_cast<const float4 *>(w + (r / p_pad) * 16 + 4 * q);
+            const float *rx = reinterpret_cast<const float *>(raw + L.rx) + r;
+            const float4 v = mask(make_float4(rx[(4 * q) * nx] * w4.x, rx[(4 * q + 1) * nx] * w4.y,
+                                              rx[(4 * q + 2) * nx] * w4.z, rx[(4 * q + 3) * nx] * w4.w), q);
+            float4 lo;
+            const float4 hi = split_hi(v, lo);
+            const uint32_t off = q * L.lx + r * 16;
+            *reinterpret_cast<float4 *>(buf + L.x_hi + off) = hi;
+            *reinterpret_cast<float4 *>(buf + L.x_lo + off) = lo;
+        }
+    }
+}
+
+// XI: head_dim padded to 32 XI; HB: heads per block (1 or 2).
+template <int XI, int HB>
+__global__ void __launch_bounds__(kSsBlock, HB * XI <= 4 ? 2 : 1)
+segment_state_tc_kernel(const ScanArgs a, const SegmentPlan plan, const __grid_constant__ CUtensorMap tm_b,
+                        const __grid_constant__ CUtensorMap tm_x)
+{
+    constexpr int p_pad = 32 * XI, nx = HB * p_pad;
+    constexpr SsLayout L = ss_layout(nx);
+    constexpr uint32_t kBoxBytes = (uint32_t)(kSsQ * (kSsRows + nx) * 4);   // both TMA boxes of a chunk
     extern __shared__ __align__(1024) unsigned char ss_smem[];
-    const int unit = blockIdx.x, h = blockIdx.y;
+    const int unit = blockIdx.x, h0 = blockIdx.y * HB;
     if (unit >= *plan.n_units)
         return;
     const int2 us = plan.units[unit];
@@ -112,164 +192,180 @@ segment_state_tc_kernel(const ScanArgs a, const SegmentPlan plan)
         return;                                       // the last segment needs no state pass
     const int len = min(plan.seg_len, seq_len - seg * plan.seg_len);
     const int nc = (len + kSsQ - 1) / kSsQ;
-    const long long tok0 = (long long)a.seq_starts[seq] + (long long)seg * plan.seg_len;
+    const int tok0 = a.seq_starts[seq] + seg * plan.seg_len;
     const int P = a.P, N = a.N, H = a.H;
-    constexpr int p_pad = 32 * XI;
-    const int grp = h / (H / a.G);
-    const SsLayout L = ss_layout(p_pad);
+    const int grp = h0 / (H / a.G);
     char *sm = reinterpret_cast<char *>(ss_smem);
     const uint32_t sbase = smem_u32(sm);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L.bar);
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + L.bar);     // per stage: TMA boxes landed
+    uint64_t *mmab = full + kSsStages;                             // per buffer: products done
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + L.tslot);
+    float *wts = reinterpret_cast<float *>(sm + L.wts);
+    float *decs = reinterpret_cast<float *>(sm + L.dec);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const uint32_t cols = ss_tmem_cols(p_pad);
-    constexpr float kLog2e = 1.4426950408889634f;
-    const float A2 = a.A[h] * kLog2e;
+    constexpr uint32_t cols = ss_tmem_cols(nx);
 
     if (warp == 0)
         tmem_alloc(tslot, cols);
     if (tid == 0) {
-        mbar_init(bars, 1);
-        mbar_init(bars + 1, 1);
+        for (int i = 0; i < kSsStages; ++i)
+            mbar_init(full + i, 1);
+        mbar_init(mmab, 1);
+        mbar_init(mmab + 1, 1);
         mbar_init_fence();
     }
     __syncthreads();
     fence_after();
     const uint32_t tmem = *tslot;
 
-    // cells of this thread: B (row n, token quad qb + 2i), x (row px[i], quad qx[i])
-    const int n = tid & (kSsRows - 1), qb = tid >> 7;
-    int px[XI], qx[XI];
+    if (warp == kSsThreads / 32) {
+        // ---- issuer warp: TMA two chunks ahead; the weights of each chunk one
+        // barrier before it is staged; a chunk's products once the block's
+        // barrier says that its operand buffer is written ----
+        // chunk j of the walk (tokens [c * 16, c * 16 + 16) of the segment, c = nc - 1 - j) into stage j % 3
+        auto issue = [&](int j) {
+            const int st = j % kSsStages, t = tok0 + (nc - 1 - j) * kSsQ;
+            char *raw = sm + L.raw + st * L.stage;
+            mbar_expect_tx(full + st, kBoxBytes);
+            tma_load_3d(raw, &tm_b, 0, grp, t, full + st);
+            tma_load_3d(raw + L.rx, &tm_x, 0, h0, t, full + st);
+        };
+        // weights: lane = head * 16 + token of the chunk
+        constexpr float kLog2e = 1.4426950408889634f;
+        const int wh = lane >> 4, ws = lane & 15;
+        const float A2 = wh < HB ? a.A[h0 + wh] * kLog2e : 0.f;
+        auto load_dt = [&](int j) {
+            const int s = (nc - 1 - j) * kSsQ + ws;
+            return (j < nc && wh < HB && s < len) ? __ldg(a.dt + (size_t)(tok0 + s) * H + h0 + wh) : 0.f;
+        };
+        float carry = 0.f;                            // this lane's head: sum of dt A log2(e) walked so far
+        // w_s = dt_s 2^(A2 * sum of dt over the tokens after s) of chunk j into slot j % 2
+        auto weights = [&](int j, float dts) {
+            float suf = dts * A2;                     // inclusive suffix sum within the 16 lanes
 #pragma unroll
-    for (int i = 0; i < XI; ++i) {
-        const int it = tid + kSsThreads * i;
-        qx[i] = it / p_pad;                           // uniform across a warp (p_pad % 32 == 0)
-        px[i] = it - qx[i] * p_pad;
+            for (int o = 1; o < kSsQ; o <<= 1) {
+                const float t = __shfl_down_sync(kFullMask, suf, o);
+                if (ws + o < kSsQ)
+                    suf += t;
+            }
+            float after = __shfl_down_sync(kFullMask, suf, 1);
+            if (ws == kSsQ - 1)
+                after = 0.f;
+            wts[(j & 1) * 32 + lane] = dts * ssd::ex2(carry + after);
+            carry += __shfl_sync(kFullMask, suf, lane & 16);
+        };
+        if (lane == 0) {
+            issue(0);
+            if (nc > 1)
+                issue(1);
+        }
+        const float dt0 = load_dt(0), dt1 = load_dt(1);
+        float dt_ahead = load_dt(2);                  // dt of chunk j + 2 at iteration j
+        weights(0, dt0);
+        __syncthreads();                              // chunk 0's weights published
+        if (nc > 1)
+            weights(1, dt1);
+        for (int j = 0; j < nc; ++j) {
+            const float dt_next = load_dt(j + 3);
+            if (__syncthreads_or(0))
+                break;                                // the staging warps gave up
+            if (lane == 0) {
+                fence_after();
+                constexpr uint32_t id = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(nx >> 3) << 17) |
+                                        ((uint32_t)(kSsRows >> 4) << 24);        // idesc_tf32(128, nx)
+                const uint32_t ba = sbase + (j & 1) * L.buf;
+#pragma unroll
+                for (int kk = 0; kk < kSsQ / 8; ++kk) {
+                    const uint64_t dah = smem_desc(ba + 2 * kk * L.la, L.la, 128);
+                    const uint64_t dal = smem_desc(ba + L.a_lo + 2 * kk * L.la, L.la, 128);
+                    const uint64_t dxh = smem_desc(ba + L.x_hi + 2 * kk * L.lx, L.lx, 128);
+                    const uint64_t dxl = smem_desc(ba + L.x_lo + 2 * kk * L.lx, L.lx, 128);
+                    mma(tmem, dal, dxh, id, (j > 0 || kk > 0) ? 1u : 0u);
+                    mma(tmem, dah, dxl, id, 1u);
+                    mma(tmem, dah, dxh, id, 1u);
+                }
+                commit(mmab + (j & 1));
+                if (j + 2 < nc)
+                    issue(j + 2);                     // its stage held chunk j - 1, consumed before the barrier
+            }
+            if (j + 2 < nc)                           // slot j % 2 was read while chunk j was staged
+                weights(j + 2, dt_ahead);
+            dt_ahead = dt_next;
+        }
+        const float dl = ssd::ex2(__shfl_sync(kFullMask, carry, 16 * (lane & 1)));   // lane hb: head hb's decay
+        if (lane < HB)
+            decs[lane] = dl;
+        __syncthreads_or(0);                          // the staging warps' epilogue decision
+        __syncthreads();
+        return;
     }
-    const size_t GN = (size_t)a.G * N, HP = (size_t)H * P;
-    const float *Bg = a.B + ((size_t)tok0 * a.G + grp) * N;
-    const float *xg = a.x + ((size_t)tok0 * H + h) * P;
-    const float *dtg = a.dt + (size_t)tok0 * H + h;
 
-    auto load = [&](int c, ChunkRegs<XI> &r) {
-        const int s0 = c * kSsQ, cnt = min(kSsQ, len - s0);
+    // ---- staging warps ----
+    const int n = tid & (kSsRows - 1), qb = tid >> 7;
+    int xr[XCells<nx>::count], xq[XCells<nx>::count];
 #pragma unroll
-        for (int i = 0; i < kSsBCells; ++i)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int s = 4 * (qb + 2 * i) + k;
-                r.b[i][k] = (n < N && s < cnt) ? __ldg(Bg + (size_t)(s0 + s) * GN + n) : 0.f;
-            }
-#pragma unroll
-        for (int i = 0; i < XI; ++i)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int s = 4 * qx[i] + k;
-                r.x[i][k] = (px[i] < P && s < cnt) ? __ldg(xg + (size_t)(s0 + s) * HP + px[i]) : 0.f;
-            }
-        r.dt = lane < cnt ? __ldg(dtg + (size_t)(s0 + lane) * H) : 0.f;
-    };
+    for (int i = 0; i < XCells<nx>::count; ++i) {
+        const int it = tid + kSsThreads * i;
+        xq[i] = it < nx * kSsQuads ? it / nx : -1;    // uniform across a warp (nx % 32 == 0)
+        xr[i] = it - (it / nx) * nx;
+    }
+    __syncthreads();                                  // chunk 0's weights published
 
-    ChunkRegs<XI> cur, nxt;
-    load(nc - 1, cur);
-    float carry = 0.f;                                // sum of dt A log2(e) over the tokens already walked
     bool ok = true;
     int last = -1;                                    // last chunk whose products were issued
+    int st = 0;                                       // stage of chunk j
     for (int j = 0; j < nc; ++j) {
-        const int c = nc - 1 - j, b = j & 1;
-        if (c > 0)
-            load(c - 1, nxt);
-
-        // w_s = dt_s 2^(A2 * sum of dt over the tokens after s), lane = token
-        const float v = cur.dt * A2;
-        float suf = v;                                // inclusive suffix sum within the chunk
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float t = __shfl_down_sync(kFullMask, suf, o);
-            if (lane + o < 32)
-                suf += t;
-        }
-        float after = __shfl_down_sync(kFullMask, suf, 1);
-        if (lane == 31)
-            after = 0.f;
-        const float w = cur.dt * ssd::ex2(carry + after);
-        carry += __shfl_sync(kFullMask, suf, 0);
-
+        const int b = j & 1;
+        const int cnt = min(kSsQ, len - (nc - 1 - j) * kSsQ);   // tokens of the chunk (16 but the first)
+        ok = mbar_wait(full + st, (uint32_t)((j / kSsStages) & 1)) && ok;
         if (j >= 2)                                   // buffer b: products of chunk j - 2 done
-            ok = mbar_wait(bars + b, (uint32_t)(((j >> 1) - 1) & 1)) && ok;
-
-        char *ah = sm + L.a_hi[b], *al = sm + L.a_lo[b], *xh = sm + L.x_hi[b], *xl = sm + L.x_lo[b];
-#pragma unroll
-        for (int i = 0; i < kSsBCells; ++i) {
-            float4 lo;
-            const float4 hi = split_hi(make_float4(cur.b[i][0], cur.b[i][1], cur.b[i][2], cur.b[i][3]), lo);
-            const uint32_t off = (qb + 2 * i) * L.la + n * 16;
-            *reinterpret_cast<float4 *>(ah + off) = hi;
-            *reinterpret_cast<float4 *>(al + off) = lo;
-        }
-#pragma unroll
-        for (int i = 0; i < XI; ++i) {
-            const int q = qx[i];
-            float4 xw;
-            xw.x = cur.x[i][0] * __shfl_sync(kFullMask, w, 4 * q);
-            xw.y = cur.x[i][1] * __shfl_sync(kFullMask, w, 4 * q + 1);
-            xw.z = cur.x[i][2] * __shfl_sync(kFullMask, w, 4 * q + 2);
-            xw.w = cur.x[i][3] * __shfl_sync(kFullMask, w, 4 * q + 3);
-            float4 lo;
-            const float4 hi = split_hi(xw, lo);
-            const uint32_t off = q * L.lx + px[i] * 16;
-            *reinterpret_cast<float4 *>(xh + off) = hi;
-            *reinterpret_cast<float4 *>(xl + off) = lo;
-        }
+            ok = mbar_wait(mmab + b, (uint32_t)(((j >> 1) - 1) & 1)) && ok;
+        const char *raw = sm + L.raw + st * L.stage;
+        char *buf = sm + b * L.buf;
+        const float *w = wts + b * 32;
+        if (cnt < kSsQ)
+            stage_chunk<XI, HB, true>(raw, buf, w, n, qb, xr, xq, cnt);
+        else
+            stage_chunk<XI, HB, false>(raw, buf, w, n, qb, xr, xq, cnt);
         fence_async_smem();
         if (__syncthreads_or(!ok))
             break;                                    // a wait gave up: issue nothing more
-        if (tid == 0) {
-            fence_after();
-            const uint32_t id = idesc_tf32(kSsRows, p_pad);
-#pragma unroll
-            for (int kk = 0; kk < kSsQ / 8; ++kk) {
-                const uint64_t dah = smem_desc(sbase + L.a_hi[b] + 2 * kk * L.la, L.la, 128);
-                const uint64_t dal = smem_desc(sbase + L.a_lo[b] + 2 * kk * L.la, L.la, 128);
-                const uint64_t dxh = smem_desc(sbase + L.x_hi[b] + 2 * kk * L.lx, L.lx, 128);
-                const uint64_t dxl = smem_desc(sbase + L.x_lo[b] + 2 * kk * L.lx, L.lx, 128);
-                mma(tmem, dal, dxh, id, (j > 0 || kk > 0) ? 1u : 0u);
-                mma(tmem, dah, dxl, id, 1u);
-                mma(tmem, dah, dxh, id, 1u);
-            }
-            commit(bars + b);
-        }
         last = j;
-        cur = nxt;
+        st = st == kSsStages - 1 ? 0 : st + 1;
     }
 
     if (ok && last == nc - 1)                         // every product of the segment issued
-        ok = mbar_wait(bars + (last & 1), (uint32_t)((last >> 1) & 1));
+        ok = mbar_wait(mmab + (last & 1), (uint32_t)((last >> 1) & 1));
     if (__syncthreads_or(!ok)) {
         if (tid == 0) {
             if (plan.status)
                 atomicExch(plan.status, 1);
-            if (last >= 0)                            // one more bounded wait for the products in flight
-                mbar_wait(bars + (last & 1), (uint32_t)((last >> 1) & 1));
+            if (last >= 0)                            // bounded waits for the products and copies in flight
+                mbar_wait(mmab + (last & 1), (uint32_t)((last >> 1) & 1));
+            for (int j = last + 1; j < min(nc, last + 3); ++j)
+                mbar_wait(full + j % kSsStages, (uint32_t)((j / kSsStages) & 1));
         }
     } else {
         fence_after();
-        const float d = ssd::ex2(carry);
         const int quad = warp & 3, half = warp >> 2;
         const int row = 32 * quad + lane;             // state row n of this thread (TMEM lane)
         const uint32_t taddr = tmem + ((uint32_t)(32 * quad) << 16);
-        float *dst = plan.seg_state + ((size_t)unit * H + h) * P * N;
-        const float *src = (seg == 0 && a.resume[seq] != 0) ? a.state + ((size_t)seq * H + h) * P * N : nullptr;
-        constexpr int cw = p_pad / 2;
+        const bool from_slot = seg == 0 && a.resume[seq] != 0;
+        constexpr int cw = nx / 2;
 #pragma unroll
         for (int c0 = 0; c0 < cw; c0 += 16) {
-            const int col = half * cw + c0;
+            const int col = half * cw + c0;           // 16 columns of one head (16 | p_pad)
+            const int hb = col / p_pad, p0 = col - hb * p_pad;
+            const float d = decs[hb];
             float v[16];
             tmem_ld16(v, taddr + col);
-            if (row < N) {
+            if (row < N && p0 < P) {
+                const size_t hoff = ((size_t)h0 + hb) * P * N;
+                float *dst = plan.seg_state + (size_t)unit * H * P * N + hoff;
+                const float *src = from_slot ? a.state + (size_t)seq * H * P * N + hoff : nullptr;
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
-                    const int p = col + k;
+                    const int p = p0 + k;
                     if (p < P) {
                         float o = v[k];
                         if (src)
@@ -279,8 +375,8 @@ segment_state_tc_kernel(const ScanArgs a, const SegmentPlan plan)
                 }
             }
         }
-        if (tid == 0)
-            plan.seg_decay[(size_t)unit * H + h] = d;
+        if (tid < HB)
+            plan.seg_decay[(size_t)unit * H + h0 + tid] = decs[tid];
     }
     fence_before();
     __syncthreads();
@@ -288,40 +384,105 @@ segment_state_tc_kernel(const ScanArgs a, const SegmentPlan plan)
         tmem_dealloc(tmem, cols);
 }
 
-template <int XI>
-cudaError_t launch_xi(const ScanArgs &a, const SegmentPlan &plan, int max_units, cudaStream_t stream)
+// cuTensorMapEncodeTiled from the driver, looked up once.
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 {
-    const size_t smem = ss_layout(32 * XI).total;
-    cudaError_t e = cudaFuncSetAttribute(segment_state_tc_kernel<XI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess || q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
+// fp32 [d2][d1][d0] tensor (d0 contiguous) read in boxes of b0 x b1 x b2.
+bool encode_3d(CUtensorMap *tm, const float *base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1,
+               uint32_t b2)
+{
+    const auto fn = encode_fn();
+    if (!fn)
+        return false;
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {d0 * 4, d0 * d1 * 4};      // bytes, dims 1 and 2
+    const cuuint32_t box[3] = {b0, b1, b2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int XI, int HB>
+cudaError_t launch_shape(const ScanArgs &a, const SegmentPlan &plan, const SegStateMaps &maps, int max_units,
+                         cudaStream_t stream)
+{
+    constexpr size_t smem = ss_layout(HB * 32 * XI).total;
+    CUtensorMap tm_b, tm_x;
+    static_assert(sizeof(CUtensorMap) == sizeof(maps.b), "tensor map size");
+    std::memcpy(&tm_b, maps.b, sizeof tm_b);
+    std::memcpy(&tm_x, maps.x, sizeof tm_x);
+    cudaError_t e = cudaFuncSetAttribute(segment_state_tc_kernel<XI, HB>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
-    segment_state_tc_kernel<XI><<<dim3((unsigned)max_units, (unsigned)a.H), kSsThreads, smem, stream>>>(a, plan);
+    segment_state_tc_kernel<XI, HB><<<dim3((unsigned)max_units, (unsigned)(a.H / HB)), kSsBlock, smem, stream>>>(
+        a, plan, tm_b, tm_x);
     return cudaGetLastError();
 }
+
+// Two heads per block where they share a group and their N (2 x head_dim
+// padded) fits one product.
+int heads_per_block(int H, int G, int P) { return ((H / G) % 2 == 0 && (P + 31) / 32 <= 4) ? 2 : 1; }
 
 }  // namespace
 
 bool segment_state_tc_supported(int N, int P, size_t smem_optin)
 {
-    if (N < 1 || N > kSsRows || P < 1 || P > 256)
+    if (N < 4 || N > kSsRows || N % 4 != 0 || P < 4 || P > 256 || P % 4 != 0 || !encode_fn())
         return false;
-    return ss_layout(32 * ((P + 31) / 32)).total <= smem_optin;
+    return ss_layout(32 * ((P + 31) / 32)).total <= smem_optin;     // one head per block at most needs this
 }
 
-cudaError_t launch_segment_state_tc(const ScanArgs &a, const SegmentPlan &plan, int max_units, cudaStream_t stream)
+bool segment_state_tc_maps(const ScanArgs &a, SegStateMaps *maps)
 {
-    if (max_units <= 0)
+    const int p_pad = 32 * ((a.P + 31) / 32), hb = heads_per_block(a.H, a.G, a.P);
+    CUtensorMap tm_b, tm_x;
+    if (a.n_tokens <= 0 ||
+        !encode_3d(&tm_b, a.B, (uint64_t)a.N, (uint64_t)a.G, (uint64_t)a.n_tokens, kSsRows, 1, kSsQ) ||
+        !encode_3d(&tm_x, a.x, (uint64_t)a.P, (uint64_t)a.H, (uint64_t)a.n_tokens, (uint32_t)p_pad, (uint32_t)hb,
+                   kSsQ))
+        return false;
+    std::memcpy(maps->b, &tm_b, sizeof tm_b);
+    std::memcpy(maps->x, &tm_x, sizeof tm_x);
+    return true;
+}
+
+cudaError_t launch_segment_state_tc(const ScanArgs &a, const SegmentPlan &plan, const SegStateMaps &maps,
+                                    int max_units, cudaStream_t stream)
+{
+    if (max_units <= 0 || a.n_tokens <= 0)
         return cudaSuccess;
-    switch ((a.P + 31) / 32) {
-    case 1: return launch_xi<1>(a, plan, max_units, stream);
-    case 2: return launch_xi<2>(a, plan, max_units, stream);
-    case 3: return launch_xi<3>(a, plan, max_units, stream);
-    case 4: return launch_xi<4>(a, plan, max_units, stream);
-    case 5: return launch_xi<5>(a, plan, max_units, stream);
-    case 6: return launch_xi<6>(a, plan, max_units, stream);
-    case 7: return launch_xi<7>(a, plan, max_units, stream);
-    case 8: return launch_xi<8>(a, plan, max_units, stream);
+    const int xi = (a.P + 31) / 32;
+    if (heads_per_block(a.H, a.G, a.P) == 2) {
+        switch (xi) {
+        case 1: return launch_shape<1, 2>(a, plan, maps, max_units, stream);
+        case 2: return launch_shape<2, 2>(a, plan, maps, max_units, stream);
+        case 3: return launch_shape<3, 2>(a, plan, maps, max_units, stream);
+        case 4: return launch_shape<4, 2>(a, plan, maps, max_units, stream);
+        default: break;
+        }
+    }
+    switch (xi) {
+    case 1: return launch_shape<1, 1>(a, plan, maps, max_units, stream);
+    case 2: return launch_shape<2, 1>(a, plan, maps, max_units, stream);
+    case 3: return launch_shape<3, 1>(a, plan, maps, max_units, stream);
+    case 4: return launch_shape<4, 1>(a, plan, maps, max_units, stream);
+    case 5: return launch_shape<5, 1>(a, plan, maps, max_units, stream);
+    case 6: return launch_shape<6, 1>(a, plan, maps, max_units, stream);
+    case 7: return launch_shape<7, 1>(a, plan, maps, max_units, stream);
+    case 8: return launch_shape<8, 1>(a, plan, maps, max_units, stream);
     default: return cudaErrorInvalidValue;
     }
 }

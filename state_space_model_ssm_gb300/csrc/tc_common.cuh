@@ -142,5 +142,24 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *mbar, uint32_t parity)
     return false;
 }
 
+// Arrive on `mbar` and add `bytes` to the transaction count its phase waits for.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *mbar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(mbar)), "r"(bytes)
+                 : "memory");
+}
+
+// TMA: the box of a 3-D tensor map at coordinates (c0 innermost, c1, c2) into
+// shared memory; completion counts the box's bytes on `mbar`.  Elements outside
+// the tensor read as zero.  c0 * element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int c0, int c1, int c2, uint64_t *mbar)
+{
+    asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3, %4}], [%5];\n"
+                 ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2),
+                   "r"(smem_u32(mbar))
+                 : "memory");
+}
+
 }  // namespace tc
 }  // namespace ssm

@@ -256,7 +256,7 @@ def test_parity_time_segments_extreme_decay(dt_scale, a_value, state_pass):
 
 # Head dims across the tensor-core state pass's register shapes (head_dim
 # padded to 32, 64, ..., 256) and d_state below the 128 rows of its product.
-TC_GEOMS = [(4, 32, 64, 2), (2, 160, 128, 1), (2, 256, 48, 2), (6, 224, 16, 3)]
+TC_GEOMS = [(4, 32, 64, 2), (3, 64, 128, 1), (2, 160, 128, 1), (2, 256, 48, 2), (6, 224, 16, 3)]
 
 
 @pytest.mark.parametrize("geom", TC_GEOMS, ids=[f"h{g[0]}_p{g[1]}_n{g[2]}" for g in TC_GEOMS])
@@ -391,3 +391,30 @@ def test_state_snapshots_refuse_prefill_paths():
             bd.ssm_scan(d.state.clone(), d.x, d.dt, d.A, d.B, d.C, d.D, d.seq_starts, d.seq_lens, d.resume,
                         snapshots=snaps, tuning=_tuning(path=path))
         assert e.value.status == bd.SSM_ERR_UNSUPPORTED
+
+
+def test_tensor_state_pass_needs_16_byte_aligned_x():
+    """x only 4-byte aligned: the automatic choice takes the sequential state
+    pass (same results); an explicit tensor-core request is refused."""
+    inp = workload("tiny")
+    y_ref, s_ref = oracle.scan_inputs(inp)
+    d = inp.to("cuda")
+    buf = torch.empty(d.x.numel() + 1, device="cuda")
+    x = buf[1:].view(d.x.shape)
+    x.copy_(d.x)
+    g = inp.geom
+    for mode in (bd.SEGMENT_STATE_AUTO, bd.SEGMENT_STATE_TENSOR):
+        t = _tuning(path=bd.PATH_PREFILL, seg=16, seg_state=mode)
+        nbytes = bd.workspace_bytes(inp.n_seqs, inp.n_tokens, g.n_heads, g.head_dim, g.d_state, g.n_groups, t)
+        ws = torch.empty(nbytes // 4, device="cuda")
+        state = d.state.clone()
+        call = lambda: bd.ssm_scan(state, x, d.dt, d.A, d.B, d.C, d.D, d.seq_starts, d.seq_lens, d.resume,
+                                   tuning=t, workspace=ws)
+        if mode == bd.SEGMENT_STATE_TENSOR:
+            with pytest.raises(bd.SsmScanError) as e:
+                call()
+            assert e.value.status == bd.SSM_ERR_UNSUPPORTED
+        else:
+            y = call()
+            torch.cuda.synchronize()
+            assert_parity(inp, y.double().cpu().numpy(), state.double().cpu().numpy(), y_ref, s_ref)
