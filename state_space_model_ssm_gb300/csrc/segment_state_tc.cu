@@ -31,14 +31,17 @@
 // ring of three stages with TMA, two chunks ahead, and forms each chunk's
 // weights (lane = head * 16 + token, carrying each head's total) into shared
 // memory one barrier before the chunk is staged.  The 8 staging warps turn
-// their cells of the staged chunk into the operand tiles: the token index is
-// K, so the values of 4 consecutive tokens of one row form a 16-byte cell of a
-// K-major tile, read as four conflict-free 4-byte words from the staged rows
-// and written whole (consecutive rows across a warp).  Two operand buffers
-// alternate.  After the block's barrier the ninth warp issues the chunk's 6
-// MMAs (K = 8 each), commits them to the buffer's mbarrier (which the writers
-// wait on two chunks later) and starts the TMA of the chunk two ahead, while
-// the staging warps go on to the next chunk.  The epilogue reads the
+// the staged chunk into operands.  B^T goes to TMEM, where the MMA takes its A
+// operand from (row n in lane n, one token per column): each thread splits
+// half of one row (8 tokens, conflict-free 4-byte reads) and writes its hi and
+// lo parts with tcgen05.st, so the tensor core reads only X from shared
+// memory.  X_w is a K-major shared-memory tile: the values of 4 consecutive
+// tokens of one row form a 16-byte cell, written whole (consecutive rows
+// across a warp).  Two operand buffers alternate.  After the block's barrier
+// the ninth warp issues the chunk's 6 MMAs (K = 8 each), commits them to the
+// buffer's mbarrier (which the writers wait on two chunks later) and starts
+// the TMA of the chunk two ahead, while the staging warps go on to the next
+// chunk.  The epilogue reads the
 // accumulator (warp w: state rows 32 (w % 4) .. +31, column half w / 4) and
 // stores L with the state-slot layout, coalesced over n.
 #include <cstring>
@@ -61,31 +64,27 @@ constexpr int kSsThreads = 256;           // warps 0-7 stage the operands; warp 
 constexpr int kSsBlock = kSsThreads + 32;
 constexpr int kSsQuads = kSsQ / 4;         // 16-byte K cells per row and chunk
 constexpr int kSsStages = 3;               // staged raw chunks: two in flight while one is used
-constexpr int kSsBCells = kSsRows * kSsQuads / kSsThreads;   // B operand cells per thread: 2
 
-// Shared memory (bytes), all offsets multiples of 1024: two buffers of the
-// four operand tiles (buffer b at b * buf; A hi at 0), the staged raw chunks
+// Shared memory (bytes), all offsets multiples of 1024: two buffers of the X
+// operand tiles (buffer b at b * buf; hi at 0, lo at x_lo), the staged raw chunks
 // (stage s at raw + s * stage; B rows at 0, x rows at rx), mbarriers (full[3]
 // per stage, mma[2] per buffer), the TMEM address, the token weights of two
 // chunks and the heads' decays.
 struct SsLayout {
-    uint32_t a_lo, x_hi, x_lo, buf;
+    uint32_t x_lo, buf;
     uint32_t raw, rx, stage;
     uint32_t bar, tslot, total;
     uint32_t wts, dec;        // weights of two chunks [2][32] (lane = head * 16 + token), decays [HB]
-    uint32_t la, lx;          // K-cell strides of the B^T tiles (128 rows) and X tiles (nx rows)
+    uint32_t lx;              // K-cell stride of the X tiles (nx rows)
 };
 
 __host__ __device__ constexpr SsLayout ss_layout(int nx)
 {
     SsLayout L{};
-    L.la = kSsRows * 16;
     L.lx = (uint32_t)nx * 16;
-    const uint32_t ta = L.la * kSsQuads, tx = L.lx * kSsQuads;
-    L.a_lo = ta;
-    L.x_hi = 2 * ta;
-    L.x_lo = 2 * ta + tx;
-    L.buf = 2 * ta + 2 * tx;
+    const uint32_t tx = L.lx * kSsQuads;
+    L.x_lo = tx;
+    L.buf = 2 * tx;
     L.raw = 2 * L.buf;
     L.rx = kSsQ * kSsRows * 4;
     L.stage = L.rx + (uint32_t)(kSsQ * nx * 4);
@@ -97,9 +96,12 @@ __host__ __device__ constexpr SsLayout ss_layout(int nx)
     return L;
 }
 
+// TMEM: the accumulator in columns [0, nx), then two buffers of the B^T
+// operand (buffer b at nx + 32 b: 16 hi columns, then 16 lo), one token per
+// column, state row n in lane n.
 __host__ __device__ constexpr uint32_t ss_tmem_cols(int nx)
 {
-    return nx <= 32 ? 32u : nx <= 64 ? 64u : nx <= 128 ? 128u : 256u;
+    return nx + 64 <= 128 ? 128u : nx + 64 <= 256 ? 256u : 512u;
 }
 
 __device__ __forceinline__ float4 split_hi(float4 v, float4 &lo)
@@ -120,15 +122,16 @@ struct XCells {
     static constexpr bool guard = (NX * kSsQuads) % kSsThreads != 0;
 };
 
-// One staged chunk (stage `raw`) into operand buffer `buf`: this thread's B^T
-// cells (row n, token quads qb + 2i) and X cells (row xr[i] = head * p_pad + p,
-// token quad xq[i]; xq < 0: none), X scaled by the chunk's weights `w`
-// ([head * 16 + token]).  PARTIAL: tokens >= cnt read as zero (only the last
-// chunk of a segment can be short).  No branch inside, so the loads, splits and
-// stores of all cells interleave.
+// One staged chunk (stage `raw`) into the operand buffers: this thread's half
+// of B^T row `row` (tokens 8 half .. +7) into TMEM at `ta` (the buffer's hi
+// columns of the warp's lanes) and its X cells (row xr[i] = head * p_pad + p,
+// token quad xq[i]; xq < 0: none) into shared memory `buf`, X scaled by the
+// chunk's weights `w` ([head * 16 + token]).  PARTIAL: tokens >= cnt read as
+// zero (only the last chunk of a segment can be short).  No branch inside, so
+// the loads, splits and stores of all cells interleave.
 template <int XI, int HB, bool PARTIAL>
-__device__ __forceinline__ void stage_chunk(const char *raw, char *buf, const float *w, int n, int qb,
-                                            const int (&xr)[XCells<32 * XI * HB>::count],
+__device__ __forceinline__ void stage_chunk(const char *raw, char *buf, const float *w, uint32_t ta, int row,
+                                            int half, const int (&xr)[XCells<32 * XI * HB>::count],
                                             const int (&xq)[XCells<32 * XI * HB>::count], int cnt)
 {
     constexpr int p_pad = 32 * XI, nx = HB * p_pad;
@@ -142,17 +145,19 @@ __device__ __forceinline__ void stage_chunk(const char *raw, char *buf, const fl
         }
         return v;
     };
-    const float *rb = reinterpret_cast<const float *>(raw) + n;
+    {
+        const float *rb = reinterpret_cast<const float *>(raw) + row + 8 * half * kSsRows;
+        float hi[8], lo[8];
 #pragma unroll
-    for (int i = 0; i < kSsBCells; ++i) {
-        const int q = qb + 2 * i;
-        const float4 v = mask(make_float4(rb[(4 * q) * kSsRows], rb[(4 * q + 1) * kSsRows],
-                                          rb[(4 * q + 2) * kSsRows], rb[(4 * q + 3) * kSsRows]), q);
-        float4 lo;
-        const float4 hi = split_hi(v, lo);
-        const uint32_t off = q * L.la + n * 16;
-        *reinterpret_cast<float4 *>(buf + off) = hi;
-        *reinterpret_cast<float4 *>(buf + L.a_lo + off) = lo;
+        for (int k = 0; k < 8; ++k) {
+            float v = rb[k * kSsRows];
+            if (PARTIAL)
+                v = 8 * half + k < cnt ? v : 0.f;
+            hi[k] = ssd::tf32_round(v);
+            lo[k] = v - hi[k];
+        }
+        tmem_st8(ta + 8 * half, hi);
+        tmem_st8(ta + 16 + 8 * half, lo);
     }
 #pragma unroll
     for (int i = 0; i < XCells<nx>::count; ++i) {
@@ -165,7 +170,7 @@ __device__ __forceinline__ void stage_chunk(const char *raw, char *buf, const fl
             float4 lo;
             const float4 hi = split_hi(v, lo);
             const uint32_t off = q * L.lx + r * 16;
-            *reinterpret_cast<float4 *>(buf + L.x_hi + off) = hi;
+            *reinterpret_cast<float4 *>(buf + off) = hi;
             *reinterpret_cast<float4 *>(buf + L.x_lo + off) = lo;
         }
     }
@@ -273,16 +278,15 @@ segment_state_tc_kernel(const ScanArgs a, const SegmentPlan plan, const __grid_c
                 fence_after();
                 constexpr uint32_t id = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(nx >> 3) << 17) |
                                         ((uint32_t)(kSsRows >> 4) << 24);        // idesc_tf32(128, nx)
-                const uint32_t ba = sbase + (j & 1) * L.buf;
+                const uint32_t bx = sbase + (j & 1) * L.buf;
+                const uint32_t tah = tmem + nx + 32 * (j & 1), tal = tah + 16;   // B^T hi, lo in TMEM
 #pragma unroll
                 for (int kk = 0; kk < kSsQ / 8; ++kk) {
-                    const uint64_t dah = smem_desc(ba + 2 * kk * L.la, L.la, 128);
-                    const uint64_t dal = smem_desc(ba + L.a_lo + 2 * kk * L.la, L.la, 128);
-                    const uint64_t dxh = smem_desc(ba + L.x_hi + 2 * kk * L.lx, L.lx, 128);
-                    const uint64_t dxl = smem_desc(ba + L.x_lo + 2 * kk * L.lx, L.lx, 128);
-                    mma(tmem, dal, dxh, id, (j > 0 || kk > 0) ? 1u : 0u);
-                    mma(tmem, dah, dxl, id, 1u);
-                    mma(tmem, dah, dxh, id, 1u);
+                    const uint64_t dxh = smem_desc(bx + 2 * kk * L.lx, L.lx, 128);
+                    const uint64_t dxl = smem_desc(bx + L.x_lo + 2 * kk * L.lx, L.lx, 128);
+                    mma_ts(tmem, tal + 8 * kk, dxh, id, (j > 0 || kk > 0) ? 1u : 0u);
+                    mma_ts(tmem, tah + 8 * kk, dxl, id, 1u);
+                    mma_ts(tmem, tah + 8 * kk, dxh, id, 1u);
                 }
                 commit(mmab + (j & 1));
                 if (j + 2 < nc)
@@ -301,7 +305,9 @@ segment_state_tc_kernel(const ScanArgs a, const SegmentPlan plan, const __grid_c
     }
 
     // ---- staging warps ----
-    const int n = tid & (kSsRows - 1), qb = tid >> 7;
+    const int quad = warp & 3, half = warp >> 2;
+    const int row = 32 * quad + lane;                 // B^T row (TMEM lane) of this thread; tokens 8 half ..
+    const uint32_t tlane = tmem + ((uint32_t)(32 * quad) << 16);
     int xr[XCells<nx>::count], xq[XCells<nx>::count];
 #pragma unroll
     for (int i = 0; i < XCells<nx>::count; ++i) {
@@ -318,15 +324,20 @@ segment_state_tc_kernel(const ScanArgs a, const SegmentPlan plan, const __grid_c
         const int b = j & 1;
         const int cnt = min(kSsQ, len - (nc - 1 - j) * kSsQ);   // tokens of the chunk (16 but the first)
         ok = mbar_wait(full + st, (uint32_t)((j / kSsStages) & 1)) && ok;
-        if (j >= 2)                                   // buffer b: products of chunk j - 2 done
+        if (j >= 2) {                                 // buffer b: products of chunk j - 2 done
             ok = mbar_wait(mmab + b, (uint32_t)(((j >> 1) - 1) & 1)) && ok;
+            fence_after();
+        }
         const char *raw = sm + L.raw + st * L.stage;
         char *buf = sm + b * L.buf;
         const float *w = wts + b * 32;
+        const uint32_t ta = tlane + nx + 32 * b;
         if (cnt < kSsQ)
-            stage_chunk<XI, HB, true>(raw, buf, w, n, qb, xr, xq, cnt);
+            stage_chunk<XI, HB, true>(raw, buf, w, ta, row, half, xr, xq, cnt);
         else
-            stage_chunk<XI, HB, false>(raw, buf, w, n, qb, xr, xq, cnt);
+            stage_chunk<XI, HB, false>(raw, buf, w, ta, row, half, xr, xq, cnt);
+        tmem_wait_st();
+        fence_before();
         fence_async_smem();
         if (__syncthreads_or(!ok))
             break;                                    // a wait gave up: issue nothing more
@@ -347,9 +358,7 @@ segment_state_tc_kernel(const ScanArgs a, const SegmentPlan plan, const __grid_c
         }
     } else {
         fence_after();
-        const int quad = warp & 3, half = warp >> 2;
-        const int row = 32 * quad + lane;             // state row n of this thread (TMEM lane)
-        const uint32_t taddr = tmem + ((uint32_t)(32 * quad) << 16);
+        const uint32_t taddr = tlane;                 // state rows 32 quad .. +31 (row: this thread's)
         const bool from_slot = seg == 0 && a.resume[seq] != 0;
         constexpr int cw = nx / 2;
 #pragma unroll

@@ -92,6 +92,19 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16])
                  : "memory");
 }
 
+// 8 consecutive fp32 TMEM columns of this thread's lane, written.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const float (&v)[8])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n"
+                 ::"r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+                   "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+                   "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
+                 : "memory");
+}
+
+// This thread's earlier TMEM writes complete.
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
+
 // 16 consecutive fp32 TMEM columns of this thread's lane.
 __device__ __forceinline__ void tmem_ld16(float (&v)[16], uint32_t taddr)
 {
