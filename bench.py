@@ -182,6 +182,25 @@ def event_pair():
     return torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
 
+def launch_event_sets(n_sets, n_launches, stream):
+    """n_sets lists of 2 * n_launches timing events for the library to record
+    around a call's kernel launches (each recorded once here so that it exists)."""
+    sets = []
+    for _ in range(n_sets):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n_launches)]
+        for e in evs:
+            e.record(stream)
+        sets.append(evs)
+    torch.cuda.synchronize()
+    return sets
+
+
+def launch_ms(sets):
+    """Mean device ms of each launch over the recorded sets."""
+    n = len(sets[0]) // 2
+    return [sum(s[2 * k].elapsed_time(s[2 * k + 1]) for s in sets) / len(sets) for k in range(n)]
+
+
 # ---------------------------------------------------------------- our arm
 
 def prefill_workspace(inp, dev):
@@ -212,9 +231,13 @@ def run_prefill(args, world, rank, dev):
     stream = torch.cuda.current_stream(dev)
     ws = prefill_workspace(inp, dev)
 
-    def step():
+    # the library records these around its launches (plan, state pass, combine, full pass)
+    n_launch = prefill_launches_per_step(inp)
+    kev = launch_event_sets(args.steps, n_launch, stream)
+
+    def step(events=None):
         bd.ssm_scan(state, d.x, d.dt, d.A, d.B, d.C, d.D, d.seq_starts, d.seq_lens, d.resume, y=y,
-                    workspace=ws)
+                    workspace=ws, launch_events=events)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -223,16 +246,31 @@ def run_prefill(args, world, rank, dev):
     evs = [event_pair() for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize(dev)
-    for e0, e1 in evs:
+    for (e0, e1), ke in zip(evs, kev):
         flush.zero_()                 # L2 flushed between timed steps
         e0.record(stream)
-        step()
+        step(ke)
         e1.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
     times_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
     step_ms = sum(times_ms) / len(times_ms)
-    return inp, d, step_ms, times_ms
+    return inp, d, step_ms, times_ms, launch_ms(kev)
+
+
+def run_prefill_fp32_state(args, dev, inp, d):
+    """The same step with the segments' state pass in the sequential kernel
+    (SEGMENT_STATE_FP32) instead of the tensor cores: mean ms per step."""
+    from state_space_model_ssm_gb300 import binding as bd
+    t = bd.Tuning()
+    t.segment_state = bd.SEGMENT_STATE_FP32
+    ws = prefill_workspace(inp, dev)
+    state = d.state.clone()
+    y = torch.empty_like(d.x)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    return _timed(lambda: bd.ssm_scan(state, d.x, d.dt, d.A, d.B, d.C, d.D, d.seq_starts, d.seq_lens,
+                                      d.resume, y=y, workspace=ws, tuning=t),
+                  max(5, args.steps // 2), flush)
 
 
 def run_prefill_e2e(args, dev, inp):
@@ -335,24 +373,35 @@ def run_ssd(args, dev, inp, d, chunk=128):
     y = torch.empty_like(d.x)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    kev = launch_event_sets(args.steps, 4, stream)     # plan, chunk states, state pass, output
 
-    def step():
+    def step(events=None):
         bd.ssm_scan_ssd(state, d.x, d.dt, d.A, d.B, d.C, d.D, d.seq_starts, d.seq_lens, d.resume,
-                        y=y, chunk=chunk, workspace=ws)
+                        y=y, chunk=chunk, workspace=ws, launch_events=events)
 
     for _ in range(max(3, args.warmup)):
         flush.zero_()
         step()
     torch.cuda.synchronize(dev)
     evs = [event_pair() for _ in range(args.steps)]
-    for e0, e1 in evs:
+    for (e0, e1), ke in zip(evs, kev):
         flush.zero_()
         e0.record(stream)
-        step()
+        step(ke)
         e1.record(stream)
     torch.cuda.synchronize(dev)
     times = [e0.elapsed_time(e1) for e0, e1 in evs]
-    return sum(times) / len(times), nbytes
+    return sum(times) / len(times), nbytes, launch_ms(kev)
+
+
+def ssd_output_flops(inp, chunk):
+    """Dense FLOPs of the output kernel alone: per chunk, G x 2 Q^2 N (C B^T)
+    plus H x (2 Q^2 P (masked product with x) + 2 Q N P (C S_in^T))."""
+    g = inp.geom
+    H, P, N, G = g.n_heads, g.head_dim, g.d_state, g.n_groups
+    chunks = sum((int(L) + chunk - 1) // chunk for L in inp.seq_lens.tolist())
+    Q = chunk
+    return chunks * (G * 2 * Q * Q * N + H * (2 * Q * Q * P + 2 * Q * N * P))
 
 
 def ssd_algorithmic_flops(inp, chunk):
@@ -466,6 +515,46 @@ def run_next_rows(dev, inp, d, peaks, steps=10):
     return out
 
 
+def segment_units(inp):
+    """(segments, segment length) of the library's automatic plan for a single
+    sequence: its workspace holds one state per unit plus a few small tables."""
+    from state_space_model_ssm_gb300 import binding as bd
+    g = inp.geom
+    slot = 4 * g.n_heads * g.head_dim * g.d_state
+    ws = bd.workspace_bytes(inp.n_seqs, inp.n_tokens, g.n_heads, g.head_dim, g.d_state, g.n_groups)
+    units = ws // slot - inp.n_seqs                # max_units = n_seqs + ceil(T / seg)
+    T = int(inp.seq_lens.sum())
+    seg = -(-T // units)
+    seg = -(-seg // 16) * 16                       # a multiple of the prefill chunk
+    return -(-T // seg), seg
+
+
+def state_pass_report(inp, ms, peaks, peaks_src, fp32_step_ms, step_ms):
+    """Roofline of the tensor-core state pass: every segment but the last, each
+    L = sum_s w_s x_s B_s^T over its tokens (one multiply-add per token and state
+    element), run as three TF32 products (hi*hi, hi*lo, lo*hi) with head_dim
+    padded to a multiple of 32 and d_state to 128."""
+    g = inp.geom
+    H, P, N, G = g.n_heads, g.head_dim, g.d_state, g.n_groups
+    units, seg = segment_units(inp)
+    Ts = (units - 1) * seg
+    alg_flops = 2 * Ts * H * P * N
+    tc_flops = 3 * 2 * Ts * H * (-(-P // 32) * 32) * 128
+    nbytes = 4 * (Ts * H * P + Ts * G * N + Ts * H + (units - 1) * H * P * N)
+    tf32_peak = peaks["bf16_tflops"] * 1e12 * 1.1 / 2.25
+    s = ms * 1e-3
+    return {"what": "segment state pass on tcgen05 (3 split-TF32 products, fp32 accumulation)",
+            "ms": ms, "tokens": Ts, "segments": units, "segment_tokens": seg,
+            "roofline": {"bound": "hbm", "achieved": nbytes / s / 1e9, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": nbytes / s / 1e9 / peaks["hbm_gbs"], "peak_src": peaks_src,
+                         "algorithmic": f"{nbytes} bytes per launch (x, B and dt of {Ts} tokens; the states out)",
+                         "tensor_frac": tc_flops / s / tf32_peak,
+                         "tensor_basis": f"{tc_flops} executed TF32 FLOPs vs measured bf16 burst x 1.1/2.25",
+                         "algorithmic_tflops": alg_flops / s / 1e12},
+            "step_ms_with_fp32_state_pass": fp32_step_ms,
+            "step_speedup": fp32_step_ms / step_ms}
+
+
 def prefill_algorithmic(inp):
     T = int(inp.seq_lens.sum())
     H, P, N, G = inp.geom.n_heads, inp.geom.head_dim, inp.geom.d_state, inp.geom.n_groups
@@ -525,7 +614,7 @@ def ours(args):
     sms = props.multi_processor_count
     sampler = ClockSampler(local)
     sampler.start()
-    inp, d, step_ms, times = run_prefill(args, world, rank, dev)
+    inp, d, step_ms, times, kms = run_prefill(args, world, rank, dev)
     clocks = sampler.stop()
     step_ms_max = max_over_ranks(step_ms, world, dev)
 
@@ -534,7 +623,8 @@ def ours(args):
     value = world * T / (step_ms_max * 1e-3)
     sm_max = (clocks or {}).get("sm_max_mhz") or peaks.get("sm_max_mhz", 2070.0)
     peak_ops = sms * FP32_LANES_PER_SM * sm_max * 1e6
-    achieved = fp32_ops / (step_ms * 1e-3)
+    full_ms = kms[-1]                              # the full pass: the step's last launch
+    achieved = fp32_ops / (full_ms * 1e-3)
     traffic = ncu_traffic("prefill_kernel", "prefill_1x4096")
     line = {
         "metric": METRIC,
@@ -561,8 +651,12 @@ def ours(args):
                      "traffic": traffic,
                      "peak_basis": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x {sm_max:.0f} MHz (max clock)",
                      "algorithmic": f"{fp32_ops} FP32 ops per launch (3 per element-update)",
-                     "hbm_frac": (alg_bytes / (step_ms * 1e-3)) / (peaks["hbm_gbs"] * 1e9),
-                     "hbm_peak_src": peaks_src},
+                     "hbm_frac": (alg_bytes / (full_ms * 1e-3)) / (peaks["hbm_gbs"] * 1e9),
+                     "hbm_peak_src": peaks_src,
+                     "timing": ("the full-pass kernel alone: CUDA events the library records around "
+                                "its launch on the call's stream, mean over the timed steps"),
+                     "kernel_ms": full_ms,
+                     "step_frac": fp32_ops / (step_ms * 1e-3) / peak_ops},
         "gpu_launches": args.steps * prefill_launches_per_step(inp),
         "clocks": clocks,
         "step_ms_min": min(times),
@@ -570,6 +664,11 @@ def ours(args):
     }
     if clocks and clocks.get("sm_mhz"):
         line["roofline"]["frac_at_sampled_clock"] = achieved / (sms * FP32_LANES_PER_SM * clocks["sm_mhz"] * 1e6)
+    if len(kms) == 4:
+        line["launches_ms"] = {"segment_plan": kms[0], "state_pass": kms[1], "combine": kms[2],
+                               "full_pass": kms[3]}
+        line["state_pass"] = state_pass_report(inp, kms[1], peaks, peaks_src,
+                                               run_prefill_fp32_state(args, dev, inp, d), step_ms)
 
     if not args.no_e2e:
         e2e_ms, h2d, d2h = run_prefill_e2e(args, dev, inp)
@@ -598,8 +697,9 @@ def ours(args):
             "vs_page": PAGE_DECODE_US / dec["cold_us"],
         }
     if not args.no_ssd:
-        ssd_ms, ssd_ws = run_ssd(args, dev, inp, d)
+        ssd_ms, ssd_ws, ssd_kms = run_ssd(args, dev, inp, d)
         flops = ssd_algorithmic_flops(inp, 128)
+        out_flops = ssd_output_flops(inp, 128)
         tf32_peak = peaks["bf16_tflops"] * TF32_PER_BF16
         line["ssd"] = {
             "what": ("ssm_scan_ssd: chunked matrix form, chunk 128, TF32 operands (rounded to nearest), "
@@ -619,6 +719,13 @@ def ours(args):
                          "timing": "whole call (plan, chunk states, state pass, output)",
                          "traffic": ncu_traffic("ssd_output_kernel", "prefill_1x4096"),
                          "traffic_kernel": "the output kernel (tcgen05), DRAM bytes per launch"},
+            "launches_ms": {"segment_plan": ssd_kms[0], "chunk_state": ssd_kms[1], "state_pass": ssd_kms[2],
+                            "output": ssd_kms[3]},
+            "output_kernel_roofline": {
+                "bound": "tensor", "achieved": out_flops / (ssd_kms[3] * 1e-3) / 1e12, "peak": tf32_peak,
+                "unit": "TFLOP/s", "frac": out_flops / (ssd_kms[3] * 1e-3) / 1e12 / tf32_peak,
+                "algorithmic": f"{out_flops} dense FLOPs per launch",
+                "timing": "CUDA events the library records around the output kernel's launch"},
         }
     if not args.no_next:
         line["next_rows"] = run_next_rows(dev, inp, d, peaks)

@@ -177,6 +177,18 @@ int ssm_scan_tuned(float *state_slots, const float *x, const float *dt,
  *       of "ssm_gated_delta.cu").  gated_y, gate_z: device [n_tokens][n_heads]
  *       [head_dim] fp32; norm_weight: device [head_dim]; norm_eps > 0.  y is
  *       still written.  gated_y NULL: off (the other three are then ignored).
+ *   launch_events, n_launch_events  timing of the call's kernels: an array of
+ *       n_launch_events CUDA events (cudaEvent_t handles the caller created on
+ *       the stream's device).  The call records launch_events[2k] on its stream
+ *       right before its k-th kernel launch and launch_events[2k+1] right
+ *       after it, while 2k+1 < n_launch_events, so cudaEventElapsedTime of a
+ *       pair is that kernel's device time.  Launch order: the dt pass (with
+ *       the dt options); then for ssm_scan_* the decode kernel, or the prefill
+ *       kernel, or with time segments the plan, state-pass, combine and
+ *       full-pass kernels; for ssm_scan_ssd the plan, chunk-state, state-pass
+ *       and output kernels; then the gated RMSNorm (with gated_y).  NULL / 0:
+ *       none; n_launch_events < 0, or > 0 with NULL events: SSM_ERR_INVALID_ARG;
+ *       a failed record: SSM_ERR_CUDA.
  */
 typedef struct {
     const float *dt_bias;
@@ -186,6 +198,8 @@ typedef struct {
     const float *norm_weight;
     float norm_eps;
     float *gated_y;
+    void *const *launch_events;
+    int n_launch_events;
 } ssm_scan_options;
 
 /*

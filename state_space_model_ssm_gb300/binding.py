@@ -50,7 +50,8 @@ class Options(ctypes.Structure):
     _fields_ = [("dt_bias", ctypes.c_void_p), ("dt_softplus", ctypes.c_int),
                 ("state_snapshots", ctypes.c_void_p), ("gate_z", ctypes.c_void_p),
                 ("norm_weight", ctypes.c_void_p), ("norm_eps", ctypes.c_float),
-                ("gated_y", ctypes.c_void_p)]
+                ("gated_y", ctypes.c_void_p), ("launch_events", ctypes.c_void_p),
+                ("n_launch_events", ctypes.c_int)]
 
 
 _P = ctypes.c_void_p
@@ -163,12 +164,28 @@ def ex_workspace_bytes(n_seqs, n_tokens, n_heads, head_dim, d_state, n_groups,
 
 
 def make_options(dev, H, P, T, *, dt_bias=None, dt_softplus=False, snapshots=None, gate_z=None,
-                 norm_weight=None, norm_eps=1e-6, gated_y=None):
-    """Options from tensors (checked for dtype, device and shape); None when all are off."""
+                 norm_weight=None, norm_eps=1e-6, gated_y=None, launch_events=None):
+    """Options from tensors (checked for dtype, device and shape); None when all are off.
+
+    launch_events: torch.cuda.Event objects (enable_timing=True), recorded by the
+    call around its kernel launches in pairs (see ``ssm_scan_options``)."""
     f32 = torch.float32
-    if dt_bias is None and not dt_softplus and snapshots is None and gated_y is None:
+    if (dt_bias is None and not dt_softplus and snapshots is None and gated_y is None
+            and not launch_events):
         return None
     o = Options()
+    if launch_events:
+        handles = []
+        for ev in launch_events:
+            h = int(ev.cuda_event)
+            if h == 0:                        # torch creates the CUDA event at its first record
+                ev.record(torch.cuda.current_stream(dev))
+                h = int(ev.cuda_event)
+            handles.append(h)
+        arr = (ctypes.c_void_p * len(handles))(*handles)
+        o._events_keepalive = arr             # the array lives as long as the options
+        o.launch_events = ctypes.cast(arr, ctypes.c_void_p)
+        o.n_launch_events = len(handles)
     if dt_bias is not None:
         _check(dt_bias, "dt_bias", f32, dev, (H,))
         o.dt_bias = dt_bias.data_ptr()
@@ -212,7 +229,7 @@ def _check(t, name, dtype, device, shape=None):
 def ssm_scan(state_slots, x, dt, A, B, C, D, seq_starts, seq_lens, resume_flags,
              y=None, *, tuning: Tuning | None = None, stream=None, workspace=None,
              dt_bias=None, dt_softplus=False, snapshots=None, gate_z=None, norm_weight=None,
-             norm_eps=1e-6, gated_y=None):
+             norm_eps=1e-6, gated_y=None, launch_events=None):
     """Run the scan on the current CUDA stream (or ``stream``).
 
     state_slots [n,H,P,N] fp32 (updated in place), x [T,H,P], dt [T,H], A [H],
@@ -225,7 +242,8 @@ def ssm_scan(state_slots, x, dt, A, B, C, D, seq_starts, seq_lens, resume_flags,
     dt_bias [H] / dt_softplus: discretise dt inside the scan; snapshots
     [T,H,P,N]: the state after every token; gated_y [T,H,P] with gate_z
     [T,H,P], norm_weight [P], norm_eps: the gated RMSNorm of y (see
-    ``ssm_scan_options`` in the C header).
+    ``ssm_scan_options`` in the C header).  launch_events: torch.cuda.Event
+    objects recorded in pairs around the call's kernel launches.
     """
     dev = state_slots.device
     if dev.type != "cuda":
@@ -255,7 +273,8 @@ def ssm_scan(state_slots, x, dt, A, B, C, D, seq_starts, seq_lens, resume_flags,
             raise ValueError("workspace must be a contiguous tensor on the scan's device")
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
     opts = make_options(dev, H, P, T, dt_bias=dt_bias, dt_softplus=dt_softplus, snapshots=snapshots,
-                        gate_z=gate_z, norm_weight=norm_weight, norm_eps=norm_eps, gated_y=gated_y)
+                        gate_z=gate_z, norm_weight=norm_weight, norm_eps=norm_eps, gated_y=gated_y,
+                        launch_events=launch_events)
     if opts is not None and (dt_bias is not None or dt_softplus):
         need = ex_workspace_bytes(n, T, H, P, N, G, tuning, opts)
         if ws_bytes < need:                   # the discretised step needs room in the workspace
@@ -274,7 +293,8 @@ def ssm_scan(state_slots, x, dt, A, B, C, D, seq_starts, seq_lens, resume_flags,
 
 def ssm_scan_ssd(state_slots, x, dt, A, B, C, D, seq_starts, seq_lens, resume_flags,
                  y=None, *, chunk: int = 0, workspace=None, stream=None, dt_bias=None,
-                 dt_softplus=False, gate_z=None, norm_weight=None, norm_eps=1e-6, gated_y=None):
+                 dt_softplus=False, gate_z=None, norm_weight=None, norm_eps=1e-6, gated_y=None,
+                 launch_events=None):
     """The scan in chunked matrix form on the TF32 tensor cores (``ssm_scan_ssd``).
 
     Same tensors as ``ssm_scan``; y matches the exact scan to about
@@ -310,7 +330,8 @@ def ssm_scan_ssd(state_slots, x, dt, A, B, C, D, seq_starts, seq_lens, resume_fl
         stream = torch.cuda.current_stream(dev)
     handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
     opts = make_options(dev, H, P, T, dt_bias=dt_bias, dt_softplus=dt_softplus, gate_z=gate_z,
-                        norm_weight=norm_weight, norm_eps=norm_eps, gated_y=gated_y)
+                        norm_weight=norm_weight, norm_eps=norm_eps, gated_y=gated_y,
+                        launch_events=launch_events)
     with torch.cuda.device(dev):
         rc = ssd_raw(state_slots.data_ptr(), x.data_ptr(), dt.data_ptr(), A.data_ptr(),
                      B.data_ptr(), C.data_ptr(), D.data_ptr(), y.data_ptr(),

@@ -275,6 +275,8 @@ int read_options(const ssm_scan_options *opts, ssm_scan_options *out)
     *out = *opts;
     if (!aligned(out->dt_bias, 4) || !aligned(out->state_snapshots, 16))
         return SSM_ERR_INVALID_ARG;
+    if (out->n_launch_events < 0 || (out->n_launch_events > 0 && !out->launch_events))
+        return SSM_ERR_INVALID_ARG;
     if (out->gated_y) {
         if (!out->gate_z || !out->norm_weight || !(out->norm_eps > 0.f))
             return SSM_ERR_INVALID_ARG;
@@ -287,7 +289,7 @@ int read_options(const ssm_scan_options *opts, ssm_scan_options *out)
 // Launches the scan kernels for a checked call (everything after the argument
 // checks); the options' post-scan steps run in scan_impl.
 int scan_kernels(const ssm::ScanArgs &a, const ssm_scan_tuning &t, const DeviceInfo &dev, void *workspace,
-                 size_t workspace_bytes, cudaStream_t stream);
+                 size_t workspace_bytes, cudaStream_t stream, ssm::LaunchTimer *tm);
 
 int scan_impl(float *state, const float *x, const float *dt, const float *A, const float *B,
               const float *C, const float *D, float *y, const int32_t *seq_starts,
@@ -360,25 +362,29 @@ int scan_impl(float *state, const float *x, const float *dt, const float *A, con
         if (rc != SSM_OK)
             return rc;
     }
+    ssm::LaunchTimer tm{o.launch_events, o.n_launch_events, 0, stream, false};
     if (dtb > 0) {
         float *step = static_cast<float *>(workspace);
-        if (ssm::launch_dt_prep(a, o.dt_bias, o.dt_softplus, step, stream) != cudaSuccess)
+        if (ssm::timed(&tm, [&] { return ssm::launch_dt_prep(a, o.dt_bias, o.dt_softplus, step, stream); }) !=
+            cudaSuccess)
             return SSM_ERR_CUDA;
         a.dt = step;
         workspace = static_cast<char *>(workspace) + dtb;
         workspace_bytes -= dtb;
     }
-    rc = scan_kernels(a, t, dev, workspace, workspace_bytes, stream);
+    rc = scan_kernels(a, t, dev, workspace, workspace_bytes, stream, &tm);
     if (rc != SSM_OK)
         return rc;
     if (o.gated_y && n_tokens > 0 &&
-        ssm::launch_gated_norm(a, o.gate_z, o.norm_weight, o.norm_eps, o.gated_y, stream) != cudaSuccess)
+        ssm::timed(&tm, [&] {
+            return ssm::launch_gated_norm(a, o.gate_z, o.norm_weight, o.norm_eps, o.gated_y, stream);
+        }) != cudaSuccess)
         return SSM_ERR_CUDA;
-    return SSM_OK;
+    return tm.failed ? SSM_ERR_CUDA : SSM_OK;
 }
 
 int scan_kernels(const ssm::ScanArgs &a, const ssm_scan_tuning &t, const DeviceInfo &dev, void *workspace,
-                 size_t workspace_bytes, cudaStream_t stream)
+                 size_t workspace_bytes, cudaStream_t stream, ssm::LaunchTimer *tm)
 {
     const int n_seqs = a.n_seqs, n_tokens = a.n_tokens, H = a.H, P = a.P, N = a.N, G = a.G;
     int rc = SSM_OK;
@@ -408,7 +414,8 @@ int scan_kernels(const ssm::ScanArgs &a, const ssm_scan_tuning &t, const DeviceI
                 grid_seqs, (long long)t.ctas_per_sm * dev.sms / std::max<long long>(1, blocks_per_seq)));
         if (blocks_per_seq > INT_MAX)
             return SSM_ERR_UNSUPPORTED;
-        if (ssm::launch_decode(a, g, lanes, vpl, rpt, (int)grid_seqs, stream) != cudaSuccess)
+        if (ssm::timed(tm, [&] { return ssm::launch_decode(a, g, lanes, vpl, rpt, (int)grid_seqs, stream); }) !=
+            cudaSuccess)
             return SSM_ERR_CUDA;
         return SSM_OK;
     }
@@ -433,14 +440,18 @@ int scan_kernels(const ssm::ScanArgs &a, const ssm_scan_tuning &t, const DeviceI
     if (pl.max_units * G * pl.g.runs_per_group > INT_MAX || (long long)n_seqs * G * pl.g.runs_per_group > INT_MAX)
         return SSM_ERR_UNSUPPORTED;
     if (!scaled) {
-        if (ssm::launch_prefill(a, pl.g, pl.lanes, pl.vpl, pl.rpt, pl.smem, dev.sms, stream) != cudaSuccess)
+        if (ssm::timed(tm, [&] {
+                return ssm::launch_prefill(a, pl.g, pl.lanes, pl.vpl, pl.rpt, pl.smem, dev.sms, stream);
+            }) != cudaSuccess)
             return SSM_ERR_CUDA;
         return SSM_OK;
     }
     ssm::SegmentPlan plan{};
     if (pl.seg_len == 0) {
-        if (ssm::launch_prefill_scaled(a, pl.g, pl.lanes, pl.vpl, pl.rpt, plan, ssm::kScanFull, n_seqs,
-                                       pl.smem, stream) != cudaSuccess)
+        if (ssm::timed(tm, [&] {
+                return ssm::launch_prefill_scaled(a, pl.g, pl.lanes, pl.vpl, pl.rpt, plan, ssm::kScanFull, n_seqs,
+                                                  pl.smem, stream);
+            }) != cudaSuccess)
             return SSM_ERR_CUDA;
         return SSM_OK;
     }
@@ -453,15 +464,19 @@ int scan_kernels(const ssm::ScanArgs &a, const ssm_scan_tuning &t, const DeviceI
     plan.seg_state = reinterpret_cast<float *>(ws + pl.off_state);
     plan.status = reinterpret_cast<int *>(ws + pl.off_status);
     const int mu = (int)pl.max_units;
-    if (ssm::launch_segment_plan(a, plan, mu, stream) != cudaSuccess)
+    if (ssm::timed(tm, [&] { return ssm::launch_segment_plan(a, plan, mu, stream); }) != cudaSuccess)
         return SSM_ERR_CUDA;
-    const cudaError_t e = pl.tc_state
-        ? ssm::launch_segment_state_tc(a, plan, maps, mu, stream)
-        : ssm::launch_prefill_scaled(a, pl.g, pl.lanes, pl.vpl, pl.rpt, plan, ssm::kScanStateOnly, mu, pl.smem,
-                                     stream);
-    if (e != cudaSuccess || ssm::launch_segment_combine(a, plan, mu, stream) != cudaSuccess ||
-        ssm::launch_prefill_scaled(a, pl.g, pl.lanes, pl.vpl, pl.rpt, plan, ssm::kScanFull, mu, pl.smem,
-                                   stream) != cudaSuccess)
+    const cudaError_t e = ssm::timed(tm, [&] {
+        return pl.tc_state ? ssm::launch_segment_state_tc(a, plan, maps, mu, stream)
+                           : ssm::launch_prefill_scaled(a, pl.g, pl.lanes, pl.vpl, pl.rpt, plan, ssm::kScanStateOnly,
+                                                        mu, pl.smem, stream);
+    });
+    if (e != cudaSuccess || ssm::timed(tm, [&] { return ssm::launch_segment_combine(a, plan, mu, stream); }) !=
+                                cudaSuccess ||
+        ssm::timed(tm, [&] {
+            return ssm::launch_prefill_scaled(a, pl.g, pl.lanes, pl.vpl, pl.rpt, plan, ssm::kScanFull, mu, pl.smem,
+                                              stream);
+        }) != cudaSuccess)
         return SSM_ERR_CUDA;
     if (pl.tc_state && check_env())         // debug: report a bounded wait that gave up
         return read_status(plan.status, stream);
@@ -619,9 +634,11 @@ int ssd_impl(float *state, const float *x, const float *dt, const float *A, cons
         if (rc != SSM_OK)
             return rc;
     }
+    ssm::LaunchTimer tm{o.launch_events, o.n_launch_events, 0, stream, false};
     if (dt_buffer_bytes(o, n_tokens, H) > 0) {
         float *step = reinterpret_cast<float *>(static_cast<char *>(workspace) + L.off_step);
-        if (ssm::launch_dt_prep(a, o.dt_bias, o.dt_softplus, step, stream) != cudaSuccess)
+        if (ssm::timed(&tm, [&] { return ssm::launch_dt_prep(a, o.dt_bias, o.dt_softplus, step, stream); }) !=
+            cudaSuccess)
             return SSM_ERR_CUDA;
         a.dt = step;
     }
@@ -642,11 +659,15 @@ int ssd_impl(float *state, const float *x, const float *dt, const float *A, cons
     plan.status = reinterpret_cast<int *>(ws + L.off_status);
     seg.status = plan.status;               // zeroed by the plan kernel
     const int mu = (int)L.max_units;
-    if (ssm::launch_segment_plan(a, seg, mu, stream) != cudaSuccess ||
-        ssm::launch_ssd(a, plan, L.g, mu, stream) != cudaSuccess)
+    if (ssm::timed(&tm, [&] { return ssm::launch_segment_plan(a, seg, mu, stream); }) != cudaSuccess ||
+        ssm::launch_ssd(a, plan, L.g, mu, stream, &tm) != cudaSuccess)
         return SSM_ERR_CUDA;
     if (o.gated_y && n_tokens > 0 &&
-        ssm::launch_gated_norm(a, o.gate_z, o.norm_weight, o.norm_eps, o.gated_y, stream) != cudaSuccess)
+        ssm::timed(&tm, [&] {
+            return ssm::launch_gated_norm(a, o.gate_z, o.norm_weight, o.norm_eps, o.gated_y, stream);
+        }) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    if (tm.failed)
         return SSM_ERR_CUDA;
     if (check_env())                        // debug: report a bounded wait that gave up
         return read_status(plan.status, stream);

@@ -202,8 +202,42 @@ struct SsdGeom {
     size_t smem_state, smem_out;
 };
 
+// Caller-supplied CUDA events recorded around a call's kernel launches, in
+// launch order: ev[2k] right before the k-th launch, ev[2k + 1] right after
+// it, while 2k + 1 < n (host side; a failed record makes the call fail).
+struct LaunchTimer {
+    void *const *ev = nullptr;
+    int n = 0, k = 0;
+    cudaStream_t stream = nullptr;
+    bool failed = false;
+    void before()
+    {
+        if (2 * k + 1 < n)
+            failed |= cudaEventRecord(static_cast<cudaEvent_t>(ev[2 * k]), stream) != cudaSuccess;
+    }
+    void after()
+    {
+        if (2 * k + 1 < n)
+            failed |= cudaEventRecord(static_cast<cudaEvent_t>(ev[2 * k + 1]), stream) != cudaSuccess;
+        ++k;
+    }
+};
+
+// The launch `launch()` (one kernel) bracketed by the timer's next event pair.
+template <class F>
+cudaError_t timed(LaunchTimer *tm, F &&launch)
+{
+    if (tm)
+        tm->before();
+    const cudaError_t e = launch();
+    if (tm)
+        tm->after();
+    return e;
+}
+
+// The chunk-state, state-pass and output kernels, each bracketed by tm's events.
 cudaError_t launch_ssd(const ScanArgs &a, const SsdPlan &plan, const SsdGeom &g, int max_units,
-                       cudaStream_t stream);
+                       cudaStream_t stream, LaunchTimer *tm = nullptr);
 bool ssd_supported_chunk(int chunk);
 int ssd_tc_buffers(int chunk, int n_pad, int P, size_t smem_optin);   // 0: not supported
 int ssd_tc_tmem_cols(int n_pad, int P);

@@ -505,7 +505,7 @@ ssd_output_kernel(const ScanArgs a, const SsdPlan p, const SsdGeom sg)
 
 template <int Q>
 cudaError_t launch_ssd_q(const ScanArgs &a, const SsdPlan &plan, const SsdGeom &g, int max_units,
-                         cudaStream_t stream)
+                         cudaStream_t stream, LaunchTimer *tm)
 {
     const int hpg = a.H / a.G;
     const dim3 grid((unsigned)max_units, (unsigned)a.G, (unsigned)((hpg + g.heads_per_cta - 1) / g.heads_per_cta));
@@ -514,8 +514,11 @@ cudaError_t launch_ssd_q(const ScanArgs &a, const SsdPlan &plan, const SsdGeom &
     cudaError_t e = cudaFuncSetAttribute(state_k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g.smem_state);
     if (e != cudaSuccess)
         return e;
-    state_k<<<grid, kStateThreads, g.smem_state, stream>>>(a, plan, g);
-    if ((e = cudaGetLastError()) != cudaSuccess)
+    e = timed(tm, [&] {
+        state_k<<<grid, kStateThreads, g.smem_state, stream>>>(a, plan, g);
+        return cudaGetLastError();
+    });
+    if (e != cudaSuccess)
         return e;
 
     const long long slot4 = (long long)a.H * a.P * (a.N >> 2);
@@ -525,12 +528,15 @@ cudaError_t launch_ssd_q(const ScanArgs &a, const SsdPlan &plan, const SsdGeom &
     e = cudaFuncSetAttribute(ssd_state_pass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, pass_smem);
     if (e != cudaSuccess)
         return e;
-    ssd_state_pass_kernel<<<pgrid, kPassThreads, pass_smem, stream>>>(a, plan, max_units);
-    if ((e = cudaGetLastError()) != cudaSuccess)
+    e = timed(tm, [&] {
+        ssd_state_pass_kernel<<<pgrid, kPassThreads, pass_smem, stream>>>(a, plan, max_units);
+        return cudaGetLastError();
+    });
+    if (e != cudaSuccess)
         return e;
 
     if (g.use_tc)
-        return launch_ssd_output_tc(a, plan, g, max_units, stream);
+        return timed(tm, [&] { return launch_ssd_output_tc(a, plan, g, max_units, stream); });
     void (*out_k)(const ScanArgs, const SsdPlan, const SsdGeom) = nullptr;
     switch (a.P / 8) {
     case 2: out_k = ssd_output_kernel<Q, 2>; break;
@@ -546,8 +552,10 @@ cudaError_t launch_ssd_q(const ScanArgs &a, const SsdPlan &plan, const SsdGeom &
     e = cudaFuncSetAttribute(out_k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g.smem_out);
     if (e != cudaSuccess)
         return e;
-    out_k<<<grid, 2 * Q, g.smem_out, stream>>>(a, plan, g);
-    return cudaGetLastError();
+    return timed(tm, [&] {
+        out_k<<<grid, 2 * Q, g.smem_out, stream>>>(a, plan, g);
+        return cudaGetLastError();
+    });
 }
 
 }  // namespace
@@ -557,13 +565,13 @@ bool ssd_supported_chunk(int chunk) { return chunk == 64 || chunk == 128; }
 int ssd_max_head_dim() { return 128; }
 
 cudaError_t launch_ssd(const ScanArgs &a, const SsdPlan &plan, const SsdGeom &g, int max_units,
-                       cudaStream_t stream)
+                       cudaStream_t stream, LaunchTimer *tm)
 {
     if (a.P % 16 != 0 || a.P > ssd_max_head_dim())
         return cudaErrorInvalidValue;
     switch (plan.chunk) {
-    case 64: return launch_ssd_q<64>(a, plan, g, max_units, stream);
-    case 128: return launch_ssd_q<128>(a, plan, g, max_units, stream);
+    case 64: return launch_ssd_q<64>(a, plan, g, max_units, stream, tm);
+    case 128: return launch_ssd_q<128>(a, plan, g, max_units, stream, tm);
     default: return cudaErrorInvalidValue;
     }
 }

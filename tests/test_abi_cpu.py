@@ -190,6 +190,8 @@ def test_header_declares_the_options_entry_point_and_struct():
     (dict(gated_y=PTR), bd.SSM_ERR_INVALID_ARG),                       # no gate, no weight
     (dict(gated_y=PTR, gate_z=PTR, norm_weight=PTR, norm_eps=0.0), bd.SSM_ERR_INVALID_ARG),
     (dict(gated_y=PTR, gate_z=PTR + 4, norm_weight=PTR, norm_eps=1e-5), bd.SSM_ERR_INVALID_ARG),
+    (dict(n_launch_events=-2), bd.SSM_ERR_INVALID_ARG),                # negative event count
+    (dict(n_launch_events=2), bd.SSM_ERR_INVALID_ARG),                 # events without an array
 ])
 def test_options_rejected_on_the_host(lib, opts, expect):
     o = bd.Options(**opts)

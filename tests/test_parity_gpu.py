@@ -10,7 +10,7 @@ import torch
 import oracle
 from state_space_model_ssm_gb300 import binding as bd
 from state_space_model_ssm_gb300.workloads import Geometry, make_inputs, workload
-from tests.gpu_helpers import assert_parity, run_gpu
+from tests.gpu_helpers import SSD_TOL, assert_parity, run_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -418,3 +418,41 @@ def test_tensor_state_pass_needs_16_byte_aligned_x():
             y = call()
             torch.cuda.synchronize()
             assert_parity(inp, y.double().cpu().numpy(), state.double().cpu().numpy(), y_ref, s_ref)
+
+
+def test_launch_events_bracket_each_kernel():
+    """Timing events recorded around the segmented prefill's four launches (plan,
+    state pass, combine, full pass) and the SSD call's four; results unchanged."""
+    inp = workload("tiny")
+    y_ref, s_ref = oracle.scan_inputs(inp)
+    d = inp.to("cuda")
+    g = inp.geom
+    stream = torch.cuda.current_stream()
+
+    def events(n):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for e in evs:
+            e.record(stream)
+        return evs
+
+    t = _tuning(path=bd.PATH_PREFILL, seg=16)
+    nbytes = bd.workspace_bytes(inp.n_seqs, inp.n_tokens, g.n_heads, g.head_dim, g.d_state, g.n_groups, t)
+    ws = torch.empty(nbytes // 4, device="cuda")
+    state = d.state.clone()
+    evs = events(8)
+    y = bd.ssm_scan(state, d.x, d.dt, d.A, d.B, d.C, d.D, d.seq_starts, d.seq_lens, d.resume, tuning=t,
+                    workspace=ws, launch_events=evs)
+    torch.cuda.synchronize()
+    assert_parity(inp, y.double().cpu().numpy(), state.double().cpu().numpy(), y_ref, s_ref)
+    times = [evs[2 * k].elapsed_time(evs[2 * k + 1]) for k in range(4)]
+    assert all(ms >= 0.0 for ms in times)
+    # the pairs are in launch order: each launch starts after the previous one ended
+    assert all(evs[2 * k + 1].elapsed_time(evs[2 * k + 2]) >= 0.0 for k in range(3))
+
+    state = d.state.clone()
+    evs = events(8)
+    y = bd.ssm_scan_ssd(state, d.x, d.dt, d.A, d.B, d.C, d.D, d.seq_starts, d.seq_lens, d.resume, chunk=64,
+                        launch_events=evs)
+    torch.cuda.synchronize()
+    assert_parity(inp, y.double().cpu().numpy(), state.double().cpu().numpy(), y_ref, s_ref, tol=SSD_TOL)
+    assert all(evs[2 * k].elapsed_time(evs[2 * k + 1]) >= 0.0 for k in range(4))
