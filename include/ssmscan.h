@@ -58,7 +58,16 @@
  *                        misaligned pointer, bad tuning value;
  *   SSM_ERR_UNSUPPORTED  d_state not a multiple of 4, d_state > 1024;
  *   SSM_ERR_CUDA         a CUDA call or launch failed (cudaGetLastError);
- *   SSM_ERR_TIMEOUT      reserved for bounded device waits.
+ *   SSM_ERR_TIMEOUT      a bounded device wait gave up (the pipelined
+ *                        tensor-core kernels: the segments' state pass and the
+ *                        SSD output kernel).  Each such wait polls an mbarrier
+ *                        a bounded number of times (seconds); on giving up the
+ *                        kernel sets a status word in the workspace, waits for
+ *                        its copies and products in flight, frees its tensor
+ *                        memory and returns, so the context stays usable.  The
+ *                        word is read back (and this code returned) only under
+ *                        SSM_SCAN_CHECK=1.  SSM_SCAN_TEST_FAIL_WAITS=1 makes
+ *                        those waits give up at once (tests of this path).
  * n_seqs == 0 is a successful no-op.
  */
 #ifndef SSMSCAN_H

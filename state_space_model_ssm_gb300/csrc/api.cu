@@ -80,6 +80,20 @@ bool check_env()
     return v == 1;
 }
 
+// Test hook (SSM_SCAN_TEST_FAIL_WAITS=1, read once): the pipelined tensor-core
+// kernels' bounded waits give up at once, so a test sees the timeout path
+// (status word, SSM_ERR_TIMEOUT under SSM_SCAN_CHECK) without a stalled GPU.
+// Their drain of the copies and products in flight keeps its full bound.
+bool fail_waits_env()
+{
+    static int v = -1;
+    if (v < 0) {
+        const char *e = std::getenv("SSM_SCAN_TEST_FAIL_WAITS");
+        v = (e && e[0] && std::strcmp(e, "0") != 0) ? 1 : 0;
+    }
+    return v == 1;
+}
+
 // Debug mode: SSM_ERR_TIMEOUT when a kernel's bounded wait gave up (the
 // device status word is nonzero); synchronises the stream.
 int read_status(const int *status, cudaStream_t stream)
@@ -463,6 +477,7 @@ int scan_kernels(const ssm::ScanArgs &a, const ssm_scan_tuning &t, const DeviceI
     plan.seg_decay = reinterpret_cast<float *>(ws + pl.off_decay);
     plan.seg_state = reinterpret_cast<float *>(ws + pl.off_state);
     plan.status = reinterpret_cast<int *>(ws + pl.off_status);
+    plan.fail_waits = fail_waits_env() ? 1 : 0;
     const int mu = (int)pl.max_units;
     if (ssm::timed(tm, [&] { return ssm::launch_segment_plan(a, plan, mu, stream); }) != cudaSuccess)
         return SSM_ERR_CUDA;
@@ -649,7 +664,7 @@ int ssd_impl(float *state, const float *x, const float *dt, const float *A, cons
     seg.n_units = reinterpret_cast<const int *>(ws + L.off_n_units);
     seg.unit_base = reinterpret_cast<const int *>(ws + L.off_unit_base);
     seg.seg_len = L.chunk;
-    ssm::SsdPlan plan;
+    ssm::SsdPlan plan{};
     plan.units = seg.units;
     plan.n_units = seg.n_units;
     plan.unit_base = seg.unit_base;
@@ -657,6 +672,7 @@ int ssd_impl(float *state, const float *x, const float *dt, const float *A, cons
     plan.chunk_logdecay = reinterpret_cast<float *>(ws + L.off_decay);
     plan.chunk_state = reinterpret_cast<float *>(ws + L.off_state);
     plan.status = reinterpret_cast<int *>(ws + L.off_status);
+    plan.fail_waits = fail_waits_env() ? 1 : 0;
     seg.status = plan.status;               // zeroed by the plan kernel
     const int mu = (int)L.max_units;
     if (ssm::timed(&tm, [&] { return ssm::launch_segment_plan(a, seg, mu, stream); }) != cudaSuccess ||

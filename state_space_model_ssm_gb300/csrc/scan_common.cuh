@@ -147,6 +147,7 @@ struct SegmentPlan {
     float *seg_decay;         // [max_units][H]: prod dA over the segment
     int *status;              // device word (may be null): zeroed by the plan kernel, nonzero
                               // when a bounded wait of the tensor-core state pass gave up
+    int fail_waits;           // test hook: nonzero makes the pipeline's bounded waits give up at once
 };
 constexpr int kScanFull = 0;        // the scan with y
 constexpr int kScanStateOnly = 1;   // one segment's state from zero, no y
@@ -185,6 +186,7 @@ struct SsdPlan {
     float *chunk_state;       // [max_units][H][P][N]: chunk state, then the chunk's incoming state
     float *chunk_logdecay;    // [max_units][H]: sum of dt*A over the chunk
     int *status;              // device word: nonzero when a kernel's bounded wait gave up
+    int fail_waits;           // test hook: nonzero makes the pipeline's bounded waits give up at once
 };
 
 // Shared-memory strides (floats) and launch shape of the SSD kernels.

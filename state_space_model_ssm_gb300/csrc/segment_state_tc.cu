@@ -204,6 +204,8 @@ segment_state_tc_kernel(const ScanArgs a, const SegmentPlan plan, const __grid_c
     const uint32_t sbase = smem_u32(sm);
     uint64_t *full = reinterpret_cast<uint64_t *>(sm + L.bar);     // per stage: TMA boxes landed
     uint64_t *mmab = full + kSsStages;                             // per buffer: products done
+    uint64_t *drain = mmab + 2;                                    // after a failed wait: all products done
+    const long cap = plan.fail_waits ? 0 : kSpinLimit;             // polls of a pipeline wait
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + L.tslot);
     float *wts = reinterpret_cast<float *>(sm + L.wts);
     float *decs = reinterpret_cast<float *>(sm + L.dec);
@@ -217,6 +219,7 @@ segment_state_tc_kernel(const ScanArgs a, const SegmentPlan plan, const __grid_c
             mbar_init(full + i, 1);
         mbar_init(mmab, 1);
         mbar_init(mmab + 1, 1);
+        mbar_init(drain, 1);
         mbar_init_fence();
     }
     __syncthreads();
@@ -264,6 +267,7 @@ segment_state_tc_kernel(const ScanArgs a, const SegmentPlan plan, const __grid_c
             if (nc > 1)
                 issue(1);
         }
+        int issued = nc > 1 ? 2 : 1;                  // chunks whose TMA was started
         const float dt0 = load_dt(0), dt1 = load_dt(1);
         float dt_ahead = load_dt(2);                  // dt of chunk j + 2 at iteration j
         weights(0, dt0);
@@ -292,6 +296,7 @@ segment_state_tc_kernel(const ScanArgs a, const SegmentPlan plan, const __grid_c
                 if (j + 2 < nc)
                     issue(j + 2);                     // its stage held chunk j - 1, consumed before the barrier
             }
+            issued = min(nc, j + 3);
             if (j + 2 < nc)                           // slot j % 2 was read while chunk j was staged
                 weights(j + 2, dt_ahead);
             dt_ahead = dt_next;
@@ -299,7 +304,12 @@ segment_state_tc_kernel(const ScanArgs a, const SegmentPlan plan, const __grid_c
         const float dl = ssd::ex2(__shfl_sync(kFullMask, carry, 16 * (lane & 1)));   // lane hb: head hb's decay
         if (lane < HB)
             decs[lane] = dl;
-        __syncthreads_or(0);                          // the staging warps' epilogue decision
+        if (__syncthreads_or(0) && lane == 0) {      // the staging warps gave up: drain before TMEM is freed
+            commit(drain);                            // arrives once every product issued so far is done
+            mbar_wait(drain, 0);
+            for (int c = max(0, issued - kSsStages); c < issued; ++c)   // each stage's last TMA
+                mbar_wait(full + c % kSsStages, (uint32_t)((c / kSsStages) & 1));
+        }
         __syncthreads();
         return;
     }
@@ -323,9 +333,9 @@ segment_state_tc_kernel(const ScanArgs a, const SegmentPlan plan, const __grid_c
     for (int j = 0; j < nc; ++j) {
         const int b = j & 1;
         const int cnt = min(kSsQ, len - (nc - 1 - j) * kSsQ);   // tokens of the chunk (16 but the first)
-        ok = mbar_wait(full + st, (uint32_t)((j / kSsStages) & 1)) && ok;
+        ok = mbar_wait(full + st, (uint32_t)((j / kSsStages) & 1), cap) && ok;
         if (j >= 2) {                                 // buffer b: products of chunk j - 2 done
-            ok = mbar_wait(mmab + b, (uint32_t)(((j >> 1) - 1) & 1)) && ok;
+            ok = mbar_wait(mmab + b, (uint32_t)(((j >> 1) - 1) & 1), cap) && ok;
             fence_after();
         }
         const char *raw = sm + L.raw + st * L.stage;
@@ -346,16 +356,10 @@ segment_state_tc_kernel(const ScanArgs a, const SegmentPlan plan, const __grid_c
     }
 
     if (ok && last == nc - 1)                         // every product of the segment issued
-        ok = mbar_wait(mmab + (last & 1), (uint32_t)((last >> 1) & 1));
-    if (__syncthreads_or(!ok)) {
-        if (tid == 0) {
-            if (plan.status)
-                atomicExch(plan.status, 1);
-            if (last >= 0)                            // bounded waits for the products and copies in flight
-                mbar_wait(mmab + (last & 1), (uint32_t)((last >> 1) & 1));
-            for (int j = last + 1; j < min(nc, last + 3); ++j)
-                mbar_wait(full + j % kSsStages, (uint32_t)((j / kSsStages) & 1));
-        }
+        ok = mbar_wait(mmab + (last & 1), (uint32_t)((last >> 1) & 1), cap);
+    if (__syncthreads_or(!ok)) {                      // the driver warp drains the products and copies
+        if (tid == 0 && plan.status)
+            atomicExch(plan.status, 1);
     } else {
         fence_after();
         const uint32_t taddr = tlane;                 // state rows 32 quad .. +31 (row: this thread's)

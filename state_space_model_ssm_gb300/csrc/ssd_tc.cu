@@ -56,7 +56,7 @@ __device__ __forceinline__ bool compute_sync_or(bool v)
 
 // Shared-memory layout (bytes) of the block.
 struct TcLayout {
-    uint32_t BM, S[2], XR[2], XT, al, dts, fcol, bar, tslot, total;   // bar: 7 mbarriers
+    uint32_t BM, S[2], XR[2], XT, al, dts, fcol, bar, tslot, total;   // bar: 8 mbarriers
     uint32_t lc;      // k-chunk stride of the 128-row tiles (B, M)
     uint32_t ls;      // k-chunk stride of S_in (P rows)
     uint32_t lx;      // k-chunk stride of the transposed x tile (P rows + 16 bytes)
@@ -203,6 +203,8 @@ ssd_output_tc_kernel(const ScanArgs a, const SsdPlan p, const SsdGeom sg)
     float *fcol = reinterpret_cast<float *>(sm + L.fcol);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L.bar);
     uint64_t *bar_g = bars, *bar_mma = bars + 1, *bar_b = bars + 2;
+    uint64_t *drain = bars + 7;                       // after a failed wait: all products done
+    const long cap = p.fail_waits ? 0 : tc::kSpinLimit;   // polls of a pipeline wait
     uint64_t *full = bars + 3, *empty = bars + 5;      // per buffer
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + L.tslot);
     constexpr float kLog2e = 1.4426950408889634f;
@@ -214,6 +216,7 @@ ssd_output_tc_kernel(const ScanArgs a, const SsdPlan p, const SsdGeom sg)
     if (tid == 0) {
         mbar_init(bar_g, 1);
         mbar_init(bar_mma, 1);
+        mbar_init(drain, 1);
         mbar_init(bar_b, 32 * kTcProducers);
         for (int i = 0; i < 2; ++i) {
             mbar_init(full + i, 32 * kTcProducers);
@@ -231,7 +234,7 @@ ssd_output_tc_kernel(const ScanArgs a, const SsdPlan p, const SsdGeom sg)
         cp_async_arrive(bar_b);
         for (int k = 0; k < nh; ++k) {
             const int b = nbuf == 2 ? (k & 1) : 0;
-            if (k >= nbuf && !mbar_wait(empty + b, (uint32_t)((k / nbuf - 1) & 1)))
+            if (k >= nbuf && !mbar_wait(empty + b, (uint32_t)((k / nbuf - 1) & 1), cap))
                 break;                                // the compute warps gave up
             const int h = g * hpg + hl0 + k;
             kmajor_copy(sm + (b ? L.S[1] : L.S[0]), L.ls, p.chunk_state + ((size_t)blockIdx.x * a.H + h) * (size_t)P * N,
@@ -274,10 +277,10 @@ ssd_output_tc_kernel(const ScanArgs a, const SsdPlan p, const SsdGeom sg)
         }
         asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
     }
-    bool ok = mbar_wait(bar_b, 0);                    // B landed
-    uint64_t *wait_bar = bar_b;                       // the barrier a failed wait was on
-    uint32_t wait_par = 0;
-    if (!compute_sync_or(!ok)) {
+    // ok is the same in every compute thread: each wait's outcome passes through a
+    // barrier OR before anyone acts on it
+    bool ok = !compute_sync_or(!mbar_wait(bar_b, 0, cap));   // B landed
+    if (ok) {
         kmajor_round(BMt, L.lc, kTcQ, Np4, warp, lane);
         fence_async_smem();
         tc::fence_before();
@@ -310,11 +313,10 @@ ssd_output_tc_kernel(const ScanArgs a, const SsdPlan p, const SsdGeom sg)
                 fcol[s] = cd.d[r] * ex2(ar - cd.a[r] * kLog2e);
             }
         }
-        wait_bar = full + b;
-        wait_par = (uint32_t)((k / nbuf) & 1);
-        ok = mbar_wait(wait_bar, wait_par);           // S_in and x of head k landed
-        if (compute_sync_or(!ok))
+        if (compute_sync_or(!mbar_wait(full + b, (uint32_t)((k / nbuf) & 1), cap))) {
+            ok = false;                               // S_in and x of head k never landed
             break;
+        }
         kmajor_round(St, L.ls, P, Np4, warp, lane);
         xraw_transpose(XTt, L.lx, XRt, P, tid);
         fence_async_smem();
@@ -326,13 +328,11 @@ ssd_output_tc_kernel(const ScanArgs a, const SsdPlan p, const SsdGeom sg)
             for (int kk = 0; kk < ksteps_n; ++kk)
                 tc::mma_ts(tm_yi, tm_c + 8 * kk, smem_desc(smem_u32(St) + 2 * kk * L.ls, L.ls, 128), id, kk > 0);
         }
-        if (k == 0) {
-            wait_bar = bar_g;
-            wait_par = 0;
-            ok = mbar_wait(bar_g, 0);                 // G formed; B no longer needed
-        }
-        if (compute_sync_or(!ok))
+        const bool g_done = k > 0 || mbar_wait(bar_g, 0, cap);   // G formed; B no longer needed
+        if (compute_sync_or(!g_done)) {
+            ok = false;
             break;
+        }
         tc::fence_after();
 
         // M = G dt_s exp(a_t - a_s) for s <= t, into the A tile (reusing B's
@@ -391,11 +391,10 @@ ssd_output_tc_kernel(const ScanArgs a, const SsdPlan p, const SsdGeom sg)
                        smem_desc(smem_u32(XTt) + 2 * kk * L.lx, L.lx, 128), id, kk > 0);
             tc::commit(bar_mma);
         }
-        wait_bar = bar_mma;
-        wait_par = (uint32_t)(k & 1);
-        ok = mbar_wait(bar_mma, wait_par);
-        if (compute_sync_or(!ok))
+        if (compute_sync_or(!mbar_wait(bar_mma, (uint32_t)(k & 1), cap))) {
+            ok = false;
             break;
+        }
         tc::fence_after();
 
         // y = exp(a_t) Yi + Yx + D x for this thread's row and column half (every
@@ -430,9 +429,10 @@ ssd_output_tc_kernel(const ScanArgs a, const SsdPlan p, const SsdGeom sg)
         compute_sync();                               // TMEM accumulators, M and x^T free
     }
     if (!ok) {                                        // a copy or product never completed
-        if (tid == 0) {
+        if (tid == 0) {                               // the thread that issued every product
             atomicExch(p.status, 1);
-            mbar_wait(wait_bar, wait_par);            // one more bounded wait for it
+            tc::commit(drain);                        // arrives once all of them are done
+            mbar_wait(drain, 0);
         }
         compute_sync();
     }

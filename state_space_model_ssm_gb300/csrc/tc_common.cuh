@@ -139,10 +139,10 @@ __device__ __forceinline__ void cp_async_arrive(uint64_t *mbar)
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(mbar)) : "memory");
 }
 
-// Poll an mbarrier phase; false after kSpinLimit polls.
-__device__ __forceinline__ bool mbar_wait(uint64_t *mbar, uint32_t parity)
+// Poll an mbarrier phase; false after `limit` polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t *mbar, uint32_t parity, long limit = kSpinLimit)
 {
-    for (long it = 0; it < kSpinLimit; ++it) {
+    for (long it = 0; it < limit; ++it) {
         uint32_t done;
         asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
                      "selp.u32 %0, 1, 0, p;\n\t}\n"
