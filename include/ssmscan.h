@@ -116,7 +116,8 @@ enum {
  *                    per SM and warps loop over the remaining rows
  *   segment_tokens   SSM_PATH_PREFILL with a workspace (ssm_scan_ws): length of
  *                    the time segments long sequences are cut into (a multiple
- *                    of the chunk); 0 = automatic, < 0 = never segment
+ *                    of the chunk; an automatic chunk is the largest of 32, 16,
+ *                    ... that divides it); 0 = automatic, < 0 = never segment
  *   segment_state    how the state pass of the time segments runs
  *                    (SSM_SEGMENT_STATE_*); ignored without segments
  */
@@ -345,9 +346,11 @@ size_t ssm_scan_ssd_workspace_bytes(int n_seqs, int n_tokens, int n_heads,
  *   - The first call on a device looks up the scratch's device address (a
  *     cudaGetSymbolAddress with that device current) and caches it; make that
  *     first call before any stream capture.
- *   - Calls whose plan needs more scratch than SSM_SCAN_STATIC_SCRATCH_BYTES
- *     (very long or many long sequences) return SSM_ERR_UNSUPPORTED before any
- *     launch; ssm_scan_ws with a caller workspace has no such limit.
+ *   - When the automatic plan's segment states would not fit the scratch
+ *     (very long or many long sequences, large states), the call runs with
+ *     longer time segments (1024 tokens, doubled until they fit) or without
+ *     segments: the same results, less parallelism than ssm_scan_ws with a
+ *     workspace of the size ssm_scan_workspace_bytes asks for.
  *   - Every call in the process shares the scratch, which keeps the last
  *     call's contents (nothing in it needs to start at zero).  Calls whose GPU
  *     work overlaps, on two streams or from two threads, race on it: the

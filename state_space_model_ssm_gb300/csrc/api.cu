@@ -213,8 +213,9 @@ int plan_prefill(const ssm_scan_tuning &t, bool scaled, int n_seqs, int n_tokens
         if ((long long)g.chunk * g.heads_cap > dt_cap || smem_of(g) > (size_t)dev.smem_optin)
             return SSM_ERR_INVALID_ARG;
     } else {
-        g.chunk = scaled ? 16 : 32;
-        while (g.chunk > 1 && ((long long)g.chunk * g.heads_cap > dt_cap || smem_of(g) > smem_cap))
+        g.chunk = 32;                       // an explicit segment length must be a multiple of it
+        while (g.chunk > 1 && ((long long)g.chunk * g.heads_cap > dt_cap || smem_of(g) > smem_cap ||
+                               (scaled && t.segment_tokens > 0 && t.segment_tokens % g.chunk != 0)))
             g.chunk >>= 1;
         if (smem_of(g) > (size_t)dev.smem_optin)
             return SSM_ERR_UNSUPPORTED;
@@ -225,8 +226,11 @@ int plan_prefill(const ssm_scan_tuning &t, bool scaled, int n_seqs, int n_tokens
     pl.vpl = vpl;
 
     // Time segments: only the rescaled kernel has the state pass.  Automatic
-    // choice: enough (sequence, segment) units for about six consumer warps
-    // per SM sub-partition.
+    // choice (the host does not see the lengths): about as many units as
+    // sequences, and at least enough for about six consumer warps per SM
+    // sub-partition, so that the tokens spread evenly over the units and no
+    // long sequence of a ragged batch runs alone; off when no sequence can be
+    // long enough to split.
     if (scaled && allow_segments && t.segment_tokens >= 0 && n_tokens > 0) {
         int seg = 0;
         if (t.segment_tokens > 0) {
@@ -236,14 +240,12 @@ int plan_prefill(const ssm_scan_tuning &t, bool scaled, int n_seqs, int n_tokens
         } else {
             const long long warps_per_unit = (long long)G * g.runs_per_group * (threads / 32);
             const long long target = 6LL * 4 * dev.sms;      // consumer warps to keep resident
-            if ((long long)n_seqs * warps_per_unit < target) {
-                const long long want = (target + warps_per_unit - 1) / warps_per_unit;
-                long long L = ((long long)n_tokens + want - 1) / want;
-                L = std::max<long long>(L, 4LL * g.chunk);
-                seg = (int)(((L + g.chunk - 1) / g.chunk) * g.chunk);
-                if (seg >= n_tokens)
-                    seg = 0;
-            }
+            const long long want = std::max<long long>((target + warps_per_unit - 1) / warps_per_unit, n_seqs);
+            long long L = ((long long)n_tokens + want - 1) / want;
+            L = std::max<long long>(L, 4LL * g.chunk);
+            L = ((L + g.chunk - 1) / g.chunk) * g.chunk;
+            const long long longest = (long long)n_tokens - std::max(0, n_seqs - 1);   // every other one >= 1
+            seg = L < longest ? (int)L : 0;
         }
         if (seg > 0) {
             // The state pass: tensor cores where the shapes fit, unless the

@@ -6,7 +6,8 @@
 // that must never enter the allocator).  This entry point gives them the
 // time-segmented prefill of ssm_scan_ws with the library's own scratch: a
 // fixed array in device global memory that exists from module load until the
-// process exits.  Nothing here calls cudaMalloc, cudaFree or any allocating
+// process exits.  A plan whose segment states would not fit it runs with
+// longer segments, or none.  Nothing here calls cudaMalloc, cudaFree or any allocating
 // library routine.
 //
 // The scratch is shared by every call in the process on a device and keeps
@@ -59,16 +60,28 @@ extern "C" int ssm_scan_static(float *state_slots, const float *x, const float *
                                const int32_t *resume_flags, int n_seqs, int n_tokens, int n_heads,
                                int head_dim, int d_state, int n_groups, void *stream)
 {
-    // Scratch this call's automatic plan needs (0: no time segments).
-    const size_t need = ssm_scan_workspace_bytes(n_seqs, n_tokens, n_heads, head_dim, d_state,
-                                                 n_groups, nullptr);
-    if (need > (size_t)SSM_SCAN_STATIC_SCRATCH_BYTES)
-        return SSM_ERR_UNSUPPORTED;
+    // The automatic plan, or, when its segment states do not fit the scratch,
+    // longer segments (fewer states: 1024 tokens, doubled until they fit), or
+    // none.  Host arithmetic only; nothing is launched before the plan fits.
+    ssm_scan_tuning t = {};
+    const size_t cap = (size_t)SSM_SCAN_STATIC_SCRATCH_BYTES;
+    if (ssm_scan_workspace_bytes(n_seqs, n_tokens, n_heads, head_dim, d_state, n_groups, &t) > cap) {
+        t.segment_tokens = -1;                        // no segments: no scratch
+        for (long long seg = 1024; seg < n_tokens; seg *= 2) {
+            ssm_scan_tuning c = {};
+            c.segment_tokens = (int)seg;
+            const size_t need = ssm_scan_workspace_bytes(n_seqs, n_tokens, n_heads, head_dim, d_state,
+                                                         n_groups, &c);
+            if (need > 0 && need <= cap) {
+                t = c;
+                break;
+            }
+        }
+    }
     void *scratch = nullptr;
     const int rc = static_scratch(&scratch);
     if (rc != SSM_OK)
         return rc;
     return ssm_scan_ws(state_slots, x, dt, A, B, C, D, y, seq_starts, seq_lens, resume_flags, n_seqs,
-                       n_tokens, n_heads, head_dim, d_state, n_groups, nullptr, scratch,
-                       (size_t)SSM_SCAN_STATIC_SCRATCH_BYTES, stream);
+                       n_tokens, n_heads, head_dim, d_state, n_groups, &t, scratch, cap, stream);
 }
