@@ -677,8 +677,13 @@ int ssd_impl(float *state, const float *x, const float *dt, const float *A, cons
     plan.fail_waits = fail_waits_env() ? 1 : 0;
     seg.status = plan.status;               // zeroed by the plan kernel
     const int mu = (int)L.max_units;
+    // The chunk states on the tensor-core state pass where its shapes fit (TMA
+    // descriptors encoded before any launch), else on the mma.sync kernel.
+    ssm::SegStateMaps maps;
+    const bool tc_states = ssm::segment_state_tc_supported(N, P, (size_t)dev.smem_optin) &&
+                           ssm::segment_state_tc_maps(a, &maps);
     if (ssm::timed(&tm, [&] { return ssm::launch_segment_plan(a, seg, mu, stream); }) != cudaSuccess ||
-        ssm::launch_ssd(a, plan, L.g, mu, stream, &tm) != cudaSuccess)
+        ssm::launch_ssd(a, plan, L.g, mu, stream, &tm, tc_states ? &maps : nullptr) != cudaSuccess)
         return SSM_ERR_CUDA;
     if (o.gated_y && n_tokens > 0 &&
         ssm::timed(&tm, [&] {

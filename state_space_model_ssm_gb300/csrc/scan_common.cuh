@@ -148,6 +148,8 @@ struct SegmentPlan {
     int *status;              // device word (may be null): zeroed by the plan kernel, nonzero
                               // when a bounded wait of the tensor-core state pass gave up
     int fail_waits;           // test hook: nonzero makes the pipeline's bounded waits give up at once
+    int chunk_states;         // tensor-core state pass for the SSD form: every unit (each sequence's
+                              // last too), no slot term, seg_decay = sum of dt*A (its log)
 };
 constexpr int kScanFull = 0;        // the scan with y
 constexpr int kScanStateOnly = 1;   // one segment's state from zero, no y
@@ -238,8 +240,10 @@ cudaError_t timed(LaunchTimer *tm, F &&launch)
 }
 
 // The chunk-state, state-pass and output kernels, each bracketed by tm's events.
+// With state_maps the chunk states run on the tensor-core state pass
+// (segment_state_tc.cu), else on the mma.sync chunk-state kernel.
 cudaError_t launch_ssd(const ScanArgs &a, const SsdPlan &plan, const SsdGeom &g, int max_units,
-                       cudaStream_t stream, LaunchTimer *tm = nullptr);
+                       cudaStream_t stream, LaunchTimer *tm = nullptr, const SegStateMaps *state_maps = nullptr);
 bool ssd_supported_chunk(int chunk);
 int ssd_tc_buffers(int chunk, int n_pad, int P, size_t smem_optin);   // 0: not supported
 int ssd_tc_tmem_cols(int n_pad, int P);

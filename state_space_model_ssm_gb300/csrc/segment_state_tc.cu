@@ -74,7 +74,8 @@ struct SsLayout {
     uint32_t x_lo, buf;
     uint32_t raw, rx, stage;
     uint32_t bar, tslot, total;
-    uint32_t wts, dec;        // weights of two chunks [2][32] (lane = head * 16 + token), decays [HB]
+    uint32_t wts, dec;        // weights of two chunks [2][32] (lane = head * 16 + token); decays [HB],
+                              // then their logs [HB] at dec + 16
     uint32_t lx;              // K-cell stride of the X tiles (nx rows)
 };
 
@@ -92,7 +93,7 @@ __host__ __device__ constexpr SsLayout ss_layout(int nx)
     L.tslot = L.bar + 8 * sizeof(uint64_t);
     L.wts = L.tslot + 16;
     L.dec = L.wts + 2 * 32 * 4;
-    L.total = L.dec + 16;
+    L.total = L.dec + 32;
     return L;
 }
 
@@ -193,12 +194,22 @@ segment_state_tc_kernel(const ScanArgs a, const SegmentPlan plan, const __grid_c
     const int seq = us.x, seg = us.y;
     const int seq_len = a.seq_lens[seq];
     const int nseg = max(1, (seq_len + plan.seg_len - 1) / plan.seg_len);
-    if (seg >= nseg - 1)
+    if (seg >= nseg - 1 && !plan.chunk_states)
         return;                                       // the last segment needs no state pass
     const int len = min(plan.seg_len, seq_len - seg * plan.seg_len);
     const int nc = (len + kSsQ - 1) / kSsQ;
     const int tok0 = a.seq_starts[seq] + seg * plan.seg_len;
     const int P = a.P, N = a.N, H = a.H;
+    if (nc <= 0) {                                    // an empty sequence (chunk states): state 0, sum 0
+        for (int hb = 0; hb < HB; ++hb) {
+            float *dst = plan.seg_state + ((size_t)unit * H + h0 + hb) * P * N;
+            for (int i = threadIdx.x; i < P * N; i += kSsBlock)
+                dst[i] = 0.f;
+        }
+        if (threadIdx.x < HB)
+            plan.seg_decay[(size_t)unit * H + h0 + threadIdx.x] = plan.chunk_states ? 0.f : 1.f;
+        return;
+    }
     const int grp = h0 / (H / a.G);
     char *sm = reinterpret_cast<char *>(ss_smem);
     const uint32_t sbase = smem_u32(sm);
@@ -301,9 +312,11 @@ segment_state_tc_kernel(const ScanArgs a, const SegmentPlan plan, const __grid_c
                 weights(j + 2, dt_ahead);
             dt_ahead = dt_next;
         }
-        const float dl = ssd::ex2(__shfl_sync(kFullMask, carry, 16 * (lane & 1)));   // lane hb: head hb's decay
-        if (lane < HB)
-            decs[lane] = dl;
+        const float cl = __shfl_sync(kFullMask, carry, 16 * (lane & 1));   // lane hb: head hb's log2 decay
+        if (lane < HB) {
+            decs[lane] = ssd::ex2(cl);
+            decs[4 + lane] = cl * 0.6931471805599453f;   // the natural log: sum of dt A
+        }
         if (__syncthreads_or(0) && lane == 0) {      // the staging warps gave up: drain before TMEM is freed
             commit(drain);                            // arrives once every product issued so far is done
             mbar_wait(drain, 0);
@@ -363,7 +376,7 @@ segment_state_tc_kernel(const ScanArgs a, const SegmentPlan plan, const __grid_c
     } else {
         fence_after();
         const uint32_t taddr = tlane;                 // state rows 32 quad .. +31 (row: this thread's)
-        const bool from_slot = seg == 0 && a.resume[seq] != 0;
+        const bool from_slot = !plan.chunk_states && seg == 0 && a.resume[seq] != 0;
         constexpr int cw = nx / 2;
 #pragma unroll
         for (int c0 = 0; c0 < cw; c0 += 16) {
@@ -389,7 +402,7 @@ segment_state_tc_kernel(const ScanArgs a, const SegmentPlan plan, const __grid_c
             }
         }
         if (tid < HB)
-            plan.seg_decay[(size_t)unit * H + h0 + tid] = decs[tid];
+            plan.seg_decay[(size_t)unit * H + h0 + tid] = plan.chunk_states ? decs[4 + tid] : decs[tid];
     }
     fence_before();
     __syncthreads();

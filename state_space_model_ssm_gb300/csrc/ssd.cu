@@ -505,19 +505,36 @@ ssd_output_kernel(const ScanArgs a, const SsdPlan p, const SsdGeom sg)
 
 template <int Q>
 cudaError_t launch_ssd_q(const ScanArgs &a, const SsdPlan &plan, const SsdGeom &g, int max_units,
-                         cudaStream_t stream, LaunchTimer *tm)
+                         cudaStream_t stream, LaunchTimer *tm, const SegStateMaps *state_maps)
 {
     const int hpg = a.H / a.G;
     const dim3 grid((unsigned)max_units, (unsigned)a.G, (unsigned)((hpg + g.heads_per_cta - 1) / g.heads_per_cta));
 
-    auto state_k = ssd_chunk_state_kernel<Q>;
-    cudaError_t e = cudaFuncSetAttribute(state_k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g.smem_state);
-    if (e != cudaSuccess)
-        return e;
-    e = timed(tm, [&] {
-        state_k<<<grid, kStateThreads, g.smem_state, stream>>>(a, plan, g);
-        return cudaGetLastError();
-    });
+    cudaError_t e;
+    if (state_maps) {
+        // The chunk states on the tensor cores: the state pass of the time
+        // segments with the chunk as segment, for every chunk (split TF32).
+        SegmentPlan sp{};
+        sp.units = plan.units;
+        sp.n_units = plan.n_units;
+        sp.unit_base = plan.unit_base;
+        sp.seg_len = plan.chunk;
+        sp.seg_state = plan.chunk_state;
+        sp.seg_decay = plan.chunk_logdecay;
+        sp.status = plan.status;
+        sp.fail_waits = plan.fail_waits;
+        sp.chunk_states = 1;
+        e = timed(tm, [&] { return launch_segment_state_tc(a, sp, *state_maps, max_units, stream); });
+    } else {
+        auto state_k = ssd_chunk_state_kernel<Q>;
+        e = cudaFuncSetAttribute(state_k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g.smem_state);
+        if (e != cudaSuccess)
+            return e;
+        e = timed(tm, [&] {
+            state_k<<<grid, kStateThreads, g.smem_state, stream>>>(a, plan, g);
+            return cudaGetLastError();
+        });
+    }
     if (e != cudaSuccess)
         return e;
 
@@ -565,13 +582,13 @@ bool ssd_supported_chunk(int chunk) { return chunk == 64 || chunk == 128; }
 int ssd_max_head_dim() { return 128; }
 
 cudaError_t launch_ssd(const ScanArgs &a, const SsdPlan &plan, const SsdGeom &g, int max_units,
-                       cudaStream_t stream, LaunchTimer *tm)
+                       cudaStream_t stream, LaunchTimer *tm, const SegStateMaps *state_maps)
 {
     if (a.P % 16 != 0 || a.P > ssd_max_head_dim())
         return cudaErrorInvalidValue;
     switch (plan.chunk) {
-    case 64: return launch_ssd_q<64>(a, plan, g, max_units, stream, tm);
-    case 128: return launch_ssd_q<128>(a, plan, g, max_units, stream, tm);
+    case 64: return launch_ssd_q<64>(a, plan, g, max_units, stream, tm, state_maps);
+    case 128: return launch_ssd_q<128>(a, plan, g, max_units, stream, tm, state_maps);
     default: return cudaErrorInvalidValue;
     }
 }
