@@ -155,17 +155,28 @@ int plan_prefill(const ssm_scan_tuning &t, bool scaled, int n_seqs, int n_tokens
     auto supported = scaled ? ssm::prefill_scaled_supported : ssm::prefill_supported;
     int lanes, rpt;
     if (scaled) {
-        // About 8 state elements of a row per lane, and up to 4 rows per lane
-        // (32 state registers) so that each B/C value read from shared memory
-        // feeds several rows.  The rows of a lane must share a head: RPT | P.
-        lanes = t.lanes_per_row ? t.lanes_per_row : std::min(32, pow2ceil((N + 7) / 8));
-        rpt = t.rows_per_thread;
-        if (!rpt) {
-            rpt = 4;
-            while (rpt > 1 && (P % rpt != 0 || rpt > lanes ||
-                               pick_vpl(N4, lanes, rpt, supported) * 4 * rpt > 32 ||
-                               pick_vpl(N4, lanes, rpt, supported) == 0))
-                rpt >>= 1;
+        // About 16 state elements of a row per lane and up to 4 rows per lane
+        // (at most 64 state registers): each B/C value read from shared memory
+        // feeds several rows, and the y reduction spans few lanes.  Where no
+        // compiled kernel has that shape, about 8 elements per lane.  The rows
+        // of a lane must share a head: RPT | P.
+        const int cand[2] = {std::min(32, pow2ceil((N + 15) / 16)), std::min(32, pow2ceil((N + 7) / 8))};
+        lanes = rpt = 0;
+        for (int ci = 0; ci < 2 && !rpt; ++ci) {
+            const int l = t.lanes_per_row ? t.lanes_per_row : cand[ci];
+            for (int r = t.rows_per_thread ? t.rows_per_thread : 4; r >= 1 && !rpt; r >>= 1) {
+                const int v = pick_vpl(N4, l, r, supported);
+                if (P % r == 0 && r <= l && v > 0 && v * 4 * r <= 64) {
+                    lanes = l;
+                    rpt = r;
+                }
+                if (t.rows_per_thread)
+                    break;
+            }
+        }
+        if (!rpt) {                          // an explicit shape the rules above reject
+            lanes = t.lanes_per_row ? t.lanes_per_row : cand[1];
+            rpt = t.rows_per_thread ? t.rows_per_thread : 1;
         }
         if (P % rpt != 0)
             return SSM_ERR_INVALID_ARG;
@@ -213,7 +224,10 @@ int plan_prefill(const ssm_scan_tuning &t, bool scaled, int n_seqs, int n_tokens
         if ((long long)g.chunk * g.heads_cap > dt_cap || smem_of(g) > (size_t)dev.smem_optin)
             return SSM_ERR_INVALID_ARG;
     } else {
-        g.chunk = 32;                       // an explicit segment length must be a multiple of it
+        // 16 tokens for the rescaled kernel: a chunk's running decay seldom
+        // crosses a re-anchor point, so its tokens run in straight-line groups
+        // of four.  An explicit segment length must be a multiple of the chunk.
+        g.chunk = scaled ? 16 : 32;
         while (g.chunk > 1 && ((long long)g.chunk * g.heads_cap > dt_cap || smem_of(g) > smem_cap ||
                                (scaled && t.segment_tokens > 0 && t.segment_tokens % g.chunk != 0)))
             g.chunk >>= 1;

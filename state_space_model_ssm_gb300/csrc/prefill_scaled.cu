@@ -32,6 +32,17 @@
 //    FULL[s] when slot s holds a staged chunk, EMPTY[s] when the consumers are
 //    done with it.
 //
+// 3. Token runs.  Consumers take a chunk's tokens in runs of eight with no
+//    anchor after the run's first token (the rescale of an anchor at the first
+//    token happens before the run), compiled as straight-line code so that the
+//    next token's shared-memory reads overlap the current token's arithmetic
+//    and reduction; tokens outside such runs go one at a time.  The default
+//    shape gives a lane 16 elements of each of 4 rows (8 lanes per row at
+//    d_state 128): 64 state registers, B/C reads shared by 4 rows and a
+//    three-step shuffle reduction.  Every lane ends the reduction holding its
+//    row's full sum, so all lanes of a row store y (the same value) and the
+//    store needs no divergent branch.
+//
 // The rescaling is an algebraic identity of the recurrence defined by "The
 // llama journey", Day 14 (decay exp(dt*A), input dt*x*B, y from the updated
 // state); only the rounding differs from the direct form.
@@ -223,26 +234,59 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan
         // Per-lane walk over (token, column) items in steps of 32 without
         // divisions: start at (lane / width, lane % width), step (32 / width, 32 % width).
         const int bt0 = lane / N4, bv0 = lane - bt0 * N4, bdt = 32 / N4, bdv = 32 - bdt * N4;
-        const int xt0 = lane / nrows, xv0 = lane - xt0 * nrows, xdt = 32 / nrows, xdv = 32 - xdt * nrows;
+        // x moves in 16-byte pieces when the block's rows start on 16 bytes in
+        // global and shared memory, else in 4-byte pieces; xw pieces per token.
+        const bool x16 = ((r0 | nrows | geo.rows_per_cta) & 3) == 0 && (HP & 3) == 0 &&
+                         (reinterpret_cast<uintptr_t>(a.x) & 15) == 0;
+        const int xw = x16 ? nrows >> 2 : nrows;
+        const int xt0 = lane / xw, xv0 = lane - xt0 * xw, xdt = 32 / xw, xdv = 32 - xdt * xw;
         auto stage = [&](int c0, int b) {
             const int t0 = c0 * geo.chunk;
             const int cnt = min(geo.chunk, len - t0);
             const long long tok0 = (long long)tok_start + t0;
             float *sB = sm.B(b), *sC = sm.C(b), *sX = sm.X(b);
-            for (int t = bt0, v = bv0; t < cnt;) {
-                const long long goff = (tok0 + t) * tokN + 4 * v;
-                cp_async16(sB + t * N + 4 * v, Bg + goff);
-                if (kFull)
-                    cp_async16(sC + t * N + 4 * v, Cg + goff);
-                t += bdt;
-                v += bdv;
-                if (v >= N4) { v -= N4; ++t; }
+            if (N4 % 32 == 0) {
+                // lane = float4 columns lane, lane + 32, ... of every token's row
+                const float *gB = Bg + tok0 * tokN + 4 * lane;
+                const float *gC = Cg + tok0 * tokN + 4 * lane;
+                float *dB = sB + 4 * lane, *dC = sC + 4 * lane;
+                for (int t = 0; t < cnt; ++t) {
+                    for (int v = 0; v < N4; v += 32) {
+                        cp_async16(dB + 4 * v, gB + 4 * v);
+                        if (kFull)
+                            cp_async16(dC + 4 * v, gC + 4 * v);
+                    }
+                    gB += tokN;
+                    gC += tokN;
+                    dB += N;
+                    dC += N;
+                }
+            } else {
+                for (int t = bt0, v = bv0; t < cnt;) {
+                    const long long goff = (tok0 + t) * tokN + 4 * v;
+                    cp_async16(sB + t * N + 4 * v, Bg + goff);
+                    if (kFull)
+                        cp_async16(sC + t * N + 4 * v, Cg + goff);
+                    t += bdt;
+                    v += bdv;
+                    if (v >= N4) { v -= N4; ++t; }
+                }
             }
-            for (int t = xt0, r = xv0; t < cnt;) {
-                cp_async4(sX + t * geo.rows_per_cta + r, a.x + (tok0 + t) * HP + r0 + r);
-                t += xdt;
-                r += xdv;
-                if (r >= nrows) { r -= nrows; ++t; }
+            const float *gx = a.x + tok0 * HP + r0;
+            if (x16) {
+                for (int t = xt0, r = xv0; t < cnt;) {
+                    cp_async16(sX + t * geo.rows_per_cta + 4 * r, gx + t * HP + 4 * r);
+                    t += xdt;
+                    r += xdv;
+                    if (r >= xw) { r -= xw; ++t; }
+                }
+            } else {
+                for (int t = xt0, r = xv0; t < cnt;) {
+                    cp_async4(sX + t * geo.rows_per_cta + r, gx + t * HP + r);
+                    t += xdt;
+                    r += xdv;
+                    if (r >= xw) { r -= xw; ++t; }
+                }
             }
             cp_async_commit();
         };
@@ -327,7 +371,7 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan
     const int hl = (r0 + rl) / P - h0;
     const float Dv = __ldg(a.D + h0 + hl);
     const int yq = reduced_row<LANES, RPT>(j);               // row of this lane's reduced sum
-    const bool ywriter = kFull && reduced_writer<LANES, RPT>(j) && rvalid;
+    const bool ystore = kFull && rvalid;
 
     // ---- A2 state load: U = S at the start (slot, segment plan, or zero) ----
     float2 u[RPT][VPL][2];
@@ -352,14 +396,20 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan
         }
     }
 
+    // Per-token strides of the staged operands, in floats.  With the exact
+    // shapes N is a compile-time constant, so the B and C reads of a group of
+    // tokens take immediate offsets from one pointer.
+    const int Ns = EXACT ? 4 * LANES * VPL : N;
+    const int xs = geo.rows_per_cta, hc = geo.heads_cap;
+
     for (int c = 0; c < n_chunks; ++c) {
         const int b = c % kSlots;
         bar_sync(kBarFull + b, nthr);
         const int cnt = min(geo.chunk, len - c * geo.chunk);
-        const float *__restrict__ sB = sm.B(b);
-        const float *__restrict__ sC = sm.C(b);
-        const float *__restrict__ sX = sm.X(b);
-        const float4 *__restrict__ sCf = sm.Coef(b) + hl;
+        const float *__restrict__ pB = sm.B(b) + 4 * j;      // this lane's first float4 of a token's B
+        const float *__restrict__ pC = sm.C(b) + 4 * j;
+        const float4 *__restrict__ pCf = sm.Coef(b) + hl;
+        const float *__restrict__ pX = sm.X(b) + rl;
         float *yrow = a.y + ((long long)tok_start + c * geo.chunk) * HP + r0 + rl + yq;
 
         // Shared-memory operands of one token.
@@ -368,27 +418,35 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan
             float xv[RPT];
             float4 b[VPL], c[VPL];
         };
-        auto load_token = [&](int tt, TokenIn &in) {
-            in.cf = sCf[tt * geo.heads_cap];
-            load_rows<RPT>(in.xv, sX + tt * geo.rows_per_cta + rl);
-            const float *bt = sB + tt * N;
-            const float *ct = sC + tt * N;
+        auto load_token = [&](int t, TokenIn &in) {
+            in.cf = pCf[t * hc];
+            load_rows<RPT>(in.xv, pX + t * xs);
+            const float *bt = pB + t * Ns;
+            const float *ct = pC + t * Ns;
 #pragma unroll
             for (int k = 0; k < VPL; ++k) {
-                const int cidx = k * LANES + j;
-                if (EXACT || cidx < N4) {
-                    in.b[k] = *reinterpret_cast<const float4 *>(bt + 4 * cidx);
+                if (EXACT || k * LANES + j < N4) {
+                    in.b[k] = *reinterpret_cast<const float4 *>(bt + 4 * k * LANES);
                     if constexpr (kFull)
-                        in.c[k] = *reinterpret_cast<const float4 *>(ct + 4 * cidx);
+                        in.c[k] = *reinterpret_cast<const float4 *>(ct + 4 * k * LANES);
                 }
             }
+        };
+        auto rescale = [&](float r) {
+            const float2 r2 = f2(r, r);
+#pragma unroll
+            for (int q = 0; q < RPT; ++q)
+#pragma unroll
+                for (int k = 0; k < VPL; ++k) {
+                    u[q][k][0] = __fmul2_rn(u[q][k][0], r2);
+                    u[q][k][1] = __fmul2_rn(u[q][k][1], r2);
+                }
         };
         // One token: U += (x dt / Lambda) B; with y: the lanes' parts of U . C
         // summed by shuffles (transposing over the RPT rows), then
         // y = Lambda (U . C) + D x from the lane that holds the row's sum.
-        float *yp = yrow;                   // y of the next token computed
-        auto compute_token = [&](const TokenIn &in, int tt) {
-            float2 a2[RPT], acc[RPT][2];
+        auto step = [&](const TokenIn &in, int t) {
+            float2 a2[RPT];
 #pragma unroll
             for (int q = 0; q < RPT; ++q) {
                 const float alpha = in.xv[q] * in.cf.x;
@@ -398,8 +456,7 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan
             // on the one issued just before it
 #pragma unroll
             for (int k = 0; k < VPL; ++k) {
-                const int cidx = k * LANES + j;
-                if (EXACT || cidx < N4) {
+                if (EXACT || k * LANES + j < N4) {
                     const float4 bb = in.b[k];
 #pragma unroll
                     for (int q = 0; q < RPT; ++q) {
@@ -409,84 +466,75 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan
                 }
             }
             if constexpr (kFull) {                                                       // A6
-                // two accumulators per row; the first product of each starts it
+                // two accumulator chains per row (one when a lane holds a
+                // single float4 of it); the first product starts each chain
+                constexpr int NACC = VPL > 1 ? 2 : 1;
+                float2 acc[RPT][NACC];
 #pragma unroll
                 for (int k = 0; k < VPL; ++k) {
-                    const int cidx = k * LANES + j;
+                    const bool live = EXACT || k * LANES + j < N4;
                     const float4 cc = in.c[k];
 #pragma unroll
                     for (int q = 0; q < RPT; ++q) {
-                        float2 &ac = acc[q][k & 1];
-                        if (EXACT || cidx < N4) {
-                            if (k < 2)
+                        float2 &ac = acc[q][k % NACC];
+                        if (live) {
+                            if (k < NACC)
                                 ac = __fmul2_rn(u[q][k][0], f2(cc.x, cc.y));
                             else
                                 ac = __ffma2_rn(u[q][k][0], f2(cc.x, cc.y), ac);
                             ac = __ffma2_rn(u[q][k][1], f2(cc.z, cc.w), ac);
-                        } else if (k < 2) {
+                        } else if (k < NACC) {
                             ac = f2(0.f, 0.f);
                         }
                     }
                 }
-            }
-            if constexpr (kFull) {
                 float part[RPT];
 #pragma unroll
                 for (int q = 0; q < RPT; ++q) {
-                    const float2 s2 = VPL > 1 ? __fadd2_rn(acc[q][0], acc[q][1]) : acc[q][0];
+                    const float2 s2 = NACC > 1 ? __fadd2_rn(acc[q][0], acc[q][NACC - 1]) : acc[q][0];
                     part[q] = s2.x + s2.y;
                 }
+                // every lane holds the full sum of its row, so all lanes of a
+                // row store the same value (no divergent branch around the store)
                 const float ysum = reduce_rows<LANES, RPT>(part, j);
-                if (ywriter)
-                    *yp = fmaf(in.cf.y, ysum, Dv * sX[tt * geo.rows_per_cta + rl + yq]);
-                yp += HP;
+                const float yv = fmaf(in.cf.y, ysum, Dv * pX[t * xs + yq]);
+                if (ystore)
+                    yrow[t * HP] = yv;
             }
         };
-        // Anchor tokens of any head of the block split the chunk into segments;
-        // a head that does not anchor at a split has r = 1 there (exact no-op).
-        // Within a segment the loop is software-pipelined over two operand
-        // buffers: the operands of token t+1 are read before token t is computed.
+        // Anchor tokens (any head of the block) rescale U before their update;
+        // a head that does not anchor there has r = 1 (exact no-op).  Token 0
+        // anchors every head.  Runs of kRun tokens with no anchor after their
+        // first go through straight-line code; the rest one token at a time.
         unsigned amask = 0;
         for (int hh = 0; hh < nheads; ++hh)
             amask |= sm.Mask(b)[hh];
-        int tt = 0;
-        while (tt < cnt) {
-            const unsigned rest = (tt + 1 < 32) ? (amask >> (tt + 1)) : 0u;
-            const int next = rest ? min(cnt, tt + __ffs(rest)) : cnt;
-            TokenIn ta, tb;
-            load_token(tt, ta);
-            {   // re-anchor: U <- r U
-                const float2 r2 = f2(ta.cf.z, ta.cf.z);
+        // The compiler schedules a run's tokens as one block of code, so
+        // the operands of the next token are read while the current one
+        // computes.
+        constexpr int kRun = 8;
+        constexpr unsigned kRunMask = (1u << kRun) - 2u;    // the run's tokens after its first
+        int t = 0;
+        while (t < cnt) {
+            if ((amask >> t) & 1u)
+                rescale(pCf[t * hc].z);
+            if (t + kRun <= cnt && ((amask >> t) & kRunMask) == 0u) {
 #pragma unroll
-                for (int q = 0; q < RPT; ++q)
-#pragma unroll
-                    for (int k = 0; k < VPL; ++k) {
-                        u[q][k][0] = __fmul2_rn(u[q][k][0], r2);
-                        u[q][k][1] = __fmul2_rn(u[q][k][1], r2);
-                    }
-            }
-            int t2 = tt;
-            for (; t2 + 1 < next; t2 += 2) {
-                load_token(t2 + 1, tb);
-                compute_token(ta, t2);
-                load_token(min(t2 + 2, cnt - 1), ta);
-                compute_token(tb, t2 + 1);
-            }
-            if (t2 < next)
-                compute_token(ta, t2);
-            tt = next;
-        }
-        {   // back to S at the chunk end: U <- Lambda_last U
-            const float lam = sCf[(cnt - 1) * geo.heads_cap].y;
-            const float2 l2 = f2(lam, lam);
-#pragma unroll
-            for (int q = 0; q < RPT; ++q)
-#pragma unroll
-                for (int k = 0; k < VPL; ++k) {
-                    u[q][k][0] = __fmul2_rn(u[q][k][0], l2);
-                    u[q][k][1] = __fmul2_rn(u[q][k][1], l2);
+                for (int v = 0; v < kRun; ++v) {
+                    TokenIn in;
+                    load_token(t + v, in);
+                    step(in, t + v);
                 }
+                t += kRun;
+            } else {
+                TokenIn in;
+                load_token(t, in);
+                step(in, t);
+                ++t;
+            }
         }
+        // back to S at the chunk end: U <- Lambda_last U
+        rescale(pCf[(cnt - 1) * hc].y);
         __syncwarp();
         if (c + kSlots < n_chunks)          // the producer refills this slot with chunk c+3
             bar_arrive(kBarEmpty + b, nthr);
