@@ -105,18 +105,21 @@ enum {
  * SSM_ERR_INVALID_ARG.
  *   path             SSM_PATH_*
  *   lanes_per_row    lanes of a warp that share one state row: 1,2,4,8,16,32
- *   rows_per_thread  state rows each lane holds (1, 2 or 4; <= lanes_per_row;
- *                    1 on SSM_PATH_PREFILL)
+ *   rows_per_thread  state rows each lane holds (a power of two, <= lanes_per_row:
+ *                    up to 8 on SSM_PATH_PREFILL, up to 4 on the other paths;
+ *                    automatic on SSM_PATH_PREFILL: about 16 state elements of a
+ *                    row per lane and 4 rows)
  *   rows_per_cta     prefill: state rows per thread block (a multiple of the
  *                    rows one warp holds, at most 256 threads, 224 on
  *                    SSM_PATH_PREFILL which adds a producer warp); decode: ignored
  *   chunk_tokens     prefill: tokens staged in shared memory per chunk (1..256;
- *                    at most 32 on SSM_PATH_PREFILL)
+ *                    at most 32 on SSM_PATH_PREFILL, automatic 16 there, 32 on
+ *                    SSM_PATH_PREFILL_DIRECT)
  *   ctas_per_sm      decode: if > 0, the grid is capped at this many blocks
  *                    per SM and warps loop over the remaining rows
  *   segment_tokens   SSM_PATH_PREFILL with a workspace (ssm_scan_ws): length of
  *                    the time segments long sequences are cut into (a multiple
- *                    of the chunk; an automatic chunk is the largest of 32, 16,
+ *                    of the chunk; an automatic chunk is the largest of 16, 8,
  *                    ... that divides it); 0 = automatic, < 0 = never segment
  *   segment_state    how the state pass of the time segments runs
  *                    (SSM_SEGMENT_STATE_*); ignored without segments
