@@ -60,14 +60,25 @@
  *   SSM_ERR_CUDA         a CUDA call or launch failed (cudaGetLastError);
  *   SSM_ERR_TIMEOUT      a bounded device wait gave up (the pipelined
  *                        tensor-core kernels: the segments' state pass and the
- *                        SSD output kernel).  Each such wait polls an mbarrier
- *                        a bounded number of times (seconds); on giving up the
- *                        kernel sets a status word in the workspace, waits for
- *                        its copies and products in flight, frees its tensor
- *                        memory and returns, so the context stays usable.  The
- *                        word is read back (and this code returned) only under
- *                        SSM_SCAN_CHECK=1.  SSM_SCAN_TEST_FAIL_WAITS=1 makes
- *                        those waits give up at once (tests of this path).
+ *                        SSD chunk-state and output kernels).  Each such wait
+ *                        polls an mbarrier a bounded number of times (seconds);
+ *                        on giving up the kernel sets a status word in the
+ *                        workspace, waits for its copies and products in
+ *                        flight, frees its tensor memory and returns, so the
+ *                        context stays usable.  The word is read back (and this
+ *                        code returned) only under SSM_SCAN_CHECK=1; the library
+ *                        never synchronises otherwise.  Without that check the
+ *                        failure shows in the outputs instead:
+ *                          - a segmented ssm_scan_* call: y is NaN for every
+ *                            owned token and every slot keeps the contents it
+ *                            had before the call;
+ *                          - ssm_scan_ssd: when the chunk states gave up, y is
+ *                            NaN for every owned token and the slots keep their
+ *                            contents; when an output block gave up, y is NaN
+ *                            over that block's chunk and heads (the slots hold
+ *                            the final states).
+ *                        SSM_SCAN_TEST_FAIL_WAITS=1 makes those waits give up
+ *                        at once (tests of this path).
  * n_seqs == 0 is a successful no-op.
  */
 #ifndef SSMSCAN_H
@@ -348,12 +359,17 @@ size_t ssm_scan_ssd_workspace_bytes(int n_seqs, int n_tokens, int n_heads,
  * library owns.  It allocates nothing.
  *   - The first call on a device looks up the scratch's device address (a
  *     cudaGetSymbolAddress with that device current) and caches it; make that
- *     first call before any stream capture.
+ *     first call before any stream capture.  The cached address belongs to
+ *     the device's context as it was then: a cudaDeviceReset while the
+ *     library is loaded is not supported.
+ *   - The stream must belong to the current device (SSM_ERR_INVALID_ARG
+ *     otherwise), since the scratch address is looked up for that device.
  *   - When the automatic plan's segment states would not fit the scratch
  *     (very long or many long sequences, large states), the call runs with
  *     longer time segments (1024 tokens, doubled until they fit) or without
- *     segments: the same results, less parallelism than ssm_scan_ws with a
- *     workspace of the size ssm_scan_workspace_bytes asks for.
+ *     segments (also when no such segment would be shorter than the longest
+ *     sequence can be): the same results, less parallelism than ssm_scan_ws
+ *     with a workspace of the size ssm_scan_workspace_bytes asks for.
  *   - Every call in the process shares the scratch, which keeps the last
  *     call's contents (nothing in it needs to start at zero).  Calls whose GPU
  *     work overlaps, on two streams or from two threads, race on it: the

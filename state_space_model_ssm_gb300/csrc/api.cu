@@ -4,6 +4,7 @@
 // argument is wrong.  Nothing is allocated and the stream is never
 // synchronised (except in the opt-in SSM_SCAN_CHECK=1 debug mode).
 #include <climits>
+#include <mutex>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -12,6 +13,39 @@
 
 #include "../../include/ssmscan.h"
 #include "scan_common.cuh"
+
+namespace ssm {
+
+cudaError_t set_dynamic_smem(const void *kernel, size_t bytes)
+{
+    struct Entry {
+        int dev;
+        const void *kernel;
+        size_t bytes;
+    };
+    static std::mutex mu;
+    static std::vector<Entry> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    std::lock_guard<std::mutex> lock(mu);
+    for (Entry &d : done)
+        if (d.dev == dev && d.kernel == kernel) {
+            if (d.bytes >= bytes)
+                return cudaSuccess;
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+            if (e == cudaSuccess)
+                d.bytes = bytes;
+            return e;
+        }
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess)
+        done.push_back(Entry{dev, kernel, bytes});
+    return e;
+}
+
+}  // namespace ssm
 
 namespace {
 

@@ -62,12 +62,16 @@ extern "C" int ssm_scan_static(float *state_slots, const float *x, const float *
 {
     // The automatic plan, or, when its segment states do not fit the scratch,
     // longer segments (fewer states: 1024 tokens, doubled until they fit), or
-    // none.  Host arithmetic only; nothing is launched before the plan fits.
+    // none once a segment would be as long as the longest sequence can be
+    // (every other sequence holds at least one token): such a plan splits
+    // nothing and would only add the segment passes.  Host arithmetic only;
+    // nothing is launched before the plan fits.
     ssm_scan_tuning t = {};
     const size_t cap = (size_t)SSM_SCAN_STATIC_SCRATCH_BYTES;
     if (ssm_scan_workspace_bytes(n_seqs, n_tokens, n_heads, head_dim, d_state, n_groups, &t) > cap) {
         t.segment_tokens = -1;                        // no segments: no scratch
-        for (long long seg = 1024; seg < n_tokens; seg *= 2) {
+        const long long longest = (long long)n_tokens - (n_seqs > 1 ? n_seqs - 1 : 0);
+        for (long long seg = 1024; seg < longest; seg *= 2) {
             ssm_scan_tuning c = {};
             c.segment_tokens = (int)seg;
             const size_t need = ssm_scan_workspace_bytes(n_seqs, n_tokens, n_heads, head_dim, d_state,
@@ -77,6 +81,15 @@ extern "C" int ssm_scan_static(float *state_slots, const float *x, const float *
                 break;
             }
         }
+    }
+    // The scratch address is the current device's: the stream must belong to it.
+    if (stream) {
+        int cur = 0, sdev = 0;
+        if (cudaGetDevice(&cur) != cudaSuccess ||
+            cudaStreamGetDevice(reinterpret_cast<cudaStream_t>(stream), &sdev) != cudaSuccess)
+            return SSM_ERR_CUDA;
+        if (cur != sdev)
+            return SSM_ERR_INVALID_ARG;
     }
     void *scratch = nullptr;
     const int rc = static_scratch(&scratch);

@@ -302,7 +302,7 @@ cudaError_t launch_one(const ScanArgs &a, const PrefillGeom &g, size_t smem, cud
     const dim3 grid((unsigned)((long long)a.n_seqs * ctas_per_seq));
     auto kern = exact ? prefill_kernel<LANES, VPL, RPT, true> : prefill_kernel<LANES, VPL, RPT, false>;
     if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaError_t e = set_dynamic_smem(reinterpret_cast<const void *>(kern), smem);
         if (e != cudaSuccess)
             return e;
     }

@@ -223,6 +223,12 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan
     const int tid = threadIdx.x, nthr = blockDim.x;
     const int lane = tid & 31, warp = tid >> 5;
     const int producer = (nthr >> 5) - 1;               // the last warp
+    if (kFull && plan.units && call_failed(plan.status)) {
+        // The state pass gave up a bounded wait, so the segments' incoming
+        // states are not valid: y becomes NaN and the slot keeps its contents.
+        poison_y(a.y, HP, tok_start, len, r0, nrows, tid, nthr);
+        return;
+    }
 
     if (warp == producer) {
         // ================= producer warp =================
@@ -578,7 +584,7 @@ cudaError_t launch_scaled_one(const ScanArgs &a, const PrefillGeom &g, const Seg
         kern = exact ? prefill_scaled_kernel<LANES, VPL, RPT, true, kScanStateOnly>
                      : prefill_scaled_kernel<LANES, VPL, RPT, false, kScanStateOnly>;
     if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaError_t e = set_dynamic_smem(reinterpret_cast<const void *>(kern), smem);
         if (e != cudaSuccess)
             return e;
     }

@@ -103,6 +103,28 @@ __device__ __forceinline__ bool reduced_writer(int j)
     return (j & (LANES / RPT - 1)) == 0;
 }
 
+// True when a bounded device wait earlier in the same call gave up: the call's
+// status word (zeroed by the call's first kernel) is nonzero.  The kernels
+// that consume the products of such a wait then write NaN to y and leave the
+// state slots as they were, so the failure shows in the outputs even when the
+// host never reads the word back.
+__device__ __forceinline__ bool call_failed(const int *status)
+{
+    return status != nullptr && *reinterpret_cast<const volatile int *>(status) != 0;
+}
+
+// NaN into rows [r0, r0 + nrows) of tokens [t0, t0 + len) of y ([T][H*P]);
+// threads tid = 0 .. nthr-1 of the caller share the stores.
+__device__ __forceinline__ void poison_y(float *y, long long HP, long long t0, int len, int r0, int nrows,
+                                         int tid, int nthr)
+{
+    const long long n = (long long)len * nrows;
+    for (long long i = tid; i < n; i += nthr) {
+        const long long t = i / nrows;
+        y[(t0 + t) * HP + r0 + (i - t * nrows)] = __int_as_float(0x7fc00000);
+    }
+}
+
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem)
 {
     const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
@@ -125,6 +147,11 @@ __device__ __forceinline__ void cp_async_wait()
 {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
+
+// cudaFuncSetAttribute(kernel, MaxDynamicSharedMemorySize, bytes) on the
+// current device, skipped when an earlier call already set at least `bytes`
+// for that (device, kernel) pair (api.cu).  Thread-safe.
+cudaError_t set_dynamic_smem(const void *kernel, size_t bytes);
 
 // Host-side launchers (defined in prefill.cu / decode.cu).  Return a
 // cudaError_t from the launch, or cudaErrorInvalidValue for a shape with no

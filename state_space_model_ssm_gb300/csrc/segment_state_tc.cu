@@ -449,8 +449,7 @@ cudaError_t launch_shape(const ScanArgs &a, const SegmentPlan &plan, const SegSt
     static_assert(sizeof(CUtensorMap) == sizeof(maps.b), "tensor map size");
     std::memcpy(&tm_b, maps.b, sizeof tm_b);
     std::memcpy(&tm_x, maps.x, sizeof tm_x);
-    cudaError_t e = cudaFuncSetAttribute(segment_state_tc_kernel<XI, HB>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = set_dynamic_smem(reinterpret_cast<const void *>(segment_state_tc_kernel<XI, HB>), smem);
     if (e != cudaSuccess)
         return e;
     segment_state_tc_kernel<XI, HB><<<dim3((unsigned)max_units, (unsigned)(a.H / HB)), kSsBlock, smem, stream>>>(

@@ -97,7 +97,7 @@ segment_combine_kernel(const ScanArgs a, const SegmentPlan plan, int max_units)
     const int N4 = a.N >> 2;
     const long long slot4 = (long long)a.H * a.P * N4;         // float4 per state slot
     const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (e >= slot4)
+    if (e >= slot4 || call_failed(plan.status))      // no valid segment states to combine
         return;
     const int head = (int)((e / N4) / a.P);
     for (int seq = blockIdx.y; seq < a.n_seqs; seq += gridDim.y) {

@@ -180,7 +180,7 @@ ssd_state_pass_kernel(const ScanArgs a, const SsdPlan p, int max_units)
     const int N4 = a.N >> 2;
     const long long slot4 = (long long)a.H * a.P * N4;
     const long long e = (long long)blockIdx.x * kPassThreads + threadIdx.x;
-    if (e >= slot4)
+    if (e >= slot4 || call_failed(p.status))          // chunk states not valid: slots stay as they were
         return;
     const int head = (int)((e / N4) / a.P);
     float4 *W = reinterpret_cast<float4 *>(p.chunk_state);
@@ -364,6 +364,10 @@ ssd_output_kernel(const ScanArgs a, const SsdPlan p, const SsdGeom sg)
         return;
     const int nh = hl1 - hl0;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (call_failed(p.status)) {                      // the chunk states are not valid
+        poison_y(a.y, (long long)a.H * a.P, c.t0, c.len, (g * hpg + hl0) * a.P, nh * a.P, tid, kThreads);
+        return;
+    }
     const int gq = lane >> 2, tq = lane & 3;
     const int lrow = lane & 7, lmat = lane >> 3;      // ldmatrix: tile and row this lane addresses
     const int N4 = N >> 2, Np4 = sg.n_pad >> 2, P4 = P >> 2;
@@ -527,7 +531,7 @@ cudaError_t launch_ssd_q(const ScanArgs &a, const SsdPlan &plan, const SsdGeom &
         e = timed(tm, [&] { return launch_segment_state_tc(a, sp, *state_maps, max_units, stream); });
     } else {
         auto state_k = ssd_chunk_state_kernel<Q>;
-        e = cudaFuncSetAttribute(state_k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g.smem_state);
+        e = set_dynamic_smem(reinterpret_cast<const void *>(state_k), g.smem_state);
         if (e != cudaSuccess)
             return e;
         e = timed(tm, [&] {
@@ -542,7 +546,7 @@ cudaError_t launch_ssd_q(const ScanArgs &a, const SsdPlan &plan, const SsdGeom &
     const dim3 pgrid((unsigned)((slot4 + kPassThreads - 1) / kPassThreads),
                      (unsigned)(a.n_seqs < 65535 ? a.n_seqs : 65535));
     const int pass_smem = kPassBatch * kPassThreads * (int)sizeof(float4);
-    e = cudaFuncSetAttribute(ssd_state_pass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, pass_smem);
+    e = set_dynamic_smem(reinterpret_cast<const void *>(ssd_state_pass_kernel), (size_t)pass_smem);
     if (e != cudaSuccess)
         return e;
     e = timed(tm, [&] {
@@ -566,7 +570,7 @@ cudaError_t launch_ssd_q(const ScanArgs &a, const SsdPlan &plan, const SsdGeom &
     case 16: out_k = ssd_output_kernel<Q, 16>; break;
     default: return cudaErrorInvalidValue;
     }
-    e = cudaFuncSetAttribute(out_k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g.smem_out);
+    e = set_dynamic_smem(reinterpret_cast<const void *>(out_k), g.smem_out);
     if (e != cudaSuccess)
         return e;
     return timed(tm, [&] {

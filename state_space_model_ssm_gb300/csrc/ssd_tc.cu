@@ -193,6 +193,10 @@ ssd_output_tc_kernel(const ScanArgs a, const SsdPlan p, const SsdGeom sg)
         return;
     const int nh = hl1 - hl0;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (call_failed(p.status)) {                      // the chunk states are not valid
+        poison_y(a.y, (long long)a.H * a.P, c.t0, c.len, (g * hpg + hl0) * a.P, nh * a.P, tid, kTcBlock);
+        return;
+    }
     const int P = a.P, N = a.N, N4 = N >> 2, Np4 = sg.n_pad >> 2;
     const int nbuf = sg.out_buffers;
     const TcLayout L = tc_layout(sg.n_pad, P, nbuf);
@@ -435,6 +439,8 @@ ssd_output_tc_kernel(const ScanArgs a, const SsdPlan p, const SsdGeom sg)
             mbar_wait(drain, 0);
         }
         compute_sync();
+        // this block's y is incomplete: NaN over its whole tile
+        poison_y(a.y, (long long)a.H * P, c.t0, c.len, (g * hpg + hl0) * P, nh * P, tid, kTcThreads);
     }
     if (warp == 0)
         tmem_dealloc(tmem, sg.tmem_cols);
@@ -468,7 +474,7 @@ cudaError_t launch_ssd_output_tc(const ScanArgs &a, const SsdPlan &plan, const S
     const int hpg = a.H / a.G;
     const dim3 grid((unsigned)max_units, (unsigned)a.G, (unsigned)((hpg + g.heads_per_cta - 1) / g.heads_per_cta));
     const size_t smem = ssd_tc_smem_bytes(g.n_pad, a.P, g.out_buffers);
-    cudaError_t e = cudaFuncSetAttribute(ssd_output_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = set_dynamic_smem(reinterpret_cast<const void *>(ssd_output_tc_kernel), smem);
     if (e != cudaSuccess)
         return e;
     ssd_output_tc_kernel<<<grid, kTcBlock, smem, stream>>>(a, plan, g);

@@ -138,15 +138,46 @@ def run_gpu_gated(inp, eps=1e-5, seed=7, ssd_chunk=None, tuning=None, workspace=
             z.double().numpy(), w.double().numpy())
 
 
-def assert_gated(inp, y_gpu, gated_gpu, z, w, eps):
-    """The gated output against the oracle's RMSNorm of the GPU's own y (fp32
-    rounding of the epilogue only), and untouched on unowned token rows."""
+def gated_bound(inp, y_ref, z, w, eps, tol=TOL):
+    """Elementwise bound on |gated_gpu - gated_ref| when gated_ref is the
+    oracle's RMSNorm of the oracle's own y.
+
+    The scan bound is |y_gpu - y_ref| <= e_p = tol*(1 + |y_p - D x_p|) on the
+    state readout, plus the fp32 rounding of the skip term D x (bounded here by
+    1e-6*|D x|).  Through ms = mean_p(y^2) + eps, inv = ms^-1/2 and
+    gated_p = y_p * inv * w_p * silu(z_p), to first order:
+        |d ms|  <= (2/P) sum_p |y_p| e_p + (1/P) sum_p e_p^2
+        |d inv| <= inv * |d ms| / (2 ms)
+        |d gated_p| <= |w_p silu(z_p)| * (e_p inv + (|y_p| + e_p) |d inv|)
+    The neglected remainder is second order, a fraction of about tol of that
+    bound, covered by a factor (1 + 20 tol); the epilogue's own fp32 rounding
+    (a few ulp) adds 2e-6*|gated_p| + 1e-7."""
+    x = inp.x.double().numpy()
+    D = inp.D.double().numpy()
+    dx = D[None, :, None] * x
+    e = tol * (1.0 + np.abs(y_ref - dx)) + 1e-6 * np.abs(dx)
+    P = y_ref.shape[-1]
+    ms = np.mean(y_ref * y_ref, axis=-1, keepdims=True) + eps
+    inv = 1.0 / np.sqrt(ms)
+    dms = (2.0 / P) * np.sum(np.abs(y_ref) * e, axis=-1, keepdims=True) + np.mean(e * e, axis=-1, keepdims=True)
+    dinv = inv * dms / (2.0 * ms)
+    zs = z / (1.0 + np.exp(-z))
+    ws = np.abs(w[None, None, :] * zs)
+    gated_ref = y_ref * inv * w[None, None, :] * zs
+    return (1.0 + 20.0 * tol) * ws * (e * inv + (np.abs(y_ref) + e) * dinv) + 2e-6 * np.abs(gated_ref) + 1e-7
+
+
+def assert_gated(inp, y_ref, gated_gpu, z, w, eps, tol=TOL):
+    """The gated output against the oracle's gated RMSNorm of the oracle's own
+    y, within the scan bound propagated through the norm (``gated_bound``),
+    and untouched on unowned token rows."""
     import oracle
     mask = covered_tokens(inp)
-    want = oracle.gated_rmsnorm(y_gpu[mask], z[mask], w, eps)
+    want = oracle.gated_rmsnorm(y_ref[mask], z[mask], w, eps)
     got = gated_gpu[mask]
     assert np.isfinite(got).all()
+    bound = gated_bound(inp, y_ref, z, w, eps, tol)[mask]
     err = np.abs(got - want)
-    assert np.all(err <= 1e-5 * (1.0 + np.abs(want))), f"gated max err {err.max():.3e}"
+    assert np.all(err <= bound), f"gated max err {err.max():.3e}, worst ratio {np.max(err / bound):.3f}"
     if (~mask).any():
         assert np.isnan(gated_gpu[~mask]).all()

@@ -189,4 +189,4 @@ def test_ssd_gated_norm(geom, chunk):
     y_ref, s_ref = oracle.scan_inputs(inp)
     y, s, gated, z, w = run_gpu_gated(inp, eps=1e-5, ssd_chunk=chunk)
     assert_parity(inp, y, s, y_ref, s_ref, tol=SSD_TOL)
-    assert_gated(inp, y, gated, z, w, 1e-5)
+    assert_gated(inp, y_ref, gated, z, w, 1e-5, tol=SSD_TOL)
