@@ -69,6 +69,9 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-ssd", action="store_true")
     ap.add_argument("--no-next", action="store_true")
+    ap.add_argument("--decode-launches", type=int, default=0,
+                    help="run only this many 16x1 decode steps as plain launches (no graph) on the "
+                         "rotating slot sets and exit: the command an ncu counter capture runs")
     return ap.parse_args()
 
 
@@ -411,6 +414,28 @@ def run_decode(dev, rank):
     cold = graph_us(True)
     warm = graph_us(False)
     return dict(cold_us=cold, warm_graph_us=warm)
+
+
+def decode_launches(n):
+    """n decode steps (16 x 1, Nemotron-H geometry) as separate launches, each on
+    the next of the rotating slot sets, then exit.  Under ncu with the L2 left
+    alone between kernels, a launch's DRAM write counter shows the write-back
+    of earlier launches' slots, which leave L2 as later launches stream through
+    it, so the average over consecutive launches is the traffic per step."""
+    from state_space_model_ssm_gb300 import binding as bd
+    from state_space_model_ssm_gb300 import build as _build
+    _build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    base = workload("decode_16x1")
+    d = base.to(dev)
+    sets = [d.state.clone() for _ in range(DECODE_SLOT_SETS)]
+    y = torch.empty_like(d.x)
+    for i in range(n):
+        bd.ssm_scan(sets[i % DECODE_SLOT_SETS], d.x, d.dt, d.A, d.B, d.C, d.D, d.seq_starts, d.seq_lens,
+                    d.resume, y=y)
+    torch.cuda.synchronize(dev)
+    print(json.dumps({"decode_launches": n, "slot_sets": DECODE_SLOT_SETS}))
 
 
 def run_ssd(args, dev, inp, d, chunk=128):
@@ -846,6 +871,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         reference(args)
+    elif args.decode_launches > 0:
+        decode_launches(args.decode_launches)
     else:
         ours(args)
 

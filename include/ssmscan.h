@@ -58,9 +58,9 @@
  *                        misaligned pointer, bad tuning value;
  *   SSM_ERR_UNSUPPORTED  d_state not a multiple of 4, d_state > 1024;
  *   SSM_ERR_CUDA         a CUDA call or launch failed (cudaGetLastError);
- *   SSM_ERR_TIMEOUT      a bounded device wait gave up (the pipelined
- *                        tensor-core kernels: the segments' state pass and the
- *                        SSD chunk-state and output kernels).  Each such wait
+ *   SSM_ERR_TIMEOUT      a bounded device wait gave up (the pipelined kernels:
+ *                        the segments' state pass, the SSD chunk-state and
+ *                        output kernels, the tile-stream decode kernel).  Each such wait
  *                        polls an mbarrier a bounded number of times (seconds);
  *                        on giving up the kernel sets a status word in the
  *                        workspace, waits for its copies and products in
@@ -76,7 +76,11 @@
  *                            NaN for every owned token and the slots keep their
  *                            contents; when an output block gave up, y is NaN
  *                            over that block's chunk and heads (the slots hold
- *                            the final states).
+ *                            the final states);
+ *                          - the tile-stream decode kernel: a block that gave
+ *                            up writes NaN to the y rows of its remaining state
+ *                            tiles and leaves those tiles' slot rows as they
+ *                            were.
  *                        SSM_SCAN_TEST_FAIL_WAITS=1 makes those waits give up
  *                        at once (tests of this path).
  * n_seqs == 0 is a successful no-op.
@@ -102,7 +106,12 @@ typedef enum {
 /* Kernel path selection for ssm_scan_tuned. */
 enum {
     SSM_PATH_AUTO = 0,           /* decode when n_tokens == n_seqs, else prefill */
-    SSM_PATH_DECODE = 1,         /* warp-per-row kernel; correct for any lengths */
+    SSM_PATH_DECODE = 1,         /* decode kernels; correct for any lengths.  With no explicit
+                                    lanes_per_row, rows_per_thread or ctas_per_sm, no
+                                    snapshots and d_state a multiple of 4 up to 128: the
+                                    tile-stream kernel (state tiles move between slot and
+                                    shared memory by bulk copies, several tiles in flight
+                                    per block); otherwise the warp-per-row kernel */
     SSM_PATH_PREFILL = 2,        /* chunk-staged kernel, decay-rescaled state with packed
                                     fp32x2 FMAs; correct for any lengths */
     SSM_PATH_PREFILL_DIRECT = 3  /* chunk-staged kernel stepping S itself (one multiply
@@ -210,7 +219,10 @@ int ssm_scan_tuned(float *state_slots, const float *x, const float *dt,
  *       the dt options); then for ssm_scan_* the decode kernel, or the prefill
  *       kernel, or with time segments the plan, state-pass, combine and
  *       full-pass kernels; for ssm_scan_ssd the plan, chunk-state, state-pass
- *       and output kernels; then the gated RMSNorm (with gated_y).  NULL / 0:
+ *       and output kernels; then the gated RMSNorm (with gated_y), except
+ *       where the rescaled prefill's last kernel writes it itself (its blocks
+ *       then hold exactly one head each, as the automatic shape does at
+ *       head_dim 64 and d_state 64 or 128, and z is 16-byte aligned).  NULL / 0:
  *       none; n_launch_events < 0, or > 0 with NULL events: SSM_ERR_INVALID_ARG;
  *       a failed record: SSM_ERR_CUDA.
  */

@@ -352,8 +352,12 @@ int read_options(const ssm_scan_options *opts, ssm_scan_options *out)
 
 // Launches the scan kernels for a checked call (everything after the argument
 // checks); the options' post-scan steps run in scan_impl.
+// With `gated` set, the full pass of the rescaled prefill writes the gated
+// RMSNorm output itself where its shape allows (*gated_done = true); otherwise
+// the caller runs the separate norm kernel after the scan.
 int scan_kernels(const ssm::ScanArgs &a, const ssm_scan_tuning &t, const DeviceInfo &dev, void *workspace,
-                 size_t workspace_bytes, cudaStream_t stream, ssm::LaunchTimer *tm);
+                 size_t workspace_bytes, cudaStream_t stream, ssm::LaunchTimer *tm, const ssm::GatedOut *gated,
+                 bool *gated_done);
 
 int scan_impl(float *state, const float *x, const float *dt, const float *A, const float *B,
               const float *C, const float *D, float *y, const int32_t *seq_starts,
@@ -436,10 +440,13 @@ int scan_impl(float *state, const float *x, const float *dt, const float *A, con
         workspace = static_cast<char *>(workspace) + dtb;
         workspace_bytes -= dtb;
     }
-    rc = scan_kernels(a, t, dev, workspace, workspace_bytes, stream, &tm);
+    const ssm::GatedOut gated{o.gate_z, o.norm_weight, o.norm_eps, o.gated_y};
+    bool gated_done = false;
+    rc = scan_kernels(a, t, dev, workspace, workspace_bytes, stream, &tm, o.gated_y ? &gated : nullptr,
+                      &gated_done);
     if (rc != SSM_OK)
         return rc;
-    if (o.gated_y && n_tokens > 0 &&
+    if (o.gated_y && n_tokens > 0 && !gated_done &&
         ssm::timed(&tm, [&] {
             return ssm::launch_gated_norm(a, o.gate_z, o.norm_weight, o.norm_eps, o.gated_y, stream);
         }) != cudaSuccess)
@@ -448,8 +455,10 @@ int scan_impl(float *state, const float *x, const float *dt, const float *A, con
 }
 
 int scan_kernels(const ssm::ScanArgs &a, const ssm_scan_tuning &t, const DeviceInfo &dev, void *workspace,
-                 size_t workspace_bytes, cudaStream_t stream, ssm::LaunchTimer *tm)
+                 size_t workspace_bytes, cudaStream_t stream, ssm::LaunchTimer *tm, const ssm::GatedOut *gated,
+                 bool *gated_done)
 {
+    *gated_done = false;
     const int n_seqs = a.n_seqs, n_tokens = a.n_tokens, H = a.H, P = a.P, N = a.N, G = a.G;
     int rc = SSM_OK;
     const int N4 = N / 4;
@@ -457,6 +466,24 @@ int scan_kernels(const ssm::ScanArgs &a, const ssm_scan_tuning &t, const DeviceI
     if (path == SSM_PATH_AUTO)
         path = (n_tokens == n_seqs) ? SSM_PATH_DECODE : SSM_PATH_PREFILL;
 
+    if (path == SSM_PATH_DECODE && !a.snaps && t.lanes_per_row == 0 && t.rows_per_thread == 0 &&
+        t.ctas_per_sm == 0 && ssm::decode_bulk_supported(N, (size_t)dev.smem_optin)) {
+        // the tile-stream kernel (decode_bulk.cu); its status word is read back
+        // only in the debug mode
+        const bool chk = check_env();
+        if (chk && ssm::decode_bulk_status(nullptr, stream, true) != cudaSuccess)
+            return SSM_ERR_CUDA;
+        if (ssm::timed(tm, [&] { return ssm::launch_decode_bulk(a, dev.sms, fail_waits_env() ? 1 : 0, stream); }) !=
+            cudaSuccess)
+            return SSM_ERR_CUDA;
+        if (chk) {
+            int st = 0;
+            if (ssm::decode_bulk_status(&st, stream, false) != cudaSuccess)
+                return SSM_ERR_CUDA;
+            return st != 0 ? SSM_ERR_TIMEOUT : SSM_OK;
+        }
+        return SSM_OK;
+    }
     if (path == SSM_PATH_DECODE) {
         const int lanes = t.lanes_per_row ? t.lanes_per_row : std::min(32, pow2ceil(N4));
         int rpt = t.rows_per_thread;
@@ -510,13 +537,32 @@ int scan_kernels(const ssm::ScanArgs &a, const ssm_scan_tuning &t, const DeviceI
             return SSM_ERR_CUDA;
         return SSM_OK;
     }
+    // Output of the full pass: the consumers store y (epi 0).  With the gated
+    // RMSNorm requested, where the shape has the output-tile variants, y goes
+    // through a shared-memory tile from which the producer warp writes y and
+    // the gated output (epi 2); its blocks must hold exactly one head (rows per
+    // block = head_dim), z be 16-byte aligned (staged like x) and the extra
+    // tiles fit the shared memory.
+    const ssm::GatedOut *fuse = nullptr;
+    int epi = 0;
+    size_t smem_full = pl.smem;
+    if (n_tokens > 0 && ssm::prefill_scaled_tile_supported(pl.lanes, pl.vpl, pl.rpt, pl.g.rows_per_cta)) {
+        if (gated && pl.g.rows_per_cta == P && P % 4 == 0 && P <= 256 && aligned(gated->z, 16) &&
+            aligned(gated->out, 16) &&
+            ssm::prefill_scaled_smem_bytes(pl.g, N, pl.lanes, 2) <= (size_t)dev.smem_optin) {
+            fuse = gated;
+            epi = 2;
+        }
+        smem_full = ssm::prefill_scaled_smem_bytes(pl.g, N, pl.lanes, epi);
+    }
     ssm::SegmentPlan plan{};
     if (pl.seg_len == 0) {
         if (ssm::timed(tm, [&] {
                 return ssm::launch_prefill_scaled(a, pl.g, pl.lanes, pl.vpl, pl.rpt, plan, ssm::kScanFull, n_seqs,
-                                                  pl.smem, stream);
+                                                  smem_full, stream, epi, fuse);
             }) != cudaSuccess)
             return SSM_ERR_CUDA;
+        *gated_done = fuse != nullptr;
         return SSM_OK;
     }
     char *ws = static_cast<char *>(workspace);
@@ -539,10 +585,11 @@ int scan_kernels(const ssm::ScanArgs &a, const ssm_scan_tuning &t, const DeviceI
     if (e != cudaSuccess || ssm::timed(tm, [&] { return ssm::launch_segment_combine(a, plan, mu, stream); }) !=
                                 cudaSuccess ||
         ssm::timed(tm, [&] {
-            return ssm::launch_prefill_scaled(a, pl.g, pl.lanes, pl.vpl, pl.rpt, plan, ssm::kScanFull, mu, pl.smem,
-                                              stream);
+            return ssm::launch_prefill_scaled(a, pl.g, pl.lanes, pl.vpl, pl.rpt, plan, ssm::kScanFull, mu, smem_full,
+                                              stream, epi, fuse);
         }) != cudaSuccess)
         return SSM_ERR_CUDA;
+    *gated_done = fuse != nullptr;
     if (pl.tc_state && check_env())         // debug: report a bounded wait that gave up
         return read_status(plan.status, stream);
     return SSM_OK;

@@ -14,8 +14,12 @@
 // tokens are computed independently: a thread owns 4 consecutive channels
 // (128-bit loads and stores, contiguous across a warp) over a run of 16 tokens
 // and keeps the last k-1 inputs in registers, so each input is read once plus
-// a k-1 halo per run.  The slot update runs as a second launch so that no
-// output reads a slot another thread has already rewritten.
+// a k-1 halo per run.  A complete run issues all 16 of its loads before any
+// arithmetic (a quarter KiB per thread in flight), and SiLU takes the hardware
+// exponential and an approximate division, v / (1 + exp(-v)) (about 1e-6
+// relative), so the kernel stays bound by memory, not by the per-element
+// arithmetic.  The slot update runs as a second launch so that no output reads
+// a slot another thread has already rewritten.
 #include "scan_common.cuh"
 
 namespace ssm {
@@ -86,6 +90,7 @@ template <int CH, int K>
 __global__ void __launch_bounds__(kConvThreads)
 conv1d_out_kernel(const ConvArgs a)
 {
+    griddep_entry();
     constexpr int KM1 = K - 1;
     const int c0 = (blockIdx.x * kConvThreads + threadIdx.x) * CH;
     if (c0 >= a.C)
@@ -120,8 +125,8 @@ conv1d_out_kernel(const ConvArgs a)
                 }
             }
             const int rend = min(len, r0 + kConvRun);
-            for (int t = r0; t < rend; ++t) {
-                const Lanes<CH> xv = load_ch<CH>(a.x + (t0 + t) * a.C + c0);
+            // token t of the run from its input xv and the window of the K-1 before it
+            auto token = [&](int t, const Lanes<CH> &xv) {
                 Lanes<CH> o;
 #pragma unroll
                 for (int q = 0; q < CH; ++q) {
@@ -129,7 +134,7 @@ conv1d_out_kernel(const ConvArgs a)
 #pragma unroll
                     for (int u = 0; u < KM1; ++u)
                         acc = fmaf(w[u][q], win[u][q], acc);
-                    o.v[q] = acc / (1.f + expf(-acc));
+                    o.v[q] = __fdividef(acc, 1.f + __expf(-acc));
                 }
                 store_ch<CH>(a.out + (t0 + t) * a.C + c0, o);
 #pragma unroll
@@ -151,6 +156,18 @@ conv1d_out_kernel(const ConvArgs a)
                             sn[u] = win[u][q];
                     }
                 }
+            };
+            if (rend - r0 == kConvRun) {                        // a complete run: every load first
+                Lanes<CH> xs[kConvRun];
+#pragma unroll
+                for (int i = 0; i < kConvRun; ++i)
+                    xs[i] = load_ch<CH>(a.x + (t0 + r0 + i) * a.C + c0);
+#pragma unroll
+                for (int i = 0; i < kConvRun; ++i)
+                    token(r0 + i, xs[i]);
+            } else {
+                for (int t = r0; t < rend; ++t)
+                    token(t, load_ch<CH>(a.x + (t0 + t) * a.C + c0));
             }
         }
     }
@@ -159,6 +176,7 @@ conv1d_out_kernel(const ConvArgs a)
 __global__ void __launch_bounds__(kConvThreads)
 conv1d_state_kernel(const ConvArgs a)
 {
+    griddep_entry();
     const int km1 = a.K - 1;
     const long long e = (long long)blockIdx.x * kConvThreads + threadIdx.x;
     if (e >= (long long)a.n_seqs * a.C)
@@ -185,8 +203,7 @@ cudaError_t launch_out(const ConvArgs &a, int gz, cudaStream_t stream)
     const int per_block = kConvThreads * CH;
     const dim3 grid((unsigned)((a.C + per_block - 1) / per_block), (unsigned)(a.n_seqs < 65535 ? a.n_seqs : 65535),
                     (unsigned)gz);
-    conv1d_out_kernel<CH, K><<<grid, kConvThreads, 0, stream>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(conv1d_out_kernel<CH, K>, grid, dim3(kConvThreads), 0, stream, a);
 }
 
 template <int CH>
@@ -224,9 +241,10 @@ cudaError_t launch_conv1d(const float *x, const float *w, const float *bias, flo
     }
     if (K > 1) {
         const long long cells = (long long)n_seqs * C;
-        conv1d_state_kernel<<<(unsigned)((cells + kConvThreads - 1) / kConvThreads), kConvThreads, 0, stream>>>(a);
+        return launch_pdl(conv1d_state_kernel, dim3((unsigned)((cells + kConvThreads - 1) / kConvThreads)),
+                          dim3(kConvThreads), 0, stream, a);
     }
-    return cudaGetLastError();
+    return cudaSuccess;
 }
 
 }  // namespace ssm

@@ -26,6 +26,7 @@ template <int LANES, int VPL, int RPT, bool EXACT>
 __global__ void __launch_bounds__(kDecodeWarps * 32)
 decode_kernel(const ScanArgs a, const DecodeGeom geo)
 {
+    griddep_entry();
     const int N = a.N, N4 = a.N >> 2, P = a.P, H = a.H;
     const int HP = H * P;
     const int lane = threadIdx.x & 31;
@@ -144,8 +145,7 @@ cudaError_t launch_one(const ScanArgs &a, const DecodeGeom &g, int grid_seqs, cu
     const bool exact = (a.N / 4) == LANES * VPL;
     auto kern = exact ? decode_kernel<LANES, VPL, RPT, true> : decode_kernel<LANES, VPL, RPT, false>;
     const dim3 grid((unsigned)((g.tasks_per_seq + kDecodeWarps - 1) / kDecodeWarps), (unsigned)grid_seqs);
-    kern<<<grid, kDecodeWarps * 32, 0, stream>>>(a, g);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, dim3(kDecodeWarps * 32), 0, stream, a, g);
 }
 
 }  // namespace

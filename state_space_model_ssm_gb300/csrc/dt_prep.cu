@@ -19,6 +19,7 @@ constexpr int kDtThreads = 256;
 __global__ void __launch_bounds__(kDtThreads)
 dt_prep_kernel(const ScanArgs a, const float *bias, int softplus, float *out)
 {
+    griddep_entry();
     const int H = a.H;
     for (int seq = blockIdx.y; seq < a.n_seqs; seq += gridDim.y) {
         const long long t0 = a.seq_starts[seq];
@@ -45,8 +46,7 @@ cudaError_t launch_dt_prep(const ScanArgs &a, const float *bias, int softplus, f
     const long long per_seq = ((long long)a.n_tokens * a.H + a.n_seqs - 1) / a.n_seqs;
     const long long gx = (per_seq + kDtThreads - 1) / kDtThreads;
     const dim3 grid((unsigned)(gx < 1 ? 1 : (gx > 4096 ? 4096 : gx)), (unsigned)(a.n_seqs < 65535 ? a.n_seqs : 65535));
-    dt_prep_kernel<<<grid, kDtThreads, 0, stream>>>(a, bias, softplus, out);
-    return cudaGetLastError();
+    return launch_pdl(dt_prep_kernel, grid, dim3(kDtThreads), 0, stream, a, bias, softplus, out);
 }
 
 }  // namespace ssm

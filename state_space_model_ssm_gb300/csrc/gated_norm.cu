@@ -17,10 +17,16 @@ namespace {
 
 constexpr int kNormWarps = 8;
 
+// silu(z) = z / (1 + e^-z) from the hardware exponential and an approximate
+// division (about 1e-6 relative; the same form the prefill kernel's fused
+// gated output uses).
+__device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.f + __expf(-z)); }
+
 // Scalar path (any head_dim): one warp per row.
 __global__ void __launch_bounds__(32 * kNormWarps)
 gated_norm_kernel(const ScanArgs a, const float *z, const float *w, float eps, float *out)
 {
+    griddep_entry();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int P = a.P, H = a.H;
     for (int seq = blockIdx.y; seq < a.n_seqs; seq += gridDim.y) {
@@ -43,7 +49,7 @@ gated_norm_kernel(const ScanArgs a, const float *z, const float *w, float eps, f
             float *outr = out + off;
             for (int p = lane; p < P; p += 32) {
                 const float zv = zr[p];
-                outr[p] = yr[p] * inv * __ldg(w + p) * (zv / (1.f + expf(-zv)));
+                outr[p] = yr[p] * inv * __ldg(w + p) * silu(zv);
             }
         }
     }
@@ -56,6 +62,7 @@ template <int G, int VPL>
 __global__ void __launch_bounds__(32 * kNormWarps)
 gated_norm_vec_kernel(const ScanArgs a, const float *z, const float *w, float eps, float *out)
 {
+    griddep_entry();
     constexpr int RPW = 32 / G;                       // rows per warp
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int j = lane % G, sub = lane / G;
@@ -92,10 +99,10 @@ gated_norm_vec_kernel(const ScanArgs a, const float *z, const float *w, float ep
                     const float4 zv = zr[c];
                     const float4 wv = __ldg(reinterpret_cast<const float4 *>(w) + c);
                     float4 o;
-                    o.x = v[k].x * inv * wv.x * (zv.x / (1.f + expf(-zv.x)));
-                    o.y = v[k].y * inv * wv.y * (zv.y / (1.f + expf(-zv.y)));
-                    o.z = v[k].z * inv * wv.z * (zv.z / (1.f + expf(-zv.z)));
-                    o.w = v[k].w * inv * wv.w * (zv.w / (1.f + expf(-zv.w)));
+                    o.x = v[k].x * inv * wv.x * silu(zv.x);
+                    o.y = v[k].y * inv * wv.y * silu(zv.y);
+                    o.z = v[k].z * inv * wv.z * silu(zv.z);
+                    o.w = v[k].w * inv * wv.w * silu(zv.w);
                     outr[c] = o;
                 }
             }
@@ -110,8 +117,7 @@ cudaError_t launch_vec(const ScanArgs &a, const float *z, const float *w, float 
     const long long per_block = (long long)kNormWarps * (32 / G);
     const long long gx = (rows_per_seq + per_block - 1) / per_block;
     const dim3 grid((unsigned)(gx < 1 ? 1 : (gx > 8192 ? 8192 : gx)), (unsigned)(a.n_seqs < 65535 ? a.n_seqs : 65535));
-    gated_norm_vec_kernel<G, VPL><<<grid, 32 * kNormWarps, 0, st>>>(a, z, w, eps, out);
-    return cudaGetLastError();
+    return launch_pdl(gated_norm_vec_kernel<G, VPL>, grid, dim3(32 * kNormWarps), 0, st, a, z, w, eps, out);
 }
 
 }  // namespace
@@ -138,8 +144,7 @@ cudaError_t launch_gated_norm(const ScanArgs &a, const float *z, const float *w,
     const long long gx = (rows_per_seq + kNormWarps - 1) / kNormWarps;
     const dim3 grid((unsigned)(gx < 1 ? 1 : (gx > 4096 ? 4096 : gx)),
                     (unsigned)(a.n_seqs < 65535 ? a.n_seqs : 65535));
-    gated_norm_kernel<<<grid, 32 * kNormWarps, 0, stream>>>(a, z, w, eps, out);
-    return cudaGetLastError();
+    return launch_pdl(gated_norm_kernel, grid, dim3(32 * kNormWarps), 0, stream, a, z, w, eps, out);
 }
 
 }  // namespace ssm

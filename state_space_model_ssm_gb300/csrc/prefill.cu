@@ -64,6 +64,7 @@ template <int LANES, int VPL, int RPT, bool EXACT>
 __global__ void __launch_bounds__(256, 1)
 prefill_kernel(const ScanArgs a, const PrefillGeom geo)
 {
+    griddep_entry();
     extern __shared__ __align__(16) float smem[];
     const int N = a.N, N4 = a.N >> 2, P = a.P, H = a.H;
     const long long HP = (long long)H * P;
@@ -306,8 +307,7 @@ cudaError_t launch_one(const ScanArgs &a, const PrefillGeom &g, size_t smem, cud
         if (e != cudaSuccess)
             return e;
     }
-    kern<<<grid, threads, smem, stream>>>(a, g);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, dim3(threads), smem, stream, a, g);
 }
 
 }  // namespace

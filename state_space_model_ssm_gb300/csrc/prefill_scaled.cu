@@ -43,6 +43,17 @@
 //    row's full sum, so all lanes of a row store y (the same value) and the
 //    store needs no divergent branch.
 //
+// 4. Output through the producer (EPI >= 1).  The consumers leave each chunk's
+//    y in a shared-memory tile instead of storing it; once they are done with
+//    the chunk, the otherwise idle producer writes the tile out with 128-bit
+//    stores.  With EPI = 2 (a block's rows are exactly one head) the kernel
+//    also applies Mamba2's output gate RMSNorm(y) * w * silu(z) per (token,
+//    head) row (kernel 3 of "ssm_gated_delta.cu"): the producer stages the
+//    chunk's z with B, C and x, and at the chunk's end the consumer warps
+//    share the row norms and the gated values (eight lanes per token), so the
+//    gated output needs no second pass over y.  (One producer warp alone
+//    would hold up the whole block with that work.)
+//
 // The rescaling is an algebraic identity of the recurrence defined by "The
 // llama journey", Day 14 (decay exp(dt*A), input dt*x*B, y from the updated
 // state); only the rounding differs from the direct form.
@@ -56,6 +67,7 @@ constexpr float kAnchorSpan = 40.f;
 constexpr int kSlots = 3;         // staging slots: two chunks in flight while one is consumed
 constexpr int kBarFull = 1;       // named barriers kBarFull + s: slot s staged
 constexpr int kBarEmpty = 4;      // named barriers kBarEmpty + s: slot s consumed
+constexpr int kBarConsumers = 7;  // the consumer warps alone (the gated output)
 
 __device__ __forceinline__ void bar_sync(int id, int nthreads)
 {
@@ -71,8 +83,10 @@ struct ScaledSmem {
     float *base;
     int cb, cx, cc, cm; // floats per buffer: B (= C), x, coefficients (float4 per token and
                         // head), anchor masks (one word per head)
-    // slot s: [B | C | x | coefficients | anchor masks], each 16-byte aligned
-    __device__ __forceinline__ float *slot(int s) const { return base + s * (2 * cb + cx + cc + cm); }
+    int cg;             // output through the producer: the y tile (cx floats) and with the
+                        // gated output the z tile (cx more), else 0
+    // slot s: [B | C | x | coefficients | anchor masks | y | z], each 16-byte aligned
+    __device__ __forceinline__ float *slot(int s) const { return base + s * (2 * cb + cx + cc + cm + cg); }
     __device__ __forceinline__ float *B(int s) const { return slot(s); }
     __device__ __forceinline__ float *C(int s) const { return slot(s) + cb; }
     __device__ __forceinline__ float *X(int s) const { return slot(s) + 2 * cb; }
@@ -84,10 +98,21 @@ struct ScaledSmem {
     {
         return reinterpret_cast<unsigned *>(slot(s) + 2 * cb + cx + cc);
     }
-    __device__ __forceinline__ float *Dec() const { return base + kSlots * (2 * cb + cx + cc + cm); }
+    __device__ __forceinline__ float *Ytile(int s) const { return slot(s) + 2 * cb + cx + cc + cm; }
+    __device__ __forceinline__ float *Ztile(int s) const { return slot(s) + 2 * cb + 2 * cx + cc + cm; }
+    __device__ __forceinline__ float *Dec() const { return base + kSlots * (2 * cb + cx + cc + cm + cg); }
 };
 
 __device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
+
+// A shared-memory store the compiler may move other shared-memory reads across
+// (no memory clobber): the y tile is written only here and read only by the
+// producer after the chunk's EMPTY barrier, which orders it.  A plain store
+// would pin every later operand read of the token run behind it.
+__device__ __forceinline__ void st_shared_unordered(float *p, float v)
+{
+    asm volatile("st.shared.f32 [%0], %1;\n" ::"r"(static_cast<unsigned>(__cvta_generic_to_shared(p))), "f"(v));
+}
 
 // R consecutive floats from shared memory (16-byte aligned when R = 4, 8 bytes when R = 2).
 template <int R>
@@ -157,22 +182,32 @@ __device__ __forceinline__ float chunk_coefficients(float dt, float A, int n, in
 
 }  // namespace
 
-size_t prefill_scaled_smem_bytes(const PrefillGeom &g, int N, int lanes)
+size_t prefill_scaled_smem_bytes(const PrefillGeom &g, int N, int lanes, int epi)
 {
     const size_t cx = ((size_t)g.chunk * g.rows_per_cta + 3) & ~(size_t)3;
     const size_t cm = ((size_t)g.heads_cap + 3) & ~(size_t)3;
-    const size_t per_slot = (size_t)g.chunk * (2 * (size_t)N + 4 * (size_t)g.heads_cap) + cx + cm;
+    const size_t per_slot = (size_t)g.chunk * (2 * (size_t)N + 4 * (size_t)g.heads_cap) + cx + cm +
+                            (size_t)epi * cx;
     (void)lanes;
     return (kSlots * per_slot + cm) * sizeof(float);
 }
 
 // MODE kScanFull: the scan with y.  MODE kScanStateOnly: one time segment's
 // state from zero (no C, no y), for the segment pass of long sequences.
-template <int LANES, int VPL, int RPT, bool EXACT, int MODE>
-__global__ void __launch_bounds__(256, 1)
-prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan plan)
+// EPI (kScanFull only): 0 the consumers store y; 1 y through a shared-memory
+// tile, stored by the producer; 2 as 1 and the gated RMSNorm output (a block's
+// rows are exactly one head).  The tile variants (prefill_scaled_tile_kernel)
+// run blocks of at most kTileThreads (four consumer warps and the producer)
+// and keep two blocks per SM.
+constexpr int kTileThreads = 160;
+
+template <int LANES, int VPL, int RPT, bool EXACT, int MODE, int EPI>
+__device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const PrefillGeom &geo,
+                                                    const SegmentPlan &plan, const GatedOut &gt)
 {
     constexpr bool kFull = (MODE == kScanFull);
+    constexpr bool TILE = EPI >= 1, GATED = EPI == 2;
+    static_assert(kFull || EPI == 0, "the output tile needs y");
     extern __shared__ __align__(16) float smem[];
     const int N = a.N, N4 = a.N >> 2, P = a.P, H = a.H;
     const long long HP = (long long)H * P;
@@ -182,6 +217,7 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan
     sm.cx = (geo.chunk * geo.rows_per_cta + 3) & ~3;     // keeps the float4 coefficients 16-byte aligned
     sm.cc = geo.chunk * geo.heads_cap * 4;
     sm.cm = (geo.heads_cap + 3) & ~3;                    // keeps the next slot 16-byte aligned
+    sm.cg = EPI * sm.cx;
 
     // ---- A1 work mapping: (work unit, group, run of rows) ----
     // A work unit is a whole sequence, or with a segment plan one time segment
@@ -227,6 +263,8 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan
         // The state pass gave up a bounded wait, so the segments' incoming
         // states are not valid: y becomes NaN and the slot keeps its contents.
         poison_y(a.y, HP, tok_start, len, r0, nrows, tid, nthr);
+        if (GATED)
+            poison_y(gt.out, HP, tok_start, len, r0, nrows, tid, nthr);
         return;
     }
 
@@ -279,9 +317,13 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan
                 }
             }
             const float *gx = a.x + tok0 * HP + r0;
+            const float *gz = GATED ? gt.z + tok0 * HP + r0 : nullptr;
+            float *sZ = GATED ? sm.Ztile(b) : nullptr;
             if (x16) {
                 for (int t = xt0, r = xv0; t < cnt;) {
                     cp_async16(sX + t * geo.rows_per_cta + 4 * r, gx + t * HP + 4 * r);
+                    if (GATED)              // z: the same layout as x (16-byte aligned: checked by the host)
+                        cp_async16(sZ + t * geo.rows_per_cta + 4 * r, gz + t * HP + 4 * r);
                     t += xdt;
                     r += xdv;
                     if (r >= xw) { r -= xw; ++t; }
@@ -289,6 +331,8 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan
             } else {
                 for (int t = xt0, r = xv0; t < cnt;) {
                     cp_async4(sX + t * geo.rows_per_cta + r, gx + t * HP + r);
+                    if (GATED)
+                        cp_async4(sZ + t * geo.rows_per_cta + r, gz + t * HP + r);
                     t += xdt;
                     r += xdv;
                     if (r >= xw) { r -= xw; ++t; }
@@ -322,9 +366,42 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan
                     seg_decay[hh] = (c0 == 0 ? 1.f : seg_decay[hh]) * dec;
             }
         };
+        // Output of chunk c0 (slot b), after the consumers are done with it: the
+        // y tile to global memory (128-bit stores where the rows allow).
+        const bool y16 = ((r0 | nrows | geo.rows_per_cta) & 3) == 0 && (HP & 3) == 0 &&
+                         (reinterpret_cast<uintptr_t>(a.y) & 15) == 0;
+        // (token, piece) walk of the y write-out: yw pieces (16 or 4 bytes) per token
+        const int yw = y16 ? nrows >> 2 : nrows;
+        const int yt0 = lane / yw, yv0 = lane - yt0 * yw, ydt = 32 / yw, ydv = 32 - ydt * yw;
+        auto epilogue = [&](int c0, int b) {
+            const int t0 = c0 * geo.chunk;
+            const int cnt = min(geo.chunk, len - t0);
+            const float *Y = sm.Ytile(b);
+            const int xs = geo.rows_per_cta;
+            float *yg = a.y + ((long long)tok_start + t0) * HP + r0;
+            if (y16) {
+                for (int t = yt0, r = yv0; t < cnt;) {
+                    *reinterpret_cast<float4 *>(yg + t * HP + 4 * r) =
+                        *reinterpret_cast<const float4 *>(Y + t * xs + 4 * r);
+                    t += ydt;
+                    r += ydv;
+                    if (r >= yw) { r -= yw; ++t; }
+                }
+            } else {
+                for (int t = yt0, r = yv0; t < cnt;) {
+                    yg[t * HP + r] = Y[t * xs + r];
+                    t += ydt;
+                    r += ydv;
+                    if (r >= yw) { r -= yw; ++t; }
+                }
+            }
+            __syncwarp();               // every read of the tile done before the slot is restaged
+        };
         // Staging runs two chunks ahead: chunks k and k+1 are in flight while the
         // consumers work on chunk k-1.  A slot is refilled only after EMPTY says
-        // the consumers are done with the chunk three back.
+        // the consumers are done with the chunk three back.  With the output
+        // tile the consumers release every chunk and the producer writes out
+        // chunk k-1 before it restages that slot.
         float dt0[kDtHeads], dt1[kDtHeads], dt2[kDtHeads];
         if (n_chunks > 0) {
             stage(0, 0);
@@ -345,9 +422,13 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan
                 cp_async_wait<0>();
             __syncwarp();
             bar_arrive(kBarFull + s, nthr);
+            if (TILE && k >= 1) {             // chunk k-1 (slot (k+2) % 3) consumed: its output
+                bar_sync(kBarEmpty + (k + 2) % kSlots, nthr);
+                epilogue(k - 1, (k + 2) % kSlots);
+            }
             if (k + 2 < n_chunks) {
                 const int s2 = (k + 2) % kSlots;
-                if (k >= 1)                   // chunk k-1 used slot s2
+                if (!TILE && k >= 1)          // chunk k-1 used slot s2
                     bar_sync(kBarEmpty + s2, nthr);
                 stage(k + 2, s2);
             }
@@ -356,6 +437,10 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan
                 dt0[q] = dt1[q];
                 dt1[q] = dt2[q];
             }
+        }
+        if (TILE && n_chunks > 0) {           // the last chunk's output
+            bar_sync(kBarEmpty + (n_chunks - 1) % kSlots, nthr);
+            epilogue(n_chunks - 1, (n_chunks - 1) % kSlots);
         }
         if (!kFull && lane == 0) {
             // the segment's decay per head, written by the block holding the head's first row
@@ -408,15 +493,71 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan
     const int Ns = EXACT ? 4 * LANES * VPL : N;
     const int xs = geo.rows_per_cta, hc = geo.heads_cap;
 
+    // The gated RMSNorm of chunk cc, shared by the consumer warps once all of
+    // the chunk's y is in its tile: eight lanes per token (lane group g of
+    // warp w takes token 4 w + g, then every 4 * warps tokens), each lane the
+    // 128-bit pieces l, l + 8, ... of the row (a quarter warp reads 128
+    // contiguous bytes: no bank conflicts); the row's sum of squares by three
+    // shuffles, then gated = y / sqrt(mean(y^2) + eps) * w * silu(z), silu from
+    // the hardware exponential and an approximate division (about 1e-6
+    // relative, far inside the scan's bound).
+    auto gate = [&](int cc) {
+        const int bb = cc % kSlots;
+        const int cnt = min(geo.chunk, len - cc * geo.chunk);
+        const int xs = geo.rows_per_cta;
+        const int nw = (nthr >> 5) - 1, sub = lane >> 3, l8 = lane & 7;
+        const float *Y = sm.Ytile(bb), *Z = sm.Ztile(bb);
+        const float inv_p = 1.f / (float)nrows;
+        float *out = gt.out + ((long long)tok_start + cc * geo.chunk) * HP + r0;
+        for (int tr = warp * 4; tr < cnt; tr += nw * 4) {
+            const int t = tr + sub;
+            const bool live = t < cnt;
+            float ss = 0.f;
+            for (int e = 4 * l8; e < nrows; e += 32) {
+                if (live) {
+                    const float4 v = *reinterpret_cast<const float4 *>(Y + t * xs + e);
+                    ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+                }
+            }
+            ss += __shfl_xor_sync(kFullMask, ss, 4);
+            ss += __shfl_xor_sync(kFullMask, ss, 2);
+            ss += __shfl_xor_sync(kFullMask, ss, 1);
+            const float inv = rsqrtf(ss * inv_p + gt.eps);
+            if (live) {
+                for (int e = 4 * l8; e < nrows; e += 32) {
+                    const float4 v = *reinterpret_cast<const float4 *>(Y + t * xs + e);
+                    const float4 z = *reinterpret_cast<const float4 *>(Z + t * xs + e);
+                    const float4 w = __ldg(reinterpret_cast<const float4 *>(gt.w + e));
+                    float4 o;
+                    o.x = v.x * inv * w.x * __fdividef(z.x, 1.f + __expf(-z.x));
+                    o.y = v.y * inv * w.y * __fdividef(z.y, 1.f + __expf(-z.y));
+                    o.z = v.z * inv * w.z * __fdividef(z.z, 1.f + __expf(-z.z));
+                    o.w = v.w * inv * w.w * __fdividef(z.w, 1.f + __expf(-z.w));
+                    *reinterpret_cast<float4 *>(out + (long long)t * HP + e) = o;
+                }
+            }
+        }
+    };
+
     for (int c = 0; c < n_chunks; ++c) {
         const int b = c % kSlots;
         bar_sync(kBarFull + b, nthr);
+        if constexpr (GATED) {
+            // every consumer warp has arrived here, so all of chunk c-1's y is
+            // in its tile: gate it, then release its slot
+            if (c >= 1) {
+                gate(c - 1);
+                __syncwarp();
+                bar_arrive(kBarEmpty + (c - 1) % kSlots, nthr);
+            }
+        }
         const int cnt = min(geo.chunk, len - c * geo.chunk);
         const float *__restrict__ pB = sm.B(b) + 4 * j;      // this lane's first float4 of a token's B
         const float *__restrict__ pC = sm.C(b) + 4 * j;
         const float4 *__restrict__ pCf = sm.Coef(b) + hl;
         const float *__restrict__ pX = sm.X(b) + rl;
         float *yrow = a.y + ((long long)tok_start + c * geo.chunk) * HP + r0 + rl + yq;
+        float *pY = TILE ? sm.Ytile(b) + rl + yq : nullptr;    // the chunk's y tile (EPI >= 1)
 
         // Shared-memory operands of one token.
         struct TokenIn {
@@ -451,7 +592,7 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan
         // One token: U += (x dt / Lambda) B; with y: the lanes' parts of U . C
         // summed by shuffles (transposing over the RPT rows), then
         // y = Lambda (U . C) + D x from the lane that holds the row's sum.
-        auto step = [&](const TokenIn &in, int t) {
+        auto step = [&](const TokenIn &in, int t) -> float {
             float2 a2[RPT];
 #pragma unroll
             for (int q = 0; q < RPT; ++q) {
@@ -504,9 +645,15 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan
                 // row store the same value (no divergent branch around the store)
                 const float ysum = reduce_rows<LANES, RPT>(part, j);
                 const float yv = fmaf(in.cf.y, ysum, Dv * pX[t * xs + yq]);
-                if (ystore)
-                    yrow[t * HP] = yv;
+                if (ystore) {
+                    if constexpr (TILE)
+                        st_shared_unordered(pY + t * xs, yv);
+                    else
+                        yrow[t * HP] = yv;
+                }
+                return yv;
             }
+            return 0.f;
         };
         // Anchor tokens (any head of the block) rescale U before their update;
         // a head that does not anchor there has r = 1 (exact no-op).  Token 0
@@ -542,8 +689,19 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan
         // back to S at the chunk end: U <- Lambda_last U
         rescale(pCf[(cnt - 1) * hc].y);
         __syncwarp();
-        if (c + kSlots < n_chunks)          // the producer refills this slot with chunk c+3
+        // release the slot: the producer refills it with chunk c+3 (with the
+        // output tile it first writes the tile out; with the gated output the
+        // release comes after the chunk's gating, at the start of chunk c+1)
+        if (!GATED && (TILE || c + kSlots < n_chunks))
             bar_arrive(kBarEmpty + b, nthr);
+    }
+    if constexpr (GATED) {
+        if (n_chunks > 0) {                 // the last chunk: every consumer warp done with it
+            bar_sync(kBarConsumers, nthr - 32);
+            gate(n_chunks - 1);
+            __syncwarp();
+            bar_arrive(kBarEmpty + (n_chunks - 1) % kSlots, nthr);
+        }
     }
 
     // ---- A7 state store: slot (last segment) or the unit's scratch (state pass) ----
@@ -567,29 +725,67 @@ prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan
     }
 }
 
+template <int LANES, int VPL, int RPT, bool EXACT, int MODE>
+__global__ void __launch_bounds__(256, 1)
+prefill_scaled_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan plan, const GatedOut gt)
+{
+    griddep_entry();
+    prefill_scaled_body<LANES, VPL, RPT, EXACT, MODE, 0>(a, geo, plan, gt);
+}
+
+// At most 168 registers: two blocks of five warps put three warps on some SM
+// sub-partition, whose register file holds 16 K registers.
+template <int LANES, int VPL, int RPT, bool EXACT, int EPI>
+__global__ void __maxnreg__(168)
+prefill_scaled_tile_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan plan, const GatedOut gt)
+{
+    griddep_entry();
+    prefill_scaled_body<LANES, VPL, RPT, EXACT, kScanFull, EPI>(a, geo, plan, gt);
+}
+
 namespace {
+
+// Shapes with the output-tile variants (EPI 1 and 2): the automatic shapes of
+// head_dim 64 at d_state 128 and 64.
+template <int LANES, int VPL, int RPT>
+constexpr bool kHasTile = LANES == 8 && RPT == 4 && (VPL == 4 || VPL == 2);
 
 template <int LANES, int VPL, int RPT>
 cudaError_t launch_scaled_one(const ScanArgs &a, const PrefillGeom &g, const SegmentPlan &plan, int mode,
-                              long long n_units, size_t smem, cudaStream_t stream)
+                              long long n_units, size_t smem, int epi, const GatedOut &gt, cudaStream_t stream)
 {
     const bool exact = (a.N / 4) == LANES * VPL;
     const int threads = (g.rows_per_cta / RPT) * LANES + 32;     // consumers + one producer warp
     const dim3 grid((unsigned)(n_units * a.G * g.runs_per_group));
-    void (*kern)(const ScanArgs, const PrefillGeom, const SegmentPlan);
-    if (mode == kScanFull)
-        kern = exact ? prefill_scaled_kernel<LANES, VPL, RPT, true, kScanFull>
-                     : prefill_scaled_kernel<LANES, VPL, RPT, false, kScanFull>;
-    else
+    void (*kern)(const ScanArgs, const PrefillGeom, const SegmentPlan, const GatedOut) = nullptr;
+    if (mode != kScanFull) {
+        if (epi != 0)
+            return cudaErrorInvalidValue;
         kern = exact ? prefill_scaled_kernel<LANES, VPL, RPT, true, kScanStateOnly>
                      : prefill_scaled_kernel<LANES, VPL, RPT, false, kScanStateOnly>;
+    } else if (epi == 0) {
+        kern = exact ? prefill_scaled_kernel<LANES, VPL, RPT, true, kScanFull>
+                     : prefill_scaled_kernel<LANES, VPL, RPT, false, kScanFull>;
+    } else {
+        if (threads > kTileThreads)
+            return cudaErrorInvalidValue;
+        if constexpr (kHasTile<LANES, VPL, RPT>) {
+            if (epi == 1)
+                kern = exact ? prefill_scaled_tile_kernel<LANES, VPL, RPT, true, 1>
+                             : prefill_scaled_tile_kernel<LANES, VPL, RPT, false, 1>;
+            else if (epi == 2 && gt.out)
+                kern = exact ? prefill_scaled_tile_kernel<LANES, VPL, RPT, true, 2>
+                             : prefill_scaled_tile_kernel<LANES, VPL, RPT, false, 2>;
+        }
+        if (!kern)
+            return cudaErrorInvalidValue;
+    }
     if (smem > 48 * 1024) {
         cudaError_t e = set_dynamic_smem(reinterpret_cast<const void *>(kern), smem);
         if (e != cudaSuccess)
             return e;
     }
-    kern<<<grid, threads, smem, stream>>>(a, g, plan);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, dim3(threads), smem, stream, a, g, plan, gt);
 }
 
 }  // namespace
@@ -609,12 +805,24 @@ bool prefill_scaled_supported(int lanes, int vpl, int rpt)
     return false;
 }
 
+bool prefill_scaled_tile_supported(int lanes, int vpl, int rpt, int rows_per_cta)
+{
+    if ((rows_per_cta / rpt) * lanes + 32 > kTileThreads)
+        return false;
+#define X(L, V, R) if (lanes == L && vpl == V && rpt == R) return kHasTile<L, V, R>;
+    SSM_SCALED_SHAPES(X)
+#undef X
+    return false;
+}
+
 cudaError_t launch_prefill_scaled(const ScanArgs &a, const PrefillGeom &g, int lanes, int vpl, int rpt,
                                   const SegmentPlan &plan, int mode, long long n_units, size_t smem,
-                                  cudaStream_t stream)
+                                  cudaStream_t stream, int epi, const GatedOut *gated)
 {
+    const GatedOut gt = gated ? *gated : GatedOut{};
 #define X(L, V, R) \
-    if (lanes == L && vpl == V && rpt == R) return launch_scaled_one<L, V, R>(a, g, plan, mode, n_units, smem, stream);
+    if (lanes == L && vpl == V && rpt == R) \
+        return launch_scaled_one<L, V, R>(a, g, plan, mode, n_units, smem, epi, gt, stream);
     SSM_SCALED_SHAPES(X)
 #undef X
     return cudaErrorInvalidValue;

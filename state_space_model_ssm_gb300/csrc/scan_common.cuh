@@ -96,11 +96,39 @@ __device__ __forceinline__ int reduced_row(int j)
     return r;
 }
 
+// The first lane (of LANES) whose reduced sum is row r: the inverse of
+// reduced_row for the lanes whose low bits are zero.
+template <int LANES, int RPT>
+__device__ __forceinline__ int reduced_lane(int r)
+{
+    constexpr int LV = Log2<RPT>::value;
+    constexpr int LL = Log2<LANES>::value;
+    int j = 0;
+#pragma unroll
+    for (int k = 0; k < LV; ++k)
+        j |= ((r >> k) & 1) << (LL - 1 - k);
+    return j;
+}
+
 // True for one lane per reduced row (the lane whose low bits are zero).
 template <int LANES, int RPT>
 __device__ __forceinline__ bool reduced_writer(int j)
 {
     return (j & (LANES / RPT - 1)) == 0;
+}
+
+// Programmatic dependent launch.  Every kernel of the library is launched with
+// programmatic stream serialization (launch_pdl), so its blocks may be
+// scheduled while the previous kernel on the stream drains.  griddep_entry()
+// is the first statement of every kernel: it waits until the previous grid has
+// completed and its writes are visible (griddepcontrol.wait; nothing of ours
+// touches global memory before it), then lets the next kernel's blocks be
+// scheduled as SMs free up (griddepcontrol.launch_dependents).  The result is
+// the same as plain stream order; only launch latency and wave tails overlap.
+__device__ __forceinline__ void griddep_entry()
+{
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 }
 
 // True when a bounded device wait earlier in the same call gave up: the call's
@@ -148,6 +176,26 @@ __device__ __forceinline__ void cp_async_wait()
     asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
+// kernel<<<grid, block, smem, stream>>>(args...) with programmatic stream
+// serialization (see griddep_entry), then cudaGetLastError().
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 // cudaFuncSetAttribute(kernel, MaxDynamicSharedMemorySize, bytes) on the
 // current device, skipped when an earlier call already set at least `bytes`
 // for that (device, kernel) pair (api.cu).  Thread-safe.
@@ -181,9 +229,19 @@ struct SegmentPlan {
 constexpr int kScanFull = 0;        // the scan with y
 constexpr int kScanStateOnly = 1;   // one segment's state from zero, no y
 
+// The gated RMSNorm output written by the full pass itself (see
+// launch_gated_norm for the operation); out == nullptr: off.
+struct GatedOut {
+    const float *z;           // [T][H][P], 16-byte aligned
+    const float *w;           // [P]
+    float eps;
+    float *out;               // [T][H][P], 16-byte aligned
+};
+
 cudaError_t launch_prefill_scaled(const ScanArgs &a, const PrefillGeom &g, int lanes, int vpl,
                                   int rpt, const SegmentPlan &plan, int mode, long long n_units,
-                                  size_t smem_bytes, cudaStream_t stream);
+                                  size_t smem_bytes, cudaStream_t stream, int epi = 0,
+                                  const GatedOut *gated = nullptr);
 cudaError_t launch_segment_plan(const ScanArgs &a, const SegmentPlan &plan, int max_units,
                                 cudaStream_t stream);
 cudaError_t launch_segment_combine(const ScanArgs &a, const SegmentPlan &plan, int max_units,
@@ -202,7 +260,11 @@ bool segment_state_tc_maps(const ScanArgs &a, SegStateMaps *maps);
 cudaError_t launch_segment_state_tc(const ScanArgs &a, const SegmentPlan &plan, const SegStateMaps &maps,
                                     int max_units, cudaStream_t stream);
 bool prefill_scaled_supported(int lanes, int vpl, int rpt);
-size_t prefill_scaled_smem_bytes(const PrefillGeom &g, int N, int lanes);
+// True for the shapes (and block sizes) whose full pass has the output-tile
+// variants: y stored by the producer warp (epi 1), and also the gated output
+// (epi 2).
+bool prefill_scaled_tile_supported(int lanes, int vpl, int rpt, int rows_per_cta);
+size_t prefill_scaled_smem_bytes(const PrefillGeom &g, int N, int lanes, int epi = 0);
 constexpr int kScaledMaxChunk = 32;    // one warp lane per token in the coefficient pass
 
 // The SSD chunked form (ssd.cu): work unit u is chunk units[u] = (sequence,
@@ -292,6 +354,15 @@ cudaError_t launch_conv1d(const float *x, const float *w, const float *bias, flo
 // Gated RMSNorm of y per (token, head) row, after the scan (gated_norm.cu).
 cudaError_t launch_gated_norm(const ScanArgs &a, const float *z, const float *w, float eps, float *out,
                               cudaStream_t stream);
+
+// Decode as a stream of state tiles through shared memory (decode_bulk.cu):
+// d_state a multiple of 4 up to 128; no snapshots.  decode_bulk_status reads
+// (clear = false; synchronises the stream) or clears the kernel's status word,
+// nonzero when one of its bounded waits gave up.
+bool decode_bulk_supported(int N, size_t smem_optin);
+size_t decode_bulk_smem_bytes(int N);
+cudaError_t launch_decode_bulk(const ScanArgs &a, int sms, int fail_waits, cudaStream_t stream);
+cudaError_t decode_bulk_status(int *status, cudaStream_t stream, bool clear);
 
 cudaError_t launch_decode(const ScanArgs &a, const DecodeGeom &g, int lanes,
                           int vpl, int rpt, int grid_seqs, cudaStream_t stream);

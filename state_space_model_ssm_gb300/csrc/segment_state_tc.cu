@@ -63,7 +63,8 @@ constexpr int kSsRows = 128;               // M: state rows n (d_state padded)
 constexpr int kSsThreads = 256;           // warps 0-7 stage the operands; warp 8 issues TMA and MMAs
 constexpr int kSsBlock = kSsThreads + 32;
 constexpr int kSsQuads = kSsQ / 4;         // 16-byte K cells per row and chunk
-constexpr int kSsStages = 3;               // staged raw chunks: two in flight while one is used
+constexpr int kSsStages = 3;               // staged raw chunks: kSsLead in flight while one is used
+constexpr int kSsLead = kSsStages - 1;     // chunks whose TMA runs ahead of the one being staged
 
 // Shared memory (bytes), all offsets multiples of 1024: two buffers of the X
 // operand tiles (buffer b at b * buf; hi at 0, lo at x_lo), the staged raw chunks
@@ -183,6 +184,7 @@ __global__ void __launch_bounds__(kSsBlock, HB * XI <= 4 ? 2 : 1)
 segment_state_tc_kernel(const ScanArgs a, const SegmentPlan plan, const __grid_constant__ CUtensorMap tm_b,
                         const __grid_constant__ CUtensorMap tm_x)
 {
+    griddep_entry();
     constexpr int p_pad = 32 * XI, nx = HB * p_pad;
     constexpr SsLayout L = ss_layout(nx);
     constexpr uint32_t kBoxBytes = (uint32_t)(kSsQ * (kSsRows + nx) * 4);   // both TMA boxes of a chunk
@@ -273,12 +275,10 @@ segment_state_tc_kernel(const ScanArgs a, const SegmentPlan plan, const __grid_c
             wts[(j & 1) * 32 + lane] = dts * ssd::ex2(carry + after);
             carry += __shfl_sync(kFullMask, suf, lane & 16);
         };
-        if (lane == 0) {
-            issue(0);
-            if (nc > 1)
-                issue(1);
-        }
-        int issued = nc > 1 ? 2 : 1;                  // chunks whose TMA was started
+        if (lane == 0)
+            for (int j = 0; j < kSsLead && j < nc; ++j)
+                issue(j);
+        int issued = min(nc, kSsLead);                // chunks whose TMA was started
         const float dt0 = load_dt(0), dt1 = load_dt(1);
         float dt_ahead = load_dt(2);                  // dt of chunk j + 2 at iteration j
         weights(0, dt0);
@@ -304,10 +304,10 @@ segment_state_tc_kernel(const ScanArgs a, const SegmentPlan plan, const __grid_c
                     mma_ts(tmem, tah + 8 * kk, dxh, id, 1u);
                 }
                 commit(mmab + (j & 1));
-                if (j + 2 < nc)
-                    issue(j + 2);                     // its stage held chunk j - 1, consumed before the barrier
+                if (j + kSsLead < nc)
+                    issue(j + kSsLead);               // its stage held chunk j - 1, consumed before the barrier
             }
-            issued = min(nc, j + 3);
+            issued = min(nc, j + kSsLead + 1);
             if (j + 2 < nc)                           // slot j % 2 was read while chunk j was staged
                 weights(j + 2, dt_ahead);
             dt_ahead = dt_next;
@@ -452,9 +452,8 @@ cudaError_t launch_shape(const ScanArgs &a, const SegmentPlan &plan, const SegSt
     cudaError_t e = set_dynamic_smem(reinterpret_cast<const void *>(segment_state_tc_kernel<XI, HB>), smem);
     if (e != cudaSuccess)
         return e;
-    segment_state_tc_kernel<XI, HB><<<dim3((unsigned)max_units, (unsigned)(a.H / HB)), kSsBlock, smem, stream>>>(
-        a, plan, tm_b, tm_x);
-    return cudaGetLastError();
+    return launch_pdl(segment_state_tc_kernel<XI, HB>, dim3((unsigned)max_units, (unsigned)(a.H / HB)),
+                      dim3(kSsBlock), smem, stream, a, plan, tm_b, tm_x);
 }
 
 // Two heads per block where they share a group and their N (2 x head_dim

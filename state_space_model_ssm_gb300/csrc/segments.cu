@@ -31,6 +31,7 @@ __global__ void __launch_bounds__(1024)
 segment_plan_kernel(const int32_t *seq_lens, int n_seqs, int seg_len, int max_units,
                     int2 *units, int *unit_base, int *n_units, int *status)
 {
+    griddep_entry();
     __shared__ int warp_tot[32];
     __shared__ int carry;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
@@ -90,28 +91,50 @@ segment_plan_kernel(const int32_t *seq_lens, int n_seqs, int seg_len, int max_un
 
 // S_in[k+1] = d_k S_in[k] + L_k for k >= 1, in place over the units' scratch
 // (unit b+k of sequence i ends up holding S_in[k+1]; unit b already holds
-// L_0 = S_in[1]).  One thread per float4 of a state slot.
+// L_0 = S_in[1]).  One thread per float4 of a state slot.  The chain is serial
+// in k but its loads are not: each thread reads the L_k and d_k of up to
+// kCombineBatch segments before it runs them through the chain, so a
+// sequence's segments wait on one memory latency per batch, not one each.
+constexpr int kCombineBatch = 8;
+
 __global__ void __launch_bounds__(256)
 segment_combine_kernel(const ScanArgs a, const SegmentPlan plan, int max_units)
 {
+    griddep_entry();
     const int N4 = a.N >> 2;
     const long long slot4 = (long long)a.H * a.P * N4;         // float4 per state slot
     const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (e >= slot4 || call_failed(plan.status))      // no valid segment states to combine
         return;
     const int head = (int)((e / N4) / a.P);
+    float4 *__restrict__ st = reinterpret_cast<float4 *>(plan.seg_state);
+    const float *__restrict__ dec = plan.seg_decay;
     for (int seq = blockIdx.y; seq < a.n_seqs; seq += gridDim.y) {
         const int b = plan.unit_base[seq];
         const int nseg = plan.unit_base[seq + 1] - b;
         if (nseg <= 2 || b + nseg > max_units)
             continue;
-        float4 *st = reinterpret_cast<float4 *>(plan.seg_state);
         float4 S = st[(long long)b * slot4 + e];
-        for (int k = 1; k <= nseg - 2; ++k) {
-            const float d = plan.seg_decay[(long long)(b + k) * a.H + head];
-            const float4 L = st[(long long)(b + k) * slot4 + e];
-            S = make_float4(fmaf(d, S.x, L.x), fmaf(d, S.y, L.y), fmaf(d, S.z, L.z), fmaf(d, S.w, L.w));
-            st[(long long)(b + k) * slot4 + e] = S;
+        for (int k0 = 1; k0 <= nseg - 2; k0 += kCombineBatch) {
+            float4 L[kCombineBatch];
+            float d[kCombineBatch];
+#pragma unroll
+            for (int i = 0; i < kCombineBatch; ++i) {
+                const int k = k0 + i;
+                if (k <= nseg - 2) {
+                    L[i] = st[(long long)(b + k) * slot4 + e];
+                    d[i] = dec[(long long)(b + k) * a.H + head];
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < kCombineBatch; ++i) {
+                const int k = k0 + i;
+                if (k <= nseg - 2) {
+                    S = make_float4(fmaf(d[i], S.x, L[i].x), fmaf(d[i], S.y, L[i].y), fmaf(d[i], S.z, L[i].z),
+                                    fmaf(d[i], S.w, L[i].w));
+                    st[(long long)(b + k) * slot4 + e] = S;
+                }
+            }
         }
     }
 }
@@ -120,19 +143,16 @@ segment_combine_kernel(const ScanArgs a, const SegmentPlan plan, int max_units)
 
 cudaError_t launch_segment_plan(const ScanArgs &a, const SegmentPlan &plan, int max_units, cudaStream_t stream)
 {
-    segment_plan_kernel<<<1, 1024, 0, stream>>>(a.seq_lens, a.n_seqs, plan.seg_len, max_units,
-                                                const_cast<int2 *>(plan.units),
-                                                const_cast<int *>(plan.unit_base),
-                                                const_cast<int *>(plan.n_units), plan.status);
-    return cudaGetLastError();
+    return launch_pdl(segment_plan_kernel, dim3(1), dim3(1024), 0, stream, a.seq_lens, a.n_seqs, plan.seg_len,
+                      max_units, const_cast<int2 *>(plan.units), const_cast<int *>(plan.unit_base),
+                      const_cast<int *>(plan.n_units), plan.status);
 }
 
 cudaError_t launch_segment_combine(const ScanArgs &a, const SegmentPlan &plan, int max_units, cudaStream_t stream)
 {
     const long long slot4 = (long long)a.H * a.P * (a.N >> 2);
     const dim3 grid((unsigned)((slot4 + 255) / 256), (unsigned)(a.n_seqs < 65535 ? a.n_seqs : 65535));
-    segment_combine_kernel<<<grid, 256, 0, stream>>>(a, plan, max_units);
-    return cudaGetLastError();
+    return launch_pdl(segment_combine_kernel, grid, dim3(256), 0, stream, a, plan, max_units);
 }
 
 }  // namespace ssm

@@ -83,6 +83,7 @@ template <int Q>
 __global__ void __launch_bounds__(kStateThreads)
 ssd_chunk_state_kernel(const ScanArgs a, const SsdPlan p, const SsdGeom sg)
 {
+    griddep_entry();
     extern __shared__ float4 smem4[];
     const int NS = sg.bs_stride, PS = sg.xw_stride, nbuf = sg.state_buffers;
     float *Bs = reinterpret_cast<float *>(smem4);     // [Q][NS]     B_s[n] (tf32)
@@ -176,6 +177,7 @@ constexpr int kPassBatch = 32;
 __global__ void __launch_bounds__(kPassThreads)
 ssd_state_pass_kernel(const ScanArgs a, const SsdPlan p, int max_units)
 {
+    griddep_entry();
     extern __shared__ float4 pass_buf[];               // [kPassBatch][kPassThreads]
     const int N4 = a.N >> 2;
     const long long slot4 = (long long)a.H * a.P * N4;
@@ -343,6 +345,7 @@ template <int Q, int NBY>
 __global__ void __launch_bounds__(2 * Q)
 ssd_output_kernel(const ScanArgs a, const SsdPlan p, const SsdGeom sg)
 {
+    griddep_entry();
     constexpr int QB = Q / 8;                         // 8-token column blocks per chunk
     constexpr int kThreads = 2 * Q;
     constexpr float kLog2e = 1.4426950408889634f;
@@ -534,10 +537,7 @@ cudaError_t launch_ssd_q(const ScanArgs &a, const SsdPlan &plan, const SsdGeom &
         e = set_dynamic_smem(reinterpret_cast<const void *>(state_k), g.smem_state);
         if (e != cudaSuccess)
             return e;
-        e = timed(tm, [&] {
-            state_k<<<grid, kStateThreads, g.smem_state, stream>>>(a, plan, g);
-            return cudaGetLastError();
-        });
+        e = timed(tm, [&] { return launch_pdl(state_k, grid, dim3(kStateThreads), g.smem_state, stream, a, plan, g); });
     }
     if (e != cudaSuccess)
         return e;
@@ -550,8 +550,8 @@ cudaError_t launch_ssd_q(const ScanArgs &a, const SsdPlan &plan, const SsdGeom &
     if (e != cudaSuccess)
         return e;
     e = timed(tm, [&] {
-        ssd_state_pass_kernel<<<pgrid, kPassThreads, pass_smem, stream>>>(a, plan, max_units);
-        return cudaGetLastError();
+        return launch_pdl(ssd_state_pass_kernel, pgrid, dim3(kPassThreads), (size_t)pass_smem, stream, a, plan,
+                          max_units);
     });
     if (e != cudaSuccess)
         return e;
@@ -573,10 +573,7 @@ cudaError_t launch_ssd_q(const ScanArgs &a, const SsdPlan &plan, const SsdGeom &
     e = set_dynamic_smem(reinterpret_cast<const void *>(out_k), g.smem_out);
     if (e != cudaSuccess)
         return e;
-    return timed(tm, [&] {
-        out_k<<<grid, 2 * Q, g.smem_out, stream>>>(a, plan, g);
-        return cudaGetLastError();
-    });
+    return timed(tm, [&] { return launch_pdl(out_k, grid, dim3(2 * Q), g.smem_out, stream, a, plan, g); });
 }
 
 }  // namespace

@@ -183,6 +183,7 @@ __device__ __forceinline__ void xraw_transpose(char *xt, uint32_t lx, const char
 __global__ void __launch_bounds__(kTcBlock, 1)
 ssd_output_tc_kernel(const ScanArgs a, const SsdPlan p, const SsdGeom sg)
 {
+    griddep_entry();
     extern __shared__ __align__(1024) unsigned char tc_smem[];
     ChunkRange c;
     if (!chunk_of(a, p, blockIdx.x, c) || c.len == 0)
@@ -477,8 +478,7 @@ cudaError_t launch_ssd_output_tc(const ScanArgs &a, const SsdPlan &plan, const S
     cudaError_t e = set_dynamic_smem(reinterpret_cast<const void *>(ssd_output_tc_kernel), smem);
     if (e != cudaSuccess)
         return e;
-    ssd_output_tc_kernel<<<grid, kTcBlock, smem, stream>>>(a, plan, g);
-    return cudaGetLastError();
+    return launch_pdl(ssd_output_tc_kernel, grid, dim3(kTcBlock), smem, stream, a, plan, g);
 }
 
 }  // namespace ssm

@@ -400,6 +400,37 @@ def test_parity_gated_norm_odd_head_dim_and_segments():
         assert_gated(inp, y_ref, gated, z, w, 1e-6)
 
 
+def test_parity_gated_norm_prefill_1x4096():
+    """The gated output at the measured prefill workload through ssm_scan_ws
+    (time segments): the full pass writes it itself (blocks of one head)."""
+    from tests.gpu_helpers import assert_gated, run_gpu_gated
+    inp = workload("prefill_1x4096")
+    y_ref, s_ref = oracle.scan_inputs(inp)
+    y, s, gated, z, w = run_gpu_gated(inp, eps=1e-5, workspace=True)
+    assert_parity(inp, y, s, y_ref, s_ref)
+    assert_gated(inp, y_ref, gated, z, w, 1e-5)
+
+
+def test_parity_y_not_16_byte_aligned():
+    """y only 4-byte aligned: the full pass's output tile falls back to scalar
+    stores (same results)."""
+    inp = make_inputs(Geometry(8, 64, 128, 2), [700, 3, 260], [1, 0, 1], seed=57)
+    y_ref, s_ref = oracle.scan_inputs(inp)
+    d = inp.to("cuda")
+    buf = torch.full((d.x.numel() + 1,), float("nan"), device="cuda")
+    y = buf[1:].view(d.x.shape)
+    for ws in (False, True):
+        state = d.state.clone()
+        wsb = None
+        if ws:
+            g = inp.geom
+            wsb = torch.empty(bd.workspace_bytes(inp.n_seqs, inp.n_tokens, g.n_heads, g.head_dim, g.d_state,
+                                                 g.n_groups), dtype=torch.uint8, device="cuda")
+        bd.ssm_scan(state, d.x, d.dt, d.A, d.B, d.C, d.D, d.seq_starts, d.seq_lens, d.resume, y=y, workspace=wsb)
+        torch.cuda.synchronize()
+        assert_parity(inp, y.double().cpu().numpy(), state.double().cpu().numpy(), y_ref, s_ref)
+
+
 # ---- per-token state snapshots (speculative verify) ----
 
 @pytest.mark.parametrize("fused_dt", [False, True], ids=["plain", "fused_dt"])
