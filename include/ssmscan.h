@@ -58,9 +58,9 @@
  *                        misaligned pointer, bad tuning value;
  *   SSM_ERR_UNSUPPORTED  d_state not a multiple of 4, d_state > 1024;
  *   SSM_ERR_CUDA         a CUDA call or launch failed (cudaGetLastError);
- *   SSM_ERR_TIMEOUT      a bounded device wait gave up (the pipelined kernels:
- *                        the segments' state pass, the SSD chunk-state and
- *                        output kernels, the tile-stream decode kernel).  Each such wait
+ *   SSM_ERR_TIMEOUT      a bounded device wait gave up (the pipelined
+ *                        tensor-core kernels: the segments' state pass and the
+ *                        SSD chunk-state and output kernels).  Each such wait
  *                        polls an mbarrier a bounded number of times (seconds);
  *                        on giving up the kernel sets a status word in the
  *                        workspace, waits for its copies and products in
@@ -76,11 +76,7 @@
  *                            NaN for every owned token and the slots keep their
  *                            contents; when an output block gave up, y is NaN
  *                            over that block's chunk and heads (the slots hold
- *                            the final states);
- *                          - the tile-stream decode kernel: a block that gave
- *                            up writes NaN to the y rows of its remaining state
- *                            tiles and leaves those tiles' slot rows as they
- *                            were.
+ *                            the final states).
  *                        SSM_SCAN_TEST_FAIL_WAITS=1 makes those waits give up
  *                        at once (tests of this path).
  * n_seqs == 0 is a successful no-op.
@@ -106,12 +102,7 @@ typedef enum {
 /* Kernel path selection for ssm_scan_tuned. */
 enum {
     SSM_PATH_AUTO = 0,           /* decode when n_tokens == n_seqs, else prefill */
-    SSM_PATH_DECODE = 1,         /* decode kernels; correct for any lengths.  With no explicit
-                                    lanes_per_row, rows_per_thread or ctas_per_sm, no
-                                    snapshots and d_state a multiple of 4 up to 128: the
-                                    tile-stream kernel (state tiles move between slot and
-                                    shared memory by bulk copies, several tiles in flight
-                                    per block); otherwise the warp-per-row kernel */
+    SSM_PATH_DECODE = 1,         /* warp-per-row kernel; correct for any lengths */
     SSM_PATH_PREFILL = 2,        /* chunk-staged kernel, decay-rescaled state with packed
                                     fp32x2 FMAs; correct for any lengths */
     SSM_PATH_PREFILL_DIRECT = 3  /* chunk-staged kernel stepping S itself (one multiply

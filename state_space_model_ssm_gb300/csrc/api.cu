@@ -466,24 +466,6 @@ int scan_kernels(const ssm::ScanArgs &a, const ssm_scan_tuning &t, const DeviceI
     if (path == SSM_PATH_AUTO)
         path = (n_tokens == n_seqs) ? SSM_PATH_DECODE : SSM_PATH_PREFILL;
 
-    if (path == SSM_PATH_DECODE && !a.snaps && t.lanes_per_row == 0 && t.rows_per_thread == 0 &&
-        t.ctas_per_sm == 0 && ssm::decode_bulk_supported(N, (size_t)dev.smem_optin)) {
-        // the tile-stream kernel (decode_bulk.cu); its status word is read back
-        // only in the debug mode
-        const bool chk = check_env();
-        if (chk && ssm::decode_bulk_status(nullptr, stream, true) != cudaSuccess)
-            return SSM_ERR_CUDA;
-        if (ssm::timed(tm, [&] { return ssm::launch_decode_bulk(a, dev.sms, fail_waits_env() ? 1 : 0, stream); }) !=
-            cudaSuccess)
-            return SSM_ERR_CUDA;
-        if (chk) {
-            int st = 0;
-            if (ssm::decode_bulk_status(&st, stream, false) != cudaSuccess)
-                return SSM_ERR_CUDA;
-            return st != 0 ? SSM_ERR_TIMEOUT : SSM_OK;
-        }
-        return SSM_OK;
-    }
     if (path == SSM_PATH_DECODE) {
         const int lanes = t.lanes_per_row ? t.lanes_per_row : std::min(32, pow2ceil(N4));
         int rpt = t.rows_per_thread;
@@ -537,12 +519,13 @@ int scan_kernels(const ssm::ScanArgs &a, const ssm_scan_tuning &t, const DeviceI
             return SSM_ERR_CUDA;
         return SSM_OK;
     }
-    // Output of the full pass: the consumers store y (epi 0).  With the gated
-    // RMSNorm requested, where the shape has the output-tile variants, y goes
-    // through a shared-memory tile from which the producer warp writes y and
-    // the gated output (epi 2); its blocks must hold exactly one head (rows per
-    // block = head_dim), z be 16-byte aligned (staged like x) and the extra
-    // tiles fit the shared memory.
+    // Output of the full pass.  Where the shape has the output-tile variants, y
+    // goes through a shared-memory tile that the producer warp writes out
+    // (epi 1; about 1 % faster than the consumers' own stores, which the other
+    // shapes keep: epi 0); with the gated RMSNorm requested, the consumer warps
+    // also apply it from that tile (epi 2), which needs blocks of exactly one
+    // head (rows per block = head_dim) and z 16-byte aligned (staged like x).
+    // Each needs its extra tiles to fit the shared memory.
     const ssm::GatedOut *fuse = nullptr;
     int epi = 0;
     size_t smem_full = pl.smem;
@@ -552,6 +535,8 @@ int scan_kernels(const ssm::ScanArgs &a, const ssm_scan_tuning &t, const DeviceI
             ssm::prefill_scaled_smem_bytes(pl.g, N, pl.lanes, 2) <= (size_t)dev.smem_optin) {
             fuse = gated;
             epi = 2;
+        } else if (ssm::prefill_scaled_smem_bytes(pl.g, N, pl.lanes, 1) <= (size_t)dev.smem_optin) {
+            epi = 1;
         }
         smem_full = ssm::prefill_scaled_smem_bytes(pl.g, N, pl.lanes, epi);
     }

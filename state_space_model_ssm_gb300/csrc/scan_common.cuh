@@ -355,15 +355,6 @@ cudaError_t launch_conv1d(const float *x, const float *w, const float *bias, flo
 cudaError_t launch_gated_norm(const ScanArgs &a, const float *z, const float *w, float eps, float *out,
                               cudaStream_t stream);
 
-// Decode as a stream of state tiles through shared memory (decode_bulk.cu):
-// d_state a multiple of 4 up to 128; no snapshots.  decode_bulk_status reads
-// (clear = false; synchronises the stream) or clears the kernel's status word,
-// nonzero when one of its bounded waits gave up.
-bool decode_bulk_supported(int N, size_t smem_optin);
-size_t decode_bulk_smem_bytes(int N);
-cudaError_t launch_decode_bulk(const ScanArgs &a, int sms, int fail_waits, cudaStream_t stream);
-cudaError_t decode_bulk_status(int *status, cudaStream_t stream, bool clear);
-
 cudaError_t launch_decode(const ScanArgs &a, const DecodeGeom &g, int lanes,
                           int vpl, int rpt, int grid_seqs, cudaStream_t stream);
 bool decode_supported(int lanes, int vpl, int rpt);
