@@ -279,14 +279,21 @@ segment_state_tc_kernel(const ScanArgs a, const SegmentPlan plan, const __grid_c
             for (int j = 0; j < kSsLead && j < nc; ++j)
                 issue(j);
         int issued = min(nc, kSsLead);                // chunks whose TMA was started
+        // dt (scattered 4-byte reads) is loaded kDtAhead iterations before its
+        // weights are formed, so a cold read's latency stays off the chunk chain:
+        // at iteration j, dtq[i] holds the dt of chunk j + 2 + i
+        constexpr int kDtAhead = 4;
         const float dt0 = load_dt(0), dt1 = load_dt(1);
-        float dt_ahead = load_dt(2);                  // dt of chunk j + 2 at iteration j
+        float dtq[kDtAhead];
+#pragma unroll
+        for (int i = 0; i < kDtAhead; ++i)
+            dtq[i] = load_dt(2 + i);
         weights(0, dt0);
         __syncthreads();                              // chunk 0's weights published
         if (nc > 1)
             weights(1, dt1);
         for (int j = 0; j < nc; ++j) {
-            const float dt_next = load_dt(j + 3);
+            const float dt_next = load_dt(j + 2 + kDtAhead);
             if (__syncthreads_or(0))
                 break;                                // the staging warps gave up
             if (lane == 0) {
@@ -309,8 +316,11 @@ segment_state_tc_kernel(const ScanArgs a, const SegmentPlan plan, const __grid_c
             }
             issued = min(nc, j + kSsLead + 1);
             if (j + 2 < nc)                           // slot j % 2 was read while chunk j was staged
-                weights(j + 2, dt_ahead);
-            dt_ahead = dt_next;
+                weights(j + 2, dtq[0]);
+#pragma unroll
+            for (int i = 0; i + 1 < kDtAhead; ++i)
+                dtq[i] = dtq[i + 1];
+            dtq[kDtAhead - 1] = dt_next;
         }
         const float cl = __shfl_sync(kFullMask, carry, 16 * (lane & 1));   // lane hb: head hb's log2 decay
         if (lane < HB) {

@@ -166,6 +166,9 @@ ssd_chunk_state_kernel(const ScanArgs a, const SsdPlan p, const SsdGeom sg)
 // State pass, in place over the units of each sequence:
 //   S = slot (resume) or 0;  for k: tmp = dS_k; W_k = S; S = exp(a_last,k) S + tmp;
 //   slot = S.
+// W_k (the incoming state of chunk k) is stored rounded to TF32: the output
+// kernels use it only as an operand of C S_in^T, whose operands are TF32, so
+// they need not round it again; the chain itself runs on the unrounded S.
 // One thread per float4 of a state slot.  The chain is serial in k but its
 // loads are not: a thread copies the dS_k of up to kPassBatch chunks into its
 // own column of shared memory with cp.async (no registers held while they fly)
@@ -208,7 +211,7 @@ ssd_state_pass_kernel(const ScanArgs a, const SsdPlan p, int max_units)
             for (int j = 0; j < kPassBatch; ++j) {
                 if (j < n) {
                     const float4 d = mine[j * kPassThreads];
-                    W[(long long)(b + k0 + j) * slot4 + e] = S;
+                    W[(long long)(b + k0 + j) * slot4 + e] = ssd::tf32_round4(S);   // an operand only
                     const float f = expf(ld[j]);
                     S = make_float4(fmaf(f, S.x, d.x), fmaf(f, S.y, d.y), fmaf(f, S.z, d.z), fmaf(f, S.w, d.w));
                 }

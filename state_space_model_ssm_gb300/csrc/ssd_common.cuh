@@ -159,6 +159,48 @@ struct ChunkDecay {
     float last;
 };
 
+// This lane's dt values of head h in the chunk (tokens lane*R .. +R-1; 0 past its end).
+template <int Q>
+__device__ __forceinline__ void chunk_dt(const ScanArgs &a, const ChunkRange &c, int h, int lane,
+                                         float (&d)[ChunkDecay<Q>::R])
+{
+    constexpr int R = ChunkDecay<Q>::R;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int t = lane * R + r;
+        d[r] = t < c.len ? a.dt[(size_t)(c.t0 + t) * a.H + h] : 0.f;
+    }
+}
+
+// chunk_decay from dt values this lane already holds (chunk_dt), A[h] = Ah.
+template <int Q>
+__device__ __forceinline__ void chunk_decay_from(float Ah, const float (&d)[ChunkDecay<Q>::R], int lane,
+                                                 ChunkDecay<Q> &cd)
+{
+    constexpr int R = ChunkDecay<Q>::R;
+    float run = 0.f;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        cd.d[r] = d[r];
+        run += cd.d[r] * Ah;
+        cd.a[r] = run;
+    }
+    float incl = run;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float v = __shfl_up_sync(kFullMask, incl, off);
+        if (lane >= off)
+            incl += v;
+    }
+    float excl = __shfl_up_sync(kFullMask, incl, 1);
+    if (lane == 0)
+        excl = 0.f;
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+        cd.a[r] += excl;
+    cd.last = __shfl_sync(kFullMask, incl, 31);
+}
+
 template <int Q>
 __device__ __forceinline__ void chunk_decay(const ScanArgs &a, const ChunkRange &c, int h, int lane,
                                             ChunkDecay<Q> &cd)

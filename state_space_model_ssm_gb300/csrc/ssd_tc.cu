@@ -261,24 +261,34 @@ ssd_output_tc_kernel(const ScanArgs a, const SsdPlan p, const SsdGeom sg)
     const uint32_t tm_c = tmem, tm_g = tmem + ccols, tm_yi = tm_g + kTcQ, tm_yx = tm_yi + P;
     const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
 
-    // C into TMEM: this thread's row t, its half of the (padded) columns
+    // C into TMEM: this thread's row t, its half of the (padded) columns (at
+    // most 64: d_state <= 128).  Every load is issued before the first TMEM
+    // store, so the setup waits on one memory latency, not one per 16 columns.
     {
         const bool row_ok = t < c.len;
         const float *crow = a.C + bc_off + (size_t)(row_ok ? t : 0) * a.G * N;
-        const int cw = ccols >> 1;
-        for (int c0 = half * cw; c0 < half * cw + cw; c0 += 16) {
-            float v[16];
+        const int cw = ccols >> 1, cbase = half * cw;
+        float4 cv[16];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float4 cv = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (row_ok && c0 + 4 * q < N)
-                    cv = __ldg(reinterpret_cast<const float4 *>(crow + c0 + 4 * q));
-                v[4 * q] = tf32_round(cv.x);
-                v[4 * q + 1] = tf32_round(cv.y);
-                v[4 * q + 2] = tf32_round(cv.z);
-                v[4 * q + 3] = tf32_round(cv.w);
+        for (int i = 0; i < 16; ++i) {
+            cv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (4 * i < cw && row_ok && cbase + 4 * i < N)
+                cv[i] = __ldg(reinterpret_cast<const float4 *>(crow + cbase + 4 * i));
+        }
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+            if (16 * cc < cw) {
+                float v[16];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float4 w = cv[4 * cc + q];
+                    v[4 * q] = tf32_round(w.x);
+                    v[4 * q + 1] = tf32_round(w.y);
+                    v[4 * q + 2] = tf32_round(w.z);
+                    v[4 * q + 3] = tf32_round(w.w);
+                }
+                tmem_st16(tm_c + lane_off + cbase + 16 * cc, v);
             }
-            tmem_st16(tm_c + lane_off + c0, v);
         }
         asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
     }
@@ -300,13 +310,20 @@ ssd_output_tc_kernel(const ScanArgs a, const SsdPlan p, const SsdGeom sg)
         tc::commit(bar_g);
     }
 
+    // warp 0 loads the next head's dt (scattered 4-byte reads) while the
+    // current head computes, so that latency stays off the per-head chain
+    float dt_next[ChunkDecay<kTcQ>::R];
+    if (warp == 0)
+        chunk_dt<kTcQ>(a, c, g * hpg + hl0, lane, dt_next);
     for (int k = 0; k < nh && ok; ++k) {
         const int h = g * hpg + hl0 + k;
         const int b = nbuf == 2 ? (k & 1) : 0;
         char *St = sm + (b ? L.S[1] : L.S[0]), *XRt = sm + (b ? L.XR[1] : L.XR[0]);
         if (warp == 0) {
             ChunkDecay<kTcQ> cd;
-            chunk_decay<kTcQ>(a, c, h, lane, cd);
+            chunk_decay_from<kTcQ>(a.A[h], dt_next, lane, cd);
+            if (k + 1 < nh)
+                chunk_dt<kTcQ>(a, c, h + 1, lane, dt_next);
             // a of the last column of each 16-column piece (lane 4i+3 holds it)
             constexpr int R = ChunkDecay<kTcQ>::R;
 #pragma unroll
@@ -322,7 +339,8 @@ ssd_output_tc_kernel(const ScanArgs a, const SsdPlan p, const SsdGeom sg)
             ok = false;                               // S_in and x of head k never landed
             break;
         }
-        kmajor_round(St, L.ls, P, Np4, warp, lane);
+        // S_in arrives rounded to TF32 (the state pass stores it so); x is rounded
+        // as it is transposed
         xraw_transpose(XTt, L.lx, XRt, P, tid);
         fence_async_smem();
         compute_sync();                               // S_in, x^T, a_t, dt of head k ready
