@@ -15,7 +15,9 @@
 // (128-bit loads and stores, contiguous across a warp) over a run of 16 tokens
 // and keeps the last k-1 inputs in registers, so each input is read once plus
 // a k-1 halo per run.  A complete run issues all 16 of its loads before any
-// arithmetic (a quarter KiB per thread in flight), and SiLU takes the hardware
+// arithmetic (a quarter KiB per thread in flight; for kernel sizes 2..5
+// registers are capped for three blocks per SM, so other blocks' loads overlap
+// a block's arithmetic and stores), and SiLU takes the hardware
 // exponential and an approximate division, v / (1 + exp(-v)) (about 1e-6
 // relative), so the kernel stays bound by memory, not by the per-element
 // arithmetic.  The slot update runs as a second launch so that no output reads
@@ -87,7 +89,7 @@ __device__ __forceinline__ void store_ch(float *p, const Lanes<CH> &r)
 constexpr int kConvRun = 16;
 
 template <int CH, int K>
-__global__ void __launch_bounds__(kConvThreads)
+__global__ void __launch_bounds__(kConvThreads, (K >= 2 && K <= 5) ? 3 : 1)
 conv1d_out_kernel(const ConvArgs a)
 {
     griddep_entry();

@@ -411,6 +411,21 @@ def test_parity_gated_norm_prefill_1x4096():
     assert_gated(inp, y_ref, gated, z, w, 1e-5)
 
 
+@pytest.mark.parametrize("chunk", [16, 32])
+def test_parity_gated_norm_fused_two_consumer_warps(chunk):
+    """The fused gated output with blocks of one 32-row head (two consumer
+    warps, so a chunk's gating takes several rounds of eight-lane groups), with
+    and without time segments."""
+    from tests.gpu_helpers import assert_gated, run_gpu_gated
+    inp = make_inputs(Geometry(4, 32, 128, 2), [300, 45, 0, 7], [1, 0, 1, 0], seed=58)
+    y_ref, s_ref = oracle.scan_inputs(inp)
+    for ws in (False, True):
+        t = _tuning(path=bd.PATH_PREFILL, rows=32, chunk=chunk, seg=64 if ws else -1)
+        y, s, gated, z, w = run_gpu_gated(inp, eps=1e-5, tuning=t, workspace=ws)
+        assert_parity(inp, y, s, y_ref, s_ref)
+        assert_gated(inp, y_ref, gated, z, w, 1e-5)
+
+
 def test_parity_y_not_16_byte_aligned():
     """y only 4-byte aligned: the full pass's output tile falls back to scalar
     stores (same results)."""
