@@ -25,23 +25,24 @@
 //
 // A block owns one (segment, HB heads) and walks the segment's 16-token chunks
 // from the last to the first, so that a token's decay exponent, the sum of
-// dt A over the tokens after it, is a running suffix sum.  A ninth warp
-// drives the pipeline: it brings the raw rows of B ([16][128] floats, d_state
-// padded by the TMA's zero fill) and x ([16][HB][head_dim padded]) into a
-// ring of three stages with TMA, two chunks ahead, and forms each chunk's
-// weights (lane = head * 16 + token, carrying each head's total) into shared
-// memory one barrier before the chunk is staged.  The 8 staging warps turn
-// the staged chunk into operands.  B^T goes to TMEM, where the MMA takes its A
-// operand from (row n in lane n, one token per column): each thread splits
+// dt A over the tokens after it, is a running suffix sum.  Three roles hand
+// chunks to each other through mbarriers, so each runs ahead as far as its
+// ring allows.  A loader warp brings the raw rows of B ([16][128] floats,
+// d_state padded by the TMA's zero fill) and x ([16][HB][head_dim padded])
+// into a ring of three stages with TMA, each chunk's load started as soon as
+// the staging threads have read the chunk its stage held, and writes the
+// chunk's token weights (lane = head * 16 + token, carrying each head's total;
+// dt fetched with cp.async eight chunks ahead) beside it.  The 8 staging warps
+// turn a staged chunk into operands.  B^T goes to TMEM, where the MMA takes its
+// A operand from (row n in lane n, one token per column): each thread splits
 // half of one row (8 tokens, conflict-free 4-byte reads) and writes its hi and
 // lo parts with tcgen05.st, so the tensor core reads only X from shared
 // memory.  X_w is a K-major shared-memory tile: the values of 4 consecutive
 // tokens of one row form a 16-byte cell, written whole (consecutive rows
-// across a warp).  Two operand buffers alternate.  After the block's barrier
-// the ninth warp issues the chunk's 6 MMAs (K = 8 each), commits them to the
-// buffer's mbarrier (which the writers wait on two chunks later) and starts
-// the TMA of the chunk two ahead, while the staging warps go on to the next
-// chunk.  The epilogue reads the
+// across a warp).  Two operand buffers alternate.  Once a buffer is written the
+// MMA warp issues the chunk's 6 MMAs (K = 8 each) and commits them to the
+// buffer's mbarrier, which the staging warps wait on before they write that
+// buffer again.  The epilogue reads the
 // accumulator (warp w: state rows 32 (w % 4) .. +31, column half w / 4) and
 // stores L with the state-slot layout, coalesced over n.
 #include <cstring>
@@ -60,23 +61,27 @@ using namespace tc;
 
 constexpr int kSsQ = 16;                   // tokens per chunk (K of a chunk's products)
 constexpr int kSsRows = 128;               // M: state rows n (d_state padded)
-constexpr int kSsThreads = 256;           // warps 0-7 stage the operands; warp 8 issues TMA and MMAs
-constexpr int kSsBlock = kSsThreads + 32;
+constexpr int kSsThreads = 256;           // warps 0-7 stage the operands
+constexpr int kSsBlock = kSsThreads + 64;  // warp 8 issues the MMAs; warp 9 the TMA loads and the token weights
 constexpr int kSsQuads = kSsQ / 4;         // 16-byte K cells per row and chunk
-constexpr int kSsStages = 3;               // staged raw chunks: kSsLead in flight while one is used
-constexpr int kSsLead = kSsStages - 1;     // chunks whose TMA runs ahead of the one being staged
+constexpr int kSsStages = 3;               // staged raw chunks
+constexpr int kSsLead = kSsStages;         // chunks whose TMA is started before the one being staged
+constexpr int kSsDtRing = 8;               // chunks of dt in flight or waiting in shared memory
+constexpr int kSsBufs = 2;                 // operand buffers: staging of chunk j waits for chunk j - kSsBufs's products
 
-// Shared memory (bytes), all offsets multiples of 1024: two buffers of the X
-// operand tiles (buffer b at b * buf; hi at 0, lo at x_lo), the staged raw chunks
-// (stage s at raw + s * stage; B rows at 0, x rows at rx), mbarriers (full[3]
-// per stage, mma[2] per buffer), the TMEM address, the token weights of two
-// chunks and the heads' decays.
+// Shared memory (bytes), all offsets multiples of 1024: kSsBufs buffers of the
+// X operand tiles (buffer b at b * buf; hi at 0, lo at x_lo), the staged raw
+// chunks (stage s at raw + s * stage; B rows at 0, x rows at rx), mbarriers
+// (full[] and empty[] per stage, written[] and mma[] per buffer, drain), the
+// TMEM address, the token weights of each stage's chunk, the heads' decays and
+// the dt ring.
 struct SsLayout {
     uint32_t x_lo, buf;
     uint32_t raw, rx, stage;
     uint32_t bar, tslot, total;
-    uint32_t wts, dec;        // weights of two chunks [2][32] (lane = head * 16 + token); decays [HB],
-                              // then their logs [HB] at dec + 16
+    uint32_t wts, dec;        // weights of each stage's chunk [kSsStages][32] (lane = head * 16 + token);
+                              // decays [HB], then their logs [HB] at dec + 16
+    uint32_t dtr;             // dt of kSsDtRing chunks [kSsDtRing][32] (chunk j in row j % kSsDtRing)
     uint32_t lx;              // K-cell stride of the X tiles (nx rows)
 };
 
@@ -87,23 +92,24 @@ __host__ __device__ constexpr SsLayout ss_layout(int nx)
     const uint32_t tx = L.lx * kSsQuads;
     L.x_lo = tx;
     L.buf = 2 * tx;
-    L.raw = 2 * L.buf;
+    L.raw = kSsBufs * L.buf;
     L.rx = kSsQ * kSsRows * 4;
     L.stage = L.rx + (uint32_t)(kSsQ * nx * 4);
     L.bar = L.raw + kSsStages * L.stage;
-    L.tslot = L.bar + 8 * sizeof(uint64_t);
+    L.tslot = L.bar + (uint32_t)((2 * kSsStages + 2 * kSsBufs + 2) / 2 * 2 * sizeof(uint64_t));
     L.wts = L.tslot + 16;
-    L.dec = L.wts + 2 * 32 * 4;
-    L.total = L.dec + 32;
+    L.dec = L.wts + kSsStages * 32 * 4;
+    L.dtr = L.dec + 32;
+    L.total = L.dtr + kSsDtRing * 32 * 4;
     return L;
 }
 
-// TMEM: the accumulator in columns [0, nx), then two buffers of the B^T
+// TMEM: the accumulator in columns [0, nx), then kSsBufs buffers of the B^T
 // operand (buffer b at nx + 32 b: 16 hi columns, then 16 lo), one token per
 // column, state row n in lane n.
 __host__ __device__ constexpr uint32_t ss_tmem_cols(int nx)
 {
-    return nx + 64 <= 128 ? 128u : nx + 64 <= 256 ? 256u : 512u;
+    return nx + 32 * kSsBufs <= 128 ? 128u : nx + 32 * kSsBufs <= 256 ? 256u : 512u;
 }
 
 __device__ __forceinline__ float4 split_hi(float4 v, float4 &lo)
@@ -215,9 +221,11 @@ segment_state_tc_kernel(const ScanArgs a, const SegmentPlan plan, const __grid_c
     const int grp = h0 / (H / a.G);
     char *sm = reinterpret_cast<char *>(ss_smem);
     const uint32_t sbase = smem_u32(sm);
-    uint64_t *full = reinterpret_cast<uint64_t *>(sm + L.bar);     // per stage: TMA boxes landed
-    uint64_t *mmab = full + kSsStages;                             // per buffer: products done
-    uint64_t *drain = mmab + 2;                                    // after a failed wait: all products done
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + L.bar);     // per stage: TMA boxes landed, weights formed
+    uint64_t *empty = full + kSsStages;                            // per stage: every staging thread read it
+    uint64_t *written = empty + kSsStages;                         // per buffer: operands written
+    uint64_t *mmab = written + kSsBufs;                            // per buffer: products done
+    uint64_t *drain = mmab + kSsBufs;                              // after a failed wait: all products done
     const long cap = plan.fail_waits ? 0 : kSpinLimit;             // polls of a pipeline wait
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + L.tslot);
     float *wts = reinterpret_cast<float *>(sm + L.wts);
@@ -228,10 +236,14 @@ segment_state_tc_kernel(const ScanArgs a, const SegmentPlan plan, const __grid_c
     if (warp == 0)
         tmem_alloc(tslot, cols);
     if (tid == 0) {
-        for (int i = 0; i < kSsStages; ++i)
-            mbar_init(full + i, 1);
-        mbar_init(mmab, 1);
-        mbar_init(mmab + 1, 1);
+        for (int i = 0; i < kSsStages; ++i) {
+            mbar_init(full + i, 1 + 32);              // the TMA's expect_tx, then the 32 weights lanes
+            mbar_init(empty + i, kSsThreads);
+        }
+        for (int i = 0; i < kSsBufs; ++i) {
+            mbar_init(written + i, kSsThreads);
+            mbar_init(mmab + i, 1);
+        }
         mbar_init(drain, 1);
         mbar_init_fence();
     }
@@ -240,28 +252,69 @@ segment_state_tc_kernel(const ScanArgs a, const SegmentPlan plan, const __grid_c
     const uint32_t tmem = *tslot;
 
     if (warp == kSsThreads / 32) {
-        // ---- issuer warp: TMA two chunks ahead; the weights of each chunk one
-        // barrier before it is staged; a chunk's products once the block's
-        // barrier says that its operand buffer is written ----
-        // chunk j of the walk (tokens [c * 16, c * 16 + 16) of the segment, c = nc - 1 - j) into stage j % 3
-        auto issue = [&](int j) {
-            const int st = j % kSsStages, t = tok0 + (nc - 1 - j) * kSsQ;
+        // ---- MMA warp: a chunk's products once its operand buffer is written ----
+        bool mok = true;
+        if (lane == 0) {
+            int b = 0;                                // operand buffer of chunk j
+            for (int j = 0; j < nc; ++j) {
+                if (!mbar_wait(written + b, (uint32_t)((j / kSsBufs) & 1), cap)) {
+                    mok = false;                      // the staging warps gave up
+                    break;
+                }
+                fence_after();
+                constexpr uint32_t id = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(nx >> 3) << 17) |
+                                        ((uint32_t)(kSsRows >> 4) << 24);        // idesc_tf32(128, nx)
+                const uint32_t bx = sbase + b * L.buf;
+                const uint32_t tah = tmem + nx + 32 * b, tal = tah + 16;         // B^T hi, lo in TMEM
+#pragma unroll
+                for (int kk = 0; kk < kSsQ / 8; ++kk) {
+                    const uint64_t dxh = smem_desc(bx + 2 * kk * L.lx, L.lx, 128);
+                    const uint64_t dxl = smem_desc(bx + L.x_lo + 2 * kk * L.lx, L.lx, 128);
+                    mma_ts(tmem, tal + 8 * kk, dxh, id, (j > 0 || kk > 0) ? 1u : 0u);
+                    mma_ts(tmem, tah + 8 * kk, dxl, id, 1u);
+                    mma_ts(tmem, tah + 8 * kk, dxh, id, 1u);
+                }
+                commit(mmab + b);
+                b = b == kSsBufs - 1 ? 0 : b + 1;
+            }
+        }
+        __syncwarp();
+        if (__syncthreads_or(!mok) && lane == 0) {   // a wait gave up: drain before TMEM is freed
+            commit(drain);                            // arrives once every product issued so far is done
+            mbar_wait(drain, 0);
+        }
+        __syncthreads();
+        return;
+    }
+    if (warp == kSsThreads / 32 + 1) {
+        // ---- loader warp: chunk j's TMA into stage j % kSsStages once the
+        // staging threads have read the chunk that stage held, then its token
+        // weights; at the end the heads' decays ----
+        // chunk j of the walk (tokens [c * 16, c * 16 + 16) of the segment, c = nc - 1 - j)
+        auto issue = [&](int j, int st) {
+            const int t = tok0 + (nc - 1 - j) * kSsQ;
             char *raw = sm + L.raw + st * L.stage;
             mbar_expect_tx(full + st, kBoxBytes);
             tma_load_3d(raw, &tm_b, 0, grp, t, full + st);
             tma_load_3d(raw + L.rx, &tm_x, 0, h0, t, full + st);
         };
-        // weights: lane = head * 16 + token of the chunk
         constexpr float kLog2e = 1.4426950408889634f;
         const int wh = lane >> 4, ws = lane & 15;
         const float A2 = wh < HB ? a.A[h0 + wh] * kLog2e : 0.f;
-        auto load_dt = [&](int j) {
+        // dt of chunk j into ring row j % kSsDtRing, one cp.async group per chunk
+        // (zeros past the segment)
+        float *dtr = reinterpret_cast<float *>(sm + L.dtr);
+        auto fetch_dt = [&](int j) {
             const int s = (nc - 1 - j) * kSsQ + ws;
-            return (j < nc && wh < HB && s < len) ? __ldg(a.dt + (size_t)(tok0 + s) * H + h0 + wh) : 0.f;
+            const bool in = j < nc && wh < HB && s < len;
+            ssd::cp_async4_zfill(dtr + (j % kSsDtRing) * 32 + lane,
+                                 in ? a.dt + (size_t)(tok0 + s) * H + h0 + wh : a.dt, in ? 4 : 0);
+            cp_async_commit();
         };
         float carry = 0.f;                            // this lane's head: sum of dt A log2(e) walked so far
-        // w_s = dt_s 2^(A2 * sum of dt over the tokens after s) of chunk j into slot j % 2
-        auto weights = [&](int j, float dts) {
+        // w_s = dt_s 2^(A2 * sum of dt over the tokens after s) of chunk j into the weights of stage st
+        auto weights = [&](int j, int st) {
+            const float dts = dtr[(j % kSsDtRing) * 32 + lane];
             float suf = dts * A2;                     // inclusive suffix sum within the 16 lanes
 #pragma unroll
             for (int o = 1; o < kSsQ; o <<= 1) {
@@ -272,65 +325,40 @@ segment_state_tc_kernel(const ScanArgs a, const SegmentPlan plan, const __grid_c
             float after = __shfl_down_sync(kFullMask, suf, 1);
             if (ws == kSsQ - 1)
                 after = 0.f;
-            wts[(j & 1) * 32 + lane] = dts * ssd::ex2(carry + after);
+            wts[st * 32 + lane] = dts * ssd::ex2(carry + after);
             carry += __shfl_sync(kFullMask, suf, lane & 16);
         };
-        if (lane == 0)
-            for (int j = 0; j < kSsLead && j < nc; ++j)
-                issue(j);
-        int issued = min(nc, kSsLead);                // chunks whose TMA was started
-        // dt (scattered 4-byte reads) is loaded kDtAhead iterations before its
-        // weights are formed, so a cold read's latency stays off the chunk chain:
-        // at iteration j, dtq[i] holds the dt of chunk j + 2 + i
-        constexpr int kDtAhead = 4;
-        const float dt0 = load_dt(0), dt1 = load_dt(1);
-        float dtq[kDtAhead];
+        // dt (scattered 4-byte reads) is fetched kSsDtRing chunks ahead, so a
+        // cold read's latency stays off the chunk chain; group g carries chunk g
 #pragma unroll
-        for (int i = 0; i < kDtAhead; ++i)
-            dtq[i] = load_dt(2 + i);
-        weights(0, dt0);
-        __syncthreads();                              // chunk 0's weights published
-        if (nc > 1)
-            weights(1, dt1);
+        for (int j = 0; j < kSsDtRing; ++j)
+            fetch_dt(j);
+        bool lok = true;
+        int issued = 0;                               // chunks whose TMA was started
+        int st = 0;                                   // stage of chunk j
         for (int j = 0; j < nc; ++j) {
-            const float dt_next = load_dt(j + 2 + kDtAhead);
-            if (__syncthreads_or(0))
-                break;                                // the staging warps gave up
-            if (lane == 0) {
-                fence_after();
-                constexpr uint32_t id = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(nx >> 3) << 17) |
-                                        ((uint32_t)(kSsRows >> 4) << 24);        // idesc_tf32(128, nx)
-                const uint32_t bx = sbase + (j & 1) * L.buf;
-                const uint32_t tah = tmem + nx + 32 * (j & 1), tal = tah + 16;   // B^T hi, lo in TMEM
-#pragma unroll
-                for (int kk = 0; kk < kSsQ / 8; ++kk) {
-                    const uint64_t dxh = smem_desc(bx + 2 * kk * L.lx, L.lx, 128);
-                    const uint64_t dxl = smem_desc(bx + L.x_lo + 2 * kk * L.lx, L.lx, 128);
-                    mma_ts(tmem, tal + 8 * kk, dxh, id, (j > 0 || kk > 0) ? 1u : 0u);
-                    mma_ts(tmem, tah + 8 * kk, dxl, id, 1u);
-                    mma_ts(tmem, tah + 8 * kk, dxh, id, 1u);
-                }
-                commit(mmab + (j & 1));
-                if (j + kSsLead < nc)
-                    issue(j + kSsLead);               // its stage held chunk j - 1, consumed before the barrier
+            if (j >= kSsStages &&                     // one decision for the warp (its shuffles need every lane)
+                !__all_sync(kFullMask, mbar_wait(empty + st, (uint32_t)((j / kSsStages - 1) & 1), cap))) {
+                lok = false;                          // the staging warps gave up
+                break;
             }
-            issued = min(nc, j + kSsLead + 1);
-            if (j + 2 < nc)                           // slot j % 2 was read while chunk j was staged
-                weights(j + 2, dtq[0]);
-#pragma unroll
-            for (int i = 0; i + 1 < kDtAhead; ++i)
-                dtq[i] = dtq[i + 1];
-            dtq[kDtAhead - 1] = dt_next;
+            if (lane == 0)
+                issue(j, st);
+            issued = j + 1;
+            cp_async_wait<kSsDtRing - 1>();           // group j (kSsDtRing + j committed)
+            weights(j, st);
+            mbar_arrive(full + st);                   // every lane: its weight is written
+            fetch_dt(j + kSsDtRing);                  // into the row just read; a group every iteration
+            st = st == kSsStages - 1 ? 0 : st + 1;
         }
+        cp_async_wait<0>();
         const float cl = __shfl_sync(kFullMask, carry, 16 * (lane & 1));   // lane hb: head hb's log2 decay
         if (lane < HB) {
             decs[lane] = ssd::ex2(cl);
             decs[4 + lane] = cl * 0.6931471805599453f;   // the natural log: sum of dt A
         }
-        if (__syncthreads_or(0) && lane == 0) {      // the staging warps gave up: drain before TMEM is freed
-            commit(drain);                            // arrives once every product issued so far is done
-            mbar_wait(drain, 0);
-            for (int c = max(0, issued - kSsStages); c < issued; ++c)   // each stage's last TMA
+        if (__syncthreads_or(!lok) && lane == 0) {   // a wait gave up: each stage's last TMA lands
+            for (int c = max(0, issued - kSsStages); c < issued; ++c)   // before the block exits
                 mbar_wait(full + c % kSsStages, (uint32_t)((c / kSsStages) & 1));
         }
         __syncthreads();
@@ -348,39 +376,43 @@ segment_state_tc_kernel(const ScanArgs a, const SegmentPlan plan, const __grid_c
         xq[i] = it < nx * kSsQuads ? it / nx : -1;    // uniform across a warp (nx % 32 == 0)
         xr[i] = it - (it / nx) * nx;
     }
-    __syncthreads();                                  // chunk 0's weights published
 
     bool ok = true;
-    int last = -1;                                    // last chunk whose products were issued
+    int last = -1;                                    // last chunk whose operands were written
     int st = 0;                                       // stage of chunk j
+    int b = 0;                                        // operand buffer of chunk j
     for (int j = 0; j < nc; ++j) {
-        const int b = j & 1;
         const int cnt = min(kSsQ, len - (nc - 1 - j) * kSsQ);   // tokens of the chunk (16 but the first)
-        ok = mbar_wait(full + st, (uint32_t)((j / kSsStages) & 1), cap) && ok;
-        if (j >= 2) {                                 // buffer b: products of chunk j - 2 done
-            ok = mbar_wait(mmab + b, (uint32_t)(((j >> 1) - 1) & 1), cap) && ok;
+        ok = mbar_wait(full + st, (uint32_t)((j / kSsStages) & 1), cap);
+        if (ok && j >= kSsBufs) {                     // buffer b: products of chunk j - kSsBufs done
+            ok = mbar_wait(mmab + b, (uint32_t)((j / kSsBufs - 1) & 1), cap);
             fence_after();
+        }
+        if (!__all_sync(kFullMask, ok)) {            // one decision for the warp (tcgen05.st is warp-wide)
+            ok = false;
+            break;                                    // a wait gave up: write nothing more
         }
         const char *raw = sm + L.raw + st * L.stage;
         char *buf = sm + b * L.buf;
-        const float *w = wts + b * 32;
+        const float *w = wts + st * 32;
         const uint32_t ta = tlane + nx + 32 * b;
         if (cnt < kSsQ)
             stage_chunk<XI, HB, true>(raw, buf, w, ta, row, half, xr, xq, cnt);
         else
             stage_chunk<XI, HB, false>(raw, buf, w, ta, row, half, xr, xq, cnt);
+        mbar_arrive(empty + st);                      // this thread's reads of the stage are done
         tmem_wait_st();
         fence_before();
         fence_async_smem();
-        if (__syncthreads_or(!ok))
-            break;                                    // a wait gave up: issue nothing more
+        mbar_arrive(written + b);
         last = j;
         st = st == kSsStages - 1 ? 0 : st + 1;
+        b = b == kSsBufs - 1 ? 0 : b + 1;
     }
 
-    if (ok && last == nc - 1)                         // every product of the segment issued
-        ok = mbar_wait(mmab + (last & 1), (uint32_t)((last >> 1) & 1), cap);
-    if (__syncthreads_or(!ok)) {                      // the driver warp drains the products and copies
+    if (ok && last == nc - 1)                         // every chunk's operands written: its products done
+        ok = mbar_wait(mmab + last % kSsBufs, (uint32_t)((last / kSsBufs) & 1), cap);
+    if (__syncthreads_or(!ok)) {                      // the MMA and loader warps drain the products and copies
         if (tid == 0 && plan.status)
             atomicExch(plan.status, 1);
     } else {

@@ -52,6 +52,14 @@ __device__ __forceinline__ void cp_async16_zfill(void *smem, const void *gmem, i
                  : "memory");
 }
 
+// 4-byte cp.async through L1; src_bytes == 0 writes a zero word and reads nothing.
+__device__ __forceinline__ void cp_async4_zfill(void *smem, const void *gmem, int src_bytes)
+{
+    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(s), "l"(gmem), "r"(src_bytes)
+                 : "memory");
+}
+
 // Four 8x8 tiles of 32-bit words (each row 16 bytes) from shared memory; lane
 // l gives the row address of tile l/8, row l%8, and receives word (l%4) of
 // row (l/4) of each tile: the m16n8k8 TF32 fragment layout.
