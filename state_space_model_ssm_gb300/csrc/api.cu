@@ -663,10 +663,12 @@ int plan_ssd(int n_seqs, int n_tokens, int H, int P, int N, int G, int chunk, co
         if (g.smem_state > cap || g.smem_out > cap)
             return SSM_ERR_UNSUPPORTED;
         // Split a group's heads over blocks until there are about four
-        // blocks per SM (C B^T is formed once per block).
+        // blocks per SM (C B^T is formed once per block).  The tcgen05 kernel
+        // runs one block per SM, so it splits only until every SM has one:
+        // each split forms C B^T and reads C and B once more.
         const int hpg = H / G;
         const long long blocks = L.max_units * G;
-        const long long want = 4LL * dev->sms;
+        const long long want = (g.use_tc ? 1LL : 4LL) * dev->sms;
         const int split = (int)std::min<long long>(hpg, std::max<long long>(1, (want + blocks - 1) / blocks));
         g.heads_per_cta = (hpg + split - 1) / split;
     }

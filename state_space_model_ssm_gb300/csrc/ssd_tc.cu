@@ -15,7 +15,11 @@
 // Warps 8-11 copy global memory into shared memory one head ahead (two
 // buffers for S_in and the staged x) and signal per-buffer mbarriers; the
 // compute warps release a buffer through another mbarrier when its head is
-// done, and meet among themselves at a named barrier.
+// done.  Warp 12 issues every MMA (one thread) and forms each head's decay
+// tables; it and the compute warps hand each other the head's steps through
+// mbarriers (C and B ready, decay tables written, M and x^T written, products
+// done, accumulators read), so C S_in^T of a head and the next head's decay
+// tables run while the compute warps transpose x and form M.
 //
 // Shared-memory operands are K-major tiles without swizzle: 16-byte rows (4
 // fp32 along K) in 8-row core matrices 128 bytes apart, consecutive 16-byte K
@@ -39,10 +43,12 @@ using namespace tc;
 constexpr int kTcQ = 128;
 constexpr int kTcThreads = 256;             // compute warps 0-7 (TMEM rows x column halves)
 constexpr int kTcProducers = 4;             // warps 8-11 issue the global -> shared copies
-constexpr int kTcBlock = kTcThreads + 32 * kTcProducers;
+constexpr int kTcMmaWarp = kTcThreads / 32 + kTcProducers;   // warp 12: the MMAs and the decay tables
+constexpr int kTcBlock = kTcThreads + 32 * kTcProducers + 32;
 
-// Barrier 1 over the 256 compute threads (the producer warp never joins it).
-__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, 256;\n" ::: "memory"); }
+// Barrier 2 over the compute warps and the MMA warp: the MMA warp has drained
+// its products before the compute warps free TMEM.
+__device__ __forceinline__ void mma_compute_sync() { asm volatile("bar.sync 2, 288;\n" ::: "memory"); }
 
 // The same barrier, returning whether any compute thread passed `v` true.
 __device__ __forceinline__ bool compute_sync_or(bool v)
@@ -56,7 +62,7 @@ __device__ __forceinline__ bool compute_sync_or(bool v)
 
 // Shared-memory layout (bytes) of the block.
 struct TcLayout {
-    uint32_t BM, S[2], XR[2], XT, al, dts, fcol, bar, tslot, total;   // bar: 8 mbarriers
+    uint32_t BM, S[2], XR[2], XT, al, dts, fcol, bar, tslot, total;   // bar: 12 mbarriers
     uint32_t lc;      // k-chunk stride of the 128-row tiles (B, M)
     uint32_t ls;      // k-chunk stride of S_in (P rows)
     uint32_t lx;      // k-chunk stride of the transposed x tile (P rows + 16 bytes)
@@ -81,7 +87,7 @@ __host__ __device__ inline TcLayout tc_layout(int n_pad, int P, int nbuf)
     L.dts = L.al + kTcQ * 4;
     L.fcol = L.dts + kTcQ * 4;
     L.bar = L.fcol + kTcQ * 4;
-    L.tslot = L.bar + 64;
+    L.tslot = L.bar + 96;
     L.total = L.tslot + 16;
     return L;
 }
@@ -208,9 +214,13 @@ ssd_output_tc_kernel(const ScanArgs a, const SsdPlan p, const SsdGeom sg)
     float *fcol = reinterpret_cast<float *>(sm + L.fcol);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L.bar);
     uint64_t *bar_g = bars, *bar_mma = bars + 1, *bar_b = bars + 2;
-    uint64_t *drain = bars + 7;                       // after a failed wait: all products done
-    const long cap = p.fail_waits ? 0 : tc::kSpinLimit;   // polls of a pipeline wait
     uint64_t *full = bars + 3, *empty = bars + 5;      // per buffer
+    uint64_t *drain = bars + 7;                       // all products issued so far done
+    uint64_t *c_ready = bars + 8;                     // C in TMEM, B rounded
+    uint64_t *m_ready = bars + 9;                     // per head: M and x^T written
+    uint64_t *epi_done = bars + 10;                   // per head: its accumulators read
+    uint64_t *dec_full = bars + 11;                   // per head: its decay tables written
+    const long cap = p.fail_waits ? 0 : tc::kSpinLimit;   // polls of a pipeline wait
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + L.tslot);
     constexpr float kLog2e = 1.4426950408889634f;
     const size_t bc_off = ((size_t)c.t0 * a.G + g) * N;
@@ -227,13 +237,17 @@ ssd_output_tc_kernel(const ScanArgs a, const SsdPlan p, const SsdGeom sg)
             mbar_init(full + i, 32 * kTcProducers);
             mbar_init(empty + i, kTcThreads);
         }
+        mbar_init(c_ready, kTcThreads);
+        mbar_init(m_ready, kTcThreads);
+        mbar_init(epi_done, kTcThreads);
+        mbar_init(dec_full, 32);
         mbar_init_fence();
     }
     __syncthreads();                                  // barriers and the TMEM address published
 
     // ---- producer warps: B, then S_in and the staged x of each head, one head
     // ahead of the compute warps (two buffers) ----
-    if (warp >= kTcThreads / 32) {
+    if (warp >= kTcThreads / 32 && warp < kTcMmaWarp) {
         const int pw = warp - kTcThreads / 32;
         kmajor_copy(BMt, L.lc, a.B + bc_off, (size_t)a.G * N, kTcQ, Np4, c.len, N4, pw, lane, kTcProducers);
         cp_async_arrive(bar_b);
@@ -252,13 +266,96 @@ ssd_output_tc_kernel(const ScanArgs a, const SsdPlan p, const SsdGeom sg)
         return;
     }
 
-    // ---- compute warps ----
-    const int quad = warp & 3, half = warp >> 2;
-    const int t = 32 * quad + lane;                   // chunk row (TMEM lane) of this thread
     tc::fence_after();
     const uint32_t tmem = *tslot;
     const int ccols = tc_c_cols(sg.n_pad);
     const uint32_t tm_c = tmem, tm_g = tmem + ccols, tm_yi = tm_g + kTcQ, tm_yx = tm_yi + P;
+    const int ksteps_n = sg.n_pad >> 3;
+
+    // ---- MMA warp: G = C B^T once; per head Yi = C S_in^T as soon as S_in has
+    // landed and the previous head's accumulators are read, Yx = M x once M and
+    // x^T are written; between them the next head's decay tables ----
+    if (warp == kTcMmaWarp) {
+        // dt of the next head is loaded (scattered 4-byte reads) one head ahead
+        float dt_next[ChunkDecay<kTcQ>::R];
+        chunk_dt<kTcQ>(a, c, g * hpg + hl0, lane, dt_next);
+        // a_t log2(e), dt_s and the column factors f_s of head k (see M below)
+        auto decay_tables = [&](int k) {
+            const int h = g * hpg + hl0 + k;
+            ChunkDecay<kTcQ> cd;
+            chunk_decay_from<kTcQ>(a.A[h], dt_next, lane, cd);
+            if (k + 1 < nh)
+                chunk_dt<kTcQ>(a, c, h + 1, lane, dt_next);
+            // a of the last column of each 16-column piece (lane 4i+3 holds it)
+            constexpr int R = ChunkDecay<kTcQ>::R;
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const int s = lane * R + r;
+                const float ar = __shfl_sync(kFullMask, cd.a[R - 1], (s | 15) / R) * kLog2e;
+                al[s] = cd.a[r] * kLog2e;
+                dts[s] = cd.d[r];
+                fcol[s] = cd.d[r] * ex2(ar - cd.a[r] * kLog2e);
+            }
+            mbar_arrive(dec_full);                    // every lane: its entries are written
+        };
+        decay_tables(0);
+        // descriptors step by 2 K-chunks (8 tokens / state columns) per MMA
+        bool mok = __all_sync(kFullMask, mbar_wait(c_ready, 0, cap));
+        if (mok && lane == 0) {                       // G = C B^T
+            tc::fence_after();
+            const uint32_t id = idesc_tf32(kTcQ, kTcQ);
+            const uint64_t db = smem_desc(smem_u32(BMt), L.lc, 128);
+            for (int kk = 0; kk < ksteps_n; ++kk)
+                tc::mma_ts(tm_g, tm_c + 8 * kk, db + (uint64_t)(kk * (2 * L.lc >> 4)), id, kk > 0);
+            tc::commit(bar_g);
+        }
+        for (int k = 0; k < nh && mok; ++k) {
+            const int b = nbuf == 2 ? (k & 1) : 0;
+            bool got = mbar_wait(full + b, (uint32_t)((k / nbuf) & 1), cap);
+            if (k > 0)
+                got = mbar_wait(epi_done, (uint32_t)((k - 1) & 1), cap) && got;
+            if (!__all_sync(kFullMask, got)) {
+                mok = false;                          // a copy never landed or the compute warps gave up
+                break;
+            }
+            if (lane == 0) {                          // Yi = C S_in^T (S_in arrives rounded to TF32)
+                tc::fence_after();
+                const uint32_t id = idesc_tf32(kTcQ, P);
+                const uint64_t ds = smem_desc(smem_u32(sm + (b ? L.S[1] : L.S[0])), L.ls, 128);
+                for (int kk = 0; kk < ksteps_n; ++kk)
+                    tc::mma_ts(tm_yi, tm_c + 8 * kk, ds + (uint64_t)(kk * (2 * L.ls >> 4)), id, kk > 0);
+            }
+            if (!__all_sync(kFullMask, mbar_wait(m_ready, (uint32_t)(k & 1), cap))) {
+                mok = false;
+                break;
+            }
+            if (lane == 0) {                          // Yx = M x, over the chunk's tokens only
+                tc::fence_after();
+                const uint32_t id = idesc_tf32(kTcQ, P);
+                const uint64_t dm = smem_desc(smem_u32(BMt), L.lc, 128);
+                const uint64_t dx = smem_desc(smem_u32(XTt), L.lx, 128);
+                const int ks = (c.len + 7) >> 3;
+                for (int kk = 0; kk < ks; ++kk)
+                    tc::mma(tm_yx, dm + (uint64_t)(kk * (2 * L.lc >> 4)), dx + (uint64_t)(kk * (2 * L.lx >> 4)), id,
+                            kk > 0);
+                tc::commit(bar_mma);                  // Yi and Yx of head k
+            }
+            __syncwarp();
+            if (k + 1 < nh)
+                decay_tables(k + 1);                  // the tables are free: M of head k is formed
+        }
+        if (lane == 0) {                              // every product issued so far done before TMEM is freed
+            tc::commit(drain);
+            mbar_wait(drain, 0);
+        }
+        __syncwarp();
+        mma_compute_sync();
+        return;
+    }
+
+    // ---- compute warps ----
+    const int quad = warp & 3, half = warp >> 2;
+    const int t = 32 * quad + lane;                   // chunk row (TMEM lane) of this thread
     const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
 
     // C into TMEM: this thread's row t, its half of the (padded) columns (at
@@ -290,69 +387,32 @@ ssd_output_tc_kernel(const ScanArgs a, const SsdPlan p, const SsdGeom sg)
                 tmem_st16(tm_c + lane_off + cbase + 16 * cc, v);
             }
         }
-        asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+        tmem_wait_st();
     }
-    // ok is the same in every compute thread: each wait's outcome passes through a
-    // barrier OR before anyone acts on it
-    bool ok = !compute_sync_or(!mbar_wait(bar_b, 0, cap));   // B landed
+    // every wait's outcome is taken per warp (__all_sync), so the warp-wide
+    // tcgen05 loads and stores always run in whole warps
+    bool ok = __all_sync(kFullMask, mbar_wait(bar_b, 0, cap));   // B landed
     if (ok) {
         kmajor_round(BMt, L.lc, kTcQ, Np4, warp, lane);
         fence_async_smem();
         tc::fence_before();
-        compute_sync();
-    }
-    const int ksteps_n = sg.n_pad >> 3;
-    if (ok && tid == 0) {                             // G = C B^T
-        tc::fence_after();
-        const uint32_t id = idesc_tf32(kTcQ, kTcQ);
-        for (int kk = 0; kk < ksteps_n; ++kk)
-            tc::mma_ts(tm_g, tm_c + 8 * kk, smem_desc(smem_u32(BMt) + 2 * kk * L.lc, L.lc, 128), id, kk > 0);
-        tc::commit(bar_g);
+        mbar_arrive(c_ready);
     }
 
-    // warp 0 loads the next head's dt (scattered 4-byte reads) while the
-    // current head computes, so that latency stays off the per-head chain
-    float dt_next[ChunkDecay<kTcQ>::R];
-    if (warp == 0)
-        chunk_dt<kTcQ>(a, c, g * hpg + hl0, lane, dt_next);
     for (int k = 0; k < nh && ok; ++k) {
         const int h = g * hpg + hl0 + k;
         const int b = nbuf == 2 ? (k & 1) : 0;
-        char *St = sm + (b ? L.S[1] : L.S[0]), *XRt = sm + (b ? L.XR[1] : L.XR[0]);
-        if (warp == 0) {
-            ChunkDecay<kTcQ> cd;
-            chunk_decay_from<kTcQ>(a.A[h], dt_next, lane, cd);
-            if (k + 1 < nh)
-                chunk_dt<kTcQ>(a, c, h + 1, lane, dt_next);
-            // a of the last column of each 16-column piece (lane 4i+3 holds it)
-            constexpr int R = ChunkDecay<kTcQ>::R;
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const int s = lane * R + r;
-                const float ar = __shfl_sync(kFullMask, cd.a[R - 1], (s | 15) / R) * kLog2e;
-                al[s] = cd.a[r] * kLog2e;
-                dts[s] = cd.d[r];
-                fcol[s] = cd.d[r] * ex2(ar - cd.a[r] * kLog2e);
-            }
-        }
-        if (compute_sync_or(!mbar_wait(full + b, (uint32_t)((k / nbuf) & 1), cap))) {
+        const char *XRt = sm + (b ? L.XR[1] : L.XR[0]);
+        if (!__all_sync(kFullMask, mbar_wait(full + b, (uint32_t)((k / nbuf) & 1), cap))) {
             ok = false;                               // S_in and x of head k never landed
             break;
         }
-        // S_in arrives rounded to TF32 (the state pass stores it so); x is rounded
-        // as it is transposed
-        xraw_transpose(XTt, L.lx, XRt, P, tid);
-        fence_async_smem();
-        compute_sync();                               // S_in, x^T, a_t, dt of head k ready
-
-        if (tid == 0) {                               // Yi = C S_in^T
-            tc::fence_after();
-            const uint32_t id = idesc_tf32(kTcQ, P);
-            for (int kk = 0; kk < ksteps_n; ++kk)
-                tc::mma_ts(tm_yi, tm_c + 8 * kk, smem_desc(smem_u32(St) + 2 * kk * L.ls, L.ls, 128), id, kk > 0);
-        }
-        const bool g_done = k > 0 || mbar_wait(bar_g, 0, cap);   // G formed; B no longer needed
-        if (compute_sync_or(!g_done)) {
+        // x^T of the previous head is no longer read: its products are done
+        xraw_transpose(XTt, L.lx, XRt, P, tid);      // rounded to TF32 as it is transposed
+        bool got = mbar_wait(dec_full, (uint32_t)(k & 1), cap);
+        if (k == 0)
+            got = mbar_wait(bar_g, 0, cap) && got;    // G formed; B's space is free for M
+        if (!__all_sync(kFullMask, got)) {
             ok = false;
             break;
         }
@@ -403,18 +463,9 @@ ssd_output_tc_kernel(const ScanArgs a, const SsdPlan p, const SsdGeom sg)
         }
         tc::fence_before();
         fence_async_smem();
-        compute_sync();                               // M ready
+        mbar_arrive(m_ready);                         // M and x^T of head k written; the tables read
 
-        if (tid == 0) {                               // Yx = M x, over the chunk's tokens only
-            tc::fence_after();
-            const uint32_t id = idesc_tf32(kTcQ, P);
-            const int ks = (c.len + 7) >> 3;
-            for (int kk = 0; kk < ks; ++kk)
-                tc::mma(tm_yx, smem_desc(smem_u32(BMt) + 2 * kk * L.lc, L.lc, 128),
-                       smem_desc(smem_u32(XTt) + 2 * kk * L.lx, L.lx, 128), id, kk > 0);
-            tc::commit(bar_mma);
-        }
-        if (compute_sync_or(!mbar_wait(bar_mma, (uint32_t)(k & 1), cap))) {
+        if (!__all_sync(kFullMask, mbar_wait(bar_mma, (uint32_t)(k & 1), cap))) {
             ok = false;
             break;
         }
@@ -448,19 +499,16 @@ ssd_output_tc_kernel(const ScanArgs a, const SsdPlan p, const SsdGeom sg)
             }
         }
         tc::fence_before();
+        mbar_arrive(epi_done);                        // Yi and Yx may be overwritten
         mbar_arrive(empty + b);                       // buffer b may be refilled
-        compute_sync();                               // TMEM accumulators, M and x^T free
     }
-    if (!ok) {                                        // a copy or product never completed
-        if (tid == 0) {                               // the thread that issued every product
+    if (compute_sync_or(!ok)) {                       // a copy or product never completed
+        if (tid == 0)
             atomicExch(p.status, 1);
-            tc::commit(drain);                        // arrives once all of them are done
-            mbar_wait(drain, 0);
-        }
-        compute_sync();
         // this block's y is incomplete: NaN over its whole tile
         poison_y(a.y, (long long)a.H * P, c.t0, c.len, (g * hpg + hl0) * P, nh * P, tid, kTcThreads);
     }
+    mma_compute_sync();                               // the MMA warp has drained its products
     if (warp == 0)
         tmem_dealloc(tmem, sg.tmem_cols);
 }
