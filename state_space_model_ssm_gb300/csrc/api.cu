@@ -529,7 +529,10 @@ int scan_kernels(const ssm::ScanArgs &a, const ssm_scan_tuning &t, const DeviceI
     const ssm::GatedOut *fuse = nullptr;
     int epi = 0;
     size_t smem_full = pl.smem;
-    if (n_tokens > 0 && ssm::prefill_scaled_tile_supported(pl.lanes, pl.vpl, pl.rpt, pl.g.rows_per_cta)) {
+    if (n_tokens > 0 && !gated && ssm::prefill_scaled_self_supported(pl.lanes, pl.vpl, pl.rpt, pl.g.rows_per_cta) &&
+        3 * (ssm::prefill_scaled_smem_bytes(pl.g, N, pl.lanes, 0) + 1024) <= (size_t)dev.smem_per_sm) {
+        epi = 3;                            // self-staged: three blocks per SM
+    } else if (n_tokens > 0 && ssm::prefill_scaled_tile_supported(pl.lanes, pl.vpl, pl.rpt, pl.g.rows_per_cta)) {
         if (gated && pl.g.rows_per_cta == P && P % 4 == 0 && P <= 256 && aligned(gated->z, 16) &&
             aligned(gated->out, 16) &&
             ssm::prefill_scaled_smem_bytes(pl.g, N, pl.lanes, 2) <= (size_t)dev.smem_optin) {

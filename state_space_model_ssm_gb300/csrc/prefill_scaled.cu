@@ -200,14 +200,15 @@ size_t prefill_scaled_smem_bytes(const PrefillGeom &g, int N, int lanes, int epi
 // run blocks of at most kTileThreads (four consumer warps and the producer)
 // and keep two blocks per SM.
 constexpr int kTileThreads = 160;
+constexpr int kSelfThreads = 128;      // self-staged (EPI 3): exactly four consumer warps, no producer
 
 template <int LANES, int VPL, int RPT, bool EXACT, int MODE, int EPI>
 __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const PrefillGeom &geo,
                                                     const SegmentPlan &plan, const GatedOut &gt)
 {
     constexpr bool kFull = (MODE == kScanFull);
-    constexpr bool TILE = EPI >= 1, GATED = EPI == 2;
-    static_assert(kFull || EPI == 0, "the output tile needs y");
+    constexpr bool TILE = EPI == 1 || EPI == 2, GATED = EPI == 2, SELF = EPI == 3;
+    static_assert(kFull || EPI == 0, "the output tile and the self-staged form need y");
     extern __shared__ __align__(16) float smem[];
     const int N = a.N, N4 = a.N >> 2, P = a.P, H = a.H;
     const long long HP = (long long)H * P;
@@ -217,7 +218,7 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
     sm.cx = (geo.chunk * geo.rows_per_cta + 3) & ~3;     // keeps the float4 coefficients 16-byte aligned
     sm.cc = geo.chunk * geo.heads_cap * 4;
     sm.cm = (geo.heads_cap + 3) & ~3;                    // keeps the next slot 16-byte aligned
-    sm.cg = EPI * sm.cx;
+    sm.cg = TILE ? EPI * sm.cx : 0;
 
     // ---- A1 work mapping: (work unit, group, run of rows) ----
     // A work unit is a whole sequence, or with a segment plan one time segment
@@ -258,7 +259,7 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
 
     const int tid = threadIdx.x, nthr = blockDim.x;
     const int lane = tid & 31, warp = tid >> 5;
-    const int producer = (nthr >> 5) - 1;               // the last warp
+    const int producer = SELF ? -1 : (nthr >> 5) - 1;   // the last warp (none when self-staged)
     if (kFull && plan.units && call_failed(plan.status)) {
         // The state pass gave up a bounded wait, so the segments' incoming
         // states are not valid: y becomes NaN and the slot keeps its contents.
@@ -268,104 +269,121 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
         return;
     }
 
+    // Staging of a chunk (A3) and its coefficients (A4): by the producer warp
+    // (sid = lane of 32), or by all the block's threads when it has no
+    // producer (sid = tid of nthr); the coefficients by one warp either way.
+    const int sid = SELF ? tid : lane;
+    constexpr int scount = SELF ? kSelfThreads : 32;      // the block size when self-staged
+    const float *Bg = a.B + (long long)grp * N;
+    const float *Cg = a.C + (long long)grp * N;
+    const long long tokN = (long long)a.G * N;
+    // A3: stage B, C and x of chunk c0 into slot b (cp.async by the staging
+    // threads, one commit group per chunk)
+    float *seg_decay = sm.Dec();     // state pass: running decay of the segment per head
+    // Walk over (token, column) items in steps of scount without divisions:
+    // start at (sid / width, sid % width), step (scount / width, scount % width).
+    const int bt0 = sid / N4, bv0 = sid - bt0 * N4, bdt = scount / N4, bdv = scount - bdt * N4;
+    // x moves in 16-byte pieces when the block's rows start on 16 bytes in
+    // global and shared memory, else in 4-byte pieces; xw pieces per token.
+    const bool x16 = ((r0 | nrows | geo.rows_per_cta) & 3) == 0 && (HP & 3) == 0 &&
+                     (reinterpret_cast<uintptr_t>(a.x) & 15) == 0;
+    const int xw = x16 ? nrows >> 2 : nrows;
+    const int xt0 = sid / xw, xv0 = sid - xt0 * xw, xdt = scount / xw, xdv = scount - xdt * xw;
+    auto stage = [&](int c0, int b) {
+        const int t0 = c0 * geo.chunk;
+        const int cnt = min(geo.chunk, len - t0);
+        const long long tok0 = (long long)tok_start + t0;
+        float *sB = sm.B(b), *sC = sm.C(b), *sX = sm.X(b);
+        if (N4 % 32 == 0) {
+            // thread sid: float4 columns sid % 32, + 32, ... of tokens sid / 32, + scount / 32, ...
+            const int col = sid & 31, tstep = scount >> 5;
+            const float *gB = Bg + (tok0 + (sid >> 5)) * tokN + 4 * col;
+            const float *gC = Cg + (tok0 + (sid >> 5)) * tokN + 4 * col;
+            float *dB = sB + (sid >> 5) * N + 4 * col, *dC = sC + (sid >> 5) * N + 4 * col;
+            for (int t = sid >> 5; t < cnt; t += tstep) {
+                for (int v = 0; v < N4; v += 32) {
+                    cp_async16(dB + 4 * v, gB + 4 * v);
+                    if (kFull)
+                        cp_async16(dC + 4 * v, gC + 4 * v);
+                }
+                gB += tstep * tokN;
+                gC += tstep * tokN;
+                dB += tstep * N;
+                dC += tstep * N;
+            }
+        } else {
+            for (int t = bt0, v = bv0; t < cnt;) {
+                const long long goff = (tok0 + t) * tokN + 4 * v;
+                cp_async16(sB + t * N + 4 * v, Bg + goff);
+                if (kFull)
+                    cp_async16(sC + t * N + 4 * v, Cg + goff);
+                t += bdt;
+                v += bdv;
+                if (v >= N4) { v -= N4; ++t; }
+            }
+        }
+        const float *gx = a.x + tok0 * HP + r0;
+        const float *gz = GATED ? gt.z + tok0 * HP + r0 : nullptr;
+        float *sZ = GATED ? sm.Ztile(b) : nullptr;
+        if (x16) {
+            for (int t = xt0, r = xv0; t < cnt;) {
+                cp_async16(sX + t * geo.rows_per_cta + 4 * r, gx + t * HP + 4 * r);
+                if (GATED)              // z: the same layout as x (16-byte aligned: checked by the host)
+                    cp_async16(sZ + t * geo.rows_per_cta + 4 * r, gz + t * HP + 4 * r);
+                t += xdt;
+                r += xdv;
+                if (r >= xw) { r -= xw; ++t; }
+            }
+        } else {
+            for (int t = xt0, r = xv0; t < cnt;) {
+                cp_async4(sX + t * geo.rows_per_cta + r, gx + t * HP + r);
+                if (GATED)
+                    cp_async4(sZ + t * geo.rows_per_cta + r, gz + t * HP + r);
+                t += xdt;
+                r += xdv;
+                if (r >= xw) { r -= xw; ++t; }
+            }
+        }
+        if (SELF && warp == c0 % (kSelfThreads / 32)) {
+            // self-staged: the warp that will form this chunk's coefficients copies
+            // its dt (lane = token) into the unused fourth word of each slot
+            float4 *cf = sm.Coef(b);
+            for (int hh = 0; hh < nheads; ++hh)
+                if (lane < cnt)
+                    cp_async4(&cf[lane * geo.heads_cap + hh].w, a.dt + (tok0 + lane) * H + h0 + hh);
+        }
+        cp_async_commit();
+    };
+    // A4: dt of chunk c0 (lane = token) for the first kDtHeads heads, read two
+    // chunks before its coefficients are needed.
+    constexpr int kDtHeads = 4;
+    auto load_dt = [&](int c0, float (&d)[kDtHeads]) {
+        const int t0 = c0 * geo.chunk;
+        const int cnt = min(geo.chunk, len - t0);
+#pragma unroll
+        for (int q = 0; q < kDtHeads; ++q)
+            d[q] = (q < nheads && lane < cnt) ? a.dt[((long long)tok_start + t0 + lane) * H + h0 + q] : 0.f;
+    };
+    auto coefficients = [&](int c0, int b, const float (&d)[kDtHeads]) {
+        const int t0 = c0 * geo.chunk;
+        const int cnt = min(geo.chunk, len - t0);
+        for (int hh = 0; hh < nheads; ++hh) {
+            float dtv = d[0];
+#pragma unroll
+            for (int q = 1; q < kDtHeads; ++q)
+                if (hh == q) dtv = d[q];
+            if (hh >= kDtHeads)
+                dtv = lane < cnt ? a.dt[((long long)tok_start + t0 + lane) * H + h0 + hh] : 0.f;
+            if (SELF)                                 // staged with the chunk (see stage)
+                dtv = lane < cnt ? sm.Coef(b)[lane * geo.heads_cap + hh].w : 0.f;
+            const float dec = chunk_coefficients(dtv, a.A[h0 + hh], cnt, lane, sm.Coef(b) + hh,
+                                                 geo.heads_cap, sm.Mask(b) + hh);
+            if (!kFull && lane == 0)
+                seg_decay[hh] = (c0 == 0 ? 1.f : seg_decay[hh]) * dec;
+        }
+    };
     if (warp == producer) {
         // ================= producer warp =================
-        const float *Bg = a.B + (long long)grp * N;
-        const float *Cg = a.C + (long long)grp * N;
-        const long long tokN = (long long)a.G * N;
-        // A3: stage B, C and x of chunk c0 into slot b (cp.async, this warp only)
-        float *seg_decay = sm.Dec();     // state pass: running decay of the segment per head
-        // Per-lane walk over (token, column) items in steps of 32 without
-        // divisions: start at (lane / width, lane % width), step (32 / width, 32 % width).
-        const int bt0 = lane / N4, bv0 = lane - bt0 * N4, bdt = 32 / N4, bdv = 32 - bdt * N4;
-        // x moves in 16-byte pieces when the block's rows start on 16 bytes in
-        // global and shared memory, else in 4-byte pieces; xw pieces per token.
-        const bool x16 = ((r0 | nrows | geo.rows_per_cta) & 3) == 0 && (HP & 3) == 0 &&
-                         (reinterpret_cast<uintptr_t>(a.x) & 15) == 0;
-        const int xw = x16 ? nrows >> 2 : nrows;
-        const int xt0 = lane / xw, xv0 = lane - xt0 * xw, xdt = 32 / xw, xdv = 32 - xdt * xw;
-        auto stage = [&](int c0, int b) {
-            const int t0 = c0 * geo.chunk;
-            const int cnt = min(geo.chunk, len - t0);
-            const long long tok0 = (long long)tok_start + t0;
-            float *sB = sm.B(b), *sC = sm.C(b), *sX = sm.X(b);
-            if (N4 % 32 == 0) {
-                // lane = float4 columns lane, lane + 32, ... of every token's row
-                const float *gB = Bg + tok0 * tokN + 4 * lane;
-                const float *gC = Cg + tok0 * tokN + 4 * lane;
-                float *dB = sB + 4 * lane, *dC = sC + 4 * lane;
-                for (int t = 0; t < cnt; ++t) {
-                    for (int v = 0; v < N4; v += 32) {
-                        cp_async16(dB + 4 * v, gB + 4 * v);
-                        if (kFull)
-                            cp_async16(dC + 4 * v, gC + 4 * v);
-                    }
-                    gB += tokN;
-                    gC += tokN;
-                    dB += N;
-                    dC += N;
-                }
-            } else {
-                for (int t = bt0, v = bv0; t < cnt;) {
-                    const long long goff = (tok0 + t) * tokN + 4 * v;
-                    cp_async16(sB + t * N + 4 * v, Bg + goff);
-                    if (kFull)
-                        cp_async16(sC + t * N + 4 * v, Cg + goff);
-                    t += bdt;
-                    v += bdv;
-                    if (v >= N4) { v -= N4; ++t; }
-                }
-            }
-            const float *gx = a.x + tok0 * HP + r0;
-            const float *gz = GATED ? gt.z + tok0 * HP + r0 : nullptr;
-            float *sZ = GATED ? sm.Ztile(b) : nullptr;
-            if (x16) {
-                for (int t = xt0, r = xv0; t < cnt;) {
-                    cp_async16(sX + t * geo.rows_per_cta + 4 * r, gx + t * HP + 4 * r);
-                    if (GATED)              // z: the same layout as x (16-byte aligned: checked by the host)
-                        cp_async16(sZ + t * geo.rows_per_cta + 4 * r, gz + t * HP + 4 * r);
-                    t += xdt;
-                    r += xdv;
-                    if (r >= xw) { r -= xw; ++t; }
-                }
-            } else {
-                for (int t = xt0, r = xv0; t < cnt;) {
-                    cp_async4(sX + t * geo.rows_per_cta + r, gx + t * HP + r);
-                    if (GATED)
-                        cp_async4(sZ + t * geo.rows_per_cta + r, gz + t * HP + r);
-                    t += xdt;
-                    r += xdv;
-                    if (r >= xw) { r -= xw; ++t; }
-                }
-            }
-            cp_async_commit();
-        };
-        // A4: dt of chunk c0 (lane = token) for the first kDtHeads heads, read two
-        // chunks before its coefficients are needed.
-        constexpr int kDtHeads = 4;
-        auto load_dt = [&](int c0, float (&d)[kDtHeads]) {
-            const int t0 = c0 * geo.chunk;
-            const int cnt = min(geo.chunk, len - t0);
-#pragma unroll
-            for (int q = 0; q < kDtHeads; ++q)
-                d[q] = (q < nheads && lane < cnt) ? a.dt[((long long)tok_start + t0 + lane) * H + h0 + q] : 0.f;
-        };
-        auto coefficients = [&](int c0, int b, const float (&d)[kDtHeads]) {
-            const int t0 = c0 * geo.chunk;
-            const int cnt = min(geo.chunk, len - t0);
-            for (int hh = 0; hh < nheads; ++hh) {
-                float dtv = d[0];
-#pragma unroll
-                for (int q = 1; q < kDtHeads; ++q)
-                    if (hh == q) dtv = d[q];
-                if (hh >= kDtHeads)
-                    dtv = lane < cnt ? a.dt[((long long)tok_start + t0 + lane) * H + h0 + hh] : 0.f;
-                const float dec = chunk_coefficients(dtv, a.A[h0 + hh], cnt, lane, sm.Coef(b) + hh,
-                                                     geo.heads_cap, sm.Mask(b) + hh);
-                if (!kFull && lane == 0)
-                    seg_decay[hh] = (c0 == 0 ? 1.f : seg_decay[hh]) * dec;
-            }
-        };
         // Output of chunk c0 (slot b), after the consumers are done with it: the
         // y tile to global memory (128-bit stores where the rows allow).
         const bool y16 = ((r0 | nrows | geo.rows_per_cta) & 3) == 0 && (HP & 3) == 0 &&
@@ -539,9 +557,39 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
         }
     };
 
+    // Self-staged (no producer warp): every thread copies its share of each
+    // chunk two chunks ahead, and the warps take turns forming the next
+    // chunk's coefficients at the end of a chunk; one block barrier per chunk.
+    constexpr int ncw = kSelfThreads / 32;
+    const float dnone[kDtHeads] = {};                 // self-staged: dt comes through shared memory
+    if constexpr (SELF) {
+        if (n_chunks > 0)
+            stage(0, 0);
+        else
+            cp_async_commit();
+        if (n_chunks > 1)
+            stage(1, 1);
+        else
+            cp_async_commit();                        // one commit group per chunk, empty past the end
+        if (warp == 0 && n_chunks > 0) {
+            cp_async_wait<1>();                       // this warp's copies of chunk 0 (its dt) landed
+            coefficients(0, 0, dnone);
+        }
+    }
     for (int c = 0; c < n_chunks; ++c) {
         const int b = c % kSlots;
-        bar_sync(kBarFull + b, nthr);
+        bool coef_warp = false;                       // self-staged: this warp forms chunk c+1's coefficients
+        if constexpr (SELF) {
+            cp_async_wait<1>();                       // this thread's copies of chunk c landed
+            __syncthreads();                          // everyone's, and chunk c's coefficients; chunk c-1 done
+            if (c + 2 < n_chunks)
+                stage(c + 2, (c + 2) % kSlots);       // its slot held chunk c-1
+            else
+                cp_async_commit();
+            coef_warp = c + 1 < n_chunks && warp == (c + 1) % ncw;
+        } else {
+            bar_sync(kBarFull + b, nthr);
+        }
         if constexpr (GATED) {
             // every consumer warp has arrived here, so all of chunk c-1's y is
             // in its tile: gate it, then release its slot
@@ -689,11 +737,17 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
         // back to S at the chunk end: U <- Lambda_last U
         rescale(pCf[(cnt - 1) * hc].y);
         __syncwarp();
-        // release the slot: the producer refills it with chunk c+3 (with the
-        // output tile it first writes the tile out; with the gated output the
-        // release comes after the chunk's gating, at the start of chunk c+1)
-        if (!GATED && (TILE || c + kSlots < n_chunks))
+        if constexpr (SELF) {
+            if (coef_warp) {                          // into chunk c+1's slot, read after the next barrier
+                cp_async_wait<1>();                   // this warp's copies of chunk c+1 (its dt) landed
+                coefficients(c + 1, (c + 1) % kSlots, dnone);
+            }
+        } else if (!GATED && (TILE || c + kSlots < n_chunks)) {
+            // release the slot: the producer refills it with chunk c+3 (with the
+            // output tile it first writes the tile out; with the gated output the
+            // release comes after the chunk's gating, at the start of chunk c+1)
             bar_arrive(kBarEmpty + b, nthr);
+        }
     }
     if constexpr (GATED) {
         if (n_chunks > 0) {                 // the last chunk: every consumer warp done with it
@@ -743,6 +797,17 @@ prefill_scaled_tile_kernel(const ScanArgs a, const PrefillGeom geo, const Segmen
     prefill_scaled_body<LANES, VPL, RPT, EXACT, kScanFull, EPI>(a, geo, plan, gt);
 }
 
+// Self-staged full pass (EPI 3): blocks of four consumer warps and no producer,
+// three per SM (three warps on every SM sub-partition, at most 168 registers).
+
+template <int LANES, int VPL, int RPT, bool EXACT>
+__global__ void __launch_bounds__(kSelfThreads, 3)
+prefill_scaled_self_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan plan, const GatedOut gt)
+{
+    griddep_entry();
+    prefill_scaled_body<LANES, VPL, RPT, EXACT, kScanFull, 3>(a, geo, plan, gt);
+}
+
 namespace {
 
 // Shapes with the output-tile variants (EPI 1 and 2): the automatic shapes of
@@ -755,7 +820,7 @@ cudaError_t launch_scaled_one(const ScanArgs &a, const PrefillGeom &g, const Seg
                               long long n_units, size_t smem, int epi, const GatedOut &gt, cudaStream_t stream)
 {
     const bool exact = (a.N / 4) == LANES * VPL;
-    const int threads = (g.rows_per_cta / RPT) * LANES + 32;     // consumers + one producer warp
+    const int threads = (g.rows_per_cta / RPT) * LANES + (epi == 3 ? 0 : 32);   // consumers (+ the producer)
     const dim3 grid((unsigned)(n_units * a.G * g.runs_per_group));
     void (*kern)(const ScanArgs, const PrefillGeom, const SegmentPlan, const GatedOut) = nullptr;
     if (mode != kScanFull) {
@@ -766,6 +831,14 @@ cudaError_t launch_scaled_one(const ScanArgs &a, const PrefillGeom &g, const Seg
     } else if (epi == 0) {
         kern = exact ? prefill_scaled_kernel<LANES, VPL, RPT, true, kScanFull>
                      : prefill_scaled_kernel<LANES, VPL, RPT, false, kScanFull>;
+    } else if (epi == 3) {
+        if (threads != kSelfThreads)
+            return cudaErrorInvalidValue;
+        if constexpr (kHasTile<LANES, VPL, RPT>)
+            kern = exact ? prefill_scaled_self_kernel<LANES, VPL, RPT, true>
+                         : prefill_scaled_self_kernel<LANES, VPL, RPT, false>;
+        if (!kern)
+            return cudaErrorInvalidValue;
     } else {
         if (threads > kTileThreads)
             return cudaErrorInvalidValue;
@@ -800,6 +873,16 @@ cudaError_t launch_scaled_one(const ScanArgs &a, const PrefillGeom &g, const Seg
 bool prefill_scaled_supported(int lanes, int vpl, int rpt)
 {
 #define X(L, V, R) if (lanes == L && vpl == V && rpt == R) return true;
+    SSM_SCALED_SHAPES(X)
+#undef X
+    return false;
+}
+
+bool prefill_scaled_self_supported(int lanes, int vpl, int rpt, int rows_per_cta)
+{
+    if ((rows_per_cta / rpt) * lanes != kSelfThreads)     // the staging walk assumes the whole block
+        return false;
+#define X(L, V, R) if (lanes == L && vpl == V && rpt == R) return kHasTile<L, V, R>;
     SSM_SCALED_SHAPES(X)
 #undef X
     return false;
