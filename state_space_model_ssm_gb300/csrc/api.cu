@@ -519,19 +519,31 @@ int scan_kernels(const ssm::ScanArgs &a, const ssm_scan_tuning &t, const DeviceI
             return SSM_ERR_CUDA;
         return SSM_OK;
     }
-    // Output of the full pass.  Where the shape has the output-tile variants, y
-    // goes through a shared-memory tile that the producer warp writes out
-    // (epi 1; about 1 % faster than the consumers' own stores, which the other
-    // shapes keep: epi 0); with the gated RMSNorm requested, the consumer warps
-    // also apply it from that tile (epi 2), which needs blocks of exactly one
-    // head (rows per block = head_dim) and z 16-byte aligned (staged like x).
-    // Each needs its extra tiles to fit the shared memory.
+    // Output of the full pass.  Blocks of exactly four consumer warps run
+    // self-staged, without a producer warp, three per SM (epi 3; the consumers
+    // store y), and with the gated RMSNorm requested through y and z tiles that
+    // all warps write out one chunk later (epi 4: blocks of exactly one head,
+    // x, y, z and the gated output 16-byte aligned).  Other shapes with the
+    // output-tile variants keep a producer warp: y goes through a shared-memory
+    // tile that it writes out (epi 1; about 1 % faster than the consumers' own
+    // stores, which the remaining shapes keep: epi 0), and the gated output is
+    // applied by the consumer warps from that tile (epi 2, one head per block,
+    // z 16-byte aligned and staged like x).  Each needs its extra tiles to fit
+    // the shared memory.
     const ssm::GatedOut *fuse = nullptr;
     int epi = 0;
     size_t smem_full = pl.smem;
-    if (n_tokens > 0 && !gated && ssm::prefill_scaled_self_supported(pl.lanes, pl.vpl, pl.rpt, pl.g.rows_per_cta) &&
-        3 * (ssm::prefill_scaled_smem_bytes(pl.g, N, pl.lanes, 0) + 1024) <= (size_t)dev.smem_per_sm) {
+    const bool self_ok = n_tokens > 0 && ssm::prefill_scaled_self_supported(pl.lanes, pl.vpl, pl.rpt, pl.g.rows_per_cta);
+    auto three_per_sm = [&](int e) {
+        return 3 * (ssm::prefill_scaled_smem_bytes(pl.g, N, pl.lanes, e) + 1024) <= (size_t)dev.smem_per_sm;
+    };
+    if (self_ok && !gated && three_per_sm(3)) {
         epi = 3;                            // self-staged: three blocks per SM
+    } else if (self_ok && gated && pl.g.rows_per_cta == P && P % 4 == 0 && aligned(gated->z, 16) &&
+               aligned(gated->out, 16) && aligned(a.y, 16) && aligned(a.x, 16) && three_per_sm(4)) {
+        fuse = gated;                       // self-staged with the gated output
+        epi = 4;
+        smem_full = ssm::prefill_scaled_smem_bytes(pl.g, N, pl.lanes, 4);
     } else if (n_tokens > 0 && ssm::prefill_scaled_tile_supported(pl.lanes, pl.vpl, pl.rpt, pl.g.rows_per_cta)) {
         if (gated && pl.g.rows_per_cta == P && P % 4 == 0 && P <= 256 && aligned(gated->z, 16) &&
             aligned(gated->out, 16) &&

@@ -101,6 +101,10 @@ struct ScaledSmem {
     __device__ __forceinline__ float *Ytile(int s) const { return slot(s) + 2 * cb + cx + cc + cm; }
     __device__ __forceinline__ float *Ztile(int s) const { return slot(s) + 2 * cb + 2 * cx + cc + cm; }
     __device__ __forceinline__ float *Dec() const { return base + kSlots * (2 * cb + cx + cc + cm + cg); }
+    // self-staged gated output (EPI 4): two y tiles (chunk c in tile c % 2) and
+    // one z tile after the decay area, cx floats each
+    __device__ __forceinline__ float *SelfY(int i) const { return Dec() + cm + i * cx; }
+    __device__ __forceinline__ float *SelfZ() const { return Dec() + cm + 2 * cx; }
 };
 
 __device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
@@ -187,27 +191,34 @@ size_t prefill_scaled_smem_bytes(const PrefillGeom &g, int N, int lanes, int epi
     const size_t cx = ((size_t)g.chunk * g.rows_per_cta + 3) & ~(size_t)3;
     const size_t cm = ((size_t)g.heads_cap + 3) & ~(size_t)3;
     const size_t per_slot = (size_t)g.chunk * (2 * (size_t)N + 4 * (size_t)g.heads_cap) + cx + cm +
-                            (size_t)epi * cx;
+                            (epi == 1 || epi == 2 ? (size_t)epi * cx : 0);
     (void)lanes;
-    return (kSlots * per_slot + cm) * sizeof(float);
+    // epi 4: two y tiles and a z tile after the slots and the decay area
+    return (kSlots * per_slot + cm + (epi == 4 ? 3 * cx : 0)) * sizeof(float);
 }
 
 // MODE kScanFull: the scan with y.  MODE kScanStateOnly: one time segment's
 // state from zero (no C, no y), for the segment pass of long sequences.
 // EPI (kScanFull only): 0 the consumers store y; 1 y through a shared-memory
 // tile, stored by the producer; 2 as 1 and the gated RMSNorm output (a block's
-// rows are exactly one head).  The tile variants (prefill_scaled_tile_kernel)
-// run blocks of at most kTileThreads (four consumer warps and the producer)
-// and keep two blocks per SM.
+// rows are exactly one head); 3 no producer warp: the consumers stage the
+// chunks and store y; 4 as 3 with the gated output (y and z through tiles,
+// written out by all warps one chunk later).  The tile variants
+// (prefill_scaled_tile_kernel) run blocks of at most kTileThreads (four
+// consumer warps and the producer) and keep two blocks per SM; the
+// self-staged ones (prefill_scaled_self_kernel) exactly kSelfThreads, three
+// per SM.
 constexpr int kTileThreads = 160;
-constexpr int kSelfThreads = 128;      // self-staged (EPI 3): exactly four consumer warps, no producer
+constexpr int kSelfThreads = 128;      // self-staged (EPI 3, 4): exactly four consumer warps, no producer
 
 template <int LANES, int VPL, int RPT, bool EXACT, int MODE, int EPI>
 __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const PrefillGeom &geo,
                                                     const SegmentPlan &plan, const GatedOut &gt)
 {
     constexpr bool kFull = (MODE == kScanFull);
-    constexpr bool TILE = EPI == 1 || EPI == 2, GATED = EPI == 2, SELF = EPI == 3;
+    // EPI 3 and 4: self-staged (no producer warp); EPI 4 with the gated output
+    constexpr bool SELF = EPI == 3 || EPI == 4;
+    constexpr bool TILE = EPI == 1 || EPI == 2 || EPI == 4, GATED = EPI == 2 || EPI == 4;
     static_assert(kFull || EPI == 0, "the output tile and the self-staged form need y");
     extern __shared__ __align__(16) float smem[];
     const int N = a.N, N4 = a.N >> 2, P = a.P, H = a.H;
@@ -218,7 +229,7 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
     sm.cx = (geo.chunk * geo.rows_per_cta + 3) & ~3;     // keeps the float4 coefficients 16-byte aligned
     sm.cc = geo.chunk * geo.heads_cap * 4;
     sm.cm = (geo.heads_cap + 3) & ~3;                    // keeps the next slot 16-byte aligned
-    sm.cg = TILE ? EPI * sm.cx : 0;
+    sm.cg = (EPI == 1 || EPI == 2) ? EPI * sm.cx : 0;
 
     // ---- A1 work mapping: (work unit, group, run of rows) ----
     // A work unit is a whole sequence, or with a segment plan one time segment
@@ -294,7 +305,7 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
         const int cnt = min(geo.chunk, len - t0);
         const long long tok0 = (long long)tok_start + t0;
         float *sB = sm.B(b), *sC = sm.C(b), *sX = sm.X(b);
-        if (N4 % 32 == 0) {
+        if ((EXACT ? LANES * VPL : N4) % 32 == 0) {   // known at compile time for the exact shapes
             // thread sid: float4 columns sid % 32, + 32, ... of tokens sid / 32, + scount / 32, ...
             const int col = sid & 31, tstep = scount >> 5;
             const float *gB = Bg + (tok0 + (sid >> 5)) * tokN + 4 * col;
@@ -323,12 +334,13 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
             }
         }
         const float *gx = a.x + tok0 * HP + r0;
-        const float *gz = GATED ? gt.z + tok0 * HP + r0 : nullptr;
-        float *sZ = GATED ? sm.Ztile(b) : nullptr;
+        constexpr bool kZ = EPI == 2;                // z staged with the chunk (self-staged: see stage_z)
+        const float *gz = kZ ? gt.z + tok0 * HP + r0 : nullptr;
+        float *sZ = kZ ? sm.Ztile(b) : nullptr;
         if (x16) {
             for (int t = xt0, r = xv0; t < cnt;) {
                 cp_async16(sX + t * geo.rows_per_cta + 4 * r, gx + t * HP + 4 * r);
-                if (GATED)              // z: the same layout as x (16-byte aligned: checked by the host)
+                if (kZ)                 // z: the same layout as x (16-byte aligned: checked by the host)
                     cp_async16(sZ + t * geo.rows_per_cta + 4 * r, gz + t * HP + 4 * r);
                 t += xdt;
                 r += xdv;
@@ -337,7 +349,7 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
         } else {
             for (int t = xt0, r = xv0; t < cnt;) {
                 cp_async4(sX + t * geo.rows_per_cta + r, gx + t * HP + r);
-                if (GATED)
+                if (kZ)
                     cp_async4(sZ + t * geo.rows_per_cta + r, gz + t * HP + r);
                 t += xdt;
                 r += xdv;
@@ -351,6 +363,21 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
             for (int hh = 0; hh < nheads; ++hh)
                 if (lane < cnt)
                     cp_async4(&cf[lane * geo.heads_cap + hh].w, a.dt + (tok0 + lane) * H + h0 + hh);
+        }
+        cp_async_commit();
+    };
+    // Self-staged gated output: z of chunk c0 into the z tile (the x layout),
+    // one commit group of its own.
+    auto stage_z = [&](int c0) {
+        const int t0 = c0 * geo.chunk;
+        const int cnt = min(geo.chunk, len - t0);
+        const float *gz = gt.z + ((long long)tok_start + t0) * HP + r0;
+        float *sZ = sm.SelfZ();
+        for (int t = xt0, r = xv0; t < cnt;) {      // 16-byte pieces (checked by the host)
+            cp_async16(sZ + t * geo.rows_per_cta + 4 * r, gz + t * HP + 4 * r);
+            t += xdt;
+            r += xdv;
+            if (r >= xw) { r -= xw; ++t; }
         }
         cp_async_commit();
     };
@@ -523,10 +550,11 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
         const int bb = cc % kSlots;
         const int cnt = min(geo.chunk, len - cc * geo.chunk);
         const int xs = geo.rows_per_cta;
-        const int nw = (nthr >> 5) - 1, sub = lane >> 3, l8 = lane & 7;
-        const float *Y = sm.Ytile(bb), *Z = sm.Ztile(bb);
+        const int nw = SELF ? kSelfThreads / 32 : (nthr >> 5) - 1, sub = lane >> 3, l8 = lane & 7;
+        const float *Y = SELF ? sm.SelfY(cc & 1) : sm.Ytile(bb), *Z = SELF ? sm.SelfZ() : sm.Ztile(bb);
         const float inv_p = 1.f / (float)nrows;
         float *out = gt.out + ((long long)tok_start + cc * geo.chunk) * HP + r0;
+        float *yout = a.y + ((long long)tok_start + cc * geo.chunk) * HP + r0;   // self-staged: y too
         for (int tr = warp * 4; tr < cnt; tr += nw * 4) {
             const int t = tr + sub;
             const bool live = t < cnt;
@@ -552,6 +580,8 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
                     o.z = v.z * inv * w.z * __fdividef(z.z, 1.f + __expf(-z.z));
                     o.w = v.w * inv * w.w * __fdividef(z.w, 1.f + __expf(-z.w));
                     *reinterpret_cast<float4 *>(out + (long long)t * HP + e) = o;
+                    if (SELF)                         // no producer writes the y tile out
+                        *reinterpret_cast<float4 *>(yout + (long long)t * HP + e) = v;
                 }
             }
         }
@@ -580,8 +610,15 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
         const int b = c % kSlots;
         bool coef_warp = false;                       // self-staged: this warp forms chunk c+1's coefficients
         if constexpr (SELF) {
-            cp_async_wait<1>();                       // this thread's copies of chunk c landed
-            __syncthreads();                          // everyone's, and chunk c's coefficients; chunk c-1 done
+            // (bar.sync as inline asm, like the y-tile stores, so the compiler keeps their order)
+            cp_async_wait<1>();                       // this thread's copies of chunk c (and z of c-1) landed
+            bar_sync(0, kSelfThreads);                // everyone's, and chunk c's coefficients; chunk c-1 done
+            if constexpr (GATED) {
+                if (c >= 1)
+                    gate(c - 1);                      // chunk c-1's y tile and z are complete
+                bar_sync(0, kSelfThreads);            // the z tile and chunk c-1's y tile are free again
+                stage_z(c);                           // read at the start of chunk c+1
+            }
             if (c + 2 < n_chunks)
                 stage(c + 2, (c + 2) % kSlots);       // its slot held chunk c-1
             else
@@ -590,7 +627,7 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
         } else {
             bar_sync(kBarFull + b, nthr);
         }
-        if constexpr (GATED) {
+        if constexpr (GATED && !SELF) {
             // every consumer warp has arrived here, so all of chunk c-1's y is
             // in its tile: gate it, then release its slot
             if (c >= 1) {
@@ -605,7 +642,8 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
         const float4 *__restrict__ pCf = sm.Coef(b) + hl;
         const float *__restrict__ pX = sm.X(b) + rl;
         float *yrow = a.y + ((long long)tok_start + c * geo.chunk) * HP + r0 + rl + yq;
-        float *pY = TILE ? sm.Ytile(b) + rl + yq : nullptr;    // the chunk's y tile (EPI >= 1)
+        float *pY = !TILE ? nullptr                            // the chunk's y tile (EPI 1, 2, 4)
+                          : (SELF ? sm.SelfY(c & 1) : sm.Ytile(b)) + rl + yq;
 
         // Shared-memory operands of one token.
         struct TokenIn {
@@ -749,7 +787,13 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
             bar_arrive(kBarEmpty + b, nthr);
         }
     }
-    if constexpr (GATED) {
+    if constexpr (GATED && SELF) {
+        if (n_chunks > 0) {                 // the last chunk: its y tile and z complete
+            cp_async_wait<0>();
+            bar_sync(0, kSelfThreads);
+            gate(n_chunks - 1);
+        }
+    } else if constexpr (GATED) {
         if (n_chunks > 0) {                 // the last chunk: every consumer warp done with it
             bar_sync(kBarConsumers, nthr - 32);
             gate(n_chunks - 1);
@@ -800,12 +844,12 @@ prefill_scaled_tile_kernel(const ScanArgs a, const PrefillGeom geo, const Segmen
 // Self-staged full pass (EPI 3): blocks of four consumer warps and no producer,
 // three per SM (three warps on every SM sub-partition, at most 168 registers).
 
-template <int LANES, int VPL, int RPT, bool EXACT>
+template <int LANES, int VPL, int RPT, bool EXACT, int EPI>
 __global__ void __launch_bounds__(kSelfThreads, 3)
 prefill_scaled_self_kernel(const ScanArgs a, const PrefillGeom geo, const SegmentPlan plan, const GatedOut gt)
 {
     griddep_entry();
-    prefill_scaled_body<LANES, VPL, RPT, EXACT, kScanFull, 3>(a, geo, plan, gt);
+    prefill_scaled_body<LANES, VPL, RPT, EXACT, kScanFull, EPI>(a, geo, plan, gt);
 }
 
 namespace {
@@ -820,7 +864,7 @@ cudaError_t launch_scaled_one(const ScanArgs &a, const PrefillGeom &g, const Seg
                               long long n_units, size_t smem, int epi, const GatedOut &gt, cudaStream_t stream)
 {
     const bool exact = (a.N / 4) == LANES * VPL;
-    const int threads = (g.rows_per_cta / RPT) * LANES + (epi == 3 ? 0 : 32);   // consumers (+ the producer)
+    const int threads = (g.rows_per_cta / RPT) * LANES + (epi >= 3 ? 0 : 32);   // consumers (+ the producer)
     const dim3 grid((unsigned)(n_units * a.G * g.runs_per_group));
     void (*kern)(const ScanArgs, const PrefillGeom, const SegmentPlan, const GatedOut) = nullptr;
     if (mode != kScanFull) {
@@ -831,12 +875,17 @@ cudaError_t launch_scaled_one(const ScanArgs &a, const PrefillGeom &g, const Seg
     } else if (epi == 0) {
         kern = exact ? prefill_scaled_kernel<LANES, VPL, RPT, true, kScanFull>
                      : prefill_scaled_kernel<LANES, VPL, RPT, false, kScanFull>;
-    } else if (epi == 3) {
-        if (threads != kSelfThreads)
+    } else if (epi == 3 || epi == 4) {
+        if (threads != kSelfThreads || (epi == 4 && !gt.out))
             return cudaErrorInvalidValue;
-        if constexpr (kHasTile<LANES, VPL, RPT>)
-            kern = exact ? prefill_scaled_self_kernel<LANES, VPL, RPT, true>
-                         : prefill_scaled_self_kernel<LANES, VPL, RPT, false>;
+        if constexpr (kHasTile<LANES, VPL, RPT>) {
+            if (epi == 3)
+                kern = exact ? prefill_scaled_self_kernel<LANES, VPL, RPT, true, 3>
+                             : prefill_scaled_self_kernel<LANES, VPL, RPT, false, 3>;
+            else
+                kern = exact ? prefill_scaled_self_kernel<LANES, VPL, RPT, true, 4>
+                             : prefill_scaled_self_kernel<LANES, VPL, RPT, false, 4>;
+        }
         if (!kern)
             return cudaErrorInvalidValue;
     } else {
