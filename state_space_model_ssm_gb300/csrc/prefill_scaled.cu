@@ -193,8 +193,9 @@ size_t prefill_scaled_smem_bytes(const PrefillGeom &g, int N, int lanes, int epi
     const size_t per_slot = (size_t)g.chunk * (2 * (size_t)N + 4 * (size_t)g.heads_cap) + cx + cm +
                             (epi == 1 || epi == 2 ? (size_t)epi * cx : 0);
     (void)lanes;
-    // epi 4: two y tiles and a z tile after the slots and the decay area
-    return (kSlots * per_slot + cm + (epi == 4 ? 3 * cx : 0)) * sizeof(float);
+    // epi 4: two y tiles and a z tile after the slots and the decay area; epi 5
+    // the two y tiles
+    return (kSlots * per_slot + cm + (epi == 4 ? 3 * cx : epi == 5 ? 2 * cx : 0)) * sizeof(float);
 }
 
 // MODE kScanFull: the scan with y.  MODE kScanStateOnly: one time segment's
@@ -203,7 +204,8 @@ size_t prefill_scaled_smem_bytes(const PrefillGeom &g, int N, int lanes, int epi
 // tile, stored by the producer; 2 as 1 and the gated RMSNorm output (a block's
 // rows are exactly one head); 3 no producer warp: the consumers stage the
 // chunks and store y; 4 as 3 with the gated output (y and z through tiles,
-// written out by all warps one chunk later).  The tile variants
+// written out by all warps one chunk later); 5 as 3 with y through tiles
+// written out by all warps one chunk later.  The tile variants
 // (prefill_scaled_tile_kernel) run blocks of at most kTileThreads (four
 // consumer warps and the producer) and keep two blocks per SM; the
 // self-staged ones (prefill_scaled_self_kernel) exactly kSelfThreads, three
@@ -216,9 +218,10 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
                                                     const SegmentPlan &plan, const GatedOut &gt)
 {
     constexpr bool kFull = (MODE == kScanFull);
-    // EPI 3 and 4: self-staged (no producer warp); EPI 4 with the gated output
-    constexpr bool SELF = EPI == 3 || EPI == 4;
-    constexpr bool TILE = EPI == 1 || EPI == 2 || EPI == 4, GATED = EPI == 2 || EPI == 4;
+    // EPI 3, 4 and 5: self-staged (no producer warp); 4 with the gated output,
+    // 5 with y through tiles
+    constexpr bool SELF = EPI == 3 || EPI == 4 || EPI == 5;
+    constexpr bool TILE = EPI == 1 || EPI == 2 || EPI == 4 || EPI == 5, GATED = EPI == 2 || EPI == 4;
     static_assert(kFull || EPI == 0, "the output tile and the self-staged form need y");
     extern __shared__ __align__(16) float smem[];
     const int N = a.N, N4 = a.N >> 2, P = a.P, H = a.H;
@@ -507,6 +510,12 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
     const int hl = (r0 + rl) / P - h0;
     const float Dv = __ldg(a.D + h0 + hl);
     const int yq = reduced_row<LANES, RPT>(j);               // row of this lane's reduced sum
+    // Pairwise reduction (two tokens of a run at once) where 2 RPT <= LANES
+    // and y goes through a tile (measured slower with the consumers' own
+    // global stores): this lane's sum is row q2 of the pair's token t2.
+    constexpr bool kPair = kFull && TILE && 2 * RPT <= LANES;
+    const int r2 = kPair ? reduced_row<LANES, (kPair ? 2 * RPT : RPT)>(j) : 0;
+    const int q2 = r2 % RPT, t2 = r2 / RPT;
     const bool ystore = kFull && rvalid;
 
     // ---- A2 state load: U = S at the start (slot, segment plan, or zero) ----
@@ -587,6 +596,31 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
         }
     };
 
+    // Self-staged y through tiles (EPI 5): chunk cc's y tile to global memory,
+    // spread over the whole block; 128-bit stores where the rows allow (then x
+    // moves in 16-byte pieces too, and its walk fits y).
+    const bool y16 = x16 && (reinterpret_cast<uintptr_t>(a.y) & 15) == 0;
+    auto flush_y = [&](int cc) {
+        const int cnt = min(geo.chunk, len - cc * geo.chunk);
+        const int xs = geo.rows_per_cta;
+        const float *Y = sm.SelfY(cc & 1);
+        float *yg = a.y + ((long long)tok_start + cc * geo.chunk) * HP + r0;
+        if (y16) {
+            for (int t = xt0, r = xv0; t < cnt;) {   // the x walk: xw = nrows / 4 pieces per token
+                *reinterpret_cast<float4 *>(yg + t * HP + 4 * r) =
+                    *reinterpret_cast<const float4 *>(Y + t * xs + 4 * r);
+                t += xdt;
+                r += xdv;
+                if (r >= xw) { r -= xw; ++t; }
+            }
+        } else {
+            for (int i = tid; i < cnt * nrows; i += kSelfThreads) {
+                const int t = i / nrows, r = i - t * nrows;
+                yg[t * HP + r] = Y[t * xs + r];
+            }
+        }
+    };
+
     // Self-staged (no producer warp): every thread copies its share of each
     // chunk two chunks ahead, and the warps take turns forming the next
     // chunk's coefficients at the end of a chunk; one block barrier per chunk.
@@ -618,6 +652,9 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
                     gate(c - 1);                      // chunk c-1's y tile and z are complete
                 bar_sync(0, kSelfThreads);            // the z tile and chunk c-1's y tile are free again
                 stage_z(c);                           // read at the start of chunk c+1
+            } else if constexpr (TILE) {
+                if (c >= 1)                           // chunk c-1's y tile is complete; it is rewritten
+                    flush_y(c - 1);                   // in chunk c+1, after the next barrier
             }
             if (c + 2 < n_chunks)
                 stage(c + 2, (c + 2) % kSlots);       // its slot held chunk c-1
@@ -644,6 +681,7 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
         float *yrow = a.y + ((long long)tok_start + c * geo.chunk) * HP + r0 + rl + yq;
         float *pY = !TILE ? nullptr                            // the chunk's y tile (EPI 1, 2, 4)
                           : (SELF ? sm.SelfY(c & 1) : sm.Ytile(b)) + rl + yq;
+        float *yrow2 = yrow - yq + q2, *pY2 = TILE ? pY - yq + q2 : nullptr;   // the pairwise reduction's row
 
         // Shared-memory operands of one token.
         struct TokenIn {
@@ -675,10 +713,9 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
                     u[q][k][1] = __fmul2_rn(u[q][k][1], r2);
                 }
         };
-        // One token: U += (x dt / Lambda) B; with y: the lanes' parts of U . C
-        // summed by shuffles (transposing over the RPT rows), then
-        // y = Lambda (U . C) + D x from the lane that holds the row's sum.
-        auto step = [&](const TokenIn &in, int t) -> float {
+        // One token: U += (x dt / Lambda) B; with y, this lane's parts of U . C
+        // for its RPT rows (before the reduction over the row's lanes).
+        auto step_part = [&](const TokenIn &in, float (&part)[RPT]) {
             float2 a2[RPT];
 #pragma unroll
             for (int q = 0; q < RPT; ++q) {
@@ -721,14 +758,21 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
                         }
                     }
                 }
-                float part[RPT];
 #pragma unroll
                 for (int q = 0; q < RPT; ++q) {
                     const float2 s2 = NACC > 1 ? __fadd2_rn(acc[q][0], acc[q][NACC - 1]) : acc[q][0];
                     part[q] = s2.x + s2.y;
                 }
-                // every lane holds the full sum of its row, so all lanes of a
-                // row store the same value (no divergent branch around the store)
+            }
+        };
+        // One token with y: the lanes' parts summed by shuffles (transposing
+        // over the RPT rows), then y = Lambda (U . C) + D x from the lane that
+        // holds the row's sum.  Every lane holds the full sum of its row, so all
+        // lanes of a row store the same value (no divergent branch).
+        auto step = [&](const TokenIn &in, int t) {
+            float part[RPT];
+            step_part(in, part);
+            if constexpr (kFull) {
                 const float ysum = reduce_rows<LANES, RPT>(part, j);
                 const float yv = fmaf(in.cf.y, ysum, Dv * pX[t * xs + yq]);
                 if (ystore) {
@@ -737,9 +781,26 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
                     else
                         yrow[t * HP] = yv;
                 }
-                return yv;
             }
-            return 0.f;
+        };
+        // Two tokens t0, t0 + 1 with y: their 2 RPT row sums in one transposing
+        // reduction (twice the independent shuffles per level); every lane ends
+        // with the sum of one (token, row) pair (q2, t2 above) and stores it.
+        auto step_pair = [&](const TokenIn &i0, const TokenIn &i1, int t0) {
+            if constexpr (kPair) {
+                float p[2 * RPT];
+                step_part(i0, reinterpret_cast<float (&)[RPT]>(p[0]));
+                step_part(i1, reinterpret_cast<float (&)[RPT]>(p[RPT]));
+                const float ysum = reduce_rows<LANES, 2 * RPT>(p, j);
+                const int tt = t0 + t2;
+                const float yv = fmaf(t2 ? i1.cf.y : i0.cf.y, ysum, Dv * pX[tt * xs + q2]);
+                if (ystore) {
+                    if constexpr (TILE)
+                        st_shared_unordered(pY2 + tt * xs, yv);
+                    else
+                        yrow2[tt * HP] = yv;
+                }
+            }
         };
         // Anchor tokens (any head of the block) rescale U before their update;
         // a head that does not anchor there has r = 1 (exact no-op).  Token 0
@@ -758,11 +819,21 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
             if ((amask >> t) & 1u)
                 rescale(pCf[t * hc].z);
             if (t + kRun <= cnt && ((amask >> t) & kRunMask) == 0u) {
+                if constexpr (kPair) {
 #pragma unroll
-                for (int v = 0; v < kRun; ++v) {
-                    TokenIn in;
-                    load_token(t + v, in);
-                    step(in, t + v);
+                    for (int v = 0; v < kRun; v += 2) {
+                        TokenIn i0, i1;
+                        load_token(t + v, i0);
+                        load_token(t + v + 1, i1);
+                        step_pair(i0, i1, t + v);
+                    }
+                } else {
+#pragma unroll
+                    for (int v = 0; v < kRun; ++v) {
+                        TokenIn in;
+                        load_token(t + v, in);
+                        step(in, t + v);
+                    }
                 }
                 t += kRun;
             } else {
@@ -792,6 +863,11 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
             cp_async_wait<0>();
             bar_sync(0, kSelfThreads);
             gate(n_chunks - 1);
+        }
+    } else if constexpr (SELF && TILE) {
+        if (n_chunks > 0) {                 // the last chunk's y tile
+            bar_sync(0, kSelfThreads);
+            flush_y(n_chunks - 1);
         }
     } else if constexpr (GATED) {
         if (n_chunks > 0) {                 // the last chunk: every consumer warp done with it
@@ -875,16 +951,19 @@ cudaError_t launch_scaled_one(const ScanArgs &a, const PrefillGeom &g, const Seg
     } else if (epi == 0) {
         kern = exact ? prefill_scaled_kernel<LANES, VPL, RPT, true, kScanFull>
                      : prefill_scaled_kernel<LANES, VPL, RPT, false, kScanFull>;
-    } else if (epi == 3 || epi == 4) {
+    } else if (epi >= 3 && epi <= 5) {
         if (threads != kSelfThreads || (epi == 4 && !gt.out))
             return cudaErrorInvalidValue;
         if constexpr (kHasTile<LANES, VPL, RPT>) {
             if (epi == 3)
                 kern = exact ? prefill_scaled_self_kernel<LANES, VPL, RPT, true, 3>
                              : prefill_scaled_self_kernel<LANES, VPL, RPT, false, 3>;
-            else
+            else if (epi == 4)
                 kern = exact ? prefill_scaled_self_kernel<LANES, VPL, RPT, true, 4>
                              : prefill_scaled_self_kernel<LANES, VPL, RPT, false, 4>;
+            else
+                kern = exact ? prefill_scaled_self_kernel<LANES, VPL, RPT, true, 5>
+                             : prefill_scaled_self_kernel<LANES, VPL, RPT, false, 5>;
         }
         if (!kern)
             return cudaErrorInvalidValue;
