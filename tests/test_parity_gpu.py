@@ -446,6 +446,43 @@ def test_parity_y_not_16_byte_aligned():
         assert_parity(inp, y.double().cpu().numpy(), state.double().cpu().numpy(), y_ref, s_ref)
 
 
+# ---- the self-staged full pass (four consumer warps stage their own chunks) ----
+
+SELF_GEOMS = [Geometry(8, 64, 128, 2), Geometry(8, 64, 100, 2), Geometry(8, 64, 64, 2),
+              Geometry(8, 32, 128, 2), Geometry(6, 48, 128, 3)]
+
+
+@pytest.mark.parametrize("geom", SELF_GEOMS, ids=lambda g: f"h{g.n_heads}_p{g.head_dim}_n{g.d_state}_g{g.n_groups}")
+def test_parity_self_staged_full_pass(geom):
+    """Shapes whose full pass runs without a producer warp (8 lanes x 4 rows per
+    lane, blocks of 64 rows, y through the two tiles): d_state 128 and 64 (every
+    lane busy), 100 (lanes past d_state idle, the general staging walk), blocks
+    holding two heads (head_dim 32) and heads that straddle blocks (head_dim
+    48); a ragged, partly resuming batch with an empty sequence, through
+    ssm_scan_ws (time segments) and with 64-row blocks and no segments."""
+    inp = make_inputs(geom, [700, 3, 260, 1500, 0, 41], [1, 0, 1, 0, 1, 1], seed=71)
+    y_ref, s_ref = oracle.scan_inputs(inp)
+    y, s = run_gpu(inp, workspace=True)
+    assert_parity(inp, y, s, y_ref, s_ref)
+    y, s = run_gpu(inp, tuning=_tuning(path=bd.PATH_PREFILL, rows=64, seg=-1))
+    assert_parity(inp, y, s, y_ref, s_ref)
+
+
+@pytest.mark.parametrize("d_state", [128, 100, 64])
+def test_parity_gated_self_staged(d_state):
+    """The gated output of the self-staged full pass (blocks of one 64-row head:
+    y and z through tiles, gated one chunk later by all four warps), with and
+    without time segments, against the oracle's y."""
+    from tests.gpu_helpers import assert_gated, run_gpu_gated
+    inp = make_inputs(Geometry(8, 64, d_state, 2), [700, 3, 260, 1500, 0, 41], [1, 0, 1, 0, 1, 1], seed=72)
+    y_ref, s_ref = oracle.scan_inputs(inp)
+    for ws in (True, False):
+        t = None if ws else _tuning(path=bd.PATH_PREFILL, rows=64, seg=-1)
+        y, s, gated, z, w = run_gpu_gated(inp, eps=1e-5, tuning=t, workspace=ws)
+        assert_parity(inp, y, s, y_ref, s_ref)
+        assert_gated(inp, y_ref, gated, z, w, 1e-5)
+
+
 # ---- per-token state snapshots (speculative verify) ----
 
 @pytest.mark.parametrize("fused_dt", [False, True], ids=["plain", "fused_dt"])
