@@ -47,8 +47,11 @@ def _run(x, w, b, st, starts, lens, resume, use_bias, snaps):
 @pytest.mark.parametrize("K", [1, 2, 4, 8])
 @pytest.mark.parametrize("use_bias,snaps", [(True, True), (False, False)], ids=["bias_snaps", "plain"])
 def test_conv1d_ragged(K, use_bias, snaps):
-    x, w, b, st, starts, lens, resume = _case(37, K, [0, 1, 2, 9, 30], [1, 0, 1, 1, 0],
-                                              starts=[0, 0, 3, 5, 15], n_tokens=47, seed=K)
+    """Ragged batch: an empty resuming sequence (slot kept), an empty fresh one
+    (slot zeroed), sequences shorter than the k-1 history (slot shifted), and
+    tokens no sequence owns."""
+    x, w, b, st, starts, lens, resume = _case(37, K, [0, 1, 2, 9, 30, 0], [1, 0, 1, 1, 0, 0],
+                                              starts=[0, 0, 3, 5, 15, 20], n_tokens=47, seed=K)
     out, state, sn = _run(x, w, b, st, starts, lens, resume, use_bias, snaps)
     o_ref, s_ref, sn_ref = ext.conv1d_silu(x, w, st, starts, lens, resume, bias=b if use_bias else None)
     own = ~np.isnan(o_ref[:, 0])
@@ -77,3 +80,25 @@ def test_conv1d_split_resume_equals_one_call():
     o2, s2, _ = _run(x[17:], w, b, torch.from_numpy(s1).float(), [0], [33], [1], True, False)
     assert np.array_equal(np.concatenate([o1, o2]), out)
     assert np.array_equal(s2, s_full)
+
+
+@pytest.mark.parametrize("K", [2, 4, 7])
+def test_conv1d_long_ragged_spans(K):
+    """Sequences much longer than the average, so the blocks of one sequence
+    walk several spans each, beside a short one; resuming and fresh."""
+    x, w, b, st, starts, lens, resume = _case(264, K, [3000, 17, 1200], [1, 0, 1], seed=20 + K)
+    out, state, _ = _run(x, w, b, st, starts, lens, resume, True, False)
+    o_ref, s_ref, _ = ext.conv1d_silu(x, w, st, starts, lens, resume, bias=b)
+    assert np.all(np.abs(out - o_ref) <= 1e-5 * (1.0 + np.abs(o_ref)))
+    assert np.array_equal(state, s_ref)
+
+
+def test_conv1d_no_tokens_rolls_the_slots():
+    """A call with no tokens at all: fresh sequences' slots become zeros,
+    resuming ones keep theirs."""
+    x, w, b, st, starts, lens, resume = _case(40, 4, [0, 0, 0], [0, 1, 0], starts=[0, 0, 0], n_tokens=0, seed=5)
+    out, state, _ = _run(x, w, b, st, starts, lens, resume, True, False)
+    _, s_ref, _ = ext.conv1d_silu(x, w, st, starts, lens, resume, bias=b)
+    assert np.array_equal(state, s_ref)
+    assert np.all(state[0] == 0) and np.all(state[2] == 0)
+    assert np.array_equal(state[1], st[1].double().numpy())
