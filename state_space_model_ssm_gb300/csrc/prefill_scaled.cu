@@ -626,6 +626,18 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
     // chunk's coefficients at the end of a chunk; one block barrier per chunk.
     constexpr int ncw = kSelfThreads / 32;
     const float dnone[kDtHeads] = {};                 // self-staged: dt comes through shared memory
+    float pend = 1.f;                                 // Lambda_last of the previous chunk, not yet applied to U
+    // U <- r U (an anchor's rescale, or Lambda_last back to S)
+    auto rescale = [&](float r) {
+        const float2 r2 = f2(r, r);
+#pragma unroll
+        for (int q = 0; q < RPT; ++q)
+#pragma unroll
+            for (int k = 0; k < VPL; ++k) {
+                u[q][k][0] = __fmul2_rn(u[q][k][0], r2);
+                u[q][k][1] = __fmul2_rn(u[q][k][1], r2);
+            }
+    };
     if constexpr (SELF) {
         if (n_chunks > 0)
             stage(0, 0);
@@ -702,16 +714,6 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
                         in.c[k] = *reinterpret_cast<const float4 *>(ct + 4 * k * LANES);
                 }
             }
-        };
-        auto rescale = [&](float r) {
-            const float2 r2 = f2(r, r);
-#pragma unroll
-            for (int q = 0; q < RPT; ++q)
-#pragma unroll
-                for (int k = 0; k < VPL; ++k) {
-                    u[q][k][0] = __fmul2_rn(u[q][k][0], r2);
-                    u[q][k][1] = __fmul2_rn(u[q][k][1], r2);
-                }
         };
         // One token: U += (x dt / Lambda) B; with y, this lane's parts of U . C
         // for its RPT rows (before the reduction over the row's lanes).
@@ -816,8 +818,8 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
         constexpr unsigned kRunMask = (1u << kRun) - 2u;    // the run's tokens after its first
         int t = 0;
         while (t < cnt) {
-            if ((amask >> t) & 1u)
-                rescale(pCf[t * hc].z);
+            if ((amask >> t) & 1u)                    // token 0 anchors: also the previous chunk's Lambda_last
+                rescale(t == 0 ? pCf[0].z * pend : pCf[t * hc].z);
             if (t + kRun <= cnt && ((amask >> t) & kRunMask) == 0u) {
                 if constexpr (kPair) {
 #pragma unroll
@@ -843,8 +845,9 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
                 ++t;
             }
         }
-        // back to S at the chunk end: U <- Lambda_last U
-        rescale(pCf[(cnt - 1) * hc].y);
+        // back to S at the chunk end (U <- Lambda_last U), folded into the next
+        // chunk's first rescale or applied after the last chunk
+        pend = pCf[(cnt - 1) * hc].y;
         __syncwarp();
         if constexpr (SELF) {
             if (coef_warp) {                          // into chunk c+1's slot, read after the next barrier
@@ -877,6 +880,9 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
             bar_arrive(kBarEmpty + (n_chunks - 1) % kSlots, nthr);
         }
     }
+
+    if (n_chunks > 0)
+        rescale(pend);                                // U <- Lambda_last U: the state S again
 
     // ---- A7 state store: slot (last segment) or the unit's scratch (state pass) ----
     float *dst = nullptr;
