@@ -521,8 +521,7 @@ int scan_kernels(const ssm::ScanArgs &a, const ssm_scan_tuning &t, const DeviceI
     }
     // Output of the full pass.  Blocks of exactly four consumer warps run
     // self-staged, without a producer warp, three per SM: y through tiles that
-    // all warps write out one chunk later (epi 5; epi 3, where the consumers
-    // store y, remains for the sweeps), and with the gated RMSNorm requested y and
+    // all warps write out one chunk later (epi 5), and with the gated RMSNorm requested y and
     // z through tiles (epi 4: blocks of exactly one head, x, y, z and the gated
     // output 16-byte aligned).  Other shapes with the
     // output-tile variants keep a producer warp: y goes through a shared-memory
@@ -541,8 +540,6 @@ int scan_kernels(const ssm::ScanArgs &a, const ssm_scan_tuning &t, const DeviceI
     if (self_ok && !gated && three_per_sm(5)) {
         epi = 5;                            // self-staged, y through tiles: three blocks per SM
         smem_full = ssm::prefill_scaled_smem_bytes(pl.g, N, pl.lanes, 5);
-    } else if (self_ok && !gated && three_per_sm(3)) {
-        epi = 3;                            // self-staged, the consumers store y
     } else if (self_ok && gated && pl.g.rows_per_cta == P && P % 4 == 0 && aligned(gated->z, 16) &&
                aligned(gated->out, 16) && aligned(a.y, 16) && aligned(a.x, 16) && three_per_sm(4)) {
         fuse = gated;                       // self-staged with the gated output

@@ -65,6 +65,10 @@ namespace {
 
 constexpr float kAnchorSpan = 40.f;
 constexpr int kSlots = 3;         // staging slots: two chunks in flight while one is consumed
+// Self-staged slots: 3 (two chunks ahead) for the plain output; 2 (one chunk
+// ahead, which a chunk's work covers many times) for the gated output, whose
+// z tiles then fit twice and need no second barrier per chunk.
+__host__ __device__ constexpr int self_slots(int epi) { return epi == 4 ? 2 : 3; }
 constexpr int kBarFull = 1;       // named barriers kBarFull + s: slot s staged
 constexpr int kBarEmpty = 4;      // named barriers kBarEmpty + s: slot s consumed
 constexpr int kBarConsumers = 7;  // the consumer warps alone (the gated output)
@@ -100,11 +104,15 @@ struct ScaledSmem {
     }
     __device__ __forceinline__ float *Ytile(int s) const { return slot(s) + 2 * cb + cx + cc + cm; }
     __device__ __forceinline__ float *Ztile(int s) const { return slot(s) + 2 * cb + 2 * cx + cc + cm; }
-    __device__ __forceinline__ float *Dec() const { return base + kSlots * (2 * cb + cx + cc + cm + cg); }
-    // self-staged gated output (EPI 4): two y tiles (chunk c in tile c % 2) and
-    // one z tile after the decay area, cx floats each
-    __device__ __forceinline__ float *SelfY(int i) const { return Dec() + cm + i * cx; }
-    __device__ __forceinline__ float *SelfZ() const { return Dec() + cm + 2 * cx; }
+    // after the NS slots (kSlots, or self_slots(EPI) when self-staged)
+    template <int NS>
+    __device__ __forceinline__ float *Dec() const { return base + NS * (2 * cb + cx + cc + cm + cg); }
+    // self-staged output (EPI 5, 4): two y tiles and (EPI 4) two z tiles after the
+    // decay area, cx floats each; chunk c in tile c % 2
+    template <int NS>
+    __device__ __forceinline__ float *SelfY(int i) const { return Dec<NS>() + cm + i * cx; }
+    template <int NS>
+    __device__ __forceinline__ float *SelfZ(int i) const { return Dec<NS>() + cm + (2 + i) * cx; }
 };
 
 __device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
@@ -193,33 +201,36 @@ size_t prefill_scaled_smem_bytes(const PrefillGeom &g, int N, int lanes, int epi
     const size_t per_slot = (size_t)g.chunk * (2 * (size_t)N + 4 * (size_t)g.heads_cap) + cx + cm +
                             (epi == 1 || epi == 2 ? (size_t)epi * cx : 0);
     (void)lanes;
-    // epi 4: two y tiles and a z tile after the slots and the decay area; epi 5
-    // the two y tiles
-    return (kSlots * per_slot + cm + (epi == 4 ? 3 * cx : epi == 5 ? 2 * cx : 0)) * sizeof(float);
+    // self-staged (epi 4, 5): self_slots(epi) slots, then two y tiles and (epi 4)
+    // two z tiles after the decay area
+    const bool self = epi == 4 || epi == 5;
+    return ((self ? self_slots(epi) : kSlots) * per_slot + cm + (epi == 4 ? 4 * cx : epi == 5 ? 2 * cx : 0)) *
+           sizeof(float);
 }
 
 // MODE kScanFull: the scan with y.  MODE kScanStateOnly: one time segment's
 // state from zero (no C, no y), for the segment pass of long sequences.
 // EPI (kScanFull only): 0 the consumers store y; 1 y through a shared-memory
 // tile, stored by the producer; 2 as 1 and the gated RMSNorm output (a block's
-// rows are exactly one head); 3 no producer warp: the consumers stage the
-// chunks and store y; 4 as 3 with the gated output (y and z through tiles,
-// written out by all warps one chunk later); 5 as 3 with y through tiles
-// written out by all warps one chunk later.  The tile variants
+// rows are exactly one head); without a producer warp (the consumers stage
+// the chunks): 5 y through tiles written out by all warps one chunk later, 4
+// as 5 with the gated output (z through a tile too).  (3, the self-staged
+// form with the consumers' own y stores, measured slower than 5 and is not
+// launched.)  The tile variants
 // (prefill_scaled_tile_kernel) run blocks of at most kTileThreads (four
 // consumer warps and the producer) and keep two blocks per SM; the
 // self-staged ones (prefill_scaled_self_kernel) exactly kSelfThreads, three
 // per SM.
 constexpr int kTileThreads = 160;
-constexpr int kSelfThreads = 128;      // self-staged (EPI 3, 4): exactly four consumer warps, no producer
+constexpr int kSelfThreads = 128;      // self-staged (EPI 4, 5): exactly four consumer warps, no producer
 
 template <int LANES, int VPL, int RPT, bool EXACT, int MODE, int EPI>
 __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const PrefillGeom &geo,
                                                     const SegmentPlan &plan, const GatedOut &gt)
 {
     constexpr bool kFull = (MODE == kScanFull);
-    // EPI 3, 4 and 5: self-staged (no producer warp); 4 with the gated output,
-    // 5 with y through tiles
+    // EPI 4 and 5 (and 3): self-staged (no producer warp); 4 with the gated
+    // output, 5 with y through tiles
     constexpr bool SELF = EPI == 3 || EPI == 4 || EPI == 5;
     constexpr bool TILE = EPI == 1 || EPI == 2 || EPI == 4 || EPI == 5, GATED = EPI == 2 || EPI == 4;
     static_assert(kFull || EPI == 0, "the output tile and the self-staged form need y");
@@ -233,6 +244,7 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
     sm.cc = geo.chunk * geo.heads_cap * 4;
     sm.cm = (geo.heads_cap + 3) & ~3;                    // keeps the next slot 16-byte aligned
     sm.cg = (EPI == 1 || EPI == 2) ? EPI * sm.cx : 0;
+    constexpr int NS = SELF ? self_slots(EPI) : kSlots;
 
     // ---- A1 work mapping: (work unit, group, run of rows) ----
     // A work unit is a whole sequence, or with a segment plan one time segment
@@ -293,7 +305,7 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
     const long long tokN = (long long)a.G * N;
     // A3: stage B, C and x of chunk c0 into slot b (cp.async by the staging
     // threads, one commit group per chunk)
-    float *seg_decay = sm.Dec();     // state pass: running decay of the segment per head
+    float *seg_decay = sm.Dec<NS>();     // state pass: running decay of the segment per head
     // Walk over (token, column) items in steps of scount without divisions:
     // start at (sid / width, sid % width), step (scount / width, scount % width).
     const int bt0 = sid / N4, bv0 = sid - bt0 * N4, bdt = scount / N4, bdv = scount - bdt * N4;
@@ -375,7 +387,7 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
         const int t0 = c0 * geo.chunk;
         const int cnt = min(geo.chunk, len - t0);
         const float *gz = gt.z + ((long long)tok_start + t0) * HP + r0;
-        float *sZ = sm.SelfZ();
+        float *sZ = sm.SelfZ<NS>(c0 & 1);
         for (int t = xt0, r = xv0; t < cnt;) {      // 16-byte pieces (checked by the host)
             cp_async16(sZ + t * geo.rows_per_cta + 4 * r, gz + t * HP + 4 * r);
             t += xdt;
@@ -560,7 +572,8 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
         const int cnt = min(geo.chunk, len - cc * geo.chunk);
         const int xs = geo.rows_per_cta;
         const int nw = SELF ? kSelfThreads / 32 : (nthr >> 5) - 1, sub = lane >> 3, l8 = lane & 7;
-        const float *Y = SELF ? sm.SelfY(cc & 1) : sm.Ytile(bb), *Z = SELF ? sm.SelfZ() : sm.Ztile(bb);
+        const float *Y = SELF ? sm.SelfY<NS>(cc & 1) : sm.Ytile(bb);
+        const float *Z = SELF ? sm.SelfZ<NS>(cc & 1) : sm.Ztile(bb);
         const float inv_p = 1.f / (float)nrows;
         float *out = gt.out + ((long long)tok_start + cc * geo.chunk) * HP + r0;
         float *yout = a.y + ((long long)tok_start + cc * geo.chunk) * HP + r0;   // self-staged: y too
@@ -603,7 +616,7 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
     auto flush_y = [&](int cc) {
         const int cnt = min(geo.chunk, len - cc * geo.chunk);
         const int xs = geo.rows_per_cta;
-        const float *Y = sm.SelfY(cc & 1);
+        const float *Y = sm.SelfY<NS>(cc & 1);
         float *yg = a.y + ((long long)tok_start + cc * geo.chunk) * HP + r0;
         if (y16) {
             for (int t = xt0, r = xv0; t < cnt;) {   // the x walk: xw = nrows / 4 pieces per token
@@ -622,8 +635,9 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
     };
 
     // Self-staged (no producer warp): every thread copies its share of each
-    // chunk two chunks ahead, and the warps take turns forming the next
-    // chunk's coefficients at the end of a chunk; one block barrier per chunk.
+    // chunk NS - 1 chunks ahead (one commit group per chunk, and one for z),
+    // and the warps take turns forming the next chunk's coefficients at the end
+    // of a chunk; one block barrier per chunk.
     constexpr int ncw = kSelfThreads / 32;
     const float dnone[kDtHeads] = {};                 // self-staged: dt comes through shared memory
     float pend = 1.f;                                 // Lambda_last of the previous chunk, not yet applied to U
@@ -643,33 +657,36 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
             stage(0, 0);
         else
             cp_async_commit();
-        if (n_chunks > 1)
-            stage(1, 1);
-        else
-            cp_async_commit();                        // one commit group per chunk, empty past the end
+        if constexpr (NS == 3) {
+            if (n_chunks > 1)
+                stage(1, 1);
+            else
+                cp_async_commit();                    // one commit group per chunk, empty past the end
+        }
         if (warp == 0 && n_chunks > 0) {
-            cp_async_wait<1>();                       // this warp's copies of chunk 0 (its dt) landed
+            cp_async_wait<NS - 2>();                  // this warp's copies of chunk 0 (its dt) landed
             coefficients(0, 0, dnone);
         }
     }
     for (int c = 0; c < n_chunks; ++c) {
-        const int b = c % kSlots;
+        const int b = c % NS;
         bool coef_warp = false;                       // self-staged: this warp forms chunk c+1's coefficients
         if constexpr (SELF) {
             // (bar.sync as inline asm, like the y-tile stores, so the compiler keeps their order)
-            cp_async_wait<1>();                       // this thread's copies of chunk c (and z of c-1) landed
+            cp_async_wait<NS - 2>();                  // this thread's copies of chunk c (and z of c-1) landed
             bar_sync(0, kSelfThreads);                // everyone's, and chunk c's coefficients; chunk c-1 done
+            // chunk c-1's y tile (and z) are complete; tile (c - 1) % 2 is rewritten in
+            // chunk c+1, after the next barrier
             if constexpr (GATED) {
                 if (c >= 1)
-                    gate(c - 1);                      // chunk c-1's y tile and z are complete
-                bar_sync(0, kSelfThreads);            // the z tile and chunk c-1's y tile are free again
-                stage_z(c);                           // read at the start of chunk c+1
+                    gate(c - 1);
+                stage_z(c);                           // into z tile c % 2 (z of c-2 was gated in chunk c-1)
             } else if constexpr (TILE) {
-                if (c >= 1)                           // chunk c-1's y tile is complete; it is rewritten
-                    flush_y(c - 1);                   // in chunk c+1, after the next barrier
+                if (c >= 1)
+                    flush_y(c - 1);
             }
-            if (c + 2 < n_chunks)
-                stage(c + 2, (c + 2) % kSlots);       // its slot held chunk c-1
+            if (c + NS - 1 < n_chunks)
+                stage(c + NS - 1, (c + NS - 1) % NS); // its slot held chunk c-1
             else
                 cp_async_commit();
             coef_warp = c + 1 < n_chunks && warp == (c + 1) % ncw;
@@ -692,7 +709,7 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
         const float *__restrict__ pX = sm.X(b) + rl;
         float *yrow = a.y + ((long long)tok_start + c * geo.chunk) * HP + r0 + rl + yq;
         float *pY = !TILE ? nullptr                            // the chunk's y tile (EPI 1, 2, 4)
-                          : (SELF ? sm.SelfY(c & 1) : sm.Ytile(b)) + rl + yq;
+                          : (SELF ? sm.SelfY<NS>(c & 1) : sm.Ytile(b)) + rl + yq;
         float *yrow2 = yrow - yq + q2, *pY2 = TILE ? pY - yq + q2 : nullptr;   // the pairwise reduction's row
 
         // Shared-memory operands of one token.
@@ -851,8 +868,8 @@ __device__ __forceinline__ void prefill_scaled_body(const ScanArgs &a, const Pre
         __syncwarp();
         if constexpr (SELF) {
             if (coef_warp) {                          // into chunk c+1's slot, read after the next barrier
-                cp_async_wait<1>();                   // this warp's copies of chunk c+1 (its dt) landed
-                coefficients(c + 1, (c + 1) % kSlots, dnone);
+                cp_async_wait<NS - 2>();              // this warp's copies of chunk c+1 (its dt) landed
+                coefficients(c + 1, (c + 1) % NS, dnone);
             }
         } else if (!GATED && (TILE || c + kSlots < n_chunks)) {
             // release the slot: the producer refills it with chunk c+3 (with the
@@ -923,7 +940,7 @@ prefill_scaled_tile_kernel(const ScanArgs a, const PrefillGeom geo, const Segmen
     prefill_scaled_body<LANES, VPL, RPT, EXACT, kScanFull, EPI>(a, geo, plan, gt);
 }
 
-// Self-staged full pass (EPI 3): blocks of four consumer warps and no producer,
+// Self-staged full pass (EPI 4, 5): blocks of four consumer warps and no producer,
 // three per SM (three warps on every SM sub-partition, at most 168 registers).
 
 template <int LANES, int VPL, int RPT, bool EXACT, int EPI>
@@ -957,14 +974,11 @@ cudaError_t launch_scaled_one(const ScanArgs &a, const PrefillGeom &g, const Seg
     } else if (epi == 0) {
         kern = exact ? prefill_scaled_kernel<LANES, VPL, RPT, true, kScanFull>
                      : prefill_scaled_kernel<LANES, VPL, RPT, false, kScanFull>;
-    } else if (epi >= 3 && epi <= 5) {
+    } else if (epi == 4 || epi == 5) {
         if (threads != kSelfThreads || (epi == 4 && !gt.out))
             return cudaErrorInvalidValue;
         if constexpr (kHasTile<LANES, VPL, RPT>) {
-            if (epi == 3)
-                kern = exact ? prefill_scaled_self_kernel<LANES, VPL, RPT, true, 3>
-                             : prefill_scaled_self_kernel<LANES, VPL, RPT, false, 3>;
-            else if (epi == 4)
+            if (epi == 4)
                 kern = exact ? prefill_scaled_self_kernel<LANES, VPL, RPT, true, 4>
                              : prefill_scaled_self_kernel<LANES, VPL, RPT, false, 4>;
             else

@@ -265,8 +265,8 @@ bool prefill_scaled_supported(int lanes, int vpl, int rpt);
 // (epi 2).
 bool prefill_scaled_tile_supported(int lanes, int vpl, int rpt, int rows_per_cta);
 // True for the shapes (and block sizes) whose full pass has the self-staged
-// variant (epi 3): no producer warp, four consumer warps stage the chunks
-// themselves, three blocks per SM.
+// variants (epi 5, and 4 with the gated output): no producer warp, four
+// consumer warps stage the chunks themselves, three blocks per SM.
 bool prefill_scaled_self_supported(int lanes, int vpl, int rpt, int rows_per_cta);
 size_t prefill_scaled_smem_bytes(const PrefillGeom &g, int N, int lanes, int epi = 0);
 constexpr int kScaledMaxChunk = 32;    // one warp lane per token in the coefficient pass
