@@ -26,6 +26,7 @@
 // (later spans start past the k-1 history), so that block also rewrites the
 // slot, after its own reads: no second launch.
 #include <algorithm>
+#include <atomic>
 
 #include "scan_common.cuh"
 
@@ -217,10 +218,19 @@ cudaError_t launch_out(const ConvArgs &a, cudaStream_t stream)
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess)
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, conv1d_out_kernel<CH, K>, kConvThreads, 0);
     if (e != cudaSuccess)
         return e;
+    // resident blocks per SM of this instantiation, asked once per device
+    constexpr int kDevs = 64;
+    static std::atomic<int> cached[kDevs];
+    per_sm = dev < kDevs ? cached[dev].load(std::memory_order_relaxed) : 0;
+    if (per_sm <= 0) {
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, conv1d_out_kernel<CH, K>, kConvThreads, 0);
+        if (e != cudaSuccess)
+            return e;
+        if (dev < kDevs)
+            cached[dev].store(per_sm, std::memory_order_relaxed);
+    }
     const long long runs = ((long long)a.n_tokens + (long long)a.n_seqs * kConvRun - 1) /
                            ((long long)a.n_seqs * kConvRun);                   // per sequence, on average
     const long long resident = (long long)(per_sm > 0 ? per_sm : 1) * sms;
