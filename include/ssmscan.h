@@ -122,7 +122,9 @@ enum {
  *                    row per lane and 4 rows)
  *   rows_per_cta     prefill: state rows per thread block (a multiple of the
  *                    rows one warp holds, at most 256 threads, 224 on
- *                    SSM_PATH_PREFILL which adds a producer warp); decode: ignored
+ *                    SSM_PATH_PREFILL, whose blocks add a producer warp except
+ *                    where they are exactly four warps of 8 lanes x 4 rows: those
+ *                    stage their own chunks, three blocks per SM); decode: ignored
  *   chunk_tokens     prefill: tokens staged in shared memory per chunk (1..256;
  *                    at most 32 on SSM_PATH_PREFILL, automatic 16 there, 32 on
  *                    SSM_PATH_PREFILL_DIRECT)
