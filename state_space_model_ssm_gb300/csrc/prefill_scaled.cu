@@ -19,18 +19,22 @@
 //    (between anchors 1/Lambda < e^40).  At the end of each chunk U is scaled
 //    back to S, so every chunk's coefficients are independent.
 //
-// 2. Warp specialisation.  The block has one producer warp and (rows/RPT)*LANES/32
-//    consumer warps.  The producer keeps two chunks of B, C and x in flight
-//    (cp.async into three slots) and computes each chunk's coefficients (lane =
-//    token: a warp prefix sum places the anchors, a segmented prefix product of
-//    dA = exp(dt*A) gives Lambda, ~1 ulp per factor).  Consumers run the token
-//    loop: per token U += alpha B, each lane's part of U . C, a shuffle
+// 2. Staging.  Each chunk's B, C and x go into shared-memory slots with
+//    cp.async ahead of use, and its coefficients are formed with lane = token
+//    (a warp prefix sum places the anchors, a segmented prefix product of
+//    dA = exp(dt*A) gives Lambda, ~1 ulp per factor).  Blocks of exactly four
+//    consumer warps of the default shapes stage their own chunks
+//    ("self-staged", three blocks per SM: three warps on every SM
+//    sub-partition): every thread copies its share, the warps take turns
+//    forming the next chunk's coefficients, and the block meets at one
+//    barrier per chunk.  Other shapes add one producer warp that stages two
+//    chunks ahead into three slots and meets the consumers at named barriers
+//    (bar.arrive / bar.sync, no spin loop): FULL[s] when slot s holds a staged
+//    chunk, EMPTY[s] when the consumers are done with it.  Consumers run the
+//    token loop: per token U += alpha B, each lane's part of U . C, a shuffle
 //    reduction over the row's lanes and the y store.  A lane holds RPT rows so
 //    that each B/C value read from shared memory (128-bit reads cost four
-//    wavefronts even when broadcast) feeds RPT rows.  The two sides meet at
-//    named barriers (bar.arrive / bar.sync: hardware barriers, no spin loop):
-//    FULL[s] when slot s holds a staged chunk, EMPTY[s] when the consumers are
-//    done with it.
+//    wavefronts even when broadcast) feeds RPT rows.
 //
 // 3. Token runs.  Consumers take a chunk's tokens in runs of eight with no
 //    anchor after the run's first token (the rescale of an anchor at the first
@@ -39,20 +43,22 @@
 //    and reduction; tokens outside such runs go one at a time.  The default
 //    shape gives a lane 16 elements of each of 4 rows (8 lanes per row at
 //    d_state 128): 64 state registers, B/C reads shared by 4 rows and a
-//    three-step shuffle reduction.  Every lane ends the reduction holding its
-//    row's full sum, so all lanes of a row store y (the same value) and the
-//    store needs no divergent branch.
+//    three-step shuffle reduction.  Where y goes through a tile, the row sums
+//    of two tokens are reduced together (8 values over the row's 8 lanes,
+//    one (token, row) sum per lane); otherwise every lane ends the reduction
+//    holding its row's full sum and all lanes of a row store y (the same
+//    value), with no divergent branch.
 //
-// 4. Output through the producer (EPI >= 1).  The consumers leave each chunk's
-//    y in a shared-memory tile instead of storing it; once they are done with
-//    the chunk, the otherwise idle producer writes the tile out with 128-bit
-//    stores.  With EPI = 2 (a block's rows are exactly one head) the kernel
-//    also applies Mamba2's output gate RMSNorm(y) * w * silu(z) per (token,
-//    head) row (kernel 3 of "ssm_gated_delta.cu"): the producer stages the
-//    chunk's z with B, C and x, and at the chunk's end the consumer warps
-//    share the row norms and the gated values (eight lanes per token), so the
-//    gated output needs no second pass over y.  (One producer warp alone
-//    would hold up the whole block with that work.)
+// 4. Output through tiles (EPI 1, 2, 4, 5).  The consumers leave each chunk's
+//    y in a shared-memory tile instead of storing it; the producer writes it
+//    out once the consumers release the chunk (EPI 1), or, self-staged, all
+//    warps write chunk c-1's tile after chunk c's barrier (EPI 5).  With
+//    EPI 2 and 4 (a block's rows are exactly one head) the kernel also applies
+//    Mamba2's output gate RMSNorm(y) * w * silu(z) per (token, head) row
+//    (kernel 3 of "ssm_gated_delta.cu"): z is staged beside the chunk, and the
+//    consumer warps share the row norms and the gated values (eight lanes per
+//    token), so the gated output needs no second pass over y.  (One producer
+//    warp alone would hold up the whole block with that work.)
 //
 // The rescaling is an algebraic identity of the recurrence defined by "The
 // llama journey", Day 14 (decay exp(dt*A), input dt*x*B, y from the updated
